@@ -1,0 +1,275 @@
+"""Python binding of the EAGLE cycle library: argument marshalling only.
+
+Every step of prefill, the draft-and-verify cycle and plain decoding runs in the CUDA
+library (libeagle.so). PyTorch supplies device memory (weights, the workspace, inputs
+and outputs) and the CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+from . import _lib as L
+from .synth import Workload
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def configs(w: Workload, max_batch: Optional[int] = None, max_ctx: Optional[int] = None,
+            prefill_chunk: int = 512):
+    m = w.model
+    mc = L.ModelCfg(m.n_layers, m.hidden, m.n_heads, m.n_kv_heads, m.head_dim, m.ffn, m.vocab,
+                    m.rope_theta, m.rms_eps, L.DTYPE_F32 if m.dtype == "f32" else L.DTYPE_BF16)
+    dc = L.DrafterCfg(w.drafter.kind, (C.c_int * 3)(*w.drafter.fuse_layers))
+    t = w.tree
+    tc = L.TreeCfg(t.topk, t.depth, t.m, t.temperature, w.seed, t.planted_p, t.planted_conf)
+    if max_ctx is None:
+        max_ctx = w.prompt_len[1] + w.new_tokens + 4 * (t.depth + 1) + 16
+    lim = L.Limits(max_batch or w.batch, max_ctx, 0, prefill_chunk)
+    return mc, dc, tc, lim
+
+
+class Engine:
+    """One context of the cycle library over caller-owned torch CUDA tensors."""
+
+    def __init__(self, w: Workload, weights: Dict[str, torch.Tensor], max_batch: Optional[int] = None,
+                 max_ctx: Optional[int] = None, prefill_chunk: int = 512,
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.lib = L.lib()
+        self.w = w
+        self.weights = weights
+        self.stream = stream
+        self.mc, self.dc, self.tc, self.lim = configs(w, max_batch, max_ctx, prefill_chunk)
+        nb = self.lib.eagle_workspace_bytes(C.byref(self.mc), C.byref(self.dc), C.byref(self.tc), C.byref(self.lim))
+        if nb == 0:
+            raise L.EagleError(L.EAGLE_EINVAL, "invalid configuration")
+        dev = next(iter(weights.values())).device
+        self.workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
+        g = lambda n: _ptr(weights.get(n))
+        layers = (L.LayerWeights * w.model.n_layers)()
+        for i in range(w.model.n_layers):
+            p = f"layers.{i}."
+            layers[i] = L.LayerWeights(g(p + "attn_norm"), g(p + "wqkv"), g(p + "wo"), g(p + "mlp_norm"),
+                                       g(p + "wgu"), g(p + "wd"))
+        self._layers = layers
+        draft = L.LayerWeights(g("draft.attn_norm"), g("draft.wqkv"), g("draft.wo"), g("draft.mlp_norm"),
+                               g("draft.wgu"), g("draft.wd"))
+        self.cw = L.Weights(g("embed"), g("lm_head"), g("final_norm"), layers, g("draft.fc"),
+                            g("draft.norm_g"), g("draft.norm_e"), draft)
+        h = C.c_void_p()
+        rc = self.lib.eagle_create(C.byref(self.mc), C.byref(self.dc), C.byref(self.tc), C.byref(self.cw),
+                                   C.byref(self.lim), self.workspace.data_ptr(), nb, _stream(stream), C.byref(h))
+        L.check(rc, "eagle_create")
+        self.h = h
+        self.batch = self.lim.max_batch
+        self._ref = None
+        self._tokens = None
+
+    # -- calls ---------------------------------------------------------------------
+    def _check(self, rc: int, what: str) -> None:
+        if rc != L.EAGLE_OK:
+            raise L.EagleError(rc, f"{what}: {self.lib.eagle_last_error(self.h).decode()}")
+
+    def prefill(self, prompts: Sequence[torch.Tensor], ref: Optional[torch.Tensor] = None) -> None:
+        """prompts: int32 CUDA tensors, one per sequence. ref: int32 CUDA [B][ref_len] plain
+        continuation (first entry = the prefill token) enabling planted mode, or None."""
+        self.batch = len(prompts)
+        self._tokens = torch.cat([p.to(torch.int32) for p in prompts]).contiguous()
+        lens = (C.c_int32 * self.batch)(*[int(p.numel()) for p in prompts])
+        self._ref = None if ref is None else ref.to(torch.int32).contiguous()
+        rc = self.lib.eagle_prefill(self.h, self.batch, self._tokens.data_ptr(), lens, _ptr(self._ref),
+                                    0 if ref is None else int(self._ref.shape[1]))
+        self._check(rc, "eagle_prefill")
+
+    def cycle(self, out_tokens: Optional[torch.Tensor] = None, out_count: Optional[torch.Tensor] = None) -> None:
+        self._check(self.lib.eagle_cycle(self.h, _ptr(out_tokens), _ptr(out_count)), "eagle_cycle")
+
+    def decode_plain(self, n: int, out: torch.Tensor) -> None:
+        self._check(self.lib.eagle_decode_plain(self.h, n, _ptr(out)), "eagle_decode_plain")
+
+    def set_graph(self, on: bool) -> None:
+        self._check(self.lib.eagle_set_graph(self.h, int(on)), "eagle_set_graph")
+
+    def set_debug(self, flags: int) -> None:
+        self._check(self.lib.eagle_set_debug(self.h, flags), "eagle_set_debug")
+
+    def sync(self) -> None:
+        """Wait for the stream and raise on latched device errors."""
+        self._check(self.lib.eagle_status_sync(self.h), "eagle_status_sync")
+
+    def profile_begin(self, max_launches: int) -> None:
+        self._check(self.lib.eagle_profile_begin(self.h, max_launches), "eagle_profile_begin")
+
+    def profile_end(self):
+        """(launches, total device ms, total algorithmic bytes) of the profiled GEMM launches."""
+        n, ms, by = C.c_int(), C.c_double(), C.c_double()
+        self._check(self.lib.eagle_profile_end(self.h, C.byref(n), C.byref(ms), C.byref(by)), "eagle_profile_end")
+        return n.value, ms.value, by.value
+
+    def kv_view(self):
+        k, v, cap = C.c_void_p(), C.c_void_p(), C.c_int()
+        self._check(self.lib.eagle_kv_view(self.h, C.byref(k), C.byref(v), C.byref(cap)), "eagle_kv_view")
+        return k.value, v.value, cap.value
+
+    def dump_raw(self, what: int) -> torch.Tensor:
+        n = self.lib.eagle_dump_bytes(self.h, what)
+        buf = torch.empty(n, dtype=torch.uint8, device=self.workspace.device)
+        self._check(self.lib.eagle_debug_dump(self.h, what, buf.data_ptr(), n), "eagle_debug_dump")
+        return buf
+
+    def dump(self, what: int):
+        """Parsed debug view (host tensors)."""
+        B = self.batch
+        t = self.w.tree
+        k, D, T1 = t.topk, t.depth, t.m + 1
+        NG = t.n_gen
+        raw = self.dump_raw(what).cpu()
+        i32 = lambda a, b: raw[a:b].view(torch.int32)
+        f32 = lambda a, b: raw[a:b].view(torch.float32)
+        if what == L.DUMP_STATE:
+            s = i32(0, 7 * B * 4).view(7, B)
+            return dict(zip(["ctx_len", "root_tok", "committed", "on_track", "cycle", "acc_len", "bonus"], s))
+        if what == L.DUMP_CAND:
+            return i32(0, B * k * 4).view(B, k), f32(B * k * 4, 2 * B * k * 4).view(B, k)
+        if what == L.DUMP_NODES:
+            n = B * NG * 4
+            return (i32(0, n).view(B, NG), i32(n, 2 * n).view(B, NG), i32(2 * n, 3 * n).view(B, NG),
+                    f32(3 * n, 4 * n).view(B, NG))
+        if what == L.DUMP_TREE:
+            n = B * T1 * 4
+            W = (T1 + 63) // 64
+            mask = raw[4 * n:4 * n + B * T1 * W * 8].view(torch.int64).view(B, T1, W)
+            return (i32(0, n).view(B, T1), i32(n, 2 * n).view(B, T1), i32(2 * n, 3 * n).view(B, T1),
+                    i32(3 * n, 4 * n).view(B, T1), mask)
+        if what == L.DUMP_ACCEPT:
+            return i32(0, B * 4), i32(B * 4, 2 * B * 4), i32(2 * B * 4, (2 * B + B * D) * 4).view(B, D)
+        if what == L.DUMP_VERIFY_HEAD:
+            K = 1 if t.temperature > 0 else 2
+            R = B * T1
+            a = R * K * 4
+            return (i32(0, a).view(R, K), f32(a, 2 * a).view(R, K), f32(2 * a, 2 * a + R * 4),
+                    f32(2 * a + R * 4, 2 * a + R * 4 + R * k * 4).view(R, k))
+        if what == L.DUMP_VERIFY_LOGITS:
+            return f32(0, raw.numel()).view(B * T1, self.w.model.vocab)
+        if what == L.DUMP_FEATURES:
+            dt = torch.float32 if self.w.model.dtype == "f32" else torch.bfloat16
+            return raw.view(dt).view(B * T1, self.w.model.hidden)
+        raise ValueError(what)
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            self.lib.eagle_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---- kernel-level entry points ----------------------------------------------------------------
+def _dtype_code(t: torch.Tensor) -> int:
+    return L.DTYPE_F32 if t.dtype == torch.float32 else L.DTYPE_BF16
+
+
+def gemm(W: torch.Tensor, X: torch.Tensor, epi: int = 0, out: Optional[torch.Tensor] = None,
+         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Y = X W^T through the library's GEMM (tcgen05 for bf16, FFMA for fp32)."""
+    lib = L.lib()
+    N, K = W.shape
+    M = X.shape[0]
+    if out is None:
+        out = torch.zeros(M, N, dtype=torch.bfloat16 if epi == 1 else torch.float32, device=X.device)
+    nb = lib.eagle_op_gemm_scratch_bytes(M, N)
+    scratch = torch.zeros(max(nb, 1), dtype=torch.uint8, device=X.device)
+    rc = lib.eagle_op_gemm(_dtype_code(W), _stream(stream), W.data_ptr(), N, K, X.data_ptr(), M, epi,
+                           out.data_ptr(), out.stride(0), scratch.data_ptr(), nb)
+    L.check(rc, "eagle_op_gemm")
+    return out
+
+
+def lm_head(W: torch.Tensor, X: torch.Tensor, K: int, inv_t: float = 1.0, gumbel: bool = False,
+            lse_excl: bool = False, specials: Optional[torch.Tensor] = None,
+            row_seq: Optional[torch.Tensor] = None, row_key: Optional[torch.Tensor] = None,
+            cycle: int = 0, seed: int = 0, stream_id: int = 4,
+            stream: Optional[torch.cuda.Stream] = None):
+    """Fused LM head: returns (top_id [M][K], top_val [M][K], lse [M], spec_logit [M][S] or None)."""
+    lib = L.lib()
+    V, H = W.shape
+    M = X.shape[0]
+    dev = X.device
+    dt = _dtype_code(W)
+    nb = lib.eagle_op_lm_head_scratch_bytes(dt, V, M, K)
+    scratch = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    top_id = torch.empty(M, K, dtype=torch.int32, device=dev)
+    top_val = torch.empty(M, K, dtype=torch.float32, device=dev)
+    lse = torch.empty(M, dtype=torch.float32, device=dev)
+    S = 0 if specials is None else specials.shape[1]
+    spec_logit = None if specials is None else torch.full((M, S), float("nan"), device=dev)
+    rc = lib.eagle_op_lm_head(dt, _stream(stream), W.data_ptr(), V, H, X.data_ptr(), M, K, inv_t, int(gumbel),
+                              int(lse_excl), _ptr(specials), S, _ptr(spec_logit), _ptr(row_seq), _ptr(row_key),
+                              cycle, seed, stream_id, top_id.data_ptr(), top_val.data_ptr(), lse.data_ptr(),
+                              scratch.data_ptr(), nb)
+    L.check(rc, "eagle_op_lm_head")
+    return top_id, top_val, lse, spec_logit
+
+
+def attention(q, kcache, vcache, row_seq, row_slot, ctx_len, rows_per_seq, mode, tree_T=0, mask=None,
+              scale=0.0, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """q [R][nq][d]; caches [B][nkv][cap][d]; returns out [R][nq][d]."""
+    lib = L.lib()
+    R, nq, d = q.shape
+    _, nkv, cap, _ = kcache.shape
+    out = torch.empty_like(q)
+    mw = 0 if mask is None else mask.shape[1]
+    rc = lib.eagle_op_attention(_dtype_code(q), _stream(stream), q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                out.data_ptr(), R, nq, nkv, d, cap, rows_per_seq, row_seq.data_ptr(),
+                                row_slot.data_ptr(), ctx_len.data_ptr(), mode, tree_T, _ptr(mask), mw, scale)
+    L.check(rc, "eagle_op_attention")
+    return out
+
+
+def tree_build(k: int, depth: int, m: int, cand_tok, cand_logc, child_tok, child_logc, ctx_len, root_tok,
+               stream: Optional[torch.cuda.Stream] = None):
+    """Injected-confidence tree growth + rerank. Returns dict of node and tree tensors."""
+    lib = L.lib()
+    B = cand_tok.shape[0]
+    dev = cand_tok.device
+    NG = k + (depth - 1) * k * k
+    T1 = m + 1
+    W = (T1 + 63) // 64
+    o = {n: torch.empty(B, NG, dtype=torch.int32, device=dev) for n in ("node_tok", "node_parent", "node_depth")}
+    o["node_logv"] = torch.empty(B, NG, dtype=torch.float32, device=dev)
+    for n in ("tree_tok", "tree_pos", "tree_parent", "tree_node"):
+        o[n] = torch.empty(B, T1, dtype=torch.int32, device=dev)
+    o["tree_mask"] = torch.empty(B, T1, W, dtype=torch.int64, device=dev)
+    nb = lib.eagle_op_tree_scratch_bytes(B, k, depth, m)
+    scratch = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    rc = lib.eagle_op_tree_build(_stream(stream), B, k, depth, m, cand_tok.data_ptr(), cand_logc.data_ptr(),
+                                 _ptr(child_tok), _ptr(child_logc), ctx_len.data_ptr(), root_tok.data_ptr(),
+                                 o["node_tok"].data_ptr(), o["node_parent"].data_ptr(), o["node_depth"].data_ptr(),
+                                 o["node_logv"].data_ptr(), o["tree_tok"].data_ptr(), o["tree_pos"].data_ptr(),
+                                 o["tree_parent"].data_ptr(), o["tree_node"].data_ptr(), o["tree_mask"].data_ptr(),
+                                 scratch.data_ptr(), nb)
+    L.check(rc, "eagle_op_tree_build")
+    return o
+
+
+def compact(kcache, vcache, n_old, acc_len, acc_path, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """In-place KV compaction; caches [layers][B][nkv][cap][d]."""
+    lib = L.lib()
+    layers, B, nkv, cap, d = kcache.shape
+    rc = lib.eagle_op_compact(_dtype_code(kcache), _stream(stream), kcache.data_ptr(), vcache.data_ptr(), layers, B,
+                              nkv, cap, d, n_old.data_ptr(), acc_len.data_ptr(), acc_path.data_ptr(),
+                              acc_path.shape[1])
+    L.check(rc, "eagle_op_compact")

@@ -1,0 +1,210 @@
+// Acceptance walk along the verified tree, KV-cache compaction of the accepted path,
+// and the row set-up kernels of the drafter update, plain decoding and prefill.
+//
+// Acceptance keeps drafted tokens from the root while they pass the test (equal to the
+// target's argmax when greedy, the rejection-sampling rule when sampling) and takes the
+// target's own token at the first rejection ("EAGLE: Feature-Level Drafting", list
+// "Speculative decoding in four moves", items 3-4; "EAGLE-2: Context-Aware Dynamic
+// Draft Trees", table "Putting It Together", step 5). The multi-candidate sampling rule
+// used is recursive point-mass rejection: at node u the kept children are tried in draft
+// rank order and child t is accepted when U * (1 - sum of p over tried children) < p(t),
+// U a Philox uniform keyed by (seed; try index, row, cycle, sequence); if all are
+// rejected the bonus is the Gumbel-argmax of p over the vocabulary minus those children,
+// computed inside the LM-head epilogue.
+#include "common.cuh"
+#include "cycle.h"
+#include "kernels.h"
+
+namespace eagle {
+
+__global__ void accept_k(CycleDev c, HeadOut h, int* out_tokens, int* out_count) {
+  const int b = blockIdx.x;
+  const int T1 = c.T1, rb = b * T1;
+  // greedy top-2 margins (diagnostic for near-ties)
+  if (!c.sampling && h.K >= 2 && c.margin)
+    for (int r = threadIdx.x; r < T1; r += blockDim.x)
+      c.margin[rb + r] = h.top_val[(size_t)(rb + r) * h.K] - h.top_val[(size_t)(rb + r) * h.K + 1];
+  if (threadIdx.x) return;
+  int u = 0, L = 0, bonus = -1;
+  while (true) {
+    const int row = rb + u;
+    int next = -1;
+    if (!c.sampling) {
+      const int a = h.top_id[(size_t)row * h.K];
+      for (int x = u + 1; x < T1; ++x)
+        if (c.tree_parent[rb + x] == u && c.tree_tok[rb + x] == a) { next = x; break; }
+      if (next < 0 || L >= c.D) { bonus = a; break; }
+    } else {
+      float tried = 0.f;
+      int i = 0;
+      for (int x = u + 1; x < T1 && i < c.k; ++x) {
+        if (c.tree_parent[rb + x] != u) continue;
+        const float pt = expf(h.spec_logit[(size_t)row * h.S + i] * c.inv_t - h.lse[row]);
+        const float U = draw_uniform(c.seed, STREAM_ACCEPT, (uint32_t)b, c.cycle[b], (uint32_t)i, (uint32_t)u);
+        if (U * (1.f - tried) < pt) { next = x; break; }
+        tried += pt;
+        ++i;
+      }
+      if (next < 0 || L >= c.D) { bonus = h.top_id[(size_t)row * h.K]; break; }
+    }
+    c.acc_path[b * c.D + L] = next;
+    ++L;
+    u = next;
+  }
+  c.acc_len[b] = L;
+  c.bonus[b] = bonus;
+  const int cc = c.committed[b];
+  int on = c.on_track[b];
+  for (int j = 0; j <= L; ++j) {
+    const int t = j < L ? c.tree_tok[rb + c.acc_path[b * c.D + j]] : bonus;
+    if (out_tokens) out_tokens[b * (c.D + 1) + j] = t;
+    if (c.ref) on = on && (cc + j < c.ref_len) && c.ref[(size_t)b * c.ref_len + cc + j] == t;
+  }
+  if (out_count) out_count[b] = L + 1;
+  c.on_track[b] = on;
+  c.committed[b] = cc + L + 1;
+  c.root_tok[b] = bonus;
+  c.ctx_len[b] = c.n_old[b] + L + 1;
+}
+
+int accept_walk(cudaStream_t st, const CycleDev& c, const HeadOut& h, int* out_tokens, int* out_count) {
+  accept_k<<<c.B, 64, 0, st>>>(c, h, out_tokens, out_count);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// slot n + j <- slot n + path[j - 1], j = 1..L, in every layer. Each thread owns fixed
+// element positions and reads all L sources before writing any target, so overlapping
+// source/target slots cannot race.
+template <typename T>
+__global__ void compact_k(T* kc, T* vc, int layers, int B, int nkv, int cap, int d, const int* n_old,
+                          const int* acc_len, const int* acc_path, int Dmax) {
+  const int layer = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int b = bh / nkv;
+  const int L = acc_len[b];
+  if (L <= 0) return;
+  const int n = n_old[b];
+  const size_t base = (((size_t)layer * B * nkv) + bh) * (size_t)cap * d;
+  T tk[8], tv[8];
+  for (int e = threadIdx.x; e < d; e += blockDim.x) {
+    for (int j = 0; j < L && j < 8; ++j) {
+      const size_t s = base + (size_t)(n + acc_path[b * Dmax + j]) * d + e;
+      tk[j] = kc[s];
+      tv[j] = vc[s];
+    }
+    for (int j = 0; j < L && j < 8; ++j) {
+      const size_t t = base + (size_t)(n + 1 + j) * d + e;
+      kc[t] = tk[j];
+      vc[t] = tv[j];
+    }
+  }
+}
+
+int compact_kv(cudaStream_t st, int dtype, void* kc, void* vc, int layers, int B, int nkv, int cap, int d,
+               const int* n_old, const int* acc_len, const int* acc_path, int Dmax) {
+  if (Dmax > 8) return -1;
+  dim3 grid(layers, B * nkv);
+  if (dtype == DT_F32)
+    compact_k<float><<<grid, 128, 0, st>>>((float*)kc, (float*)vc, layers, B, nkv, cap, d, n_old, acc_len,
+                                           acc_path, Dmax);
+  else
+    compact_k<__nv_bfloat16><<<grid, 128, 0, st>>>((__nv_bfloat16*)kc, (__nv_bfloat16*)vc, layers, B, nkv, cap,
+                                                   d, n_old, acc_len, acc_path, Dmax);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// Drafter rows after acceptance: drafter position n + j carries (feature of target
+// position n + j, token at n + j + 1), j = 0..L; rows L+1..D are padding whose outputs
+// are ignored and whose KV lands beyond the new context.
+__global__ void update_rows_k(CycleDev c, int* row_tok, int* row_pos, int* row_slot, int* row_seq,
+                              int* row_featsrc) {
+  const int b = blockIdx.x, j = threadIdx.x;
+  if (j > c.D) return;
+  const int L = c.acc_len[b];
+  const int jj = j < L ? j : L;
+  const int tr = jj == 0 ? 0 : c.acc_path[b * c.D + jj - 1];
+  const int row = b * (c.D + 1) + j;
+  row_featsrc[row] = b * c.T1 + tr;
+  row_tok[row] = jj < L ? c.tree_tok[b * c.T1 + c.acc_path[b * c.D + jj]] : c.bonus[b];
+  row_pos[row] = c.n_old[b] + j;
+  row_slot[row] = c.n_old[b] + j;
+  row_seq[row] = b;
+}
+
+int update_rows(cudaStream_t st, const CycleDev& c, int* row_tok, int* row_pos, int* row_slot, int* row_seq,
+                int* row_featsrc) {
+  if (c.D + 1 > 32) return -1;
+  update_rows_k<<<c.B, 32, 0, st>>>(c, row_tok, row_pos, row_slot, row_seq, row_featsrc);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+__global__ void plain_rows_k(CycleDev c, int* row_tok, int* row_pos, int* row_slot, int* row_seq) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= c.B) return;
+  row_tok[b] = c.root_tok[b];
+  row_pos[b] = c.ctx_len[b];
+  row_slot[b] = c.ctx_len[b];
+  row_seq[b] = b;
+}
+
+int plain_rows(cudaStream_t st, const CycleDev& c, int* row_tok, int* row_pos, int* row_slot, int* row_seq) {
+  plain_rows_k<<<(c.B + 127) / 128, 128, 0, st>>>(c, row_tok, row_pos, row_slot, row_seq);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+__global__ void plain_advance_k(CycleDev c, const int* next_tok, int K, int* out, int ld_out, int step) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= c.B) return;
+  const int t = next_tok[b * K];
+  if (out) out[(size_t)b * ld_out + step] = t;
+  c.root_tok[b] = t;
+  c.ctx_len[b] += 1;
+}
+
+int plain_advance(cudaStream_t st, const CycleDev& c, const int* next_tok, int* out, int ld_out, int step) {
+  // next_tok points at the head's top_id with K = 1
+  plain_advance_k<<<(c.B + 127) / 128, 128, 0, st>>>(c, next_tok, 1, out, ld_out, step);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// Prefill rows p0 .. p0+n-1 of one sequence. shift = 0: target rows (token p); shift = 1:
+// drafter rows (token p + 1, the first generated token for the last prompt position).
+__global__ void prefill_rows_k(const int* prompt, int n_total, int seq, int p0, int n, int shift,
+                               const int* root_tok, int* row_tok, int* row_pos, int* row_slot, int* row_seq) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int p = p0 + i;
+  row_tok[i] = shift ? (p + 1 < n_total ? prompt[p + 1] : root_tok[seq]) : prompt[p];
+  row_pos[i] = p;
+  row_slot[i] = p;
+  row_seq[i] = seq;
+}
+
+int prefill_rows(cudaStream_t st, const int* prompt, int seq, int p0, int n, int n_total_shift,
+                 const int* root_tok, int* row_tok, int* row_pos, int* row_slot, int* row_seq, int shift) {
+  if (n <= 0) return 0;
+  prefill_rows_k<<<(n + 127) / 128, 128, 0, st>>>(prompt, n_total_shift, seq, p0, n, shift, root_tok, row_tok,
+                                                  row_pos, row_slot, row_seq);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+__global__ void prefill_finish_k(CycleDev c, int seq, int n, const int* first_tok) {
+  if (threadIdx.x) return;
+  const int t = first_tok[0];
+  c.root_tok[seq] = t;
+  c.committed[seq] = 1;
+  const int on = c.ref ? (c.ref_len > 0 && c.ref[(size_t)seq * c.ref_len] == t) : 1;
+  c.on_track[seq] = on;
+  c.ctx_len[seq] = n;
+  c.n_old[seq] = n;
+  c.acc_len[seq] = 0;
+  c.cycle[seq] = 0;
+  c.root_plant[seq] = (c.ref && on && 1 < c.ref_len) ? c.ref[(size_t)seq * c.ref_len + 1] : -1;
+}
+
+int prefill_finish(cudaStream_t st, const CycleDev& c, int seq, int n, const int* first_tok) {
+  prefill_finish_k<<<1, 32, 0, st>>>(c, seq, n, first_tok);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace eagle

@@ -1,0 +1,391 @@
+// bf16 weight-streaming GEMM on the 5th-generation tensor cores (tcgen05 + TMA + TMEM).
+//
+//   Y[M][N] = X[M][K] * W[N][K]^T      (X: activations/tokens, W: nn.Linear-layout weight)
+//
+// Decode-time projections are skinny (M = 1..61 tokens at batch 1), so the weight is the
+// 128-row "A" operand of tcgen05.mma and the tokens are the N-side operand (BN = 16..256
+// columns, zero-filled by TMA past M). The accumulator tile D[128 features][BN tokens]
+// lives in TMEM, double-buffered so the epilogue of one tile overlaps the next tile's
+// main loop.
+//
+// Work split: stream-K. The (tile, k-block) units of the whole GEMM are cut into
+// gridDim.x equal contiguous ranges, one per persistent CTA, so every SM streams the
+// same number of weight bytes whatever the shape. A tile split across CTAs is finished
+// by the last contributor to arrive (atomic ticket, no waiting): it sums the fp32
+// partials in contributor order, so results do not depend on timing.
+//
+// Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM owner,
+// warps 2-5 = epilogue (TMEM -> registers -> global / fused LM-head reduction).
+// Every mbarrier wait is bounded; on a timeout the CTA latches an error, drains its
+// in-flight copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <map>
+#include <tuple>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "lmhead.cuh"
+
+namespace eagle {
+
+struct GemmArgs {
+  int M, N, K;
+  int tiles_t;        // token tiles
+  int kb;             // 64-wide k-blocks
+  long long units;    // tiles_n * tiles_t * kb
+  int epi;
+  void* out;
+  int ldo;
+  float* partials;
+  int* counters;
+  int* err;
+  HeadParams head;
+};
+
+template <int BN>
+struct TcCfg {
+  static constexpr int A_BYTES = 128 * 64 * 2;
+  static constexpr int B_BYTES = BN * 64 * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE) > 12 ? 12 : (196608 / STAGE);
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int CH = BN < 32 ? BN : 32;
+  static constexpr int STAGING = 32 * 128 * 4;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + STAGING + 512;
+};
+
+// K-major operand tile, rows of 64 bf16 (128 bytes) with the 128-byte swizzle, 8-row
+// atoms 1024 bytes apart. Start address, stride byte offset 1024, descriptor version 1,
+// layout SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
+  return (int)(((u + 1) * G - 1) / U);
+}
+
+template <int CH>
+__device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int BN, int row, int c0,
+                                          const float* v, float* staging, int ew, int lane) {
+  const int f = tn * 128 + row;
+  if (a.epi != EPI_HEAD) {
+    if (f < a.N) {
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const int j = tt * BN + c0 + i;
+        if (j < a.M) {
+          const size_t o = (size_t)j * a.ldo + f;
+          if (a.epi == EPI_F32) reinterpret_cast<float*>(a.out)[o] = v[i];
+          else if (a.epi == EPI_BF16) reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(v[i]);
+          else reinterpret_cast<float*>(a.out)[o] += v[i];
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < CH; ++i) staging[i * 128 + row] = v[i];
+    named_bar_sync(2, 128);
+    for (int i = ew; i < CH; i += 4) {
+      const int j = tt * BN + c0 + i;
+      if (j < a.M) head_tile_row(staging + i * 128, tn, j, a.head, lane);
+    }
+    named_bar_sync(2, 128);
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_bf16_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const GemmArgs a) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* staging = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + C::STAGING);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long U = a.units;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const long long u_begin = (long long)cta * U / G, u_end = (long long)(cta + 1) * U / G;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(tfull + b), 1);
+      mbar_init(smem_u32(tempty + b), 128);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, parity = 0;
+      for (long long u = u_begin; u < u_end; ++u) {
+        const long long tile = u / a.kb;
+        const int kb = (int)(u - tile * a.kb);
+        const int tn = (int)(tile / a.tiles_t), tt = (int)(tile % a.tiles_t);
+        if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, abort_flag, a.err)) break;
+        const uint32_t fb = smem_u32(full + stage);
+        mbar_expect_tx(fb, C::STAGE);
+        const uint32_t sa = smem_u32(smem + stage * C::STAGE);
+        tma_load_2d(sa, &tmW, kb * 64, tn * 128, fb, pol_w);
+        tma_load_2d(sa + C::A_BYTES, &tmX, kb * 64, tt * BN, fb, pol_x);
+        issued |= 1u << stage;
+        parity = (parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (*abort_flag) {
+        for (int s = 0; s < C::STAGES; ++s)
+          if ((issued >> s) & 1) mbar_wait(smem_u32(full + s), (parity >> s) & 1, abort_flag, a.err, false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                 ((uint32_t)(128 >> 4) << 24);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      long long u = u_begin;
+      while (ok && u < u_end) {
+        const long long tile = u / a.kb;
+        const long long seg_end = min(u_end, (tile + 1) * a.kb);
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1, abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        const long long seg_begin = u;
+        for (; u < seg_end; ++u) {
+          if (!mbar_wait(smem_u32(full + stage), phase, abort_flag, a.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE);
+          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc_mma_bf16(d, da + 2 * k, db + 2 * k, IDESC, (u != seg_begin || k) ? 1u : 0u);
+          tc_commit(smem_u32(empty + stage));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(tfull + acc));
+        acc ^= 1;
+        if (!acc) acc_phase ^= 1;
+      }
+      if (!ok) {
+        tc_commit(smem_u32(drain));
+        mbar_wait(smem_u32(drain), 0, abort_flag, a.err, false);
+      }
+    }
+  } else {
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const bool leader = (ew == 0 && lane == 0);
+    const long long first_tile = u_begin / a.kb;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    long long u = u_begin;
+    while (u < u_end) {
+      const long long tile = u / a.kb;
+      const long long seg_end = min(u_end, (tile + 1) * a.kb);
+      const bool whole = (u == tile * a.kb) && (seg_end == (tile + 1) * a.kb);
+      const int tn = (int)(tile / a.tiles_t), tt = (int)(tile % a.tiles_t);
+      if (leader) bcast[0] = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag, a.err) ? 1 : 0;
+      named_bar_sync(1, 128);
+      const int ok = bcast[0];
+      named_bar_sync(1, 128);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      if (whole) {
+        for (int c0 = 0; c0 < BN; c0 += C::CH) {
+          float v[C::CH];
+          if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
+          epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(tempty + acc));
+      } else {
+        const int slot = (tile == first_tile) ? 0 : 1;
+        float* part = a.partials + (size_t)(cta * 2 + slot) * BN * 128;
+        for (int c0 = 0; c0 < BN; c0 += C::CH) {
+          float v[C::CH];
+          if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
+#pragma unroll
+          for (int i = 0; i < C::CH; ++i) part[(c0 + i) * 128 + row] = v[i];
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(tempty + acc));
+        __threadfence();
+        named_bar_sync(1, 128);
+        const int cf = cta_of_unit(tile * a.kb, U, G);
+        const int cl = cta_of_unit((tile + 1) * a.kb - 1, U, G);
+        if (leader) {
+          const int old = atomicAdd(a.counters + tile, 1);
+          bcast[1] = (old == cl - cf) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        if (bcast[1]) {
+          __threadfence();
+          for (int c0 = 0; c0 < BN; c0 += C::CH) {
+            float v[C::CH];
+#pragma unroll
+            for (int i = 0; i < C::CH; ++i) v[i] = 0.f;
+            for (int cc = cf; cc <= cl; ++cc) {
+              const long long ft = ((long long)cc * U / G) / a.kb;
+              const int sl = (tile == ft) ? 0 : 1;
+              const float* pp = a.partials + (size_t)(cc * 2 + sl) * BN * 128;
+#pragma unroll
+              for (int i = 0; i < C::CH; ++i) v[i] += __ldcg(pp + (c0 + i) * 128 + row);
+            }
+            epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+          }
+          if (leader) a.counters[tile] = 0;
+        }
+        named_bar_sync(1, 128);
+      }
+      u = seg_end;
+      acc ^= 1;
+      if (!acc) acc_phase ^= 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---- host side ----------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 row-major [rows][K] matrix, boxes of 64 (K) x box_rows, 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long K, int box_rows) {
+  static std::map<std::tuple<const void*, long long, long long, int>, CUtensorMap> cache;
+  auto key = std::make_tuple(ptr, rows, K, box_rows);
+  auto it = cache.find(key);
+  if (it != cache.end()) { *m = it->second; return true; }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = *m;
+  return true;
+}
+
+static int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+int gemm_bn_for(int M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+size_t gemm_bf16_scratch_bytes() { return (size_t)num_sms_cap() * 2 * 256 * 128 * sizeof(float); }
+
+template <int BN>
+static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int tiles_n,
+                             cudaStream_t st) {
+  using C = TcCfg<BN>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  a.tiles_t = (a.M + BN - 1) / BN;
+  a.kb = (a.K + 63) / 64;
+  a.units = (long long)tiles_n * a.tiles_t * a.kb;
+  int G = num_sms();
+  if (G > num_sms_cap()) G = num_sms_cap();
+  if ((long long)G > a.units) G = (int)a.units;
+  gemm_bf16_tc<BN><<<G, 192, C::SMEM, st>>>(mw, mx, a);
+  return cudaGetLastError();
+}
+
+int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
+              int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head) {
+  if (M <= 0 || N <= 0 || K <= 0 || (K % 8) != 0 || !W || !X) return -1;
+  if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(X)) & 15) return -1;
+  const int BN = gemm_bn_for(M);
+  const int tiles_n = (N + 127) / 128;
+  if ((long long)tiles_n * ((M + BN - 1) / BN) > counters_len) return -2;
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, W, N, K, 128)) return -3;
+  if (!make_map(&mx, X, M, K, BN)) return -3;
+  GemmArgs a{};
+  a.M = M; a.N = N; a.K = K; a.epi = epi; a.out = out; a.ldo = ldo;
+  a.partials = partials; a.counters = counters; a.err = err;
+  if (head) a.head = *head;
+  cudaError_t e;
+  switch (BN) {
+    case 16: e = launch_bn<16>(mw, mx, a, tiles_n, st); break;
+    case 32: e = launch_bn<32>(mw, mx, a, tiles_n, st); break;
+    case 64: e = launch_bn<64>(mw, mx, a, tiles_n, st); break;
+    case 128: e = launch_bn<128>(mw, mx, a, tiles_n, st); break;
+    default: e = launch_bn<256>(mw, mx, a, tiles_n, st); break;
+  }
+  return e == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace eagle

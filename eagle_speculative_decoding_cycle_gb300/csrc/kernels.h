@@ -1,0 +1,70 @@
+// Host-side launchers of the cycle's CUDA kernels (internal to the library).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+struct HeadParams;
+
+namespace eagle {
+
+enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_ADD_F32 = 2, EPI_HEAD = 3 };
+enum { DT_F32 = 0, DT_BF16 = 1 };
+
+inline int num_sms_cap() { return 192; }
+
+// ---- GEMMs -------------------------------------------------------------------------------
+int gemm_bn_for(int M);
+size_t gemm_bf16_scratch_bytes();
+// bf16 tcgen05 GEMM, Y[M][N] = X[M][K] W[N][K]^T. Returns 0 or a negative code.
+int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
+              int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head);
+// fp32 SIMT GEMM with the same contract (EPI_F32 / EPI_ADD_F32).
+int gemm_f32(cudaStream_t st, const float* W, int N, int K, const float* X, int M, int epi, float* out,
+             int ldo);
+
+// ---- LM head reductions ------------------------------------------------------------------
+// Partial records from materialised logits [n_rows][ld] (fp32 path).
+int head_partials_from_logits(cudaStream_t st, const float* logits, int ld, const HeadParams& p);
+int head_merge(cudaStream_t st, const HeadParams& p);
+size_t head_part_bytes(int vocab, int rows, int K);
+
+// ---- element-wise / row ops (dtype = DT_F32 or DT_BF16 storage) --------------------------
+int embed_rows(cudaStream_t st, int dtype, const void* E, int V, int H, const int* tok, int R, float* x,
+               int* err);
+int rmsnorm_rows(cudaStream_t st, int dtype_in, const void* x, int ldx, const void* g, int H, float eps,
+                 int R, int dtype_out, void* out, int ldo);
+int rope_store(cudaStream_t st, int dtype, const float* qkv, int R, int nq, int nkv, int d,
+               const int* row_pos, const int* row_slot, const int* row_seq, const float* rope_cos,
+               const float* rope_sin, void* q_out, void* kcache, void* vcache, int cap, int* err, int slot_limit);
+int swiglu_rows(cudaStream_t st, int dtype, const float* gu, int F, int R, void* out);
+int concat_emb_feat(cudaStream_t st, int dtype, const void* E, int V, int H, const int* tok,
+                    const void* feat, const int* feat_row, int R, void* out, int* err);
+int convert_rows(cudaStream_t st, int dtype, const float* x, int H, int R, void* out, int ldo);
+int gather_rows(cudaStream_t st, size_t row_bytes, const void* src, size_t src_ld, const int* idx, int R,
+                void* dst, size_t dst_ld, const int* dst_idx = nullptr);
+int widen_rows(cudaStream_t st, int dtype, const void* x, int ldx, int H, int R, float* out);
+
+// ---- attention -----------------------------------------------------------------------------
+struct AttnArgs {
+  const void* q;        // [R][nq][d]
+  const void* kcache;   // this layer: [(seq * nkv + h) * cap + slot][d]
+  const void* vcache;
+  void* out;            // [R][nq][d]
+  int R, nq, nkv, d, cap;
+  int rows_per_seq;     // rows of one sequence are contiguous; a row block never straddles two
+  const int* row_seq;   // [R]
+  const int* row_slot;  // [R]  slot of the row's own key
+  const int* ctx_len;   // [B] slots [0, ctx_len) are visible to every row of the sequence
+  int mode;             // 0 = causal (slot <= row_slot), 1 = tree (ctx + mask bits over slots ctx..ctx+T)
+  int tree_T;
+  const uint64_t* mask; // [R][mask_words]
+  int mask_words;
+  float scale;
+};
+int attention(cudaStream_t st, int dtype, const AttnArgs& a);
+
+// ---- tree policy, acceptance, compaction ---------------------------------------------------
+struct TreeState;   // defined in tree.cu / engine
+}  // namespace eagle

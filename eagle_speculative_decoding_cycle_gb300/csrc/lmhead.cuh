@@ -1,0 +1,172 @@
+// Fused LM-head epilogue: per (vocab tile, row) partial softmax statistics and top-K.
+//
+// The LM head is "a single matrix followed by softmax" ("EAGLE: Feature-Level
+// Drafting", section "The big idea: draft at the feature level"). Instead of writing
+// full-vocabulary logits, each 128-wide vocabulary tile reduces its logits per row to
+// a record (running max, sum of exp relative to that max, and the K best entries by a
+// ranking value). A second kernel merges the records of all tiles in a fixed order.
+// The same routine serves three uses:
+//   drafter top-k + confidence: rank = logit, lse over all but the planted candidate;
+//   greedy verify: K = 2 (argmax and top-2 margin);
+//   sampling verify: rank = logit/T + Gumbel noise, the row's kept children excluded
+//   from the ranking (their logits are reported separately), lse over everything.
+#pragma once
+
+#include "common.cuh"
+
+struct HeadParams {
+  int vocab;
+  int n_rows;            // rows (tokens) of this launch
+  int K;                 // entries kept per row, 1..16
+  float inv_t;           // logits are scaled by this for lse and ranking
+  int gumbel;            // add Gumbel(0,1) noise to the ranking value
+  int lse_excl;          // leave the special ids out of max / sum-exp
+  const int* specials;   // [n_rows][S] ids excluded from ranking (-1 = unused), or null
+  int S;
+  float* spec_logit;     // [n_rows][S] raw logit of each special id (written by its tile)
+  const int* row_seq;    // Philox sequence field per row (null = seq_base)
+  int seq_base;
+  const int* row_key;    // Philox row field per row (null = row % key_mod, or row if key_mod = 0)
+  int key_mod;
+  const uint32_t* cycle; // cycle counter(s) on the device (null = cycle_const)
+  int cycle_per_seq;     // 1: cycle[seq], 0: cycle[0]
+  uint32_t cycle_const;
+  uint32_t stream;       // Philox stream id of the Gumbel draws
+  uint64_t seed;
+  float* part;           // [n_tiles][n_rows][2 + 2K] partial records
+  int n_tiles;
+  int* top_id;           // merge outputs: [n_rows][K]
+  float* top_val;        // [n_rows][K] ranking values
+  float* lse;            // [n_rows]
+};
+
+EAGLE_DEV float gumbel_noise(const HeadParams& p, int row, int id) {
+  const uint32_t seq = p.row_seq ? (uint32_t)p.row_seq[row] : (uint32_t)p.seq_base;
+  const uint32_t key = p.row_key ? (uint32_t)p.row_key[row]
+                                 : (p.key_mod ? (uint32_t)(row % p.key_mod) : (uint32_t)row);
+  const uint32_t cyc = p.cycle ? (p.cycle_per_seq ? p.cycle[seq] : p.cycle[0]) : p.cycle_const;
+  u32x4 o = philox4x32_10(u32x4{(uint32_t)id >> 2, key, cyc, (seq << 8) | p.stream},
+                          (uint32_t)p.seed, (uint32_t)(p.seed >> 32));
+  const uint32_t w = (id & 3) == 0 ? o.x : (id & 3) == 1 ? o.y : (id & 3) == 2 ? o.z : o.w;
+  const float u = philox_uniform(w);
+  return -logf(-logf(u));
+}
+
+// One warp reduces the 128 logits `vals` (shared memory) of vocabulary tile `tile`
+// for row `row` into its partial record.
+EAGLE_DEV void head_tile_row(const float* vals, int tile, int row, const HeadParams& p, int lane) {
+  float rv[4];
+  int rid[4];
+  float mx = -INFINITY;
+  float sv[4];
+  bool in_lse[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = lane + 32 * q;
+    const int id = tile * 128 + i;
+    const bool valid = id < p.vocab;
+    const float x = vals[i];
+    bool special = false;
+    if (valid && p.specials) {
+      for (int s = 0; s < p.S; ++s) {
+        if (p.specials[row * p.S + s] == id) {
+          special = true;
+          p.spec_logit[row * p.S + s] = x;
+        }
+      }
+    }
+    sv[q] = x * p.inv_t;
+    in_lse[q] = valid && !(special && p.lse_excl);
+    if (in_lse[q]) mx = fmaxf(mx, sv[q]);
+    const bool rank_ok = valid && !special;
+    rv[q] = rank_ok ? (p.gumbel ? sv[q] + gumbel_noise(p, row, id) : sv[q]) : -INFINITY;
+    rid[q] = rank_ok ? id : 0x7fffffff;
+  }
+  mx = warp_max(mx);
+  float se = 0.f;
+  if (mx != -INFINITY) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (in_lse[q]) se += expf(sv[q] - mx);
+  }
+  se = warp_sum(se);
+  float* rec = p.part + ((size_t)tile * p.n_rows + row) * (2 + 2 * p.K);
+  if (lane == 0) {
+    rec[0] = mx;
+    rec[1] = se;
+  }
+  for (int k = 0; k < p.K; ++k) {
+    // lane's best remaining candidate
+    float bv = rv[0];
+    int bi = rid[0];
+#pragma unroll
+    for (int q = 1; q < 4; ++q)
+      if (rank_before(rv[q], rid[q], bv, bi)) { bv = rv[q]; bi = rid[q]; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (rank_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (rid[q] == bi) { rv[q] = -INFINITY; rid[q] = 0x7fffffff; }
+    if (lane == 0) {
+      rec[2 + 2 * k] = bv;
+      rec[3 + 2 * k] = __int_as_float(bi == 0x7fffffff ? -1 : bi);
+    }
+  }
+}
+
+// Merge kernel body: one warp per row, tiles visited in a fixed order.
+EAGLE_DEV void head_merge_row(const HeadParams& p, int row, int lane) {
+  const int K = p.K;
+  float lv[16];
+  int li[16];
+  for (int k = 0; k < 16; ++k) { lv[k] = -INFINITY; li[k] = 0x7fffffff; }
+  float M = -INFINITY, S = 0.f;
+  for (int t = lane; t < p.n_tiles; t += 32) {
+    const float* rec = p.part + ((size_t)t * p.n_rows + row) * (2 + 2 * K);
+    const float m2 = rec[0], s2 = rec[1];
+    if (m2 != -INFINITY) {
+      if (m2 > M) { S = S * expf(M - m2) + s2; M = m2; }
+      else S += s2 * expf(m2 - M);
+    }
+    for (int k = 0; k < K; ++k) {
+      float v = rec[2 + 2 * k];
+      int id = __float_as_int(rec[3 + 2 * k]);
+      if (id < 0) break;
+      if (!rank_before(v, id, lv[K - 1], li[K - 1])) break;   // records are sorted
+      int j = K - 1;
+      while (j > 0 && rank_before(v, id, lv[j - 1], li[j - 1])) { lv[j] = lv[j - 1]; li[j] = li[j - 1]; --j; }
+      lv[j] = v; li[j] = id;
+    }
+  }
+  // butterfly combine of (M, S)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const float mn = fmaxf(M, m2);
+    if (mn != -INFINITY) S = S * expf(M - mn) + s2 * expf(m2 - mn);
+    M = mn;
+  }
+  int head = 0;
+  for (int k = 0; k < K; ++k) {
+    float bv = head < K ? lv[head] : -INFINITY;
+    int bi = head < K ? li[head] : 0x7fffffff;
+    const int mine = bi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (rank_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (mine == bi && bi != 0x7fffffff) ++head;
+    if (lane == 0) {
+      p.top_id[row * K + k] = bi == 0x7fffffff ? -1 : bi;
+      p.top_val[row * K + k] = bv;
+    }
+  }
+  if (lane == 0) p.lse[row] = (M == -INFINITY) ? -INFINITY : M + logf(S);
+}

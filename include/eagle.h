@@ -1,0 +1,199 @@
+/*
+ * eagle.h -- C ABI of the GB300 (sm_103a) EAGLE draft-and-verify cycle.
+ *
+ * One cycle, as the EAGLE pages define it:
+ *   - feature-level drafting: the drafter embeds the one-step-advanced token,
+ *     concatenates it with the target feature (EAGLE-1) or with g = FC([l; m; h]) of
+ *     three target layers (EAGLE-3, its own output a replacing g on new draft
+ *     positions), applies an FC and one decoder layer, and reuses the target's frozen
+ *     embedding and LM head ("EAGLE: Feature-Level Drafting" lesson, sections "The big
+ *     idea: draft at the feature level" and "Resolving the uncertainty by feeding back
+ *     the token"; "EAGLE 三代" page, sections 2.3 and 4.3);
+ *   - EAGLE-2 dynamic tree: path value = product of draft confidences, top-k
+ *     expansion per depth, global top-m rerank, flattening with an ancestry mask
+ *     ("EAGLE-2: Context-Aware Dynamic Draft Trees" page, sections "Path Value Ranks
+ *     Prefixes", "Global Reranking", "The Mask Preserves Tree Semantics");
+ *   - one tree-attention verify pass of the target over its KV cache;
+ *   - lossless acceptance (greedy match, or rejection sampling along the tree) and
+ *     compaction of the accepted path's KV entries (EAGLE lesson, "Speculative
+ *     decoding in four moves"; EAGLE-2 page, table "Putting It Together", step 5).
+ *
+ * Conventions
+ *   - Memory: weights, the workspace, inputs and outputs are caller-owned DEVICE
+ *     memory. The library never allocates device memory; it carves everything it
+ *     needs (KV caches, node tables, activations, scratch) out of the workspace.
+ *     Host memory is used only for the context object and small host tables.
+ *   - Streams: every call enqueues work on the context's stream and returns without
+ *     waiting for the GPU (eagle_prefill reads its host length array; eagle_create
+ *     and eagle_status_sync synchronise). Pass the stream as a cudaStream_t cast to
+ *     void*. Graph replay (eagle_set_graph) needs a non-default stream.
+ *   - Errors: every entry point returns an eagle_status. Host-detected problems are
+ *     returned immediately with a message in eagle_last_error. Problems detected on
+ *     the device (an out-of-range token or slot, a timed-out wait) are latched into a
+ *     device status word and reported by eagle_status_sync. No kernel traps.
+ *   - A context is not thread-safe.
+ *
+ * Weight layout (row-major, "out x in", storage type = dtype):
+ *   embed [V][H], lm_head [V][H], final_norm [H]
+ *   per layer: attn_norm [H], wqkv [(nq+2*nkv)*d][H] = [Wq; Wk; Wv],
+ *              wo [H][nq*d], mlp_norm [H], wgu [2F][H] = [Wgate; Wup], wd [H][F]
+ *   drafter kind 1: fc [H][2H] applied to [emb; f], then a layer shaped as above.
+ *   drafter kind 3: fc [H][3H] applied to [l; m; h]; norm_g [H], norm_e [H];
+ *              wqkv [(nq+2*nkv)*d][2H] applied to [RMSNorm(g); RMSNorm(emb)];
+ *              wo, mlp_norm, wgu, wd as above (attn_norm unused).
+ */
+#ifndef EAGLE_H
+#define EAGLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EAGLE_OK = 0,
+  EAGLE_EINVAL = -1,       /* bad argument or configuration */
+  EAGLE_ECAPACITY = -2,    /* a length would exceed max_ctx / max_batch / the workspace */
+  EAGLE_ECUDA = -3,        /* a CUDA runtime call or kernel launch failed */
+  EAGLE_EDEVICE = -4,      /* a device-side check failed (bounds, capacity) */
+  EAGLE_ETIMEOUT = -5,     /* a device-side wait exceeded its time limit */
+  EAGLE_EUNSUPPORTED = -6  /* valid request this build does not implement */
+} eagle_status;
+
+enum { EAGLE_DTYPE_F32 = 0, EAGLE_DTYPE_BF16 = 1 };
+
+typedef struct {
+  int n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rope_theta, rms_eps;
+  int dtype; /* EAGLE_DTYPE_F32 or EAGLE_DTYPE_BF16: storage and GEMM input type */
+} eagle_model_cfg;
+
+typedef struct {
+  int kind;           /* 1 = EAGLE-1 feature drafter, 3 = EAGLE-3 fused drafter */
+  int fuse_layers[3]; /* kind 3: 0-based target layers whose outputs are l, m, h */
+} eagle_drafter_cfg;
+
+typedef struct {
+  int topk;           /* k: nodes expanded per depth and children per expanded node */
+  int depth;          /* D: draft depths */
+  int m;              /* nodes kept by the rerank (the verify pass scores m + 1 rows) */
+  float temperature;  /* 0 = greedy, > 0 = speculative sampling at this temperature */
+  uint64_t seed;      /* key of the counter-based (Philox4x32-10) draws */
+  float planted_p;    /* planted-drafter probability per depth (0 = off) */
+  float planted_conf; /* confidence given to a planted token */
+} eagle_tree_cfg;
+
+typedef struct {
+  int max_batch;      /* sequences per context */
+  int max_ctx;        /* KV entries per sequence (prompt + generated) */
+  int kv_block;       /* 0 = contiguous KV (only mode of this build) */
+  int prefill_chunk;  /* prompt rows per prefill pass (0 = 512) */
+} eagle_limits;
+
+typedef struct {
+  const void *attn_norm, *wqkv, *wo, *mlp_norm, *wgu, *wd;
+} eagle_layer_weights;
+
+typedef struct {
+  const void *embed, *lm_head, *final_norm;
+  const eagle_layer_weights* layers; /* host array of n_layers entries (copied) */
+  const void *fc, *norm_g, *norm_e;  /* drafter input projections / EAGLE-3 norms */
+  eagle_layer_weights draft;         /* the drafter's decoder layer */
+} eagle_weights;
+
+typedef struct eagle_ctx eagle_ctx;
+
+/* Bytes of device workspace eagle_create needs for these configurations (0 on error). */
+size_t eagle_workspace_bytes(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
+                             const eagle_tree_cfg* tree, const eagle_limits* limits);
+
+/* Validate the configuration, carve `workspace` (ws_bytes >= eagle_workspace_bytes),
+ * build the rotary tables (synchronous copy) and return a context in *out.
+ * The weights must stay valid for the context's lifetime. */
+int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter, const eagle_tree_cfg* tree,
+                 const eagle_weights* weights, const eagle_limits* limits, void* workspace, size_t ws_bytes,
+                 void* stream, eagle_ctx** out);
+
+/* Prefill `batch` prompts. d_tokens: device int32, prompts concatenated; h_lens: HOST
+ * int32 [batch]. Runs the target over each prompt (causal), picks its first token
+ * (greedy or sampled), runs the drafter over the prompt positions and prepares the
+ * root's depth-1 candidates. d_ref (nullable): device int32 [batch][ref_len], the
+ * target's own plain continuation of each prompt (its first entry being the prefill
+ * token), which turns on planted-drafter mode (tree.planted_p). */
+int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int32_t* h_lens,
+                  const int32_t* d_ref, int ref_len);
+
+/* One draft-and-verify cycle for every sequence. d_out_tokens: device int32
+ * [batch][depth + 1] receives the committed tokens (accepted path then the bonus
+ * token); d_out_count: device int32 [batch] receives how many (L + 1). Either may be
+ * null. Returns EAGLE_ECAPACITY, before launching anything, when a sequence could
+ * outgrow max_ctx. */
+int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count);
+
+/* Plain (non-speculative) decoding of n_steps tokens per sequence from the current
+ * state, one target pass per token: the lossless comparator and the speedup
+ * baseline. d_out_tokens: device int32 [batch][n_steps]. */
+int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens);
+
+/* Capture eagle_cycle into a CUDA graph on first use and replay it afterwards
+ * (enable = 1), or launch kernels directly (enable = 0, the default). */
+int eagle_set_graph(eagle_ctx* ctx, int enable);
+
+/* Synchronise the context's stream and report latched device errors (clears them).
+ * It also refreshes the host's bound on the sequences' KV lengths, which eagle_cycle
+ * otherwise grows by depth + 1 per call to refuse cycles that could overflow. */
+int eagle_status_sync(eagle_ctx* ctx);
+
+/* Debug views: copy internal device state into the caller's device buffer `dst` of
+ * `bytes` bytes (stream-ordered). Layouts (int32 unless noted, B = current batch):
+ *   EAGLE_DUMP_STATE : ctx_len, root_tok, committed, on_track, cycle, acc_len, bonus  [7][B]
+ *   EAGLE_DUMP_CAND  : cand_tok [B][k] int32, then cand_logc [B][k] float
+ *   EAGLE_DUMP_NODES : tok, parent, depth [3][B][NG] int32, then logv [B][NG] float
+ *                      (NG = k + (depth-1) k^2 nodes in generation order)
+ *   EAGLE_DUMP_TREE  : tok, pos, parent, node [4][B][m+1] int32, then the ancestry
+ *                      bitmask [B][m+1][ceil((m+1)/64)] uint64
+ *   EAGLE_DUMP_ACCEPT: acc_len [B], bonus [B], acc_path [B][depth]
+ *   EAGLE_DUMP_VERIFY_HEAD: top_id [B(m+1)][K] int32, top_val [B(m+1)][K] float,
+ *                      lse [B(m+1)] float, child logits [B(m+1)][k] float
+ *                      (K = 2 greedy, 1 sampling)
+ *   EAGLE_DUMP_VERIFY_LOGITS: full verify logits [B(m+1)][V] float (only when
+ *                      eagle_set_debug(ctx, EAGLE_DEBUG_LOGITS) was set before the cycle)
+ *   EAGLE_DUMP_FEATURES: target features of the verify rows [B(m+1)][H] (storage type)
+ * eagle_dump_bytes gives the size of each view. */
+enum {
+  EAGLE_DUMP_STATE = 0,
+  EAGLE_DUMP_CAND = 1,
+  EAGLE_DUMP_NODES = 2,
+  EAGLE_DUMP_TREE = 3,
+  EAGLE_DUMP_ACCEPT = 4,
+  EAGLE_DUMP_VERIFY_HEAD = 5,
+  EAGLE_DUMP_VERIFY_LOGITS = 6,
+  EAGLE_DUMP_FEATURES = 7
+};
+size_t eagle_dump_bytes(const eagle_ctx* ctx, int what);
+int eagle_debug_dump(eagle_ctx* ctx, int what, void* dst, size_t bytes);
+
+enum { EAGLE_DEBUG_LOGITS = 1 };
+int eagle_set_debug(eagle_ctx* ctx, int flags);
+
+/* Device pointers of the target KV cache, layout [layer][batch][kv_head][slot][head_dim]
+ * with `cap` slots per sequence (storage type); for tests and tools. */
+int eagle_kv_view(const eagle_ctx* ctx, void** k, void** v, int* cap);
+
+/* Per-launch timing of the tensor-core GEMMs inside real cycles (graph replay off):
+ * eagle_profile_begin arms CUDA events (host-created, no device allocation) around the
+ * next max_launches GEMM launches; eagle_profile_end synchronises and returns the number
+ * of launches timed, their summed device time (ms) and their algorithmic bytes (weight
+ * + activation input + output). */
+int eagle_profile_begin(eagle_ctx* ctx, int max_launches);
+int eagle_profile_end(eagle_ctx* ctx, int* launches, double* total_ms, double* total_bytes);
+
+const char* eagle_last_error(const eagle_ctx* ctx);
+void eagle_destroy(eagle_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE_H */

@@ -1,0 +1,84 @@
+/*
+ * eagle_ops.h -- kernel-level entry points of the EAGLE cycle library.
+ *
+ * Each call runs one of the cycle's kernels on caller-provided device buffers, so it
+ * can be checked on its own against the CPU oracle with injected inputs. All pointers
+ * are DEVICE pointers unless stated; `stream` is a cudaStream_t cast to void*; calls
+ * are stream-ordered and return an eagle_status (see eagle.h) without waiting.
+ * `scratch` is caller-owned device memory of at least the size the matching
+ * *_scratch_bytes function returns; the library never allocates device memory.
+ */
+#ifndef EAGLE_OPS_H
+#define EAGLE_OPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Projection GEMM Y[M][N] = X[M][K] * W[N][K]^T (the nn.Linear layout used for every
+ * target and drafter projection and the LM head). dtype EAGLE_DTYPE_BF16: tcgen05
+ * tensor-core kernel, X and W bf16 row-major with K a multiple of 8 and 16-byte
+ * aligned bases; dtype EAGLE_DTYPE_F32: fp32 FFMA kernel. epi: 0 = store fp32 Y,
+ * 1 = store bf16 Y (bf16 only), 2 = Y += result (fp32 residual update). out has row
+ * stride ldo elements. Scratch holds split-tile partial sums and per-tile tickets; it
+ * must be zero-filled before the first call and is left zeroed by every call. */
+size_t eagle_op_gemm_scratch_bytes(int M, int N);
+int eagle_op_gemm(int dtype, void* stream, const void* W, int N, int K, const void* X, int M, int epi,
+                  void* out, int ldo, void* scratch, size_t scratch_bytes);
+
+/* Fused LM head: logits = X[M][H] * W_lm[V][H]^T reduced per row without writing the
+ * logits (bf16), or through an fp32 logits buffer inside the scratch (f32). Per row it
+ * returns the K best entries by ranking value (value desc, token id asc) and the
+ * log-sum-exp of logit * inv_t. Ranking value = logit * inv_t, plus Gumbel(0,1) noise
+ * when gumbel != 0, drawn from Philox4x32-10 keyed by (seed; counter = (id >> 2,
+ * row_key[row], cycle, row_seq[row] << 8 | stream_id)), word id & 3. specials
+ * [M][S] (nullable, -1 = unused): ids left out of the ranking (and out of the
+ * log-sum-exp when lse_excl != 0) whose raw logits go to spec_logit [M][S].
+ * Outputs: top_id [M][K] int32, top_val [M][K] float, lse [M] float. K in 1..16. */
+size_t eagle_op_lm_head_scratch_bytes(int dtype, int V, int M, int K);
+int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, const void* X, int M, int K,
+                     float inv_t, int gumbel, int lse_excl, const int32_t* specials, int S, float* spec_logit,
+                     const int32_t* row_seq, const int32_t* row_key, uint32_t cycle, uint64_t seed,
+                     int stream_id, int32_t* top_id, float* top_val, float* lse, void* scratch,
+                     size_t scratch_bytes);
+
+/* Tree-masked attention of R query rows over a KV cache laid out
+ * [seq][kv_head][slot][d] with `cap` slots (storage type dtype). q, out: [R][nq][d].
+ * Rows of one sequence are contiguous, rows_per_seq each; row r belongs to sequence
+ * row_seq[r] and its own key sits at slot row_slot[r]. mode 0 (causal): row r sees
+ * slots <= row_slot[r]. mode 1 (tree): row r sees slots < ctx_len[seq] and slot
+ * ctx_len[seq] + t for t < tree_T where bit t of mask[r][t / 64] is set.
+ * Scale = 1/sqrt(d) when scale <= 0. d <= 128, nq a multiple of nkv. */
+int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcache, const void* vcache,
+                       void* out, int R, int nq, int nkv, int d, int cap, int rows_per_seq,
+                       const int32_t* row_seq, const int32_t* row_slot, const int32_t* ctx_len, int mode,
+                       int tree_T, const uint64_t* mask, int mask_words, float scale);
+
+/* EAGLE-2 tree growth and rerank with injected draft confidences, for B sequences:
+ * cand_tok/cand_logc [B][k]: the root's children (token, log confidence) in rank order;
+ * child_tok/child_logc [B][depth-1][k][k]: children of the r-th node selected at depth
+ * d (entry [b][d-1][r][i], rank order). ctx_len [B], root_tok [B].
+ * Outputs: node tables [B][NG] (tok, parent, depth int32; logv float), flattened tree
+ * [B][m+1] (tok, pos, parent, node int32) and ancestry bitmask [B][m+1][W] uint64 with
+ * W = ceil((m+1)/64). */
+size_t eagle_op_tree_scratch_bytes(int B, int k, int depth, int m);
+int eagle_op_tree_build(void* stream, int B, int k, int depth, int m, const int32_t* cand_tok,
+                        const float* cand_logc, const int32_t* child_tok, const float* child_logc,
+                        const int32_t* ctx_len, const int32_t* root_tok, int32_t* node_tok, int32_t* node_parent,
+                        int32_t* node_depth, float* node_logv, int32_t* tree_tok, int32_t* tree_pos,
+                        int32_t* tree_parent, int32_t* tree_node, uint64_t* tree_mask, void* scratch,
+                        size_t scratch_bytes);
+
+/* KV compaction: in every layer, slot n_old[b] + j <- slot n_old[b] + acc_path[b][j-1]
+ * for j = 1..acc_len[b] (acc_path rows are flattened-tree rows, Dmax per sequence,
+ * Dmax <= 8). Cache layout [layer][seq][kv_head][slot][d], cap slots per sequence. */
+int eagle_op_compact(int dtype, void* stream, void* kcache, void* vcache, int layers, int B, int nkv, int cap,
+                     int d, const int32_t* n_old, const int32_t* acc_len, const int32_t* acc_path, int Dmax);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE_OPS_H */

@@ -1,0 +1,93 @@
+"""CPU checks of the C ABI: the library builds/loads, exports every declared symbol,
+and sizes its workspace (pure host logic, no GPU needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from eagle_speculative_decoding_cycle_gb300 import _lib as L
+from eagle_speculative_decoding_cycle_gb300 import api, synth
+
+
+def _declared():
+    names = []
+    for h in ("eagle.h", "eagle_ops.h"):
+        txt = open(os.path.join(ROOT, "include", h)).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        names += re.findall(r"\b(eagle_[a-z0-9_]+)\s*\(", txt)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from eagle_speculative_decoding_cycle_gb300 import build
+    build.build()
+    return L.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert sorted(L.EXPORTED) == declared
+    for n in declared:
+        assert hasattr(lib, n), n
+
+
+def _cfg(w, **kw):
+    return api.configs(w, **kw)
+
+
+@pytest.mark.parametrize("w", [synth.TINY, synth.LLAMA2_7B, synth.LLAMA31_8B_SAMPLE, synth.LLAMA_13B_LONG,
+                               synth.SMALL_BF16, synth.SMALL_BF16_E3])
+def test_workspace_sizes(lib, w):
+    mc, dc, tc, lim = _cfg(w)
+    nb = lib.eagle_workspace_bytes(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(lim))
+    m = w.model
+    es = 4 if m.dtype == "f32" else 2
+    kv = 2 * m.n_layers * lim.max_batch * m.n_kv_heads * lim.max_ctx * m.head_dim * es
+    assert nb > kv and nb < kv * 3 + (4 << 30)
+
+
+def test_workspace_rejects_bad_configs(lib):
+    w = synth.TINY
+    for mutate in (lambda mc, dc, tc, lim: setattr(tc, "topk", 0),
+                   lambda mc, dc, tc, lim: setattr(tc, "topk", 17),
+                   lambda mc, dc, tc, lim: setattr(tc, "m", 10 ** 6),
+                   lambda mc, dc, tc, lim: setattr(tc, "depth", 9),
+                   lambda mc, dc, tc, lim: setattr(mc, "n_kv_heads", 3),
+                   lambda mc, dc, tc, lim: setattr(mc, "head_dim", 256),
+                   lambda mc, dc, tc, lim: setattr(dc, "kind", 2),
+                   lambda mc, dc, tc, lim: setattr(lim, "kv_block", 16),
+                   lambda mc, dc, tc, lim: setattr(tc, "planted_conf", 1.0)):
+        mc, dc, tc, lim = _cfg(w)
+        mutate(mc, dc, tc, lim)
+        assert lib.eagle_workspace_bytes(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(lim)) == 0
+
+
+def test_create_rejects_without_touching_gpu(lib):
+    """Argument errors are caught on the host before any CUDA call."""
+    mc, dc, tc, lim = _cfg(synth.TINY)
+    h = C.c_void_p()
+    w = L.Weights()
+    rc = lib.eagle_create(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(w), C.byref(lim), None, 0, None, C.byref(h))
+    assert rc == L.EAGLE_EINVAL and not h.value
+    tc.topk = 0
+    rc = lib.eagle_create(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(w), C.byref(lim), None, 0, None, C.byref(h))
+    assert rc == L.EAGLE_EINVAL
+
+
+def test_op_scratch_sizes(lib):
+    assert lib.eagle_op_gemm_scratch_bytes(61, 12288) > 0
+    assert lib.eagle_op_gemm_scratch_bytes(0, 10) == 0
+    assert lib.eagle_op_lm_head_scratch_bytes(1, 32000, 61, 2) > 0
+    assert lib.eagle_op_lm_head_scratch_bytes(1, 32000, 61, 17) == 0
+    assert lib.eagle_op_tree_scratch_bytes(1, 10, 6, 60) > 0
+    assert lib.eagle_op_tree_scratch_bytes(1, 10, 9, 60) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(L, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        L.lib()

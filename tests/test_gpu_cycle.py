@@ -1,0 +1,237 @@
+"""End-to-end GPU parity of prefill, the draft-and-verify cycle and plain decoding.
+
+- Index work is checked in lock step: after every GPU cycle the oracle's tree policy
+  is rerun on the GPU's own path values and its acceptance walk on the GPU's own verify
+  head outputs; expansion order, kept set, flattened tree, mask, accepted path and
+  bonus must agree bit for bit.
+- Floats: verify-row features/logits against the oracle, 1e-4 (fp32 model) or 5e-2
+  (bf16 model) max-abs.
+- Greedy losslessness: speculative output equals plain greedy decoding (the GPU's own
+  decode_plain and the oracle's)."""
+import numpy as np
+import pytest
+import torch
+
+from eagle_speculative_decoding_cycle_gb300 import _lib as L
+from eagle_speculative_decoding_cycle_gb300 import api, synth
+from oracle import philox
+from oracle.accept import greedy_walk, sample_walk
+from oracle.cycle import OracleSeq, build_model, plain_decode
+from oracle.tree import NodeTable, flatten, rerank, select_expand
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def setup(wl, planted=True, extra=8):
+    weights = synth.make_weights(wl, "cpu")
+    M = build_model(synth.weights_to_numpy(weights), wl)
+    prompt = synth.make_prompts(wl)[0]
+    R = plain_decode(M, wl, prompt.numpy(), wl.new_tokens + wl.tree.depth + extra) if planted else None
+    eng = api.Engine(wl, {k: v.to(DEV) for k, v in weights.items()})
+    return weights, M, prompt, R, eng
+
+
+def gpu_table(eng, b=0):
+    tok, par, dep, logv = eng.dump(L.DUMP_NODES)
+    t = NodeTable()
+    t.token = tok[b].tolist()
+    t.parent = par[b].tolist()
+    t.depth = dep[b].tolist()
+    t.logv = [np.float32(x) for x in logv[b].numpy()]
+    return t
+
+
+def check_tree_policy(eng, wl, b=0):
+    """Oracle policy on the GPU's path values reproduces the GPU's expansion, rerank,
+    flattening and mask."""
+    k, D, m = wl.tree.topk, wl.tree.depth, wl.tree.m
+    t = gpu_table(eng, b)
+    # expansion order: children of the r-th selected depth-d node occupy block r
+    for d in range(1, D):
+        sel = select_expand(NodeTable(t.token, t.parent, t.depth, t.logv), d, k)
+        base = k + (d - 1) * k * k
+        for r, v in enumerate(sel):
+            assert all(t.parent[base + r * k + i] == v for i in range(k))
+    st = eng.dump(L.DUMP_STATE)
+    ft = flatten(t, rerank(t, m), int(eng.dump(L.DUMP_TREE)[0][b, 0]))
+    tok, pos, par, node, mask = eng.dump(L.DUMP_TREE)
+    assert tok[b].tolist() == ft.token.tolist()
+    assert par[b].tolist() == ft.parent.tolist()
+    assert node[b].tolist() == ft.node.tolist()
+    assert np.array_equal(mask[b].numpy().view(np.uint64), ft.mask_words())
+    return t, ft, pos[b].numpy()
+
+
+def run_lockstep(wl, n_cycles=None, planted=True, check_feats_tol=None):
+    weights, M, prompt, R, eng = setup(wl, planted)
+    ref = None if R is None else torch.tensor([R], dtype=torch.int32, device=DEV)
+    eng.prefill([prompt.to(DEV)], ref)
+    eng.set_debug(L.DEBUG_LOGITS)
+    o = OracleSeq(M, wl)
+    o.prefill(prompt.numpy(), R)
+    st = eng.dump(L.DUMP_STATE)
+    assert int(st["root_tok"][0]) == o.committed[0]
+    D = wl.tree.depth
+    out = torch.zeros(1, D + 1, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = [int(st["root_tok"][0])]
+    stats = {"cycles": 0, "tree_match": 0, "max_feat_err": 0.0, "max_logit_err": 0.0, "accepted": []}
+    T = wl.tree.temperature
+    while len(got) < wl.new_tokens and (n_cycles is None or stats["cycles"] < n_cycles):
+        n_before = int(eng.dump(L.DUMP_STATE)["ctx_len"][0])
+        eng.cycle(out, cnt)
+        eng.sync()
+        t, ft, pos = check_tree_policy(eng, wl)
+        assert pos.tolist() == (n_before + ft.depth).tolist()
+        acc_len, bonus, path = eng.dump(L.DUMP_ACCEPT)
+        L_ = int(acc_len[0])
+        hid, hval, lse, spec = eng.dump(L.DUMP_VERIFY_HEAD)
+        if T == 0:
+            gp, gb = greedy_walk(ft, hid[:, 0].tolist())
+        else:
+            def p_child(row, tok):
+                i = [int(ft.token[v]) for v in ft.children(row)].index(tok)
+                return np.float32(np.exp(np.float32(spec[row, i]) * np.float32(1 / T) - np.float32(lse[row])))
+
+            cyc = int(eng.dump(L.DUMP_STATE)["cycle"][0]) - 1
+            gp, gb = sample_walk(ft, p_child,
+                                 lambda row, i: philox.draw_uniform(wl.seed, philox.STREAM_ACCEPT, 0, cyc, i, row),
+                                 lambda row, ex: int(hid[row, 0]))
+        assert gp == path[0, :L_].tolist() and gb == int(bonus[0])
+        new = out[0, :int(cnt[0])].tolist()
+        assert new == [int(ft.token[r]) for r in gp] + [gb]
+        # oracle in lock step: same tree -> compare floats of the verify rows, then let the
+        # oracle commit the GPU's decisions; a different tree (a near-tie decided the other
+        # way in fp32 vs fp64) ends the float comparison for this run
+        if o is not None:
+            plan = o.draft_and_verify()
+            if plan.flat.token.tolist() == ft.token.tolist() and plan.flat.parent.tolist() == ft.parent.tolist():
+                stats["tree_match"] += 1
+                gl = eng.dump(L.DUMP_VERIFY_LOGITS).double().numpy()
+                stats["max_logit_err"] = max(stats["max_logit_err"], float(np.max(np.abs(gl - plan.logits))))
+                gf = eng.dump(L.DUMP_FEATURES).double().numpy()
+                stats["max_feat_err"] = max(stats["max_feat_err"], float(np.max(np.abs(gf - plan.feats))))
+                o.commit(plan, gp, gb)
+            else:
+                stats["diverged_at"] = stats["cycles"]
+                o = None
+        got += new
+        stats["cycles"] += 1
+        stats["accepted"].append(L_)
+    eng.close()
+    return got, R, stats
+
+
+def test_tiny_fp32_lockstep_and_lossless():
+    wl = synth.TINY
+    got, R, st = run_lockstep(wl)
+    N = wl.new_tokens
+    assert got[:N] == R[:N]                     # greedy speculative == plain greedy
+    assert st["tree_match"] == st["cycles"]     # same trees every cycle
+    assert st["max_logit_err"] < 1e-4 and st["max_feat_err"] < 1e-4
+    assert max(st["accepted"]) >= 2
+
+
+def test_tiny_fp32_plain_decode_matches_oracle():
+    wl = synth.TINY
+    weights, M, prompt, R, eng = setup(wl)
+    eng.prefill([prompt.to(DEV)])
+    n = 40
+    out = torch.zeros(1, n, dtype=torch.int32, device=DEV)
+    first = int(eng.dump(L.DUMP_STATE)["root_tok"][0])
+    eng.decode_plain(n, out)
+    eng.sync()
+    assert [first] + out[0].tolist() == R[:n + 1]
+    eng.close()
+
+
+def test_small_bf16_lockstep_and_lossless():
+    wl = synth.SMALL_BF16
+    got, R, st = run_lockstep(wl)
+    N = wl.new_tokens
+    assert got[:N] == R[:N]
+    assert st["tree_match"] >= 1
+    assert st["max_logit_err"] < 5e-2
+
+
+def test_small_bf16_spec_equals_gpu_plain():
+    wl = synth.SMALL_BF16.replace(new_tokens=48)
+    weights, M, prompt, R, eng = setup(wl)
+    eng.prefill([prompt.to(DEV)])
+    n = wl.new_tokens
+    plain = torch.zeros(1, n, dtype=torch.int32, device=DEV)
+    first = int(eng.dump(L.DUMP_STATE)["root_tok"][0])
+    eng.decode_plain(n - 1, plain)
+    eng.sync()
+    gp = [first] + plain[0, :n - 1].tolist()
+    ref = torch.tensor([gp + [0] * (wl.tree.depth + 2)], dtype=torch.int32, device=DEV)
+    eng.prefill([prompt.to(DEV)], ref)
+    D = wl.tree.depth
+    out = torch.zeros(1, D + 1, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = [int(eng.dump(L.DUMP_STATE)["root_tok"][0])]
+    while len(got) < n:
+        eng.cycle(out, cnt)
+        got += out[0, :int(cnt[0])].tolist()
+    eng.sync()
+    assert got[:n] == gp[:n]
+    eng.close()
+
+
+def test_eagle3_sampling_lockstep():
+    wl = synth.SMALL_BF16_E3
+    got, R, st = run_lockstep(wl, planted=False)
+    assert st["cycles"] >= 3
+
+
+def test_eagle3_greedy_lossless():
+    wl = synth.SMALL_BF16_E3.replace(tree=synth.TreeShape(topk=4, depth=5, m=14, temperature=0.0, planted_p=0.8))
+    got, R, st = run_lockstep(wl)
+    N = wl.new_tokens
+    assert got[:N] == R[:N]
+    assert max(st["accepted"]) >= 2
+
+
+def test_graph_replay_equals_eager():
+    wl = synth.TINY
+    weights, M, prompt, R, eng = setup(wl)
+    ref = torch.tensor([R], dtype=torch.int32, device=DEV)
+    D = wl.tree.depth
+    res = []
+    for graph in (False, True):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            e2 = api.Engine(wl, {k: v.to(DEV) for k, v in weights.items()}, stream=s)
+            e2.set_graph(graph)
+            e2.prefill([prompt.to(DEV)], ref)
+            out = torch.zeros(1, D + 1, dtype=torch.int32, device=DEV)
+            cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+            toks = []
+            for _ in range(10):
+                e2.cycle(out, cnt)
+                e2.sync()
+                toks += out[0, :int(cnt[0])].tolist()
+            res.append(toks)
+            e2.close()
+    assert res[0] == res[1]
+    eng.close()
+
+
+def test_capacity_error_before_launch():
+    wl = synth.TINY
+    weights, M, prompt, R, _ = setup(wl, planted=False)
+    eng = api.Engine(wl, {k: v.to(DEV) for k, v in weights.items()}, max_ctx=40)
+    eng.prefill([prompt.to(DEV)])
+    with pytest.raises(L.EagleError) as e:
+        for _ in range(10):
+            eng.cycle()
+    assert e.value.code == L.EAGLE_ECAPACITY
+    eng.sync()
+    eng.close()
