@@ -24,10 +24,10 @@ DEBUG_LOGITS = 1
 # every symbol the headers declare (checked by the CPU test suite)
 EXPORTED = [
     "eagle_workspace_bytes", "eagle_create", "eagle_prefill", "eagle_cycle", "eagle_decode_plain",
-    "eagle_set_graph", "eagle_status_sync", "eagle_dump_bytes", "eagle_debug_dump", "eagle_set_debug",
+    "eagle_set_graph", "eagle_cycle_kernel_launches", "eagle_status_sync", "eagle_dump_bytes", "eagle_debug_dump", "eagle_set_debug",
     "eagle_kv_view", "eagle_profile_begin", "eagle_profile_end", "eagle_last_error", "eagle_destroy",
     "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
-    "eagle_op_attention", "eagle_op_tree_scratch_bytes", "eagle_op_tree_build", "eagle_op_compact",
+    "eagle_op_attention_scratch_bytes", "eagle_op_attention", "eagle_op_tree_scratch_bytes", "eagle_op_tree_build", "eagle_op_compact",
 ]
 
 
@@ -72,8 +72,9 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_create": (i32, [P(ModelCfg), P(DrafterCfg), P(TreeCfg), P(Weights), P(Limits), vp, sz, vp, P(vp)]),
         "eagle_prefill": (i32, [vp, i32, vp, P(C.c_int32), vp, i32]),
         "eagle_cycle": (i32, [vp, vp, vp]),
-        "eagle_decode_plain": (i32, [vp, i32, vp]),
+        "eagle_decode_plain": (i32, [vp, i32, vp, vp]),
         "eagle_set_graph": (i32, [vp, i32]),
+        "eagle_cycle_kernel_launches": (i32, [vp]),
         "eagle_status_sync": (i32, [vp]),
         "eagle_dump_bytes": (sz, [vp, i32]),
         "eagle_debug_dump": (i32, [vp, i32, vp, sz]),
@@ -88,8 +89,9 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_op_lm_head_scratch_bytes": (sz, [i32, i32, i32, i32]),
         "eagle_op_lm_head": (i32, [i32, vp, vp, i32, i32, vp, i32, i32, f32, i32, i32, vp, i32, vp, vp, vp, u32,
                                    u64, i32, vp, vp, vp, vp, sz]),
+        "eagle_op_attention_scratch_bytes": (sz, [i32, i32, i32]),
         "eagle_op_attention": (i32, [i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, i32, i32,
-                                     vp, i32, f32]),
+                                     vp, i32, f32, vp, sz]),
         "eagle_op_tree_scratch_bytes": (sz, [i32, i32, i32, i32]),
         "eagle_op_tree_build": (i32, [vp, i32, i32, i32, i32] + [vp] * 15 + [sz]),
         "eagle_op_compact": (i32, [i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32]),

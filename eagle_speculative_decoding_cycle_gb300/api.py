@@ -93,8 +93,8 @@ class Engine:
     def cycle(self, out_tokens: Optional[torch.Tensor] = None, out_count: Optional[torch.Tensor] = None) -> None:
         self._check(self.lib.eagle_cycle(self.h, _ptr(out_tokens), _ptr(out_count)), "eagle_cycle")
 
-    def decode_plain(self, n: int, out: torch.Tensor) -> None:
-        self._check(self.lib.eagle_decode_plain(self.h, n, _ptr(out)), "eagle_decode_plain")
+    def decode_plain(self, n: int, out: torch.Tensor, margin: Optional[torch.Tensor] = None) -> None:
+        self._check(self.lib.eagle_decode_plain(self.h, n, _ptr(out), _ptr(margin)), "eagle_decode_plain")
 
     def set_graph(self, on: bool) -> None:
         self._check(self.lib.eagle_set_graph(self.h, int(on)), "eagle_set_graph")
@@ -225,16 +225,19 @@ def lm_head(W: torch.Tensor, X: torch.Tensor, K: int, inv_t: float = 1.0, gumbel
 
 
 def attention(q, kcache, vcache, row_seq, row_slot, ctx_len, rows_per_seq, mode, tree_T=0, mask=None,
-              scale=0.0, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+              scale=0.0, split_kv: bool = True, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """q [R][nq][d]; caches [B][nkv][cap][d]; returns out [R][nq][d]."""
     lib = L.lib()
     R, nq, d = q.shape
     _, nkv, cap, _ = kcache.shape
     out = torch.empty_like(q)
     mw = 0 if mask is None else mask.shape[1]
+    nb = lib.eagle_op_attention_scratch_bytes(R, nq, d) if split_kv else 0
+    scratch = torch.empty(max(nb, 1), dtype=torch.uint8, device=q.device)
     rc = lib.eagle_op_attention(_dtype_code(q), _stream(stream), q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
                                 out.data_ptr(), R, nq, nkv, d, cap, rows_per_seq, row_seq.data_ptr(),
-                                row_slot.data_ptr(), ctx_len.data_ptr(), mode, tree_T, _ptr(mask), mw, scale)
+                                row_slot.data_ptr(), ctx_len.data_ptr(), mode, tree_T, _ptr(mask), mw, scale,
+                                scratch.data_ptr() if nb else None, nb)
     L.check(rc, "eagle_op_attention")
     return out
 

@@ -18,6 +18,7 @@
 namespace eagle {
 
 __global__ void accept_k(CycleDev c, HeadOut h, int* out_tokens, int* out_count) {
+  PDL_ENTRY();
   const int b = blockIdx.x;
   const int T1 = c.T1, rb = b * T1;
   // greedy top-2 margins (diagnostic for near-ties)
@@ -68,7 +69,7 @@ __global__ void accept_k(CycleDev c, HeadOut h, int* out_tokens, int* out_count)
 }
 
 int accept_walk(cudaStream_t st, const CycleDev& c, const HeadOut& h, int* out_tokens, int* out_count) {
-  accept_k<<<c.B, 64, 0, st>>>(c, h, out_tokens, out_count);
+  launch_k(accept_k, c.B, 64, 0, st, c, h, out_tokens, out_count);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
@@ -78,6 +79,7 @@ int accept_walk(cudaStream_t st, const CycleDev& c, const HeadOut& h, int* out_t
 template <typename T>
 __global__ void compact_k(T* kc, T* vc, int layers, int B, int nkv, int cap, int d, const int* n_old,
                           const int* acc_len, const int* acc_path, int Dmax) {
+  PDL_ENTRY();
   const int layer = blockIdx.x;
   const int bh = blockIdx.y;
   const int b = bh / nkv;
@@ -105,10 +107,10 @@ int compact_kv(cudaStream_t st, int dtype, void* kc, void* vc, int layers, int B
   if (Dmax > 8) return -1;
   dim3 grid(layers, B * nkv);
   if (dtype == DT_F32)
-    compact_k<float><<<grid, 128, 0, st>>>((float*)kc, (float*)vc, layers, B, nkv, cap, d, n_old, acc_len,
+    launch_k(compact_k<float>, grid, 128, 0, st, (float*)kc, (float*)vc, layers, B, nkv, cap, d, n_old, acc_len,
                                            acc_path, Dmax);
   else
-    compact_k<__nv_bfloat16><<<grid, 128, 0, st>>>((__nv_bfloat16*)kc, (__nv_bfloat16*)vc, layers, B, nkv, cap,
+    launch_k(compact_k<__nv_bfloat16>, grid, 128, 0, st, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, layers, B, nkv, cap,
                                                    d, n_old, acc_len, acc_path, Dmax);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
@@ -118,6 +120,7 @@ int compact_kv(cudaStream_t st, int dtype, void* kc, void* vc, int layers, int B
 // are ignored and whose KV lands beyond the new context.
 __global__ void update_rows_k(CycleDev c, int* row_tok, int* row_pos, int* row_slot, int* row_seq,
                               int* row_featsrc) {
+  PDL_ENTRY();
   const int b = blockIdx.x, j = threadIdx.x;
   if (j > c.D) return;
   const int L = c.acc_len[b];
@@ -134,11 +137,12 @@ __global__ void update_rows_k(CycleDev c, int* row_tok, int* row_pos, int* row_s
 int update_rows(cudaStream_t st, const CycleDev& c, int* row_tok, int* row_pos, int* row_slot, int* row_seq,
                 int* row_featsrc) {
   if (c.D + 1 > 32) return -1;
-  update_rows_k<<<c.B, 32, 0, st>>>(c, row_tok, row_pos, row_slot, row_seq, row_featsrc);
+  launch_k(update_rows_k, c.B, 32, 0, st, c, row_tok, row_pos, row_slot, row_seq, row_featsrc);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 __global__ void plain_rows_k(CycleDev c, int* row_tok, int* row_pos, int* row_slot, int* row_seq) {
+  PDL_ENTRY();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= c.B) return;
   row_tok[b] = c.root_tok[b];
@@ -148,22 +152,25 @@ __global__ void plain_rows_k(CycleDev c, int* row_tok, int* row_pos, int* row_sl
 }
 
 int plain_rows(cudaStream_t st, const CycleDev& c, int* row_tok, int* row_pos, int* row_slot, int* row_seq) {
-  plain_rows_k<<<(c.B + 127) / 128, 128, 0, st>>>(c, row_tok, row_pos, row_slot, row_seq);
+  launch_k(plain_rows_k, (c.B + 127) / 128, 128, 0, st, c, row_tok, row_pos, row_slot, row_seq);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-__global__ void plain_advance_k(CycleDev c, const int* next_tok, int K, int* out, int ld_out, int step) {
+__global__ void plain_advance_k(CycleDev c, const int* next_tok, int K, const float* top_val, int* out,
+                                float* margin, int ld_out, int step) {
+  PDL_ENTRY();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= c.B) return;
   const int t = next_tok[b * K];
   if (out) out[(size_t)b * ld_out + step] = t;
+  if (margin) margin[(size_t)b * ld_out + step] = K >= 2 ? top_val[b * K] - top_val[b * K + 1] : NAN;
   c.root_tok[b] = t;
   c.ctx_len[b] += 1;
 }
 
-int plain_advance(cudaStream_t st, const CycleDev& c, const int* next_tok, int* out, int ld_out, int step) {
-  // next_tok points at the head's top_id with K = 1
-  plain_advance_k<<<(c.B + 127) / 128, 128, 0, st>>>(c, next_tok, 1, out, ld_out, step);
+int plain_advance(cudaStream_t st, const CycleDev& c, const int* next_tok, int K, const float* top_val, int* out,
+                  float* margin, int ld_out, int step) {
+  launch_k(plain_advance_k, (c.B + 127) / 128, 128, 0, st, c, next_tok, K, top_val, out, margin, ld_out, step);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
@@ -171,6 +178,7 @@ int plain_advance(cudaStream_t st, const CycleDev& c, const int* next_tok, int* 
 // drafter rows (token p + 1, the first generated token for the last prompt position).
 __global__ void prefill_rows_k(const int* prompt, int n_total, int seq, int p0, int n, int shift,
                                const int* root_tok, int* row_tok, int* row_pos, int* row_slot, int* row_seq) {
+  PDL_ENTRY();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const int p = p0 + i;
@@ -183,12 +191,13 @@ __global__ void prefill_rows_k(const int* prompt, int n_total, int seq, int p0, 
 int prefill_rows(cudaStream_t st, const int* prompt, int seq, int p0, int n, int n_total_shift,
                  const int* root_tok, int* row_tok, int* row_pos, int* row_slot, int* row_seq, int shift) {
   if (n <= 0) return 0;
-  prefill_rows_k<<<(n + 127) / 128, 128, 0, st>>>(prompt, n_total_shift, seq, p0, n, shift, root_tok, row_tok,
+  launch_k(prefill_rows_k, (n + 127) / 128, 128, 0, st, prompt, n_total_shift, seq, p0, n, shift, root_tok, row_tok,
                                                   row_pos, row_slot, row_seq);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 __global__ void prefill_finish_k(CycleDev c, int seq, int n, const int* first_tok) {
+  PDL_ENTRY();
   if (threadIdx.x) return;
   const int t = first_tok[0];
   c.root_tok[seq] = t;
@@ -203,7 +212,7 @@ __global__ void prefill_finish_k(CycleDev c, int seq, int n, const int* first_to
 }
 
 int prefill_finish(cudaStream_t st, const CycleDev& c, int seq, int n, const int* first_tok) {
-  prefill_finish_k<<<1, 32, 0, st>>>(c, seq, n, first_tok);
+  launch_k(prefill_finish_k, 1, 32, 0, st, c, seq, n, first_tok);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

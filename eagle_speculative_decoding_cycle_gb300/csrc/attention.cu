@@ -13,6 +13,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <algorithm>
+
 namespace eagle {
 
 constexpr int QPW = 2;            // query vectors per warp
@@ -23,6 +25,7 @@ constexpr int DMAX = 128;
 
 template <typename T>
 __global__ void __launch_bounds__(128) attn_simt_k(AttnArgs a) {
+  PDL_ENTRY();
   __shared__ float sq[QV][DMAX];
   __shared__ float sk[KT][DMAX + 1];
   __shared__ float sv[KT][DMAX];
@@ -130,8 +133,11 @@ __global__ void __launch_bounds__(128) attn_simt_k(AttnArgs a) {
   }
 }
 
+int attention_bf16_mma(cudaStream_t st, const AttnArgs& a);
+
 int attention(cudaStream_t st, int dtype, const AttnArgs& a) {
   if (a.R <= 0) return 0;
+  if (dtype == DT_BF16) return attention_bf16_mma(st, a);
   if (a.d > DMAX || a.nq % a.nkv) return -1;
   const int G = a.nq / a.nkv;
   if (G > QV || QV % G) return -1;
@@ -139,9 +145,338 @@ int attention(cudaStream_t st, int dtype, const AttnArgs& a) {
   const int nseq = (a.R + a.rows_per_seq - 1) / a.rows_per_seq;
   const int nb = (a.rows_per_seq + RB - 1) / RB;
   dim3 grid(a.nkv, nseq * nb);
-  if (dtype == DT_F32) attn_simt_k<float><<<grid, 128, 0, st>>>(a);
-  else attn_simt_k<__nv_bfloat16><<<grid, 128, 0, st>>>(a);
+  if (dtype == DT_F32) launch_k(attn_simt_k<float>, grid, 128, 0, st, a);
+  else launch_k(attn_simt_k<__nv_bfloat16>, grid, 128, 0, st, a);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace eagle
+
+// ------------------------------------------------------------------------------------------------
+// Tensor-core path (bf16): mma.sync m16n8k16 with fp32 accumulation, FlashAttention-style
+// online softmax in the exp2 domain, K/V tiles of 64 keys double-buffered in shared memory
+// by cp.async, and split-KV over the key range with a fixed-order log-sum-exp combine.
+// A CTA covers one KV head and 64 query vectors (rows x the GQA group); warp w owns query
+// vectors 16w .. 16w+15.
+// ------------------------------------------------------------------------------------------------
+namespace eagle {
+
+constexpr int MT_KEYS = 64;
+constexpr int MT_QV = 64;
+
+__device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// (lo, hi) -> bf16 pairs of their high parts and of the residuals x - bf16(x).
+__device__ __forceinline__ void split_bf16(float lo, float hi, uint32_t& h, uint32_t& l) {
+  const __nv_bfloat162 hv = __floats2bfloat162_rn(lo, hi);
+  const float2 back = __bfloat1622float2(hv);
+  const __nv_bfloat162 lv = __floats2bfloat162_rn(lo - back.x, hi - back.y);
+  h = *reinterpret_cast<const uint32_t*>(&hv);
+  l = *reinterpret_cast<const uint32_t*>(&lv);
+}
+
+struct RowVis {
+  int valid, slot;
+  uint64_t mw[4];
+};
+
+__device__ __forceinline__ bool visible(const AttnArgs& a, const RowVis& rv, int ctx, int key) {
+  if (!rv.valid) return false;
+  if (a.mode == 0) return key <= rv.slot;
+  if (key < ctx) return true;
+  const int t = key - ctx;
+  if (t >= a.tree_T) return false;
+  return (rv.mw[t >> 6] >> (t & 63)) & 1ull;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_mma_k(AttnArgs a, int splits) {
+  PDL_ENTRY();
+  constexpr int LD = D + 8;                      // padded smem row (bf16 elements)
+  extern __shared__ __align__(16) uint8_t attn_smem[];
+  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(attn_smem);              // [2][64][LD]
+  __nv_bfloat16* sV = sK + 2 * MT_KEYS * LD;                                    // [2][64][LD]
+  const int G = a.nq / a.nkv;
+  const int RB = MT_QV / G;
+  const int nb = (a.rows_per_seq + RB - 1) / RB;
+  const int kvh = blockIdx.x;
+  const int sidx = blockIdx.y / nb, rb = blockIdx.y % nb;
+  const int split = blockIdx.z;
+  const int r0 = sidx * a.rows_per_seq + rb * RB;
+  const int r1 = min(r0 + RB, min((sidx + 1) * a.rows_per_seq, a.R));
+  if (r0 >= r1) return;
+  const int seq = a.row_seq[r0];
+  const int ctx = a.ctx_len[seq];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.kcache) + (size_t)(seq * a.nkv + kvh) * a.cap * D;
+  const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.vcache) + (size_t)(seq * a.nkv + kvh) * a.cap * D;
+
+  int kend = 0;
+  for (int r = r0; r < r1; ++r) kend = max(kend, a.mode == 0 ? a.row_slot[r] + 1 : ctx + a.tree_T);
+  kend = min(kend, a.cap);
+  const int n_tiles = (kend + MT_KEYS - 1) / MT_KEYS;
+  const int tps = (n_tiles + splits - 1) / splits;
+  const int t_begin = split * tps, t_end = min(n_tiles, t_begin + tps);
+
+  // the two query vectors (rows of the mma fragment) this thread holds
+  const int qv_a = warp * 16 + (lane >> 2), qv_b = qv_a + 8;
+  RowVis va, vb;
+  auto setup_row = [&](int qv, RowVis& v, int& row, int& head) {
+    row = r0 + qv / G;
+    head = kvh * G + qv % G;
+    v.valid = row < r1;
+    v.slot = v.valid ? a.row_slot[row] : -1;
+    for (int w = 0; w < 4; ++w) v.mw[w] = (v.valid && a.mode == 1 && w < a.mask_words) ? a.mask[(size_t)row * a.mask_words + w] : 0ull;
+  };
+  int row_a, head_a, row_b, head_b;
+  setup_row(qv_a, va, row_a, head_a);
+  setup_row(qv_b, vb, row_b, head_b);
+
+  // Q fragments (bf16 pairs), zero for rows past the block
+  uint32_t qf[D / 16][4];
+  {
+    const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* pa = qp + ((size_t)row_a * a.nq + head_a) * D;
+    const __nv_bfloat16* pb = qp + ((size_t)row_b * a.nq + head_b) * D;
+    const int c = (lane & 3) * 2;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; ++kt) {
+      qf[kt][0] = va.valid ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + c) : 0u;
+      qf[kt][1] = vb.valid ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + c) : 0u;
+      qf[kt][2] = va.valid ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + 8 + c) : 0u;
+      qf[kt][3] = vb.valid ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + 8 + c) : 0u;
+    }
+  }
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+  const float sl2 = a.scale * 1.4426950408889634f;
+
+  auto load_tile = [&](int t, int buf) {
+    constexpr int CH = D / 8;   // 16-byte chunks per row
+    for (int i = threadIdx.x; i < MT_KEYS * CH; i += 128) {
+      const int kr = i / CH, c = i % CH;
+      const int key = t * MT_KEYS + kr;
+      const bool in = key < kend;
+      const size_t goff = (size_t)(in ? key : 0) * D + c * 8;
+      const uint32_t dk = smem_u32(sK + (buf * MT_KEYS + kr) * LD + c * 8);
+      const uint32_t dv = smem_u32(sV + (buf * MT_KEYS + kr) * LD + c * 8);
+      cp_async16(dk, kc + goff, in ? 16 : 0);
+      cp_async16(dv, vc + goff, in ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+
+  if (t_begin < t_end) load_tile(t_begin, 0);
+  for (int t = t_begin; t < t_end; ++t) {
+    const int buf = (t - t_begin) & 1;
+    if (t + 1 < t_end) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
+    else cp_async_wait<0>();
+    __syncthreads();
+    const __nv_bfloat16* K = sK + buf * MT_KEYS * LD;
+    const __nv_bfloat16* Vt = sV + buf * MT_KEYS * LD;
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const __nv_bfloat16* kr = K + (nt * 8 + (lane >> 2)) * LD + (lane & 3) * 2;
+#pragma unroll
+      for (int kt = 0; kt < D / 16; ++kt) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + kt * 16);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + kt * 16 + 8);
+        mma_bf16_16816(s[nt], qf[kt], b0, b1);
+      }
+    }
+    // mask, scale to the exp2 domain, running max
+    float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = t * MT_KEYS + nt * 8 + (lane & 3) * 2 + e;
+        s[nt][e] = visible(a, va, ctx, key) ? s[nt][e] * sl2 : -INFINITY;
+        s[nt][2 + e] = visible(a, vb, ctx, key) ? s[nt][2 + e] * sl2 : -INFINITY;
+        mx_a = fmaxf(mx_a, s[nt][e]);
+        mx_b = fmaxf(mx_b, s[nt][2 + e]);
+      }
+    }
+    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+    const float base_a = mn_a == -INFINITY ? 0.f : mn_a, base_b = mn_b == -INFINITY ? 0.f : mn_b;
+    const float corr_a = exp2f(m_a - base_a), corr_b = exp2f(m_b - base_b);
+    m_a = mn_a;
+    m_b = mn_b;
+    float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - base_a);
+      s[nt][1] = exp2f(s[nt][1] - base_a);
+      s[nt][2] = exp2f(s[nt][2] - base_b);
+      s[nt][3] = exp2f(s[nt][3] - base_b);
+      ps_a += s[nt][0] + s[nt][1];
+      ps_b += s[nt][2] + s[nt][3];
+    }
+    l_a = l_a * corr_a + ps_a;
+    l_b = l_b * corr_b + ps_b;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= corr_a; o[i][1] *= corr_a;
+      o[i][2] *= corr_b; o[i][3] *= corr_b;
+    }
+    // O += P V. P is split into a bf16 high part and a bf16 residual so that the product
+    // carries ~16 bits of P (a single bf16 P would perturb every attention output by up to
+    // 2^-9 relative, an error that then accumulates across the layers).
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t ph[4], pl[4];
+      split_bf16(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+      split_bf16(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+      split_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+      split_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+      const int mi = lane >> 3;
+      const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        uint32_t b[4];
+        ldsm_x4_trans(smem_u32(Vt + key * LD + dp * 16 + (mi >> 1) * 8), b);
+        mma_bf16_16816(o[2 * dp], ph, b[0], b[1]);
+        mma_bf16_16816(o[2 * dp + 1], ph, b[2], b[3]);
+        mma_bf16_16816(o[2 * dp], pl, b[0], b[1]);
+        mma_bf16_16816(o[2 * dp + 1], pl, b[2], b[3]);
+      }
+    }
+    __syncthreads();
+  }
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+  const int c = (lane & 3) * 2;
+  if (splits == 1) {
+    __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out);
+    const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      if (va.valid)
+        *reinterpret_cast<__nv_bfloat162*>(op + ((size_t)row_a * a.nq + head_a) * D + i * 8 + c) =
+            __floats2bfloat162_rn(o[i][0] * ia, o[i][1] * ia);
+      if (vb.valid)
+        *reinterpret_cast<__nv_bfloat162*>(op + ((size_t)row_b * a.nq + head_b) * D + i * 8 + c) =
+            __floats2bfloat162_rn(o[i][2] * ib, o[i][3] * ib);
+    }
+  } else {
+    const size_t sa = ((size_t)split * a.R + row_a) * a.nq + head_a;
+    const size_t sb = ((size_t)split * a.R + row_b) * a.nq + head_b;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      if (va.valid) *reinterpret_cast<float2*>(a.part_o + sa * D + i * 8 + c) = make_float2(o[i][0], o[i][1]);
+      if (vb.valid) *reinterpret_cast<float2*>(a.part_o + sb * D + i * 8 + c) = make_float2(o[i][2], o[i][3]);
+    }
+    if ((lane & 3) == 0) {
+      if (va.valid) { a.part_ml[sa * 2] = m_a; a.part_ml[sa * 2 + 1] = l_a; }
+      if (vb.valid) { a.part_ml[sb * 2] = m_b; a.part_ml[sb * 2 + 1] = l_b; }
+    }
+  }
+}
+
+// out[r][h] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), splits in order.
+template <int D>
+__global__ void attn_combine_k(AttnArgs a, int splits) {
+  PDL_ENTRY();
+  const int qi = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (qi >= a.R * a.nq) return;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, a.part_ml[((size_t)s * a.R * a.nq + qi) * 2]);
+  float L = 0.f;
+  float acc[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const size_t si = (size_t)s * a.R * a.nq + qi;
+    const float ms = a.part_ml[si * 2], ls = a.part_ml[si * 2 + 1];
+    if (ms == -INFINITY) continue;
+    const float w = exp2f(ms - M);
+    L += ls * w;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) acc[i] += a.part_o[si * D + lane + 32 * i] * w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) op[(size_t)qi * D + lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+}
+
+size_t attention_scratch_floats(int rows, int nq, int d) { return (size_t)16 * rows * nq * (d + 2); }
+
+template <int D>
+static int launch_mma(cudaStream_t st, const AttnArgs& a) {
+  const int G = a.nq / a.nkv;
+  const int RB = MT_QV / G;
+  const int nseq = (a.R + a.rows_per_seq - 1) / a.rows_per_seq;
+  const int nb = (a.rows_per_seq + RB - 1) / RB;
+  const int base = a.nkv * nseq * nb;
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  int splits = (2 * sms + base - 1) / base;
+  const int max_tiles = (a.cap + MT_KEYS - 1) / MT_KEYS;
+  splits = std::min(std::min(splits, 16), max_tiles);
+  while (splits > 1 && (size_t)splits * a.R * a.nq * D > a.part_floats) --splits;
+  if (!a.part_o || !a.part_ml) splits = 1;
+  if (splits < 1) splits = 1;
+  const size_t smem = (size_t)4 * MT_KEYS * (D + 8) * sizeof(__nv_bfloat16);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(attn_mma_k<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr = true;
+  }
+  launch_k(attn_mma_k<D>, dim3(a.nkv, nseq * nb, splits), 128, smem, st, a, splits);
+  if (splits > 1) launch_k(attn_combine_k<D>, (a.R * a.nq + 3) / 4, 128, 0, st, a, splits);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+int attention_bf16_mma(cudaStream_t st, const AttnArgs& a) {
+  const int G = a.nq / a.nkv;
+  if (G < 1 || G > MT_QV || MT_QV % G) return -1;
+  if (a.mode == 1 && (a.mask_words > 4 || a.tree_T > 256)) return -1;
+  switch (a.d) {
+    case 32: return launch_mma<32>(st, a);
+    case 64: return launch_mma<64>(st, a);
+    case 128: return launch_mma<128>(st, a);
+  }
+  return -1;
 }
 
 }  // namespace eagle

@@ -22,6 +22,18 @@ enum : int {
 // A wait that has not completed within this many nanoseconds is abandoned.
 #define EAGLE_WAIT_LIMIT_NS 2000000000ull
 
+// Programmatic dependent launch: every kernel waits for its predecessor grid (and so,
+// transitively, for all earlier ones) before reading their outputs or writing anything,
+// and lets its own dependents start launching right away. Both are no-ops for a launch
+// without the programmatic-serialization attribute.
+EAGLE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+EAGLE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#define PDL_ENTRY() \
+  do {              \
+    pdl_wait();     \
+    pdl_trigger();  \
+  } while (0)
+
 EAGLE_DEV void latch_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
@@ -157,6 +169,14 @@ EAGLE_DEV void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint3
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
+}
+
+// Bring one 2D tile of a tensor into L2 without touching shared memory.
+EAGLE_DEV void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 
 EAGLE_DEV uint64_t l2_policy_evict_first() {

@@ -82,7 +82,8 @@ int root_prepare(cudaStream_t st, const CycleDev& c, int rows_per_seq, int* root
 int root_candidates(cudaStream_t st, const CycleDev& c, const HeadOut& h, int advance);
 // plain decoding / prefill helpers
 int plain_rows(cudaStream_t st, const CycleDev& c, int* row_tok, int* row_pos, int* row_slot, int* row_seq);
-int plain_advance(cudaStream_t st, const CycleDev& c, const int* next_tok, int* out, int ld_out, int step);
+int plain_advance(cudaStream_t st, const CycleDev& c, const int* next_tok, int K, const float* top_val, int* out,
+                  float* margin, int ld_out, int step);
 int prefill_rows(cudaStream_t st, const int* prompt, int seq, int p0, int n, int last_tok_from_root,
                  const int* root_tok, int* row_tok, int* row_pos, int* row_slot, int* row_seq, int shift);
 int prefill_finish(cudaStream_t st, const CycleDev& c, int seq, int n, const int* first_tok);

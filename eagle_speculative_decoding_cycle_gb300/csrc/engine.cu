@@ -114,6 +114,11 @@ struct eagle_ctx {
   int ref_len = 0;
   int graph_enabled = 0;
   cudaGraphExec_t graph = nullptr;
+  const int32_t* graph_out = nullptr;   // output pointers baked into the captured graph
+  const int32_t* graph_cnt = nullptr;
+  const int32_t* graph_ref = nullptr;
+  int graph_batch = 0;
+  int graph_kernels = 0;                // kernel nodes of the captured cycle
   int debug = 0;
   // per-launch GEMM profiling (events around every tensor-core GEMM launch)
   std::vector<cudaEvent_t> prof_ev;
@@ -134,6 +139,7 @@ struct eagle_ctx {
   float *h_part, *h_val, *h_lse, *h_spec; int* h_id;        // drafter / root / plain heads
   float *v_val, *v_lse, *v_spec, *v_logits; int* v_id;       // verify head (kept for the cycle's dump)
   float* gemm_part; int* gemm_cnt; int gemm_cnt_len;
+  float *attn_po, *attn_pml; size_t attn_pfloats;
   float *rope_cos, *rope_sin;
   void *kc, *vc, *dkc, *dvc;
   int* prompt_copy;   // unused placeholder
@@ -189,6 +195,12 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
   x->gemm_part = c.take<float>(gemm_bf16_scratch_bytes() / sizeof(float));
   x->gemm_cnt_len = 65536;
   x->gemm_cnt = c.take<int>(x->gemm_cnt_len);
+  {
+    const int rs = std::max(std::max(z.B * z.T1, z.B * (z.D + 1)), z.B * z.k);
+    x->attn_pfloats = (size_t)16 * rs * z.nq * z.d;
+    x->attn_po = c.take<float>(x->attn_pfloats);
+    x->attn_pml = c.take<float>((size_t)16 * rs * z.nq * 2);
+  }
   x->rope_cos = c.take<float>((size_t)z.rope_pos * (z.d / 2));
   x->rope_sin = c.take<float>((size_t)z.rope_pos * (z.d / 2));
   x->kc = c.take<uint8_t>((size_t)z.L * B * z.nkv * z.cap * z.d * es);
@@ -282,6 +294,7 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   a.R = R; a.nq = z.nq; a.nkv = z.nkv; a.d = z.d; a.cap = cap; a.rows_per_seq = rows_per_seq;
   a.row_seq = seq; a.row_slot = slot; a.ctx_len = ctx->ctx_len; a.mode = mode; a.tree_T = tree_T;
   a.mask = mask; a.mask_words = mask_words; a.scale = 1.f / sqrtf((float)z.d);
+  a.part_o = ctx->attn_po; a.part_ml = ctx->attn_pml; a.part_floats = ctx->attn_pfloats;
   CK(attention(ctx->st, z.dt, a));
   CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
   CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
@@ -383,12 +396,14 @@ void fill_cd(eagle_ctx* ctx) {
 }
 
 __global__ void iota_k(int* p, int n) {
+  PDL_ENTRY();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = i;
 }
 
 // rows of the expansion outputs inside the [B][fsrc_rows][H] feature-source buffer
 __global__ void drow_out_k(int* out, int B, int k, int fsrc_rows, int d) {
+  PDL_ENTRY();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B * k) out[i] = (i / k) * fsrc_rows + 1 + (d - 1) * k + (i % k);
 }
@@ -406,7 +421,7 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
                             ctx->dmask, z.dmw, ctx->fsrc, ctx->drow_feat);
     if (r) return r;
     if (d + 1 < z.D) {
-      drow_out_k<<<(B * z.k + 127) / 128, 128, 0, ctx->st>>>(ctx->drow_out, B, z.k, z.fsrc_rows, d);
+      launch_k(drow_out_k, (B * z.k + 127) / 128, 128, 0, ctx->st, ctx->drow_out, B, z.k, z.fsrc_rows, d);
       CK(gather_rows(ctx->st, rb, ctx->dout, rb, nullptr, B * z.k, ctx->fsrc, rb, ctx->drow_out));
     }
     HeadParams p = head_params(ctx, B * z.k, z.k);
@@ -575,7 +590,7 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
     delete ctx;
     return EAGLE_ECUDA;
   }
-  iota_k<<<(std::max(z.B, z.R) + 127) / 128, 128, 0, ctx->st>>>(ctx->iota, std::max(z.B, z.R));
+  launch_k(iota_k, (std::max(z.B, z.R) + 127) / 128, 128, 0, ctx->st, ctx->iota, std::max(z.B, z.R));
   if (cudaStreamSynchronize(ctx->st) != cudaSuccess) { delete ctx; return EAGLE_ECUDA; }
   ctx->batch = z.B;
   fill_cd(ctx);
@@ -597,7 +612,11 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
   if (mx + z.D + 1 > z.max_ctx) return fail(ctx, EAGLE_ECAPACITY, "prompt longer than max_ctx allows");
   if (getenv("EAGLE_FAULT") && strcmp(getenv("EAGLE_FAULT"), "prefill") == 0)
     return fail(ctx, EAGLE_ECUDA, "injected prefill fault");
-  if (ctx->graph) { cudaGraphExecDestroy(ctx->graph); ctx->graph = nullptr; }
+  // the captured cycle bakes in the batch size and the reference pointer
+  if (ctx->graph && (ctx->graph_batch != batch || ctx->graph_ref != d_ref || ctx->ref_len != (d_ref ? ref_len : 0))) {
+    cudaGraphExecDestroy(ctx->graph);
+    ctx->graph = nullptr;
+  }
   ctx->batch = batch;
   ctx->ref_len = d_ref ? ref_len : 0;
   fill_cd(ctx);
@@ -679,9 +698,7 @@ int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count) {
     return fail(ctx, EAGLE_ECUDA, "injected cycle fault");
   ctx->host_ctx_bound += z.D + 1;
   if (ctx->graph_enabled) {
-    static thread_local int32_t* last_out = nullptr;
-    static thread_local int32_t* last_cnt = nullptr;
-    if (ctx->graph && (last_out != d_out_tokens || last_cnt != d_out_count)) {
+    if (ctx->graph && (ctx->graph_out != d_out_tokens || ctx->graph_cnt != d_out_count)) {
       cudaGraphExecDestroy(ctx->graph);
       ctx->graph = nullptr;
     }
@@ -693,11 +710,23 @@ int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count) {
       cudaError_t e = cudaStreamEndCapture(ctx->st, &g);
       if (r) return r;
       if (e != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "stream capture failed");
+      size_t nn = 0;
+      cudaGraphGetNodes(g, nullptr, &nn);
+      std::vector<cudaGraphNode_t> nodes(nn);
+      if (nn) cudaGraphGetNodes(g, nodes.data(), &nn);
+      int kn = 0;
+      for (auto n : nodes) {
+        cudaGraphNodeType ty;
+        if (cudaGraphNodeGetType(n, &ty) == cudaSuccess && ty == cudaGraphNodeTypeKernel) ++kn;
+      }
       e = cudaGraphInstantiate(&ctx->graph, g, 0);
       cudaGraphDestroy(g);
       if (e != cudaSuccess) { ctx->graph = nullptr; return fail(ctx, EAGLE_ECUDA, "graph instantiation failed"); }
-      last_out = d_out_tokens;
-      last_cnt = d_out_count;
+      ctx->graph_out = d_out_tokens;
+      ctx->graph_cnt = d_out_count;
+      ctx->graph_ref = ctx->cd.ref;
+      ctx->graph_batch = ctx->batch;
+      ctx->graph_kernels = kn;
     }
     if (cudaGraphLaunch(ctx->graph, ctx->st) != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "graph launch failed");
     return EAGLE_OK;
@@ -705,7 +734,7 @@ int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count) {
   return enqueue_cycle(ctx, d_out_tokens, d_out_count);
 }
 
-int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens) {
+int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens, float* d_out_margin) {
   if (!ctx) return EAGLE_EINVAL;
   const Dims& z = ctx->z;
   if (n_steps < 0) return fail(ctx, EAGLE_EINVAL, "n_steps must be >= 0");
@@ -718,7 +747,8 @@ int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens) {
     int r = target_forward(ctx, B, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, 1, 0, 0, nullptr, 0,
                            ctx->feat_t, nullptr, 0, 0);
     if (r) return r;
-    HeadParams p = head_params(ctx, B, 1);
+    // greedy keeps the top two (argmax and the top-2 margin); sampling keeps the Gumbel-argmax
+    HeadParams p = head_params(ctx, B, sampling ? 1 : 2);
     if (sampling) {
       p.inv_t = 1.f / ctx->tc.temperature;
       p.gumbel = 1;
@@ -729,11 +759,13 @@ int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens) {
     }
     r = lm_head(ctx, ctx->feat_t, B, p);
     if (r) return r;
-    CK(plain_advance(ctx->st, c, ctx->h_id, d_out_tokens, n_steps, s));
+    CK(plain_advance(ctx->st, c, ctx->h_id, p.K, ctx->h_val, d_out_tokens, d_out_margin, n_steps, s));
   }
   ctx->host_ctx_bound += n_steps;
   return EAGLE_OK;
 }
+
+int eagle_cycle_kernel_launches(const eagle_ctx* ctx) { return ctx ? ctx->graph_kernels : -1; }
 
 int eagle_set_graph(eagle_ctx* ctx, int enable) {
   if (!ctx) return EAGLE_EINVAL;
@@ -864,3 +896,14 @@ void eagle_destroy(eagle_ctx* ctx) {
 }
 
 }  // extern "C"
+
+namespace eagle {
+bool pdl_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("EAGLE_PDL");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+}  // namespace eagle

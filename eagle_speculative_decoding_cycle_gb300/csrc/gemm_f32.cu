@@ -11,6 +11,7 @@ constexpr int FT_M = 32, FT_N = 64, FT_K = 32;
 __global__ void __launch_bounds__(256) gemm_f32_k(const float* __restrict__ W, int N, int K,
                                                   const float* __restrict__ X, int M, int epi,
                                                   float* __restrict__ out, int ldo) {
+  PDL_ENTRY();
   __shared__ float xs[FT_M][FT_K + 1];
   __shared__ float ws[FT_N][FT_K + 1];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -57,7 +58,7 @@ int gemm_f32(cudaStream_t st, const float* W, int N, int K, const float* X, int 
   if (M <= 0 || N <= 0 || K <= 0) return -1;
   if (epi != EPI_F32 && epi != EPI_ADD_F32) return -1;
   dim3 grid((N + FT_N - 1) / FT_N, (M + FT_M - 1) / FT_M);
-  gemm_f32_k<<<grid, 256, 0, st>>>(W, N, K, X, M, epi, out, ldo);
+  launch_k(gemm_f32_k, grid, 256, 0, st, W, N, K, X, M, epi, out, ldo);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -151,7 +152,29 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, issued = 0, parity = 0;
-      for (long long u = u_begin; u < u_end; ++u) {
+      // The first ring of weight tiles does not depend on the previous kernel: issue it
+      // before waiting for that kernel, then add the activation halves of those stages
+      // once its outputs are visible.
+      const int n_pre = (int)min((long long)C::STAGES, u_end - u_begin);
+      for (int i = 0; i < n_pre; ++i) {
+        const long long u = u_begin + i;
+        const long long tile = u / a.kb;
+        const uint32_t fb = smem_u32(full + i);
+        mbar_expect_tx(fb, C::STAGE);
+        tma_load_2d(smem_u32(smem + i * C::STAGE), &tmW, (int)(u - tile * a.kb) * 64, (int)(tile / a.tiles_t) * 128,
+                    fb, pol_w);
+        issued |= 1u << i;
+      }
+      pdl_wait();
+      for (int i = 0; i < n_pre; ++i) {
+        const long long u = u_begin + i;
+        const long long tile = u / a.kb;
+        tma_load_2d(smem_u32(smem + i * C::STAGE) + C::A_BYTES, &tmX, (int)(u - tile * a.kb) * 64,
+                    (int)(tile % a.tiles_t) * BN, smem_u32(full + i), pol_x);
+      }
+      stage = n_pre % C::STAGES;
+      phase = (n_pre == C::STAGES) ? 1u : 0u;
+      for (long long u = u_begin + n_pre; u < u_end; ++u) {
         const long long tile = u / a.kb;
         const int kb = (int)(u - tile * a.kb);
         const int tn = (int)(tile / a.tiles_t), tt = (int)(tile % a.tiles_t);
@@ -207,6 +230,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
+    pdl_wait();
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -302,11 +326,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // bf16 row-major [rows][K] matrix, boxes of 64 (K) x box_rows, 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long K, int box_rows) {
+static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long K, int box_rows,
+                     bool use_cache = true) {
   static std::map<std::tuple<const void*, long long, long long, int>, CUtensorMap> cache;
   auto key = std::make_tuple(ptr, rows, K, box_rows);
-  auto it = cache.find(key);
-  if (it != cache.end()) { *m = it->second; return true; }
+  if (use_cache) {
+    auto it = cache.find(key);
+    if (it != cache.end()) { *m = it->second; return true; }
+  }
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
@@ -317,6 +344,7 @@ static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long 
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
+  if (!use_cache) return true;
   if (cache.size() > 4096) cache.clear();
   cache[key] = *m;
   return true;
@@ -359,20 +387,21 @@ static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmA
   int G = num_sms();
   if (G > num_sms_cap()) G = num_sms_cap();
   if ((long long)G > a.units) G = (int)a.units;
-  gemm_bf16_tc<BN><<<G, 192, C::SMEM, st>>>(mw, mx, a);
+  launch_k(gemm_bf16_tc<BN>, G, 192, C::SMEM, st, mw, mx, a);
   return cudaGetLastError();
 }
 
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
-              int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head) {
+              int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head,
+              bool cache_maps) {
   if (M <= 0 || N <= 0 || K <= 0 || (K % 8) != 0 || !W || !X) return -1;
   if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(X)) & 15) return -1;
   const int BN = gemm_bn_for(M);
   const int tiles_n = (N + 127) / 128;
   if ((long long)tiles_n * ((M + BN - 1) / BN) > counters_len) return -2;
   CUtensorMap mw, mx;
-  if (!make_map(&mw, W, N, K, 128)) return -3;
-  if (!make_map(&mx, X, M, K, BN)) return -3;
+  if (!make_map(&mw, W, N, K, 128, cache_maps)) return -3;
+  if (!make_map(&mx, X, M, K, BN, cache_maps)) return -3;
   GemmArgs a{};
   a.M = M; a.N = N; a.K = K; a.epi = epi; a.out = out; a.ldo = ldo;
   a.partials = partials; a.counters = counters; a.err = err;

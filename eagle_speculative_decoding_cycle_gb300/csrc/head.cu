@@ -10,6 +10,7 @@ namespace eagle {
 constexpr int HP_ROWS = 8;
 
 __global__ void __launch_bounds__(128) head_partials_k(const float* logits, int ld, HeadParams p) {
+  PDL_ENTRY();
   __shared__ float vals[HP_ROWS][128];
   const int tile = blockIdx.x;
   const int r0 = blockIdx.y * HP_ROWS;
@@ -27,6 +28,7 @@ __global__ void __launch_bounds__(128) head_partials_k(const float* logits, int 
 }
 
 __global__ void __launch_bounds__(128) head_merge_k(HeadParams p) {
+  PDL_ENTRY();
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row < p.n_rows) head_merge_row(p, row, threadIdx.x & 31);
 }
@@ -39,14 +41,14 @@ int head_partials_from_logits(cudaStream_t st, const float* logits, int ld, cons
   if (p.n_rows <= 0) return 0;
   if (p.K < 1 || p.K > 16) return -1;
   dim3 grid(p.n_tiles, (p.n_rows + HP_ROWS - 1) / HP_ROWS);
-  head_partials_k<<<grid, 128, 0, st>>>(logits, ld, p);
+  launch_k(head_partials_k, grid, 128, 0, st, logits, ld, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int head_merge(cudaStream_t st, const HeadParams& p) {
   if (p.n_rows <= 0) return 0;
   if (p.K < 1 || p.K > 16) return -1;
-  head_merge_k<<<(p.n_rows + 3) / 4, 128, 0, st>>>(p);
+  launch_k(head_merge_k, (p.n_rows + 3) / 4, 128, 0, st, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -9,6 +9,26 @@ struct HeadParams;
 
 namespace eagle {
 
+// Launch with programmatic stream serialization, so the kernel may begin launching while
+// its predecessor finishes (each kernel calls griddepcontrol.wait before touching data).
+// EAGLE_PDL=0 in the environment turns this off.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_ADD_F32 = 2, EPI_HEAD = 3 };
 enum { DT_F32 = 0, DT_BF16 = 1 };
 
@@ -19,7 +39,8 @@ int gemm_bn_for(int M);
 size_t gemm_bf16_scratch_bytes();
 // bf16 tcgen05 GEMM, Y[M][N] = X[M][K] W[N][K]^T. Returns 0 or a negative code.
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
-              int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head);
+              int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head,
+              bool cache_maps = true);
 // fp32 SIMT GEMM with the same contract (EPI_F32 / EPI_ADD_F32).
 int gemm_f32(cudaStream_t st, const float* W, int N, int K, const float* X, int M, int epi, float* out,
              int ldo);
@@ -62,8 +83,13 @@ struct AttnArgs {
   const uint64_t* mask; // [R][mask_words]
   int mask_words;
   float scale;
+  // split-KV scratch for the tensor-core path (bf16): partial outputs and (max, sum) pairs
+  float* part_o;        // [splits][R][nq][d]
+  float* part_ml;       // [splits][R][nq][2]
+  size_t part_floats;   // capacity of part_o in floats (splits are capped to fit)
 };
 int attention(cudaStream_t st, int dtype, const AttnArgs& a);
+size_t attention_scratch_floats(int rows, int nq, int d);
 
 // ---- tree policy, acceptance, compaction ---------------------------------------------------
 struct TreeState;   // defined in tree.cu / engine

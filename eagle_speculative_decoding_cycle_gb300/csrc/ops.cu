@@ -8,6 +8,7 @@ namespace eagle {
 
 template <typename T>
 __global__ void embed_k(const T* E, int V, int H, const int* tok, float* x, int* err) {
+  PDL_ENTRY();
   const int r = blockIdx.x;
   int t = tok[r];
   if (t < 0 || t >= V) {
@@ -21,34 +22,50 @@ __global__ void embed_k(const T* E, int V, int H, const int* tok, float* x, int*
 int embed_rows(cudaStream_t st, int dtype, const void* E, int V, int H, const int* tok, int R, float* x,
                int* err) {
   if (R <= 0) return 0;
-  if (dtype == DT_F32) embed_k<float><<<R, 256, 0, st>>>((const float*)E, V, H, tok, x, err);
-  else embed_k<__nv_bfloat16><<<R, 256, 0, st>>>((const __nv_bfloat16*)E, V, H, tok, x, err);
+  if (dtype == DT_F32) launch_k(embed_k<float>, R, 256, 0, st, (const float*)E, V, H, tok, x, err);
+  else launch_k(embed_k<__nv_bfloat16>, R, 256, 0, st, (const __nv_bfloat16*)E, V, H, tok, x, err);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-// out = x / sqrt(mean(x^2) + eps) * g, one block per row; fixed reduction order.
+// out = x / sqrt(mean(x^2) + eps) * g. One block per row; each thread keeps up to
+// RN_PER_THREAD elements of the row in registers, so the row is read once. Fixed
+// reduction order (per-thread sums, then a fixed warp/block tree).
+constexpr int RN_THREADS = 256;
+constexpr int RN_PER_THREAD = 24;   // rows up to 6144 elements stay in registers
+
 template <typename TX, typename TG, typename TO>
-__global__ void rmsnorm_k(const TX* x, int ldx, const TG* g, int H, float eps, TO* out, int ldo) {
+__global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, const TG* g, int H, float eps, TO* out,
+                                                        int ldo) {
+  PDL_ENTRY();
   const int r = blockIdx.x;
   const TX* xr = x + (size_t)r * ldx;
+  float v[RN_PER_THREAD];
   float s = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    const float v = Elem<TX>::to_f(xr[i]);
-    s += v * v;
+#pragma unroll
+  for (int j = 0; j < RN_PER_THREAD; ++j) {
+    const int i = threadIdx.x + j * RN_THREADS;
+    v[j] = i < H ? Elem<TX>::to_f(xr[i]) : 0.f;
+    s += v[j] * v[j];
   }
-  __shared__ float red[32];
+  for (int i = threadIdx.x + RN_PER_THREAD * RN_THREADS; i < H; i += RN_THREADS) {
+    const float t = Elem<TX>::to_f(xr[i]);
+    s += t * t;
+  }
+  __shared__ float red[RN_THREADS / 32];
   s = warp_sum(s);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-    t = warp_sum(t);
-    if (threadIdx.x == 0) red[0] = t;
-  }
-  __syncthreads();
-  const float rs = rsqrtf(red[0] / (float)H + eps);
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < RN_THREADS / 32; ++w) tot += red[w];
+  const float rs = rsqrtf(tot / (float)H + eps);
   TO* o = out + (size_t)r * ldo;
-  for (int i = threadIdx.x; i < H; i += blockDim.x)
+#pragma unroll
+  for (int j = 0; j < RN_PER_THREAD; ++j) {
+    const int i = threadIdx.x + j * RN_THREADS;
+    if (i < H) o[i] = Elem<TO>::from_f(v[j] * rs * Elem<TG>::to_f(g[i]));
+  }
+  for (int i = threadIdx.x + RN_PER_THREAD * RN_THREADS; i < H; i += RN_THREADS)
     o[i] = Elem<TO>::from_f(Elem<TX>::to_f(xr[i]) * rs * Elem<TG>::to_f(g[i]));
 }
 
@@ -58,54 +75,49 @@ int rmsnorm_rows(cudaStream_t st, int dtype_in, const void* x, int ldx, const vo
   // gains are stored in the model's storage type, which equals dtype_out
   if (dtype_out == DT_F32) {
     if (dtype_in != DT_F32) return -1;
-    rmsnorm_k<float, float, float><<<R, 256, 0, st>>>((const float*)x, ldx, (const float*)g, H, eps, (float*)out, ldo);
+    launch_k(rmsnorm_k<float, float, float>, R, RN_THREADS, 0, st, (const float*)x, ldx, (const float*)g, H, eps, (float*)out, ldo);
   } else if (dtype_in == DT_F32) {
-    rmsnorm_k<float, __nv_bfloat16, __nv_bfloat16><<<R, 256, 0, st>>>(
+    launch_k(rmsnorm_k<float, __nv_bfloat16, __nv_bfloat16>, R, RN_THREADS, 0, st, 
         (const float*)x, ldx, (const __nv_bfloat16*)g, H, eps, (__nv_bfloat16*)out, ldo);
   } else {
-    rmsnorm_k<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16><<<R, 256, 0, st>>>(
+    launch_k(rmsnorm_k<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>, R, RN_THREADS, 0, st, 
         (const __nv_bfloat16*)x, ldx, (const __nv_bfloat16*)g, H, eps, (__nv_bfloat16*)out, ldo);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-// Rotate-half RoPE on q and k of each row (angle table precomputed on the host in double
-// precision), q written to q_out, k and v written into the cache at the row's slot.
+// Rotate-half RoPE on q and k (angle table precomputed on the host in double precision);
+// q written to q_out, k and v into the cache at the row's slot. One block per (row, head)
+// of the fused [q | k | v] projection output, one thread per rotation pair.
 template <typename T>
-__global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int* row_pos,
-                             const int* row_slot, const int* row_seq, const float* rc, const float* rsn,
-                             T* q_out, T* kc, T* vc, int cap, int* err, int slot_limit) {
-  const int r = blockIdx.x;
+__global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int* row_pos, const int* row_slot,
+                             const int* row_seq, const float* rc, const float* rsn, T* q_out, T* kc, T* vc, int cap,
+                             int* err, int slot_limit) {
+  PDL_ENTRY();
+  const int r = blockIdx.x, h = blockIdx.y;
   const int half = d / 2;
-  const int pos = row_pos[r];
   const int slot = row_slot[r];
-  const int seq = row_seq[r];
   const bool slot_ok = slot >= 0 && slot < cap && slot < slot_limit;
-  if (!slot_ok && threadIdx.x == 0) latch_error(err, DEVERR_CAPACITY);
-  const float* src = qkv + (size_t)r * (nq + 2 * nkv) * d;
+  if (!slot_ok) {
+    if (h == 0 && threadIdx.x == 0) latch_error(err, DEVERR_CAPACITY);
+    if (h >= nq) return;
+  }
+  const float* src = qkv + (size_t)r * (nq + 2 * nkv) * d + (size_t)h * d;
+  const int seq = row_seq[r];
+  if (h >= nq + nkv) {   // value head: plain copy
+    T* v = vc + ((size_t)(seq * nkv + (h - nq - nkv)) * cap + slot) * d;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) v[i] = Elem<T>::from_f(src[i]);
+    return;
+  }
+  const int pos = row_pos[r];
   const float* cr = rc + (size_t)pos * half;
   const float* sr = rsn + (size_t)pos * half;
-  const int npairs = (nq + nkv) * half;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    const int h = p / half, i = p % half;
-    const float a = src[h * d + i], b = src[h * d + i + half];
+  T* dst = h < nq ? q_out + ((size_t)r * nq + h) * d : kc + ((size_t)(seq * nkv + (h - nq)) * cap + slot) * d;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    const float a = src[i], b = src[i + half];
     const float c = cr[i], s = sr[i];
-    const float o0 = a * c - b * s, o1 = b * c + a * s;
-    if (h < nq) {
-      T* q = q_out + (size_t)r * nq * d + h * d;
-      q[i] = Elem<T>::from_f(o0);
-      q[i + half] = Elem<T>::from_f(o1);
-    } else if (slot_ok) {
-      T* k = kc + ((size_t)(seq * nkv + (h - nq)) * cap + slot) * d;
-      k[i] = Elem<T>::from_f(o0);
-      k[i + half] = Elem<T>::from_f(o1);
-    }
-  }
-  if (slot_ok) {
-    for (int p = threadIdx.x; p < nkv * d; p += blockDim.x) {
-      const int h = p / d, i = p % d;
-      vc[((size_t)(seq * nkv + h) * cap + slot) * d + i] = Elem<T>::from_f(src[(nq + nkv) * d + p]);
-    }
+    dst[i] = Elem<T>::from_f(a * c - b * s);
+    dst[i + half] = Elem<T>::from_f(b * c + a * s);
   }
 }
 
@@ -114,30 +126,40 @@ int rope_store(cudaStream_t st, int dtype, const float* qkv, int R, int nq, int 
                const float* rope_sin, void* q_out, void* kcache, void* vcache, int cap, int* err,
                int slot_limit) {
   if (R <= 0) return 0;
+  dim3 grid(R, nq + 2 * nkv);
+  const int threads = d / 2 < 32 ? 32 : (d / 2 > 128 ? 128 : d / 2);
   if (dtype == DT_F32)
-    rope_store_k<float><<<R, 256, 0, st>>>(qkv, nq, nkv, d, row_pos, row_slot, row_seq, rope_cos, rope_sin,
-                                           (float*)q_out, (float*)kcache, (float*)vcache, cap, err, slot_limit);
+    launch_k(rope_store_k<float>, grid, threads, 0, st, qkv, nq, nkv, d, row_pos, row_slot, row_seq, rope_cos, rope_sin,
+                                                  (float*)q_out, (float*)kcache, (float*)vcache, cap, err, slot_limit);
   else
-    rope_store_k<__nv_bfloat16><<<R, 256, 0, st>>>(qkv, nq, nkv, d, row_pos, row_slot, row_seq, rope_cos,
-                                                   rope_sin, (__nv_bfloat16*)q_out, (__nv_bfloat16*)kcache,
-                                                   (__nv_bfloat16*)vcache, cap, err, slot_limit);
+    launch_k(rope_store_k<__nv_bfloat16>, grid, threads, 0, st, qkv, nq, nkv, d, row_pos, row_slot, row_seq, rope_cos,
+                                                          rope_sin, (__nv_bfloat16*)q_out, (__nv_bfloat16*)kcache,
+                                                          (__nv_bfloat16*)vcache, cap, err, slot_limit);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// h = silu(gate) * up over a 2D grid (row, 1024-element chunk), 4 elements per thread.
 template <typename T>
 __global__ void swiglu_k(const float* gu, int F, T* out) {
+  PDL_ENTRY();
   const int r = blockIdx.x;
   const float* g = gu + (size_t)r * 2 * F;
-  for (int i = threadIdx.x; i < F; i += blockDim.x) {
-    const float a = g[i];
-    out[(size_t)r * F + i] = Elem<T>::from_f(a / (1.f + expf(-a)) * g[F + i]);
+  const int i0 = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = i0 + j;
+    if (i < F) {
+      const float a = g[i];
+      out[(size_t)r * F + i] = Elem<T>::from_f(a / (1.f + expf(-a)) * g[F + i]);
+    }
   }
 }
 
 int swiglu_rows(cudaStream_t st, int dtype, const float* gu, int F, int R, void* out) {
   if (R <= 0) return 0;
-  if (dtype == DT_F32) swiglu_k<float><<<R, 256, 0, st>>>(gu, F, (float*)out);
-  else swiglu_k<__nv_bfloat16><<<R, 256, 0, st>>>(gu, F, (__nv_bfloat16*)out);
+  dim3 grid(R, (F + 1023) / 1024);
+  if (dtype == DT_F32) launch_k(swiglu_k<float>, grid, 256, 0, st, gu, F, (float*)out);
+  else launch_k(swiglu_k<__nv_bfloat16>, grid, 256, 0, st, gu, F, (__nv_bfloat16*)out);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
@@ -145,6 +167,7 @@ int swiglu_rows(cudaStream_t st, int dtype, const float* gu, int F, int R, void*
 template <typename T>
 __global__ void concat_k(const T* E, int V, int H, const int* tok, const T* feat, const int* feat_row, T* out,
                          int* err) {
+  PDL_ENTRY();
   const int r = blockIdx.x;
   int t = tok[r];
   if (t < 0 || t >= V) {
@@ -164,42 +187,45 @@ int concat_emb_feat(cudaStream_t st, int dtype, const void* E, int V, int H, con
                     const int* feat_row, int R, void* out, int* err) {
   if (R <= 0) return 0;
   if (dtype == DT_F32)
-    concat_k<float><<<R, 256, 0, st>>>((const float*)E, V, H, tok, (const float*)feat, feat_row, (float*)out, err);
+    launch_k(concat_k<float>, R, 256, 0, st, (const float*)E, V, H, tok, (const float*)feat, feat_row, (float*)out, err);
   else
-    concat_k<__nv_bfloat16><<<R, 256, 0, st>>>((const __nv_bfloat16*)E, V, H, tok, (const __nv_bfloat16*)feat,
+    launch_k(concat_k<__nv_bfloat16>, R, 256, 0, st, (const __nv_bfloat16*)E, V, H, tok, (const __nv_bfloat16*)feat,
                                                feat_row, (__nv_bfloat16*)out, err);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 template <typename T>
 __global__ void convert_k(const float* x, int H, T* out, int ldo) {
+  PDL_ENTRY();
   const int r = blockIdx.x;
   for (int i = threadIdx.x; i < H; i += blockDim.x) out[(size_t)r * ldo + i] = Elem<T>::from_f(x[(size_t)r * H + i]);
 }
 
 template <typename T>
 __global__ void widen_k(const T* x, int ldx, int H, float* out) {
+  PDL_ENTRY();
   const int r = blockIdx.x;
   for (int i = threadIdx.x; i < H; i += blockDim.x) out[(size_t)r * H + i] = Elem<T>::to_f(x[(size_t)r * ldx + i]);
 }
 
 int widen_rows(cudaStream_t st, int dtype, const void* x, int ldx, int H, int R, float* out) {
   if (R <= 0) return 0;
-  if (dtype == DT_F32) widen_k<float><<<R, 256, 0, st>>>((const float*)x, ldx, H, out);
-  else widen_k<__nv_bfloat16><<<R, 256, 0, st>>>((const __nv_bfloat16*)x, ldx, H, out);
+  if (dtype == DT_F32) launch_k(widen_k<float>, R, 256, 0, st, (const float*)x, ldx, H, out);
+  else launch_k(widen_k<__nv_bfloat16>, R, 256, 0, st, (const __nv_bfloat16*)x, ldx, H, out);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int convert_rows(cudaStream_t st, int dtype, const float* x, int H, int R, void* out, int ldo) {
   if (R <= 0) return 0;
-  if (dtype == DT_F32) convert_k<float><<<R, 256, 0, st>>>(x, H, (float*)out, ldo);
-  else convert_k<__nv_bfloat16><<<R, 256, 0, st>>>(x, H, (__nv_bfloat16*)out, ldo);
+  if (dtype == DT_F32) launch_k(convert_k<float>, R, 256, 0, st, x, H, (float*)out, ldo);
+  else launch_k(convert_k<__nv_bfloat16>, R, 256, 0, st, x, H, (__nv_bfloat16*)out, ldo);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 // dst row didx[r] <- src row sidx[r] (identity when an index is null); 16-byte words when aligned.
 __global__ void gather_k(const uint8_t* src, size_t src_ld, const int* sidx, size_t row_bytes, uint8_t* dst,
                          size_t dst_ld, const int* didx) {
+  PDL_ENTRY();
   const int r = blockIdx.x;
   const uint8_t* s = src + (size_t)(sidx ? sidx[r] : r) * src_ld;
   uint8_t* d = dst + (size_t)(didx ? didx[r] : r) * dst_ld;
@@ -214,7 +240,7 @@ __global__ void gather_k(const uint8_t* src, size_t src_ld, const int* sidx, siz
 int gather_rows(cudaStream_t st, size_t row_bytes, const void* src, size_t src_ld, const int* idx, int R,
                 void* dst, size_t dst_ld, const int* dst_idx) {
   if (R <= 0) return 0;
-  gather_k<<<R, 128, 0, st>>>((const uint8_t*)src, src_ld, idx, row_bytes, (uint8_t*)dst, dst_ld, dst_idx);
+  launch_k(gather_k, R, 128, 0, st, (const uint8_t*)src, src_ld, idx, row_bytes, (uint8_t*)dst, dst_ld, dst_idx);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -84,10 +84,15 @@ int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, co
   return head_merge(st, p) == 0 ? EAGLE_OK : EAGLE_ECUDA;
 }
 
+size_t eagle_op_attention_scratch_bytes(int R, int nq, int d) {
+  if (R <= 0 || nq <= 0 || d <= 0) return 0;
+  return al(attention_scratch_floats(R, nq, d) * sizeof(float));
+}
+
 int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcache, const void* vcache, void* out, int R,
                        int nq, int nkv, int d, int cap, int rows_per_seq, const int32_t* row_seq,
                        const int32_t* row_slot, const int32_t* ctx_len, int mode, int tree_T, const uint64_t* mask,
-                       int mask_words, float scale) {
+                       int mask_words, float scale, void* scratch, size_t scratch_bytes) {
   if (!q || !kcache || !vcache || !out || !row_seq || !row_slot || !ctx_len || R <= 0 || nq <= 0 || nkv <= 0 ||
       d <= 0 || d > 128 || nq % nkv || rows_per_seq <= 0 || (mode == 1 && (!mask || mask_words < 1)))
     return EAGLE_EINVAL;
@@ -96,6 +101,11 @@ int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcach
   a.R = R; a.nq = nq; a.nkv = nkv; a.d = d; a.cap = cap; a.rows_per_seq = rows_per_seq;
   a.row_seq = row_seq; a.row_slot = row_slot; a.ctx_len = ctx_len; a.mode = mode; a.tree_T = tree_T;
   a.mask = mask; a.mask_words = mask_words; a.scale = scale > 0.f ? scale : 1.f / sqrtf((float)d);
+  if (scratch && scratch_bytes >= eagle_op_attention_scratch_bytes(R, nq, d)) {
+    a.part_o = reinterpret_cast<float*>(scratch);
+    a.part_floats = (size_t)16 * R * nq * d;
+    a.part_ml = a.part_o + a.part_floats;
+  }
   const int r = attention(reinterpret_cast<cudaStream_t>(stream), dtype == EAGLE_DTYPE_F32 ? DT_F32 : DT_BF16, a);
   return r == 0 ? EAGLE_OK : (r == -1 ? EAGLE_EINVAL : EAGLE_ECUDA);
 }

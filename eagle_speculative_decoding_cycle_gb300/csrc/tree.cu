@@ -55,6 +55,7 @@ __device__ void compose_candidates(const HeadOut& h, int row, int special, bool 
 }
 
 __global__ void tree_start_k(CycleDev c) {
+  PDL_ENTRY();
   const int b = blockIdx.x;
   const int base = b * c.NG;
   for (int i = threadIdx.x; i < c.NG; i += blockDim.x) c.node_rank[base + i] = -1;
@@ -68,12 +69,13 @@ __global__ void tree_start_k(CycleDev c) {
 }
 
 int tree_start(cudaStream_t st, const CycleDev& c) {
-  tree_start_k<<<c.B, 128, 0, st>>>(c);
+  launch_k(tree_start_k, c.B, 128, 0, st, c);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 // Expansion at depth d: pick the k best depth-d nodes and lay out their drafter rows.
 __global__ void tree_select_k(CycleDev c, int d) {
+  PDL_ENTRY();
   const int b = blockIdx.x, lane = threadIdx.x;
   const int base = b * c.NG;
   const int k = c.k;
@@ -138,12 +140,13 @@ __global__ void tree_select_k(CycleDev c, int d) {
 
 int tree_select(cudaStream_t st, const CycleDev& c, int d) {
   if (c.k > 32 || c.k * c.k > 32 * 32) return -1;
-  tree_select_k<<<c.B, 32, 0, st>>>(c, d);
+  launch_k(tree_select_k, c.B, 32, 0, st, c, d);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 // Children of the depth-d expansion rows: log V_child = log V_parent + log c_child.
 __global__ void tree_add_k(CycleDev c, int d, HeadOut h) {
+  PDL_ENTRY();
   const int b = blockIdx.x, r = threadIdx.x;
   const int k = c.k;
   if (r >= k) return;
@@ -168,12 +171,13 @@ __global__ void tree_add_k(CycleDev c, int d, HeadOut h) {
 
 int tree_add(cudaStream_t st, const CycleDev& c, int d, const HeadOut& h) {
   if (c.k > 16) return -1;
-  tree_add_k<<<c.B, 32, 0, st>>>(c, d, h);
+  launch_k(tree_add_k, c.B, 32, 0, st, c, d, h);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 // Global top-m rerank and flattening.
 __global__ void tree_finalize_k(CycleDev c) {
+  PDL_ENTRY();
   extern __shared__ uint8_t sm[];
   const int NG = c.NG;
   uint64_t* key = reinterpret_cast<uint64_t*>(sm);
@@ -247,12 +251,13 @@ __global__ void tree_finalize_k(CycleDev c) {
 int tree_finalize(cudaStream_t st, const CycleDev& c) {
   if (c.m > c.NG) return -1;
   const size_t sm = (size_t)c.NG * (sizeof(uint64_t) + sizeof(int));
-  tree_finalize_k<<<c.B, 256, sm, st>>>(c);
+  launch_k(tree_finalize_k, c.B, 256, sm, st, c);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 // Row whose drafter output feeds the root's next candidates, and its planted token.
 __global__ void root_prepare_k(CycleDev c, int rows_per_seq, int* root_row) {
+  PDL_ENTRY();
   const int b = blockIdx.x;
   if (threadIdx.x) return;
   root_row[b] = b * rows_per_seq + c.acc_len[b];
@@ -265,13 +270,14 @@ __global__ void root_prepare_k(CycleDev c, int rows_per_seq, int* root_row) {
 }
 
 int root_prepare(cudaStream_t st, const CycleDev& c, int rows_per_seq, int* root_row) {
-  root_prepare_k<<<c.B, 32, 0, st>>>(c, rows_per_seq, root_row);
+  launch_k(root_prepare_k, c.B, 32, 0, st, c, rows_per_seq, root_row);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 // Depth-1 candidates of the root for the next cycle (`advance` = 1 after a cycle, 0 at
 // prefill); the planted draw is keyed by the cycle that will use them.
 __global__ void root_candidates_k(CycleDev c, HeadOut h, int seq_lo, int advance) {
+  PDL_ENTRY();
   const int b = seq_lo + blockIdx.x;
   const int row = blockIdx.x;
   if (threadIdx.x == 0) {
@@ -291,12 +297,12 @@ __global__ void root_candidates_k(CycleDev c, HeadOut h, int seq_lo, int advance
 }
 
 int root_candidates(cudaStream_t st, const CycleDev& c, const HeadOut& h, int advance) {
-  root_candidates_k<<<c.B, 32, 0, st>>>(c, h, 0, advance);
+  launch_k(root_candidates_k, c.B, 32, 0, st, c, h, 0, advance);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int root_candidates_seq(cudaStream_t st, const CycleDev& c, const HeadOut& h, int seq) {
-  root_candidates_k<<<1, 32, 0, st>>>(c, h, seq, 0);
+  launch_k(root_candidates_k, 1, 32, 0, st, c, h, seq, 0);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

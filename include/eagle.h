@@ -134,12 +134,17 @@ int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count);
 
 /* Plain (non-speculative) decoding of n_steps tokens per sequence from the current
  * state, one target pass per token: the lossless comparator and the speedup
- * baseline. d_out_tokens: device int32 [batch][n_steps]. */
-int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens);
+ * baseline. d_out_tokens: device int32 [batch][n_steps]. d_out_margin (nullable):
+ * device float [batch][n_steps], the top-2 logit margin of each greedy pick (NaN
+ * when sampling), used to tell near-ties from real disagreements. */
+int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens, float* d_out_margin);
 
 /* Capture eagle_cycle into a CUDA graph on first use and replay it afterwards
  * (enable = 1), or launch kernels directly (enable = 0, the default). */
 int eagle_set_graph(eagle_ctx* ctx, int enable);
+
+/* Kernel launches one captured cycle replays (0 before the first captured cycle). */
+int eagle_cycle_kernel_launches(const eagle_ctx* ctx);
 
 /* Synchronise the context's stream and report latched device errors (clears them).
  * It also refreshes the host's bound on the sequences' KV lengths, which eagle_cycle

@@ -51,11 +51,16 @@ int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, co
  * row_seq[r] and its own key sits at slot row_slot[r]. mode 0 (causal): row r sees
  * slots <= row_slot[r]. mode 1 (tree): row r sees slots < ctx_len[seq] and slot
  * ctx_len[seq] + t for t < tree_T where bit t of mask[r][t / 64] is set.
- * Scale = 1/sqrt(d) when scale <= 0. d <= 128, nq a multiple of nkv. */
+ * Scale = 1/sqrt(d) when scale <= 0. fp32: d <= 128; bf16 (tensor cores): d in {32, 64,
+ * 128}, 64 divisible by nq/nkv, tree_T <= 256. Scratch (nullable) enables split-KV on
+ * the bf16 path: the key range is cut across CTAs and merged by a fixed-order
+ * log-sum-exp combine. */
+size_t eagle_op_attention_scratch_bytes(int R, int nq, int d);
 int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcache, const void* vcache,
                        void* out, int R, int nq, int nkv, int d, int cap, int rows_per_seq,
                        const int32_t* row_seq, const int32_t* row_slot, const int32_t* ctx_len, int mode,
-                       int tree_T, const uint64_t* mask, int mask_words, float scale);
+                       int tree_T, const uint64_t* mask, int mask_words, float scale, void* scratch,
+                       size_t scratch_bytes);
 
 /* EAGLE-2 tree growth and rerank with injected draft confidences, for B sequences:
  * cand_tok/cand_logc [B][k]: the root's children (token, log confidence) in rank order;

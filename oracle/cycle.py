@@ -264,9 +264,11 @@ class OracleSeq:
         return o
 
 
-def plain_decode(model: Model, wl, prompt: Sequence[int], steps: int, seq: int = 0) -> List[int]:
+def plain_decode(model: Model, wl, prompt: Sequence[int], steps: int, seq: int = 0, margins: Optional[list] = None) \
+        -> List[int]:
     """Plain autoregressive decoding of the target: the prefill token then `steps - 1`
-    one-token passes. Greedy (argmax, lowest id on ties) or Gumbel-argmax sampling."""
+    one-token passes. Greedy (argmax, lowest id on ties) or Gumbel-argmax sampling.
+    If `margins` is a list, the top-2 logit margin of every greedy pick is appended to it."""
     s = wl.model
     prompt = np.asarray(prompt, dtype=np.int64)
     n = len(prompt)
@@ -278,6 +280,9 @@ def plain_decode(model: Model, wl, prompt: Sequence[int], steps: int, seq: int =
     T = wl.tree.temperature
 
     def pick(lrow, cycle, stream):
+        if margins is not None:
+            top = np.sort(lrow)[-2:]
+            margins.append(float(top[1] - top[0]))
         if T == 0.0:
             return argmax_lowest(lrow)
         g = philox.gumbel_row(wl.seed, stream, seq, cycle, 0, lrow.shape[0])

@@ -161,27 +161,78 @@ def test_small_bf16_lockstep_and_lossless():
     assert st["max_logit_err"] < 5e-2
 
 
-def test_small_bf16_spec_equals_gpu_plain():
-    wl = synth.SMALL_BF16.replace(new_tokens=48)
-    weights, M, prompt, R, eng = setup(wl)
-    eng.prefill([prompt.to(DEV)])
+NEAR_TIE = 1e-2
+
+
+def _first_diff(a, b):
+    n = min(len(a), len(b))
+    return next((i for i in range(n) if a[i] != b[i]), n)
+
+
+@pytest.mark.parametrize("wl", [synth.SMALL_BF16.replace(new_tokens=48),
+                                synth.SMALL_BF16_E3.replace(tree=synth.TreeShape(topk=4, depth=5, m=14,
+                                                                                 planted_p=0.8), new_tokens=40)])
+def test_bf16_spec_equals_gpu_plain_up_to_near_ties(wl):
+    """Greedy speculative output equals the GPU's own plain greedy decoding, except where
+    the plain decode's top-2 margin is below 1e-2; each such divergence is counted and the
+    run is re-prefilled with the common prefix and continued."""
+    weights = synth.make_weights(wl, "cpu")
+    prompt = synth.make_prompts(wl)[0].tolist()
     n = wl.new_tokens
-    plain = torch.zeros(1, n, dtype=torch.int32, device=DEV)
-    first = int(eng.dump(L.DUMP_STATE)["root_tok"][0])
-    eng.decode_plain(n - 1, plain)
-    eng.sync()
-    gp = [first] + plain[0, :n - 1].tolist()
-    ref = torch.tensor([gp + [0] * (wl.tree.depth + 2)], dtype=torch.int32, device=DEV)
-    eng.prefill([prompt.to(DEV)], ref)
     D = wl.tree.depth
+    eng = api.Engine(wl, {k: v.to(DEV) for k, v in weights.items()}, max_ctx=len(prompt) + 4 * n + 64)
     out = torch.zeros(1, D + 1, dtype=torch.int32, device=DEV)
     cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
-    got = [int(eng.dump(L.DUMP_STATE)["root_tok"][0])]
-    while len(got) < n:
-        eng.cycle(out, cnt)
-        got += out[0, :int(cnt[0])].tolist()
+    prefix, total, divergences, rounds = list(prompt), [], 0, 0
+    while len(total) < n and rounds < 20:
+        rounds += 1
+        need = n - len(total)
+        p_d = torch.tensor(prefix, dtype=torch.int32, device=DEV)
+        eng.prefill([p_d])
+        plain = torch.zeros(1, need + D + 2, dtype=torch.int32, device=DEV)
+        marg = torch.zeros(1, need + D + 2, dtype=torch.float32, device=DEV)
+        first = int(eng.dump(L.DUMP_STATE)["root_tok"][0])
+        eng.decode_plain(need + D + 1, plain, marg)
+        eng.sync()
+        gp = [first] + plain[0, :need + D + 1].tolist()
+        gm = [float("inf")] + marg[0, :need + D + 1].tolist()
+        eng.prefill([p_d], torch.tensor([gp], dtype=torch.int32, device=DEV))
+        got = [int(eng.dump(L.DUMP_STATE)["root_tok"][0])]
+        while len(got) < need:
+            eng.cycle(out, cnt)
+            eng.sync()
+            got += out[0, :int(cnt[0])].tolist()
+            if _first_diff(got, gp) < len(got):
+                break
+        i = _first_diff(got, gp)
+        if i >= need:
+            total += got[:need]
+            break
+        assert gm[i] < NEAR_TIE, f"divergence at {len(total) + i} with plain margin {gm[i]}"
+        divergences += 1
+        total += gp[:i + 1]
+        prefix += gp[:i + 1]
+    assert len(total) >= n
+    eng.close()
+    print(f"near-tie divergences: {divergences}")
+
+
+def test_bf16_plain_decode_matches_oracle_up_to_near_ties():
+    wl = synth.SMALL_BF16
+    weights = synth.make_weights(wl, "cpu")
+    M = build_model(synth.weights_to_numpy(weights), wl)
+    prompt = synth.make_prompts(wl)[0]
+    margins = []
+    R = plain_decode(M, wl, prompt.numpy(), 40, margins=margins)
+    eng = api.Engine(wl, {k: v.to(DEV) for k, v in weights.items()})
+    eng.prefill([prompt.to(DEV)])
+    out = torch.zeros(1, 39, dtype=torch.int32, device=DEV)
+    first = int(eng.dump(L.DUMP_STATE)["root_tok"][0])
+    eng.decode_plain(39, out)
     eng.sync()
-    assert got[:n] == gp[:n]
+    got = [first] + out[0].tolist()
+    i = _first_diff(got, R)
+    assert i == len(R) or margins[i] < NEAR_TIE, (i, margins[i])
     eng.close()
 
 

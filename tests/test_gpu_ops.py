@@ -266,3 +266,37 @@ def test_compaction_bit_exact(dtype):
     api.compact(kd, vd, n_old.to(DEV), acc_len.to(DEV), acc_path.to(DEV))
     assert np.array_equal(kd.cpu().float().numpy(), k_ref)
     assert np.array_equal(vd.cpu().float().numpy(), v_ref)
+
+
+@pytest.mark.parametrize("nq,nkv,T,ctx", [(40, 40, 49, 4100), (32, 8, 61, 1300), (32, 32, 1, 700)])
+def test_attention_split_kv_long_context(nq, nkv, T, ctx):
+    """Long-context tree/causal attention (split-KV with the log-sum-exp combine) equals the
+    oracle, and equals the single-split result within bf16 output rounding."""
+    g = torch.Generator().manual_seed(ctx)
+    rng = np.random.default_rng(ctx)
+    d, cap = 128, ctx + T + 8
+    kc = _rand((1, nkv, cap, d), g, torch.bfloat16)
+    vc = _rand((1, nkv, cap, d), g, torch.bfloat16)
+    q = _rand((T, nq, d), g, torch.bfloat16)
+    parent = [-1] + [int(rng.integers(0, i)) for i in range(1, T)]
+    m = np.zeros((T, T), dtype=bool)
+    for i in range(T):
+        a = i
+        while a >= 0:
+            m[i, a] = True
+            a = parent[a]
+    mask = _mask_words(m).to(DEV)
+    ctx_len = torch.tensor([ctx], dtype=torch.int32, device=DEV)
+    row_seq = torch.zeros(T, dtype=torch.int32, device=DEV)
+    row_slot = (ctx + torch.arange(T, dtype=torch.int32)).to(DEV)
+    args = (q.to(DEV), kc.to(DEV), vc.to(DEV), row_seq, row_slot, ctx_len, T, 1, T, mask)
+    split = api.attention(*args).cpu().double().numpy()
+    single = api.attention(*args, split_kv=False).cpu().double().numpy()
+    vis = np.zeros((T, ctx + T), dtype=bool)
+    vis[:, :ctx] = True
+    vis[:, ctx:] = m
+    want = oracle_attention(q.double().numpy(), kc[0, :, :ctx + T].double().numpy(),
+                            vc[0, :, :ctx + T].double().numpy(), vis)
+    assert np.max(np.abs(split - want)) < 2e-2
+    assert np.max(np.abs(single - want)) < 2e-2
+    assert np.max(np.abs(split - single)) < 2e-2
