@@ -26,7 +26,7 @@ EXPORTED = [
     "eagle_workspace_bytes", "eagle_create", "eagle_prefill", "eagle_cycle", "eagle_decode_plain",
     "eagle_set_graph", "eagle_cycle_kernel_launches", "eagle_status_sync", "eagle_dump_bytes", "eagle_debug_dump", "eagle_set_debug",
     "eagle_kv_view", "eagle_profile_begin", "eagle_profile_end", "eagle_last_error", "eagle_destroy",
-    "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
+    "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_gemm_noalloc", "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
     "eagle_op_attention_scratch_bytes", "eagle_op_attention", "eagle_op_tree_scratch_bytes", "eagle_op_tree_build", "eagle_op_compact",
 ]
 
@@ -86,6 +86,7 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_destroy": (None, [vp]),
         "eagle_op_gemm_scratch_bytes": (sz, [i32, i32]),
         "eagle_op_gemm": (i32, [i32, vp, vp, i32, i32, vp, i32, i32, vp, i32, vp, sz]),
+        "eagle_op_gemm_noalloc": (i32, [vp, vp, i32, i32, vp, i32, i32, vp, i32]),
         "eagle_op_lm_head_scratch_bytes": (sz, [i32, i32, i32, i32]),
         "eagle_op_lm_head": (i32, [i32, vp, vp, i32, i32, vp, i32, i32, f32, i32, i32, vp, i32, vp, vp, vp, u32,
                                    u64, i32, vp, vp, vp, vp, sz]),

@@ -29,6 +29,22 @@ size_t eagle_op_gemm_scratch_bytes(int M, int N);
 int eagle_op_gemm(int dtype, void* stream, const void* W, int N, int K, const void* X, int M, int epi,
                   void* out, int ldo, void* scratch, size_t scratch_bytes);
 
+/* Allocation-free variant of eagle_op_gemm (bf16 only) for callers that cannot
+ * allocate device memory where they run a projection, e.g. plugins of a host framework
+ * that hands them only input and output buffers, or runtimes that pool all device
+ * memory in advance. The paper has no counterpart: this is a deployment convenience.
+ * Its split-tile scratch lives in file-scope device arrays of the library (about 6 MiB
+ * on every GPU that loads it, held until the process exits), so the call allocates
+ * nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ * Limits: M <= 32 rows and at most 8192 output tiles (ceil(N/128) tiles for M <= 32);
+ * larger requests return EAGLE_ECAPACITY. epi as eagle_op_gemm (0, 1 or 2).
+ * The first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture. All calls
+ * share the one scratch area and the last call's contents remain in it: calls that may
+ * overlap on the GPU (different streams without ordering) race and must not be issued. */
+int eagle_op_gemm_noalloc(void* stream, const void* W, int N, int K, const void* X, int M, int epi, void* out,
+                          int ldo);
+
 /* Fused LM head: logits = X[M][H] * W_lm[V][H]^T reduced per row without writing the
  * logits (bf16), or through an fp32 logits buffer inside the scratch (f32). Per row it
  * returns the K best entries by ranking value (value desc, token id asc) and the
