@@ -244,7 +244,9 @@ def run_ours(args, ws, rank, local):
             ref += out_d[0, :int(cnt_d[0])].tolist()
         n_cyc = W + K + args.prof_steps + 4
         ref_iters = 0
-        for ref_iters in range(1, 12):
+        # under sampling the committed tokens follow the draws, so the reference cannot be
+        # a fixed point beyond the first non-greedy draw (planting then goes inert)
+        for ref_iters in range(1, 12 if t.temperature == 0.0 else 2):
             rb = torch.tensor([ref[:n_ref]], dtype=torch.int32, device=dev)
             eng.prefill([prompt_d], rb)
             got = [ref[0]]

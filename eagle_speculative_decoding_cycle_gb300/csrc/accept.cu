@@ -211,6 +211,47 @@ __global__ void prefill_finish_k(CycleDev c, int seq, int n, const int* first_to
   c.root_plant[seq] = (c.ref && on && 1 < c.ref_len) ? c.ref[(size_t)seq * c.ref_len + 1] : -1;
 }
 
+// Batched prefill rows for B equal-length prompts (row b * n + p): shift as above.
+__global__ void prefill_rows_batched_k(const int* tokens, int B, int n, int shift, const int* root_tok, int* row_tok,
+                                       int* row_pos, int* row_slot, int* row_seq) {
+  PDL_ENTRY();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * n) return;
+  const int b = i / n, p = i % n;
+  row_tok[i] = shift ? (p + 1 < n ? tokens[b * n + p + 1] : root_tok[b]) : tokens[b * n + p];
+  row_pos[i] = p;
+  row_slot[i] = p;
+  row_seq[i] = b;
+}
+
+int prefill_rows_batched(cudaStream_t st, const int* tokens, int B, int n, int shift, const int* root_tok,
+                         int* row_tok, int* row_pos, int* row_slot, int* row_seq) {
+  launch_k(prefill_rows_batched_k, (B * n + 127) / 128, 128, 0, st, tokens, B, n, shift, root_tok, row_tok, row_pos,
+           row_slot, row_seq);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+__global__ void prefill_finish_batched_k(CycleDev c, int n, const int* first_tok, int K) {
+  PDL_ENTRY();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= c.B) return;
+  const int t = first_tok[b * K];
+  c.root_tok[b] = t;
+  c.committed[b] = 1;
+  const int on = c.ref ? (c.ref_len > 0 && c.ref[(size_t)b * c.ref_len] == t) : 1;
+  c.on_track[b] = on;
+  c.ctx_len[b] = n;
+  c.n_old[b] = n;
+  c.acc_len[b] = 0;
+  c.cycle[b] = 0;
+  c.root_plant[b] = (c.ref && on && 1 < c.ref_len) ? c.ref[(size_t)b * c.ref_len + 1] : -1;
+}
+
+int prefill_finish_batched(cudaStream_t st, const CycleDev& c, int n, const int* first_tok, int K) {
+  launch_k(prefill_finish_batched_k, (c.B + 127) / 128, 128, 0, st, c, n, first_tok, K);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
 int prefill_finish(cudaStream_t st, const CycleDev& c, int seq, int n, const int* first_tok) {
   launch_k(prefill_finish_k, 1, 32, 0, st, c, seq, n, first_tok);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;

@@ -87,5 +87,8 @@ int plain_advance(cudaStream_t st, const CycleDev& c, const int* next_tok, int K
 int prefill_rows(cudaStream_t st, const int* prompt, int seq, int p0, int n, int last_tok_from_root,
                  const int* root_tok, int* row_tok, int* row_pos, int* row_slot, int* row_seq, int shift);
 int prefill_finish(cudaStream_t st, const CycleDev& c, int seq, int n, const int* first_tok);
+int prefill_rows_batched(cudaStream_t st, const int* tokens, int B, int n, int shift, const int* root_tok,
+                         int* row_tok, int* row_pos, int* row_slot, int* row_seq);
+int prefill_finish_batched(cudaStream_t st, const CycleDev& c, int n, const int* first_tok, int K);
 
 }  // namespace eagle

@@ -489,6 +489,59 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   return 0;
 }
 
+// Prefill of B equal-length prompts in one batched pass (rows b * n + p), used when all of
+// them fit the activation buffers at once.
+int prefill_batched(eagle_ctx* ctx, int B, int n, const int* tokens) {
+  const Dims& z = ctx->z;
+  CycleDev& c = ctx->cd;
+  const size_t rb = (size_t)z.H * z.esz;
+  const int R = B * n;
+  CK(prefill_rows_batched(ctx->st, tokens, B, n, 0, ctx->root_tok, ctx->row_tok, ctx->row_pos, ctx->row_slot,
+                          ctx->row_seq));
+  int r = target_forward(ctx, R, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, n, 0, 0, nullptr, 0,
+                         ctx->feat_t, ctx->caps, (size_t)z.Rt, 0);
+  if (r) return r;
+  // first generated token of every sequence from its last row
+  CK(gather_rows(ctx->st, rb, (const uint8_t*)ctx->feat_t + (size_t)(n - 1) * rb, (size_t)n * rb, nullptr, B,
+                 ctx->ebuf, rb));
+  const bool sampling = ctx->tc.temperature > 0.f;
+  HeadParams p = head_params(ctx, B, 1);
+  if (sampling) {
+    p.inv_t = 1.f / ctx->tc.temperature;
+    p.gumbel = 1;
+    p.row_seq = ctx->iota;
+    p.key_mod = 1;
+    p.cycle_const = PREFILL_CYCLE;
+  }
+  r = lm_head(ctx, ctx->ebuf, B, p);
+  if (r) return r;
+  CK(prefill_finish_batched(ctx->st, c, n, ctx->h_id, 1));
+  // drafter over the prompt positions (token advanced by one step)
+  CK(prefill_rows_batched(ctx->st, tokens, B, n, 1, ctx->root_tok, ctx->row_tok, ctx->row_pos, ctx->row_slot,
+                          ctx->row_seq));
+  if (z.kind == 1) {
+    r = drafter_forward(ctx, R, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, n, 0, 0, nullptr, 0,
+                        ctx->feat_t, ctx->iota);
+  } else {
+    r = fuse_rows(ctx, ctx->caps, (size_t)z.Rt, nullptr, R);
+    if (r) return r;
+    r = drafter_forward(ctx, R, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, n, 0, 0, nullptr, 0,
+                        ctx->gbuf, nullptr);
+  }
+  if (r) return r;
+  const uint8_t* last = (const uint8_t*)ctx->dout + (size_t)(n - 1) * rb;
+  CK(gather_rows(ctx->st, rb, last, (size_t)n * rb, nullptr, B, ctx->fsrc, (size_t)z.fsrc_rows * rb));
+  CK(gather_rows(ctx->st, rb, last, (size_t)n * rb, nullptr, B, ctx->ebuf, rb));
+  HeadParams q = head_params(ctx, B, z.k);
+  q.lse_excl = 1;
+  q.specials = ctx->root_plant;
+  q.S = 1;
+  r = lm_head(ctx, ctx->ebuf, B, q);
+  if (r) return r;
+  CK(root_candidates(ctx->st, c, head_out(ctx, z.k, 1), 0));
+  return 0;
+}
+
 int check_dev_error(eagle_ctx* ctx) {
   int h[4] = {0, 0, 0, 0};
   std::vector<int> lens(ctx->batch > 0 ? ctx->batch : 1, 0);
@@ -624,6 +677,14 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
   ctx->cd.ref_len = ctx->ref_len;
   CycleDev& c = ctx->cd;
   const size_t rb = (size_t)z.H * z.esz;
+  bool uniform = true;
+  for (int b = 1; b < batch; ++b) uniform = uniform && h_lens[b] == h_lens[0];
+  if (batch > 1 && uniform && (long long)batch * h_lens[0] <= std::min(z.Rt, z.Rd)) {
+    const int r = prefill_batched(ctx, batch, h_lens[0], d_tokens);
+    if (r) return r;
+    ctx->host_ctx_bound = mx;
+    return EAGLE_OK;
+  }
   long long off = 0;
   for (int b = 0; b < batch; ++b) {
     const int n = h_lens[b];
