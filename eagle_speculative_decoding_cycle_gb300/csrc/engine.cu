@@ -17,6 +17,7 @@
 #include "../../include/eagle.h"
 #include "common.cuh"
 #include "cycle.h"
+#include "chain.h"
 #include "kernels.h"
 #include "lmhead.cuh"
 
@@ -140,6 +141,8 @@ struct eagle_ctx {
   float *v_val, *v_lse, *v_spec, *v_logits; int* v_id;       // verify head (kept for the cycle's dump)
   float* gemm_part; int* gemm_cnt; int gemm_cnt_len;
   float *attn_po, *attn_pml; size_t attn_pfloats;
+  unsigned* chain_bar;                  // grid-barrier words of the layer-chain kernel
+  int use_chain = 0;                    // bf16: run each layer as chain launches (EAGLE_CHAIN=1 turns them on)
   float *rope_cos, *rope_sin;
   void *kc, *vc, *dkc, *dvc;
   int* prompt_copy;   // unused placeholder
@@ -201,6 +204,7 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
     x->attn_po = c.take<float>(x->attn_pfloats);
     x->attn_pml = c.take<float>((size_t)16 * rs * z.nq * 2);
   }
+  x->chain_bar = c.take<unsigned>(4);
   x->rope_cos = c.take<float>((size_t)z.rope_pos * (z.d / 2));
   x->rope_sin = c.take<float>((size_t)z.rope_pos * (z.d / 2));
   x->kc = c.take<uint8_t>((size_t)z.L * B * z.nkv * z.cap * z.d * es);
@@ -281,14 +285,11 @@ int lm_head(eagle_ctx* ctx, const void* X, int M, HeadParams& p, float* logits_b
   return 0;
 }
 
-// One decoder layer over R rows. attn_in: rounded QKV input [R][kin]; x: fp32 residual.
-int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const void* attn_in, int kin, void* kcache,
-                  void* vcache, int cap, int rows_per_seq, const int* pos, const int* slot, const int* seq, int mode,
-                  int tree_T, const uint64_t* mask, int mask_words) {
+// Self-attention of one layer over R rows (q in ctx->qb, keys/values already in the cache)
+// into ctx->att.
+int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_per_seq, const int* slot,
+           const int* seq, int mode, int tree_T, const uint64_t* mask, int mask_words) {
   const Dims& z = ctx->z;
-  CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_F32, ctx->qkv, z.QKV));
-  CK(rope_store(ctx->st, z.dt, ctx->qkv, R, z.nq, z.nkv, z.d, pos, slot, seq, ctx->rope_cos, ctx->rope_sin, ctx->qb,
-                kcache, vcache, cap, ctx->dev_err, cap));
   AttnArgs a{};
   a.q = ctx->qb; a.kcache = kcache; a.vcache = vcache; a.out = ctx->att;
   a.R = R; a.nq = z.nq; a.nkv = z.nkv; a.d = z.d; a.cap = cap; a.rows_per_seq = rows_per_seq;
@@ -296,11 +297,145 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   a.mask = mask; a.mask_words = mask_words; a.scale = 1.f / sqrtf((float)z.d);
   a.part_o = ctx->attn_po; a.part_ml = ctx->attn_pml; a.part_floats = ctx->attn_pfloats;
   CK(attention(ctx->st, z.dt, a));
+  return 0;
+}
+
+// One decoder layer over R rows with per-op launches. attn_in: rounded QKV input
+// [R][kin]; x: fp32 residual.
+int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const void* attn_in, int kin, void* kcache,
+                  void* vcache, int cap, int rows_per_seq, const int* pos, const int* slot, const int* seq, int mode,
+                  int tree_T, const uint64_t* mask, int mask_words) {
+  const Dims& z = ctx->z;
+  CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_F32, ctx->qkv, z.QKV));
+  CK(rope_store(ctx->st, z.dt, ctx->qkv, R, z.nq, z.nkv, z.d, pos, slot, seq, ctx->rope_cos, ctx->rope_sin, ctx->qb,
+                kcache, vcache, cap, ctx->dev_err, cap));
+  int r = attend(ctx, kcache, vcache, cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words);
+  if (r) return r;
   CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
   CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
   CK(gemm(ctx, lw.wgu, 2 * z.F, z.H, ctx->ain, R, EPI_F32, ctx->gu, 2 * z.F));
   CK(swiglu_rows(ctx->st, z.dt, ctx->gu, z.F, R, ctx->hb));
   CK(gemm(ctx, lw.wd, z.H, z.F, ctx->hb, R, EPI_ADD_F32, ctx->x, z.H));
+  return 0;
+}
+
+// ---- layer chains (bf16): each launch runs the steps between two attentions ---------------------
+// The chain's vectorised row ops need head_dim % 8 == 0 and ffn % 4 == 0 (bf16 sizes are
+// already multiples of 8); other shapes run per-op.
+bool chained(const eagle_ctx* ctx) {
+  return ctx->z.dt == DT_BF16 && ctx->use_chain && ctx->z.d % 8 == 0 && ctx->z.F % 4 == 0;
+}
+
+ChainProgram chain_prog(eagle_ctx* ctx, int M) {
+  ChainProgram p;
+  p.M = M;
+  p.partials = ctx->gemm_part;
+  p.counters = ctx->gemm_cnt;
+  p.counters_len = ctx->gemm_cnt_len;
+  p.bar = ctx->chain_bar;
+  p.err = ctx->dev_err;
+  return p;
+}
+
+// Bytes a chain step must move (weights, activations read and written).
+double chain_step_bytes(const ChainStep& s, const ChainProgram& p, int M) {
+  switch (s.kind) {
+    case CH_GEMM: {
+      const double ob = (double)M * s.N * (s.epi == EPI_BF16 ? 2 : 4) * (s.epi == EPI_ADD_F32 ? 2 : 1);
+      return (double)s.N * s.K * 2 + (double)M * s.K * 2 + ob;
+    }
+    case CH_RMSNORM: return (double)M * s.H * ((s.in_bf16 ? 2 : 4) + 2) + s.H * 2.0;
+    case CH_SWIGLU: return (double)M * s.H * (8 + 2);
+    case CH_ROPE: return (double)M * (p.args.rope.nq + 2 * p.args.rope.nkv) * p.args.rope.d * (4 + 2);
+    case CH_CONVERT: return (double)M * s.H * (4 + 2);
+    case CH_EMBED: return (double)M * s.H * (2 + 4);
+    case CH_CONCAT: return (double)M * 2 * s.H * (2 + 2);
+  }
+  return 0.0;
+}
+
+int run_chain(eagle_ctx* ctx, ChainProgram& p) {
+  const bool prof = ctx->prof_on && 2 * (ctx->prof_n + 1) <= (int)ctx->prof_ev.size();
+  if (prof) cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n], ctx->st);
+  const int r = chain_run(ctx->st, p);
+  if (r) return fail(ctx, EAGLE_ECUDA, "layer chain launch failed (" + std::to_string(r) + ")");
+  if (prof) {
+    cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n + 1], ctx->st);
+    double b = 0.0;
+    for (int s = 0; s < p.nsteps; ++s) b += chain_step_bytes(p.args.s[s], p, p.M);
+    ctx->prof_bytes[ctx->prof_n] = b;
+    ++ctx->prof_n;
+  }
+  return 0;
+}
+
+void add_rmsnorm(ChainProgram& p, const void* in, int in_bf16, int ldi, const void* g, int H, float eps, void* out,
+                 int ldo) {
+  ChainStep& s = p.add(CH_RMSNORM);
+  s.in = in; s.in_bf16 = in_bf16; s.ldi = ldi; s.aux = g; s.H = H; s.eps = eps; s.out = out; s.ldo = ldo;
+}
+
+void add_convert(ChainProgram& p, const float* in, int H, void* out, int ldo) {
+  ChainStep& s = p.add(CH_CONVERT);
+  s.in = in; s.ldi = H; s.H = H; s.out = out; s.ldo = ldo;
+}
+
+// QKV projection of ain [R][kin] and the rotary embedding / KV-cache write.
+void add_qkv(ChainProgram& p, eagle_ctx* ctx, const eagle_layer_weights& lw, int kin, void* kcache, void* vcache,
+             int cap, const int* pos, const int* slot, const int* seq) {
+  const Dims& z = ctx->z;
+  p.add_gemm(lw.wqkv, z.QKV, kin, ctx->ain, EPI_F32, ctx->qkv, z.QKV);
+  p.add(CH_ROPE);
+  ChainRope& r = p.args.rope;
+  r.qkv = ctx->qkv; r.nq = z.nq; r.nkv = z.nkv; r.d = z.d; r.cap = cap;
+  r.pos = pos; r.slot = slot; r.seq = seq; r.cos = ctx->rope_cos; r.sin = ctx->rope_sin;
+  r.q = ctx->qb; r.kc = kcache; r.vc = vcache;
+}
+
+// Output projection (+ residual), MLP RMSNorm, gate/up, SwiGLU, down (+ residual).
+void add_post(ChainProgram& p, eagle_ctx* ctx, const eagle_layer_weights& lw) {
+  const Dims& z = ctx->z;
+  p.add_gemm(lw.wo, z.H, z.A, ctx->att, EPI_ADD_F32, ctx->x, z.H);
+  add_rmsnorm(p, ctx->x, 0, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, ctx->ain, z.H);
+  p.add_gemm(lw.wgu, 2 * z.F, z.H, ctx->ain, EPI_F32, ctx->gu, 2 * z.F);
+  ChainStep& sw = p.add(CH_SWIGLU);
+  sw.in = ctx->gu; sw.H = z.F; sw.out = ctx->hb;
+  p.add_gemm(lw.wd, z.H, z.F, ctx->hb, EPI_ADD_F32, ctx->x, z.H);
+}
+
+int target_forward_chain(eagle_ctx* ctx, int R, const int* tok, const int* pos, const int* slot, const int* seq,
+                         int rows_per_seq, int mode, int tree_T, const uint64_t* mask, int mask_words, void* feat_out,
+                         void* caps_out, size_t caps_ld, size_t caps_row0) {
+  const Dims& z = ctx->z;
+  const size_t lstride = (size_t)z.B * z.nkv * z.cap * z.d * z.esz;
+  auto kc = [&](int l) { return (void*)((uint8_t*)ctx->kc + l * lstride); };
+  auto vc = [&](int l) { return (void*)((uint8_t*)ctx->vc + l * lstride); };
+  ChainProgram p = chain_prog(ctx, R);
+  ChainStep& e = p.add(CH_EMBED);
+  e.aux = ctx->w.embed; e.V = z.V; e.H = z.H; e.idx = tok; e.out = ctx->x;
+  add_rmsnorm(p, ctx->x, 0, z.H, ctx->layers[0].attn_norm, z.H, ctx->mc.rms_eps, ctx->ain, z.H);
+  add_qkv(p, ctx, ctx->layers[0], z.H, kc(0), vc(0), z.cap, pos, slot, seq);
+  int r = run_chain(ctx, p);
+  if (r) return r;
+  for (int l = 0; l < z.L; ++l) {
+    r = attend(ctx, kc(l), vc(l), z.cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words);
+    if (r) return r;
+    p = chain_prog(ctx, R);
+    add_post(p, ctx, ctx->layers[l]);
+    if (z.kind == 3 && caps_out) {
+      for (int j = 0; j < 3; ++j)
+        if (ctx->dc.fuse_layers[j] == l)
+          add_convert(p, ctx->x, z.H, (uint8_t*)caps_out + ((size_t)j * caps_ld + caps_row0) * z.H * z.esz, z.H);
+    }
+    if (l + 1 < z.L) {
+      add_rmsnorm(p, ctx->x, 0, z.H, ctx->layers[l + 1].attn_norm, z.H, ctx->mc.rms_eps, ctx->ain, z.H);
+      add_qkv(p, ctx, ctx->layers[l + 1], z.H, kc(l + 1), vc(l + 1), z.cap, pos, slot, seq);
+    } else {
+      add_rmsnorm(p, ctx->x, 0, z.H, ctx->w.final_norm, z.H, ctx->mc.rms_eps, feat_out, z.H);
+    }
+    r = run_chain(ctx, p);
+    if (r) return r;
+  }
   return 0;
 }
 
@@ -310,6 +445,9 @@ int target_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const 
                    int rows_per_seq, int mode, int tree_T, const uint64_t* mask, int mask_words, void* feat_out,
                    void* caps_out, size_t caps_ld, size_t caps_row0) {
   const Dims& z = ctx->z;
+  if (chained(ctx))
+    return target_forward_chain(ctx, R, tok, pos, slot, seq, rows_per_seq, mode, tree_T, mask, mask_words, feat_out,
+                                caps_out, caps_ld, caps_row0);
   CK(embed_rows(ctx->st, z.dt, ctx->w.embed, z.V, z.H, tok, R, ctx->x, ctx->dev_err));
   const size_t lstride = (size_t)z.B * z.nkv * z.cap * z.d * z.esz;
   for (int l = 0; l < z.L; ++l) {
@@ -349,11 +487,20 @@ int drafter_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const
   const Dims& z = ctx->z;
   const eagle_layer_weights& lw = ctx->w.draft;
   const size_t rb = (size_t)z.H * z.esz;
+  const bool ch = chained(ctx);
+  ChainProgram p = chain_prog(ctx, R);
   int kin;
   if (z.kind == 1) {
-    CK(concat_emb_feat(ctx->st, z.dt, ctx->w.embed, z.V, z.H, tok, feat, feat_row, R, ctx->ain, ctx->dev_err));
-    CK(gemm(ctx, ctx->w.fc, z.H, 2 * z.H, ctx->ain, R, EPI_F32, ctx->x, z.H));
-    CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
+    if (ch) {
+      ChainStep& c = p.add(CH_CONCAT);
+      c.aux = ctx->w.embed; c.V = z.V; c.H = z.H; c.idx = tok; c.in = feat; c.idx2 = feat_row; c.out = ctx->ain;
+      p.add_gemm(ctx->w.fc, z.H, 2 * z.H, ctx->ain, EPI_F32, ctx->x, z.H);
+      add_rmsnorm(p, ctx->x, 0, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, ctx->ain, z.H);
+    } else {
+      CK(concat_emb_feat(ctx->st, z.dt, ctx->w.embed, z.V, z.H, tok, feat, feat_row, R, ctx->ain, ctx->dev_err));
+      CK(gemm(ctx, ctx->w.fc, z.H, 2 * z.H, ctx->ain, R, EPI_F32, ctx->x, z.H));
+      CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
+    }
     kin = z.H;
   } else {
     if (feat != ctx->gbuf || feat_row)
@@ -364,6 +511,17 @@ int drafter_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const
     CK(rmsnorm_rows(ctx->st, z.dt, ctx->ebuf, z.H, ctx->w.norm_e, z.H, ctx->mc.rms_eps, R, z.dt,
                     (uint8_t*)ctx->ain + rb, 2 * z.H));
     kin = 2 * z.H;
+  }
+  if (ch) {
+    add_qkv(p, ctx, lw, kin, ctx->dkc, ctx->dvc, z.dcap, pos, slot, seq);
+    int r = run_chain(ctx, p);
+    if (r) return r;
+    r = attend(ctx, ctx->dkc, ctx->dvc, z.dcap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words);
+    if (r) return r;
+    p = chain_prog(ctx, R);
+    add_post(p, ctx, lw);
+    add_convert(p, ctx->x, z.H, ctx->dout, z.H);
+    return run_chain(ctx, p);
   }
   int r = layer_forward(ctx, lw, R, ctx->ain, kin, ctx->dkc, ctx->dvc, z.dcap, rows_per_seq, pos, slot, seq, mode,
                         tree_T, mask, mask_words);
@@ -622,6 +780,7 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
   ctx->layers.assign(weights->layers, weights->layers + model->n_layers);
   ctx->w.layers = ctx->layers.data();
   ctx->st = reinterpret_cast<cudaStream_t>(stream);
+  if (getenv("EAGLE_CHAIN")) ctx->use_chain = strcmp(getenv("EAGLE_CHAIN"), "0") != 0;
   Carver c;
   c.base = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(workspace), 256));
   carve(c, ctx, z);
@@ -672,6 +831,10 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
   }
   ctx->batch = batch;
   ctx->ref_len = d_ref ? ref_len : 0;
+  // barrier words of the layer chain start from zero (a launch that gave up on an error
+  // may have left them inconsistent)
+  if (cudaMemsetAsync(ctx->chain_bar, 0, 4 * sizeof(unsigned), ctx->st) != cudaSuccess)
+    return fail(ctx, EAGLE_ECUDA, "memset failed");
   fill_cd(ctx);
   ctx->cd.ref = d_ref;
   ctx->cd.ref_len = ctx->ref_len;

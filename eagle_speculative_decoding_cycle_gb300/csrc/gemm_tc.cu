@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "lmhead.cuh"
+#include "tc_common.cuh"
 
 namespace eagle {
 
@@ -45,40 +46,23 @@ struct GemmArgs {
   HeadParams head;
 };
 
-template <int BN>
-struct TcCfg {
-  static constexpr int A_BYTES = 128 * 64 * 2;
-  static constexpr int B_BYTES = BN * 64 * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196608 / STAGE) > 12 ? 12 : (196608 / STAGE);
-  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
-  static constexpr int CH = BN < 32 ? BN : 32;
-  static constexpr int STAGING = 32 * 128 * 4;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + STAGING + 512;
-};
-
-// K-major operand tile, rows of 64 bf16 (128 bytes) with the 128-byte swizzle, 8-row
-// atoms 1024 bytes apart. Start address, stride byte offset 1024, descriptor version 1,
-// layout SWIZZLE_128B.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
-  d |= (uint64_t)1 << 16;
-  d |= (uint64_t)(1024 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-__device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
-  return (int)(((u + 1) * G - 1) / U);
-}
-
 template <int CH>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int BN, int row, int c0,
                                           const float* v, float* staging, int ew, int lane) {
   const int f = tn * 128 + row;
-  if (a.epi != EPI_HEAD) {
+  if (a.epi == EPI_ADD_F32) {
+    if (f < a.N) {
+      // residual update: all reads first (one round trip), then the writes
+      const int j0 = tt * BN + c0;
+      float* o = reinterpret_cast<float*>(a.out) + (size_t)j0 * a.ldo + f;
+      float old[CH];
+#pragma unroll
+      for (int i = 0; i < CH; ++i) old[i] = (j0 + i < a.M) ? o[(size_t)i * a.ldo] : 0.f;
+#pragma unroll
+      for (int i = 0; i < CH; ++i)
+        if (j0 + i < a.M) o[(size_t)i * a.ldo] = old[i] + v[i];
+    }
+  } else if (a.epi != EPI_HEAD) {
     if (f < a.N) {
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
@@ -86,8 +70,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int
         if (j < a.M) {
           const size_t o = (size_t)j * a.ldo + f;
           if (a.epi == EPI_F32) reinterpret_cast<float*>(a.out)[o] = v[i];
-          else if (a.epi == EPI_BF16) reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(v[i]);
-          else reinterpret_cast<float*>(a.out)[o] += v[i];
+          else reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(v[i]);
         }
       }
     }
@@ -195,8 +178,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                                 ((uint32_t)(128 >> 4) << 24);
+      constexpr uint32_t IDESC = idesc_bf16<BN>();
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -270,13 +252,17 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_before();
         mbar_arrive(smem_u32(tempty + acc));
+        // publish the partial: every thread fences, the CTA synchronises, one thread
+        // takes the ticket between gpu-scope fences
         __threadfence();
         named_bar_sync(1, 128);
         const int cf = cta_of_unit(tile * a.kb, U, G);
         const int cl = cta_of_unit((tile + 1) * a.kb - 1, U, G);
         if (leader) {
+          __threadfence();
           const int old = atomicAdd(a.counters + tile, 1);
           bcast[1] = (old == cl - cf) ? 1 : 0;
+          __threadfence();
         }
         named_bar_sync(1, 128);
         if (bcast[1]) {
@@ -325,11 +311,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 row-major [rows][K] matrix, boxes of 64 (K) x box_rows, 128-byte swizzle.
+// bf16 row-major [rows][K] matrix (row stride ld, 0 = K), boxes of 64 (K) x box_rows,
+// 128-byte swizzle.
 static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long K, int box_rows,
-                     bool use_cache = true) {
-  static std::map<std::tuple<const void*, long long, long long, int>, CUtensorMap> cache;
-  auto key = std::make_tuple(ptr, rows, K, box_rows);
+                     bool use_cache = true, long long ld = 0) {
+  if (ld <= 0) ld = K;
+  static std::map<std::tuple<const void*, long long, long long, int, long long>, CUtensorMap> cache;
+  auto key = std::make_tuple(ptr, rows, K, box_rows, ld);
   if (use_cache) {
     auto it = cache.find(key);
     if (it != cache.end()) { *m = it->second; return true; }
@@ -337,7 +325,7 @@ static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long 
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
@@ -348,6 +336,10 @@ static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long 
   if (cache.size() > 4096) cache.clear();
   cache[key] = *m;
   return true;
+}
+
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, long long K, int box_rows, long long ld) {
+  return make_map(m, ptr, rows, K, box_rows, true, ld);
 }
 
 static int num_sms() {

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 struct HeadParams;
@@ -41,6 +42,9 @@ size_t gemm_bf16_scratch_bytes();
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
               int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head,
               bool cache_maps = true);
+// Tensor map of a bf16 row-major [rows][K] matrix (row stride ld elements, 0 = K): boxes of
+// 64 (K) x box_rows, 128-byte swizzle. Cached by (ptr, rows, K, box_rows, ld).
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, long long K, int box_rows, long long ld = 0);
 // fp32 SIMT GEMM with the same contract (EPI_F32 / EPI_ADD_F32).
 int gemm_f32(cudaStream_t st, const float* W, int N, int K, const float* X, int M, int epi, float* out,
              int ldo);
