@@ -15,7 +15,8 @@
 // and TMEM owner, warps 2-5 = GEMM epilogue and the row ops.
 //
 // Barrier protocol: bar[0] counts CTA arrivals. Every CTA arrives once at the end of each
-// step except the last; step s may read what steps < s wrote once bar[0] >= s * G. Data
+// step except the last, and only after it has seen the previous barrier complete, so
+// bar[0] >= s * G means every CTA has finished steps < s: step s may then read them. Data
 // written inside the launch is read back through L2 (ld.global.cg) or by TMA after a proxy
 // fence. The last CTA to leave resets bar[0] and bar[1] (its exit ticket) for the next
 // launch. Every wait is bounded; a timeout latches an error and the CTA unwinds.
@@ -135,7 +136,102 @@ EAGLE_DEV void chain_epi(const ChainStep& st, int M, int tn, int tt, int BN, int
   }
 }
 
-// ---- row ops: 128 threads per CTA (tid), G CTAs ------------------------------------------------
+// ---- completing a GEMM step's split tiles -------------------------------------------------------
+// Tile t of a GEMM step is split over CTAs cf..cl of its stream-K range. Every contributor
+// but the first starts its range inside t, so holds t in partial slot 0; the first holds t
+// in slot 1 when its range began in an earlier tile. Table entry: cf << 16 | ncon << 1 | that
+// slot. Built per CTA in shared memory (32-bit unit arithmetic: the host checks units * G
+// < 2^31).
+constexpr int CHAIN_MAX_TILES = 32 * 128 * 4 / 4;   // entries that fit the staging buffer
+
+__device__ __noinline__ void build_tile_table(const ChainStep& g, int G, int tid, uint32_t* tab) {
+  const int U = (int)g.units, gs = step_ctas(g.units, G);
+  const int tiles = U / g.kb;
+  for (int t = tid; t < tiles; t += 128) {
+    const int u0 = t * g.kb;
+    const int cf = ((u0 + 1) * gs - 1) / U, cl = ((u0 + g.kb) * gs - 1) / U;
+    const int first_unit = cf * U / gs;
+    tab[t] = ((uint32_t)cf << 16) | ((uint32_t)(cl - cf + 1) << 1) | (first_unit < u0 ? 1u : 0u);
+  }
+}
+
+// out = (out for a residual update) + the sum of the split tiles' partials in contributor order,
+// for every element of a split tile; whole tiles were written by the epilogue. Items of 4
+// features, NB items per thread in flight, contributors in groups of RC.
+template <int BN>
+__device__ __noinline__ void row_reduce(const ChainArgs& a, const ChainStep& g, int M, int t0, int stride, const uint32_t* tab) {
+  constexpr int NB = 2, RC = 4;
+  float* out = reinterpret_cast<float*>(g.out);
+  const bool add = g.epi == EPI_ADD_F32;
+  const int N4 = g.N / 4, n = M * N4;
+  for (int i0 = t0; i0 < n; i0 += NB * stride) {
+    int cf[NB], ncon[NB], s0[NB];
+    size_t off[NB], dst[NB];
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      const int i = i0 + q * stride;
+      ncon[q] = 0;
+      if (i < n) {
+        const int j = i / N4, f = (i - j * N4) * 4;
+        const int tt = j / BN, tile = (f >> 7) * g.tiles_t + tt;
+        const uint32_t e = tab[tile];
+        const int nc = (int)((e >> 1) & 0x7FFFu);
+        if (nc > 1) {
+          cf[q] = (int)(e >> 16);
+          ncon[q] = nc;
+          s0[q] = (int)(e & 1u);
+          off[q] = (size_t)(j - tt * BN) * 128 + (f & 127);
+          dst[q] = (size_t)j * g.ldo + f;
+        }
+      }
+    }
+    // partials summed in contributor order first, then added to the old value: the order
+    // of the single GEMM's split-tile epilogue
+    float4 acc[NB], base[NB];
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      base[q] = (ncon[q] && add) ? __ldcg(reinterpret_cast<const float4*>(out + dst[q])) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    int nmax = 0;
+#pragma unroll
+    for (int q = 0; q < NB; ++q) nmax = max(nmax, ncon[q]);
+    for (int c0 = 0; c0 < nmax; c0 += RC) {
+      float4 v[NB][RC];
+#pragma unroll
+      for (int q = 0; q < NB; ++q)
+#pragma unroll
+        for (int c = 0; c < RC; ++c)
+          if (c0 + c < ncon[q]) {
+            const int cc = cf[q] + c0 + c;
+            const int slot = (c0 + c == 0) ? s0[q] : 0;
+            v[q][c] = __ldcg(reinterpret_cast<const float4*>(a.partials + (size_t)(cc * 2 + slot) * BN * 128 + off[q]));
+          }
+#pragma unroll
+      for (int q = 0; q < NB; ++q)
+#pragma unroll
+        for (int c = 0; c < RC; ++c)
+          if (c0 + c < ncon[q]) {
+            acc[q].x += v[q][c].x; acc[q].y += v[q][c].y; acc[q].z += v[q][c].z; acc[q].w += v[q][c].w;
+          }
+    }
+#pragma unroll
+    for (int q = 0; q < NB; ++q)
+      if (ncon[q]) {
+        if (add) { acc[q].x = base[q].x + acc[q].x; acc[q].y = base[q].y + acc[q].y; acc[q].z = base[q].z + acc[q].z; acc[q].w = base[q].w + acc[q].w; }
+        *reinterpret_cast<float4*>(out + dst[q]) = acc[q];
+      }
+  }
+}
+
+EAGLE_DEV void store4(__nv_bfloat16* p, float x, float y, float z, float w) {
+  __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(p);
+  q[0] = __floats2bfloat162_rn(x, y);
+  q[1] = __floats2bfloat162_rn(z, w);
+}
+
+// ---- row ops: 128 threads per CTA (tid), G CTAs. Kept out of line so their registers do
+// not add to the GEMM roles' live ranges. ------------------------------------------------
 EAGLE_DEV float load_in(const ChainStep& st, size_t i) {
   return st.in_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(st.in)[i])
                     : __ldcg(reinterpret_cast<const float*>(st.in) + i);
@@ -147,7 +243,7 @@ EAGLE_DEV float load_in(const ChainStep& st, size_t i) {
 // vector loads and kept in registers; others take a two-pass loop.
 constexpr int RN_V = 10;
 
-EAGLE_DEV void row_rmsnorm(const ChainStep& st, int M, int cta, int G, int tid, float* red) {
+__device__ __noinline__ void row_rmsnorm(const ChainStep& st, int M, int cta, int G, int tid, float* red) {
   const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(st.aux);
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(st.out);
   const bool vec = !st.in_bf16 && st.H % 4 == 0 && st.ldi % 4 == 0 && st.ldo % 4 == 0 && st.H <= 128 * 4 * RN_V;
@@ -206,15 +302,16 @@ EAGLE_DEV void row_rmsnorm(const ChainStep& st, int M, int cta, int G, int tid, 
 // items in flight per thread.
 EAGLE_DEV float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
-EAGLE_DEV void row_swiglu(const ChainStep& st, int M, int t0, int stride) {
+__device__ __noinline__ void row_swiglu(const ChainStep& st, int M, int t0, int stride) {
   const float* gu = reinterpret_cast<const float*>(st.in);
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(st.out);
   const int F = st.H, F4 = F / 4, n = M * F4;
-  for (int i0 = t0; i0 < n; i0 += 4 * stride) {
-    float4 g[4], u[4];
-    int off[4];
+  constexpr int SB = 4;
+  for (int i0 = t0; i0 < n; i0 += SB * stride) {
+    float4 g[SB], u[SB];
+    int off[SB];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < SB; ++q) {
       const int i = i0 + q * stride;
       if (i < n) {
         const int r = i / F4, c = (i - r * F4) * 4;
@@ -224,7 +321,7 @@ EAGLE_DEV void row_swiglu(const ChainStep& st, int M, int t0, int stride) {
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < SB; ++q) {
       if (i0 + q * stride < n) {
         __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + off[q]);
         o[0] = __floats2bfloat162_rn(silu_mul(g[q].x, u[q].x), silu_mul(g[q].y, u[q].y));
@@ -234,17 +331,18 @@ EAGLE_DEV void row_swiglu(const ChainStep& st, int M, int t0, int stride) {
   }
 }
 
-EAGLE_DEV void row_convert(const ChainStep& st, int M, int t0, int stride) {
+__device__ __noinline__ void row_convert(const ChainStep& st, int M, int t0, int stride) {
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(st.out);
-  const int H = st.H, n = M * H;
+  const float* in = reinterpret_cast<const float*>(st.in);
+  const int H4 = st.H / 4, n = M * H4;
   for (int i = t0; i < n; i += stride) {
-    const int r = i / H, c = i - r * H;
-    out[(size_t)r * st.ldo + c] =
-        __float2bfloat16_rn(__ldcg(reinterpret_cast<const float*>(st.in) + (size_t)r * st.ldi + c));
+    const int r = i / H4, c = (i - r * H4) * 4;
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(in + (size_t)r * st.ldi + c));
+    store4(out + (size_t)r * st.ldo + c, v.x, v.y, v.z, v.w);
   }
 }
 
-EAGLE_DEV void row_embed(const ChainStep& st, int M, int t0, int stride, int* err) {
+__device__ __noinline__ void row_embed(const ChainStep& st, int M, int t0, int stride, int* err) {
   const __nv_bfloat16* E = reinterpret_cast<const __nv_bfloat16*>(st.aux);
   float* out = reinterpret_cast<float*>(st.out);
   const int H = st.H, n = M * H;
@@ -260,7 +358,7 @@ EAGLE_DEV void row_embed(const ChainStep& st, int M, int t0, int stride, int* er
 }
 
 // [E[idx[r]] ; feat[idx2[r]]] -> out [M][2H] (bf16)
-EAGLE_DEV void row_concat(const ChainStep& st, int M, int t0, int stride, int* err) {
+__device__ __noinline__ void row_concat(const ChainStep& st, int M, int t0, int stride, int* err) {
   const __nv_bfloat16* E = reinterpret_cast<const __nv_bfloat16*>(st.aux);
   const __nv_bfloat16* feat = reinterpret_cast<const __nv_bfloat16*>(st.in);
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(st.out);
@@ -283,13 +381,8 @@ EAGLE_DEV void row_concat(const ChainStep& st, int M, int t0, int stride, int* e
 // Rotate-half RoPE on the q and k heads of the fused [q | k | v] projection; q to its
 // buffer, k and v into the cache at the row's slot (a slot outside [0, cap) latches a
 // capacity error and skips the cache write). Items of 4 consecutive elements (d % 8 == 0).
-EAGLE_DEV void store4(__nv_bfloat16* p, float x, float y, float z, float w) {
-  __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(p);
-  q[0] = __floats2bfloat162_rn(x, y);
-  q[1] = __floats2bfloat162_rn(z, w);
-}
 
-EAGLE_DEV void row_rope(const ChainRope& p, int M, int t0, int stride, int* err) {
+__device__ __noinline__ void row_rope(const ChainRope& p, int M, int t0, int stride, int* err) {
   const int half = p.d / 2, h4 = half / 4, d4 = p.d / 4;
   const int rot = (p.nq + p.nkv) * h4;
   const int per_row = rot + p.nkv * d4;
@@ -313,15 +406,18 @@ EAGLE_DEV void row_rope(const ChainRope& p, int M, int t0, int stride, int* err)
       seq[u] = p.seq[r[u]];
       pos[u] = p.pos[r[u]];
       const float* src = p.qkv + (size_t)r[u] * ld;
+      int c0, c1 = -1;
       if (j[u] < rot) {
         const int h = j[u] / h4, e = (j[u] - h * h4) * 4;
-        x0[u] = __ldcg(reinterpret_cast<const float4*>(src + h * p.d + e));
-        x1[u] = __ldcg(reinterpret_cast<const float4*>(src + h * p.d + e + half));
+        c0 = h * p.d + e;
+        c1 = c0 + half;
       } else {
         const int jj = j[u] - rot;
         const int h = jj / d4, e = (jj - h * d4) * 4;
-        x0[u] = __ldcg(reinterpret_cast<const float4*>(src + (p.nq + p.nkv + h) * p.d + e));
+        c0 = (p.nq + p.nkv + h) * p.d + e;
       }
+      x0[u] = __ldcg(reinterpret_cast<const float4*>(src + c0));
+      if (c1 >= 0) x1[u] = __ldcg(reinterpret_cast<const float4*>(src + c1));
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -568,53 +664,6 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_before();
             mbar_arrive(smem_u32(tempty + acc));
-            // publish the partial: every thread fences, the CTA synchronises, one thread
-            // takes the ticket between gpu-scope fences
-            __threadfence();
-            named_bar_sync(1, 128);
-            const int cf = cta_of_unit(tile * st.kb, U, gs);
-            const int cl = cta_of_unit((tile + 1) * st.kb - 1, U, gs);
-            if (leader) {
-              __threadfence();
-              const int old = atomicAdd(a.counters + tile, 1);
-              bcast[1] = (old == cl - cf) ? 1 : 0;
-              __threadfence();
-            }
-            named_bar_sync(1, 128);
-            if (bcast[1]) {
-              __threadfence();
-              // sum the contributors' partials in contributor order; loads of four
-              // contributors are in flight together
-              constexpr int FC = 8;
-              const int ncon = cl - cf + 1;
-              for (int c0 = 0; c0 < BN; c0 += FC) {
-                float v[FC];
-#pragma unroll
-                for (int i = 0; i < FC; ++i) v[i] = 0.f;
-                for (int q0 = 0; q0 < ncon; q0 += 4) {
-                  float t[4][FC];
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) {
-                    if (q0 + q < ncon) {
-                      const int cc = cf + q0 + q;
-                      const long long ft = ((long long)cc * U / gs) / st.kb;
-                      const float* pp = a.partials + (size_t)(cc * 2 + (tile == ft ? 0 : 1)) * BN * 128;
-#pragma unroll
-                      for (int i = 0; i < FC; ++i) t[q][i] = __ldcg(pp + (c0 + i) * 128 + row);
-                    }
-                  }
-#pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    if (q0 + q < ncon) {
-#pragma unroll
-                      for (int i = 0; i < FC; ++i) v[i] += t[q][i];
-                    }
-                }
-                chain_epi<FC>(st, a.M, tn, tt, BN, row, c0, v);
-              }
-              if (leader) a.counters[tile] = 0;
-            }
-            named_bar_sync(1, 128);
           }
           u = seg_end;
           acc ^= 1;
@@ -633,6 +682,13 @@ __global__ void __launch_bounds__(192, 1)
           if (!ok) break;
         }
         switch (st.kind) {
+          case CH_REDUCE: {
+            uint32_t* tab = reinterpret_cast<uint32_t*>(staging);
+            build_tile_table(a.s[st.src], G, tid, tab);
+            named_bar_sync(1, 128);
+            row_reduce<BN>(a, a.s[st.src], a.M, t0, tstride, tab);
+            break;
+          }
           case CH_RMSNORM: row_rmsnorm(st, a.M, cta, G, tid, staging); break;
           case CH_SWIGLU: row_swiglu(st, a.M, t0, tstride); break;
           case CH_ROPE: row_rope(a.rope, a.M, t0, tstride, a.err); break;
@@ -649,9 +705,20 @@ __global__ void __launch_bounds__(192, 1)
         fence_proxy_async();
         named_bar_sync(1, 128);
         if (leader) {
-          __threadfence();
-          red_release_add(a.bar, 1u);
+          // a CTA arrives at barrier s only after barrier s - 1 has completed: a CTA with no
+          // units in a GEMM step would otherwise run ahead and add a second arrival before
+          // the slow CTAs of step s - 1 have arrived, opening step s + 1 early
+          const bool ok = !(s > 0 && st.kind == CH_GEMM) || grid_wait(a.bar, (unsigned)s * (unsigned)G, abort_flag, a.err);
+          if (ok) {
+            __threadfence();
+            red_release_add(a.bar, 1u);
+          }
+          bcast[1] = ok ? 1 : 0;
         }
+        named_bar_sync(1, 128);
+        const bool arrived = bcast[1] != 0;
+        named_bar_sync(1, 128);
+        if (!arrived) break;
       }
     }
   }
@@ -720,43 +787,45 @@ static cudaError_t chain_launch_bn(cudaStream_t st, const ChainMaps& maps, const
   return e;
 }
 
+static_assert(sizeof(ChainArgs) + sizeof(ChainMaps) <= 4000, "chain kernel parameters exceed 4 KB");
+
 int chain_run(cudaStream_t st, const ChainProgram& p) {
-  if (p.M <= 0 || p.nsteps <= 0 || p.nsteps > CHAIN_MAX_STEPS || !p.bar || !p.partials || !p.counters) return -1;
+  if (p.M <= 0 || p.nsteps <= 0 || p.nsteps > CHAIN_MAX_STEPS || !p.bar || !p.partials) return -1;
   const int BN = gemm_bn_for(p.M);
+  const int G = chain_sms();
   ChainMaps maps;
   memset(&maps, 0, sizeof(maps));
   ChainArgs a = p.args;
   a.nsteps = p.nsteps;
   a.M = p.M;
   a.partials = p.partials;
-  a.counters = p.counters;
   a.bar = p.bar;
   a.err = p.err;
-  for (int s = 0; s < p.nsteps; ++s) {   // row ops index elements with 32-bit integers
-    const ChainStep& c = a.s[s];
-    if (c.kind == CH_SWIGLU &&
-        (c.H % 4 || ((reinterpret_cast<uintptr_t>(c.in) | reinterpret_cast<uintptr_t>(c.out)) & 15)))
-      return -1;
-    if (c.kind == CH_ROPE && (a.rope.d % 8 || (reinterpret_cast<uintptr_t>(a.rope.qkv) & 15))) return -1;
-    const long long w = c.kind == CH_ROPE ? (long long)(a.rope.nq + 2 * a.rope.nkv) * a.rope.d : 2LL * c.H;
-    if ((long long)p.M * w >= (1LL << 31)) return -1;
-  }
+  auto aligned16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
   int ng = 0;
   for (int s = 0; s < p.nsteps; ++s) {
     ChainStep& c = a.s[s];
+    // row ops index elements with 32-bit integers
+    const long long w = c.kind == CH_ROPE ? (long long)(a.rope.nq + 2 * a.rope.nkv) * a.rope.d : 2LL * c.H;
+    if ((long long)p.M * w >= (1LL << 31)) return -1;
+    if (c.kind == CH_SWIGLU && (c.H % 4 || !aligned16(c.in) || !aligned16(c.out))) return -1;
+    if (c.kind == CH_ROPE && (a.rope.d % 8 || !aligned16(a.rope.qkv))) return -1;
+    if (c.kind == CH_CONVERT && (c.H % 4 || c.ldi % 4 || c.ldo % 4 || !aligned16(c.in))) return -1;
+    if (c.kind == CH_REDUCE && (c.src != s - 1 || s == 0 || a.s[c.src].kind != CH_GEMM)) return -1;
     if (c.kind != CH_GEMM) continue;
     if (ng >= CHAIN_MAX_GEMMS) return -1;
     const ChainGemm& g = p.gemm[s];
-    if (!g.W || !g.X || c.K % 8 || ((reinterpret_cast<uintptr_t>(g.W) | reinterpret_cast<uintptr_t>(g.X)) & 15))
-      return -1;
+    if (!g.W || !g.X || c.K % 8 || !aligned16(g.W) || !aligned16(g.X) || !aligned16(c.out)) return -1;
+    // fp32 outputs whose split tiles the next step completes
+    if ((c.epi != EPI_F32 && c.epi != EPI_ADD_F32) || c.N % 4 || c.ldo % 4) return -1;
+    if (s + 1 >= p.nsteps || a.s[s + 1].kind != CH_REDUCE) return -1;
     if (!make_tmap_bf16(&maps.w[ng], g.W, c.N, c.K, 128)) return -3;
     if (!make_tmap_bf16(&maps.x[ng], g.X, p.M, c.K, BN, g.ldx)) return -3;
     c.gemm = ng++;
     c.tiles_t = (p.M + BN - 1) / BN;
     c.kb = (c.K + 63) / 64;
-    const long long tiles = (long long)((c.N + 127) / 128) * c.tiles_t;
-    if (tiles > p.counters_len) return -2;
-    c.units = tiles * c.kb;
+    c.units = (long long)((c.N + 127) / 128) * c.tiles_t * c.kb;
+    if (c.units * G >= (1LL << 31) || c.units / c.kb > CHAIN_MAX_TILES) return -2;
   }
   cudaError_t e;
   switch (BN) {

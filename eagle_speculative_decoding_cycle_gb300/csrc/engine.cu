@@ -320,18 +320,16 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
 }
 
 // ---- layer chains (bf16): each launch runs the steps between two attentions ---------------------
-// The chain's vectorised row ops need head_dim % 8 == 0 and ffn % 4 == 0 (bf16 sizes are
-// already multiples of 8); other shapes run per-op.
+// The chain's vectorised row ops need head_dim % 8 == 0, ffn % 4 == 0 (bf16 sizes are
+// already multiples of 8) and rows of at most 5120 features; other shapes run per-op.
 bool chained(const eagle_ctx* ctx) {
-  return ctx->z.dt == DT_BF16 && ctx->use_chain && ctx->z.d % 8 == 0 && ctx->z.F % 4 == 0;
+  return ctx->z.dt == DT_BF16 && ctx->use_chain && ctx->z.d % 8 == 0 && ctx->z.F % 4 == 0 && ctx->z.H <= 5120;
 }
 
 ChainProgram chain_prog(eagle_ctx* ctx, int M) {
   ChainProgram p;
   p.M = M;
   p.partials = ctx->gemm_part;
-  p.counters = ctx->gemm_cnt;
-  p.counters_len = ctx->gemm_cnt_len;
   p.bar = ctx->chain_bar;
   p.err = ctx->dev_err;
   return p;
@@ -350,6 +348,7 @@ double chain_step_bytes(const ChainStep& s, const ChainProgram& p, int M) {
     case CH_CONVERT: return (double)M * s.H * (4 + 2);
     case CH_EMBED: return (double)M * s.H * (2 + 4);
     case CH_CONCAT: return (double)M * 2 * s.H * (2 + 2);
+    case CH_REDUCE: return 0.0;   // scratch traffic, not part of the layer's algorithmic bytes
   }
   return 0.0;
 }

@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(tempty + acc));
       } else {
+        // partial tile [BN tokens][128 features]: a warp's stores cover whole 128-byte lines
         const int slot = (tile == first_tile) ? 0 : 1;
         float* part = a.partials + (size_t)(cta * 2 + slot) * BN * 128;
         for (int c0 = 0; c0 < BN; c0 += C::CH) {
@@ -267,16 +268,30 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         if (bcast[1]) {
           __threadfence();
+          // Sum the contributors' rows in contributor order, two contributors' loads in
+          // flight together. Every contributor after the first began its range inside this
+          // tile (slot 0); the first holds it in slot 1 when its range began earlier.
+          const int s_first = ((long long)cf * U / G < tile * a.kb) ? 1 : 0;
           for (int c0 = 0; c0 < BN; c0 += C::CH) {
             float v[C::CH];
 #pragma unroll
             for (int i = 0; i < C::CH; ++i) v[i] = 0.f;
-            for (int cc = cf; cc <= cl; ++cc) {
-              const long long ft = ((long long)cc * U / G) / a.kb;
-              const int sl = (tile == ft) ? 0 : 1;
-              const float* pp = a.partials + (size_t)(cc * 2 + sl) * BN * 128;
+            for (int cc = cf; cc <= cl; cc += 2) {
+              const bool two = cc + 1 <= cl;
+              const float* p0 = a.partials + (size_t)(cc * 2 + (cc == cf ? s_first : 0)) * BN * 128 + c0 * 128 + row;
+              const float* p1 = a.partials + (size_t)((cc + 1) * 2) * BN * 128 + c0 * 128 + row;
+              float x0[C::CH], x1[C::CH];
 #pragma unroll
-              for (int i = 0; i < C::CH; ++i) v[i] += __ldcg(pp + (c0 + i) * 128 + row);
+              for (int i = 0; i < C::CH; ++i) {
+                x0[i] = __ldcg(p0 + i * 128);
+                x1[i] = two ? __ldcg(p1 + i * 128) : 0.f;
+              }
+#pragma unroll
+              for (int i = 0; i < C::CH; ++i) v[i] += x0[i];
+              if (two) {
+#pragma unroll
+                for (int i = 0; i < C::CH; ++i) v[i] += x1[i];
+              }
             }
             epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
           }

@@ -39,14 +39,17 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, co
   PDL_ENTRY();
   const int r = blockIdx.x;
   const TX* xr = x + (size_t)r * ldx;
-  float v[RN_PER_THREAD];
+  float v[RN_PER_THREAD], gv[RN_PER_THREAD];
   float s = 0.f;
+  // the row and the gains in one round of loads
 #pragma unroll
   for (int j = 0; j < RN_PER_THREAD; ++j) {
     const int i = threadIdx.x + j * RN_THREADS;
     v[j] = i < H ? Elem<TX>::to_f(xr[i]) : 0.f;
-    s += v[j] * v[j];
+    gv[j] = i < H ? Elem<TG>::to_f(g[i]) : 0.f;
   }
+#pragma unroll
+  for (int j = 0; j < RN_PER_THREAD; ++j) s += v[j] * v[j];
   for (int i = threadIdx.x + RN_PER_THREAD * RN_THREADS; i < H; i += RN_THREADS) {
     const float t = Elem<TX>::to_f(xr[i]);
     s += t * t;
@@ -63,7 +66,7 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, co
 #pragma unroll
   for (int j = 0; j < RN_PER_THREAD; ++j) {
     const int i = threadIdx.x + j * RN_THREADS;
-    if (i < H) o[i] = Elem<TO>::from_f(v[j] * rs * Elem<TG>::to_f(g[i]));
+    if (i < H) o[i] = Elem<TO>::from_f(v[j] * rs * gv[j]);
   }
   for (int i = threadIdx.x + RN_PER_THREAD * RN_THREADS; i < H; i += RN_THREADS)
     o[i] = Elem<TO>::from_f(Elem<TX>::to_f(xr[i]) * rs * Elem<TG>::to_f(g[i]));
