@@ -379,15 +379,20 @@ def run_ours(args, ws, rank, local):
 
 
 def traffic_per_launch():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it matches this build."""
-    p = os.path.join(ROOT, "profiles", "gemm_bf16_tc_traffic.json")
+    """DRAM bytes per GEMM launch from the committed ncu summary, if the GEMM kernel's sources
+    are unchanged since the counters were taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "gemm_bf16_tc_cycle_llama2-7b-eagle1.md")
     try:
+        vals = {}
         with open(p) as f:
-            j = json.load(f)
-        from eagle_speculative_decoding_cycle_gb300.build import _digest
-        if j.get("source_digest") != _digest():
+            for line in f:
+                if line.startswith("- ") and ": " in line:
+                    k, v = line[2:].strip().split(": ", 1)
+                    vals[k] = v.strip("` ")
+        from eagle_speculative_decoding_cycle_gb300.build import gemm_digest
+        if vals.get("gemm source digest") != gemm_digest():
             return None
-        return j.get("dram_bytes_per_launch")
+        return float(vals["dram bytes per launch"])
     except Exception:
         return None
 
@@ -401,6 +406,8 @@ def run_ncu_region(args):
     build()
     dev = torch.device("cuda:0")
     wl = synth.WORKLOADS[args.workload]
+    if args.layers:   # a shallower model of the same width: the small case for multi-pass captures
+        wl = wl.replace(model=dataclasses.replace(wl.model, n_layers=args.layers))
     D = wl.tree.depth
     weights = synth.make_weights(wl, device=str(dev))
     prompt = synth.make_prompts(wl)[0].to(dev)
@@ -498,6 +505,8 @@ def main():
                     help="only time one projection GEMM of this shape (for ncu and tuning)")
     ap.add_argument("--ncu-region", action="store_true",
                     help="only run a short NVTX-marked region for an ncu launch list")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="with --ncu-region: truncate the target to this many layers (small profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.ncu_region:

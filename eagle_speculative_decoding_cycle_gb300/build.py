@@ -47,6 +47,18 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+GEMM_FILES = ["gemm_tc.cu", "tc_common.cuh", "common.cuh", "lmhead.cuh", "kernels.h"]
+
+
+def gemm_digest() -> str:
+    """Digest of the tensor-core GEMM kernel's sources (names its profile's counters)."""
+    h = hashlib.sha256()
+    for f in GEMM_FILES:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile (if sources changed) and return the path of libeagle.so."""
     os.makedirs(BUILD, exist_ok=True)
