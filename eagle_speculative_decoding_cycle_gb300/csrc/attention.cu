@@ -214,7 +214,7 @@ __device__ __forceinline__ bool visible(const AttnArgs& a, const RowVis& rv, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) attn_mma_k(AttnArgs a, int splits) {
+__global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   PDL_ENTRY();
   constexpr int LD = D + 8;                      // padded smem row (bf16 elements)
   extern __shared__ __align__(16) uint8_t attn_smem[];
@@ -444,24 +444,24 @@ static int launch_mma(cudaStream_t st, const AttnArgs& a) {
   const int nseq = (a.R + a.rows_per_seq - 1) / a.rows_per_seq;
   const int nb = (a.rows_per_seq + RB - 1) / RB;
   const int base = a.nkv * nseq * nb;
-  static int sms = 0;
+  const size_t smem = (size_t)4 * MT_KEYS * (D + 8) * sizeof(__nv_bfloat16);
+  static int sms = 0, per_sm = 1;
   if (!sms) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaFuncSetAttribute(attn_mma_k<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_mma_k<D>, 128, smem) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
   }
-  int splits = (2 * sms + base - 1) / base;
+  // as many key splits as one wave of resident CTAs holds (a second, partial wave would
+  // double the time of this latency-bound kernel)
+  int splits = per_sm * sms / base;
   const int max_tiles = (a.cap + MT_KEYS - 1) / MT_KEYS;
   splits = std::min(std::min(splits, 16), max_tiles);
   while (splits > 1 && (size_t)splits * a.R * a.nq * D > a.part_floats) --splits;
   if (!a.part_o || !a.part_ml) splits = 1;
   if (splits < 1) splits = 1;
-  const size_t smem = (size_t)4 * MT_KEYS * (D + 8) * sizeof(__nv_bfloat16);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(attn_mma_k<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr = true;
-  }
   launch_k(attn_mma_k<D>, dim3(a.nkv, nseq * nb, splits), 128, smem, st, a, splits);
   if (splits > 1) launch_k(attn_combine_k<D>, (a.R * a.nq + 3) / 4, 128, 0, st, a, splits);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;

@@ -27,10 +27,39 @@ __global__ void __launch_bounds__(128) head_partials_k(const float* logits, int 
   }
 }
 
-__global__ void __launch_bounds__(128) head_merge_k(HeadParams p) {
+// One CTA per row: 8 warps fold the tile records (one round of loads per thread when the
+// vocabulary has at most 256 tiles), each warp reduces its lanes, warp 0 reduces the warps.
+constexpr int HM_WARPS = 8;
+
+__global__ void __launch_bounds__(HM_WARPS * 32) head_merge_k(HeadParams p) {
   PDL_ENTRY();
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (row < p.n_rows) head_merge_row(p, row, threadIdx.x & 31);
+  __shared__ float s_m[HM_WARPS], s_s[HM_WARPS], s_v[HM_WARPS][16];
+  __shared__ int s_i[HM_WARPS][16];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.K;
+  float lv[16], M, S;
+  int li[16];
+  head_merge_fold(p, row, threadIdx.x, HM_WARPS * 32, lv, li, M, S);
+  head_merge_warp(K, lv, li, M, S, lane, s_v[warp], s_i[warp]);
+  if (lane == 0) { s_m[warp] = M; s_s[warp] = S; }
+  __syncthreads();
+  if (warp != 0) return;
+  // lane w < HM_WARPS holds warp w's sorted list
+  for (int k = 0; k < 16; ++k) {
+    lv[k] = (lane < HM_WARPS && k < K) ? s_v[lane][k] : -INFINITY;
+    li[k] = (lane < HM_WARPS && k < K) ? s_i[lane][k] : 0x7fffffff;
+  }
+  M = lane < HM_WARPS ? s_m[lane] : -INFINITY;
+  S = lane < HM_WARPS ? s_s[lane] : 0.f;
+  __syncwarp();
+  head_merge_warp(K, lv, li, M, S, lane, s_v[0], s_i[0]);   // warp 0's own slot, already read
+  __syncwarp();
+  if (lane < K) {
+    p.top_id[row * K + lane] = s_i[0][lane] == 0x7fffffff ? -1 : s_i[0][lane];
+    p.top_val[row * K + lane] = s_v[0][lane];
+  }
+  if (lane == 0) p.lse[row] = (M == -INFINITY) ? -INFINITY : M + logf(S);
 }
 
 size_t head_part_bytes(int vocab, int rows, int K) {
@@ -48,7 +77,7 @@ int head_partials_from_logits(cudaStream_t st, const float* logits, int ld, cons
 int head_merge(cudaStream_t st, const HeadParams& p) {
   if (p.n_rows <= 0) return 0;
   if (p.K < 1 || p.K > 16) return -1;
-  launch_k(head_merge_k, (p.n_rows + 3) / 4, 128, 0, st, p);
+  launch_k(head_merge_k, p.n_rows, HM_WARPS * 32, 0, st, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

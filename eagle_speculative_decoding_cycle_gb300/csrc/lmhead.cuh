@@ -118,31 +118,57 @@ EAGLE_DEV void head_tile_row(const float* vals, int tile, int row, const HeadPar
   }
 }
 
-// Merge kernel body: one warp per row, tiles visited in a fixed order.
-EAGLE_DEV void head_merge_row(const HeadParams& p, int row, int lane) {
+// Merge: each thread folds the records of tiles t0, t0 + stride, ... into its sorted
+// list (lv, li; K entries, the rest -inf) and its (max, sum-exp) pair. A thread's first
+// record is taken as is (records are sorted); later ones are inserted.
+EAGLE_DEV void head_merge_fold(const HeadParams& p, int row, int t0, int stride, float* lv, int* li, float& M,
+                               float& S) {
   const int K = p.K;
-  float lv[16];
-  int li[16];
+#pragma unroll
   for (int k = 0; k < 16; ++k) { lv[k] = -INFINITY; li[k] = 0x7fffffff; }
-  float M = -INFINITY, S = 0.f;
-  for (int t = lane; t < p.n_tiles; t += 32) {
+  M = -INFINITY;
+  S = 0.f;
+  for (int t = t0; t < p.n_tiles; t += stride) {
     const float* rec = p.part + ((size_t)t * p.n_rows + row) * (2 + 2 * K);
-    const float m2 = rec[0], s2 = rec[1];
+    float r[2 + 2 * 16];
+#pragma unroll
+    for (int j = 0; j < 2 + 2 * 16; ++j) r[j] = j < 2 + 2 * K ? rec[j] : 0.f;
+    const float m2 = r[0], s2 = r[1];
     if (m2 != -INFINITY) {
       if (m2 > M) { S = S * expf(M - m2) + s2; M = m2; }
       else S += s2 * expf(m2 - M);
     }
-    for (int k = 0; k < K; ++k) {
-      float v = rec[2 + 2 * k];
-      int id = __float_as_int(rec[3 + 2 * k]);
-      if (id < 0) break;
-      if (!rank_before(v, id, lv[K - 1], li[K - 1])) break;   // records are sorted
-      int j = K - 1;
-      while (j > 0 && rank_before(v, id, lv[j - 1], li[j - 1])) { lv[j] = lv[j - 1]; li[j] = li[j - 1]; --j; }
-      lv[j] = v; li[j] = id;
+    if (t == t0) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int id = __float_as_int(r[3 + 2 * k]);
+        if (k < K && id >= 0) { lv[k] = r[2 + 2 * k]; li[k] = id; }
+      }
+      continue;
+    }
+    // insert each entry by a compare-and-swap pass (fixed indices keep the lists in registers)
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float cv = r[2 + 2 * k];
+      int ci = __float_as_int(r[3 + 2 * k]);
+      if (k >= K || ci < 0) continue;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (j < K && rank_before(cv, ci, lv[j], li[j])) {
+          const float tv = lv[j];
+          const int ti = li[j];
+          lv[j] = cv; li[j] = ci;
+          cv = tv; ci = ti;
+        }
+      }
     }
   }
-  // butterfly combine of (M, S)
+}
+
+// Warp reduction of the lanes' sorted lists and (max, sum-exp) pairs, in a fixed
+// butterfly order: lane 0 receives the K best (out_v, out_i) and the combined pair. Each
+// round takes the best list head over the lanes and pops it from its owner's list.
+EAGLE_DEV void head_merge_warp(int K, float* lv, int* li, float& M, float& S, int lane, float* out_v, int* out_i) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
@@ -151,10 +177,9 @@ EAGLE_DEV void head_merge_row(const HeadParams& p, int row, int lane) {
     if (mn != -INFINITY) S = S * expf(M - mn) + s2 * expf(m2 - mn);
     M = mn;
   }
-  int head = 0;
   for (int k = 0; k < K; ++k) {
-    float bv = head < K ? lv[head] : -INFINITY;
-    int bi = head < K ? li[head] : 0x7fffffff;
+    float bv = lv[0];
+    int bi = li[0];
     const int mine = bi;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -162,11 +187,15 @@ EAGLE_DEV void head_merge_row(const HeadParams& p, int row, int lane) {
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (rank_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
-    if (mine == bi && bi != 0x7fffffff) ++head;
+    if (mine == bi && bi != 0x7fffffff) {
+#pragma unroll
+      for (int j = 0; j < 15; ++j) { lv[j] = lv[j + 1]; li[j] = li[j + 1]; }
+      lv[15] = -INFINITY;
+      li[15] = 0x7fffffff;
+    }
     if (lane == 0) {
-      p.top_id[row * K + k] = bi == 0x7fffffff ? -1 : bi;
-      p.top_val[row * K + k] = bv;
+      out_v[k] = bv;
+      out_i[k] = bi;
     }
   }
-  if (lane == 0) p.lse[row] = (M == -INFINITY) ? -INFINITY : M + logf(S);
 }
