@@ -136,94 +136,6 @@ EAGLE_DEV void chain_epi(const ChainStep& st, int M, int tn, int tt, int BN, int
   }
 }
 
-// ---- completing a GEMM step's split tiles -------------------------------------------------------
-// Tile t of a GEMM step is split over CTAs cf..cl of its stream-K range. Every contributor
-// but the first starts its range inside t, so holds t in partial slot 0; the first holds t
-// in slot 1 when its range began in an earlier tile. Table entry: cf << 16 | ncon << 1 | that
-// slot. Built per CTA in shared memory (32-bit unit arithmetic: the host checks units * G
-// < 2^31).
-constexpr int CHAIN_MAX_TILES = 32 * 128 * 4 / 4;   // entries that fit the staging buffer
-
-__device__ __noinline__ void build_tile_table(const ChainStep& g, int G, int tid, uint32_t* tab) {
-  const int U = (int)g.units, gs = step_ctas(g.units, G);
-  const int tiles = U / g.kb;
-  for (int t = tid; t < tiles; t += 128) {
-    const int u0 = t * g.kb;
-    const int cf = ((u0 + 1) * gs - 1) / U, cl = ((u0 + g.kb) * gs - 1) / U;
-    const int first_unit = cf * U / gs;
-    tab[t] = ((uint32_t)cf << 16) | ((uint32_t)(cl - cf + 1) << 1) | (first_unit < u0 ? 1u : 0u);
-  }
-}
-
-// out = (out for a residual update) + the sum of the split tiles' partials in contributor order,
-// for every element of a split tile; whole tiles were written by the epilogue. Items of 4
-// features, NB items per thread in flight, contributors in groups of RC.
-template <int BN>
-__device__ __noinline__ void row_reduce(const ChainArgs& a, const ChainStep& g, int M, int t0, int stride, const uint32_t* tab) {
-  constexpr int NB = 2, RC = 4;
-  float* out = reinterpret_cast<float*>(g.out);
-  const bool add = g.epi == EPI_ADD_F32;
-  const int N4 = g.N / 4, n = M * N4;
-  for (int i0 = t0; i0 < n; i0 += NB * stride) {
-    int cf[NB], ncon[NB], s0[NB];
-    size_t off[NB], dst[NB];
-#pragma unroll
-    for (int q = 0; q < NB; ++q) {
-      const int i = i0 + q * stride;
-      ncon[q] = 0;
-      if (i < n) {
-        const int j = i / N4, f = (i - j * N4) * 4;
-        const int tt = j / BN, tile = (f >> 7) * g.tiles_t + tt;
-        const uint32_t e = tab[tile];
-        const int nc = (int)((e >> 1) & 0x7FFFu);
-        if (nc > 1) {
-          cf[q] = (int)(e >> 16);
-          ncon[q] = nc;
-          s0[q] = (int)(e & 1u);
-          off[q] = (size_t)(j - tt * BN) * 128 + (f & 127);
-          dst[q] = (size_t)j * g.ldo + f;
-        }
-      }
-    }
-    // partials summed in contributor order first, then added to the old value: the order
-    // of the single GEMM's split-tile epilogue
-    float4 acc[NB], base[NB];
-#pragma unroll
-    for (int q = 0; q < NB; ++q) {
-      acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      base[q] = (ncon[q] && add) ? __ldcg(reinterpret_cast<const float4*>(out + dst[q])) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    int nmax = 0;
-#pragma unroll
-    for (int q = 0; q < NB; ++q) nmax = max(nmax, ncon[q]);
-    for (int c0 = 0; c0 < nmax; c0 += RC) {
-      float4 v[NB][RC];
-#pragma unroll
-      for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int c = 0; c < RC; ++c)
-          if (c0 + c < ncon[q]) {
-            const int cc = cf[q] + c0 + c;
-            const int slot = (c0 + c == 0) ? s0[q] : 0;
-            v[q][c] = __ldcg(reinterpret_cast<const float4*>(a.partials + (size_t)(cc * 2 + slot) * BN * 128 + off[q]));
-          }
-#pragma unroll
-      for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int c = 0; c < RC; ++c)
-          if (c0 + c < ncon[q]) {
-            acc[q].x += v[q][c].x; acc[q].y += v[q][c].y; acc[q].z += v[q][c].z; acc[q].w += v[q][c].w;
-          }
-    }
-#pragma unroll
-    for (int q = 0; q < NB; ++q)
-      if (ncon[q]) {
-        if (add) { acc[q].x = base[q].x + acc[q].x; acc[q].y = base[q].y + acc[q].y; acc[q].z = base[q].z + acc[q].z; acc[q].w = base[q].w + acc[q].w; }
-        *reinterpret_cast<float4*>(out + dst[q]) = acc[q];
-      }
-  }
-}
-
 EAGLE_DEV void store4(__nv_bfloat16* p, float x, float y, float z, float w) {
   __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(p);
   q[0] = __floats2bfloat162_rn(x, y);
@@ -664,6 +576,50 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_before();
             mbar_arrive(smem_u32(tempty + acc));
+            // publish the partial: every thread fences, the CTA synchronises, one thread
+            // takes the tile's ticket between gpu-scope fences; the last contributor sums
+            // the partials in contributor order (two contributors' loads in flight)
+            __threadfence();
+            named_bar_sync(1, 128);
+            const int cf = cta_of_unit(tile * st.kb, U, gs);
+            const int cl = cta_of_unit((tile + 1) * st.kb - 1, U, gs);
+            if (leader) {
+              __threadfence();
+              const int old = atomicAdd(a.counters + tile, 1);
+              bcast[1] = (old == cl - cf) ? 1 : 0;
+              __threadfence();
+            }
+            named_bar_sync(1, 128);
+            if (bcast[1]) {
+              __threadfence();
+              // every contributor after the first began its range inside this tile (slot 0)
+              const int s_first = ((long long)cf * U / gs < tile * st.kb) ? 1 : 0;
+              for (int c0 = 0; c0 < BN; c0 += C::CH) {
+                float v[C::CH];
+#pragma unroll
+                for (int i = 0; i < C::CH; ++i) v[i] = 0.f;
+                for (int cc = cf; cc <= cl; cc += 2) {
+                  const bool two = cc + 1 <= cl;
+                  const float* p0 = a.partials + (size_t)(cc * 2 + (cc == cf ? s_first : 0)) * BN * 128 + c0 * 128 + row;
+                  const float* p1 = a.partials + (size_t)((cc + 1) * 2) * BN * 128 + c0 * 128 + row;
+                  float x0[C::CH], x1[C::CH];
+#pragma unroll
+                  for (int i = 0; i < C::CH; ++i) {
+                    x0[i] = __ldcg(p0 + i * 128);
+                    x1[i] = two ? __ldcg(p1 + i * 128) : 0.f;
+                  }
+#pragma unroll
+                  for (int i = 0; i < C::CH; ++i) v[i] += x0[i];
+                  if (two) {
+#pragma unroll
+                    for (int i = 0; i < C::CH; ++i) v[i] += x1[i];
+                  }
+                }
+                chain_epi<C::CH>(st, a.M, tn, tt, BN, row, c0, v);
+              }
+              if (leader) a.counters[tile] = 0;
+            }
+            named_bar_sync(1, 128);
           }
           u = seg_end;
           acc ^= 1;
@@ -682,13 +638,6 @@ __global__ void __launch_bounds__(192, 1)
           if (!ok) break;
         }
         switch (st.kind) {
-          case CH_REDUCE: {
-            uint32_t* tab = reinterpret_cast<uint32_t*>(staging);
-            build_tile_table(a.s[st.src], G, tid, tab);
-            named_bar_sync(1, 128);
-            row_reduce<BN>(a, a.s[st.src], a.M, t0, tstride, tab);
-            break;
-          }
           case CH_RMSNORM: row_rmsnorm(st, a.M, cta, G, tid, staging); break;
           case CH_SWIGLU: row_swiglu(st, a.M, t0, tstride); break;
           case CH_ROPE: row_rope(a.rope, a.M, t0, tstride, a.err); break;
@@ -790,7 +739,7 @@ static cudaError_t chain_launch_bn(cudaStream_t st, const ChainMaps& maps, const
 static_assert(sizeof(ChainArgs) + sizeof(ChainMaps) <= 4000, "chain kernel parameters exceed 4 KB");
 
 int chain_run(cudaStream_t st, const ChainProgram& p) {
-  if (p.M <= 0 || p.nsteps <= 0 || p.nsteps > CHAIN_MAX_STEPS || !p.bar || !p.partials) return -1;
+  if (p.M <= 0 || p.nsteps <= 0 || p.nsteps > CHAIN_MAX_STEPS || !p.bar || !p.partials || !p.counters) return -1;
   const int BN = gemm_bn_for(p.M);
   const int G = chain_sms();
   ChainMaps maps;
@@ -799,6 +748,7 @@ int chain_run(cudaStream_t st, const ChainProgram& p) {
   a.nsteps = p.nsteps;
   a.M = p.M;
   a.partials = p.partials;
+  a.counters = p.counters;
   a.bar = p.bar;
   a.err = p.err;
   auto aligned16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
@@ -811,21 +761,18 @@ int chain_run(cudaStream_t st, const ChainProgram& p) {
     if (c.kind == CH_SWIGLU && (c.H % 4 || !aligned16(c.in) || !aligned16(c.out))) return -1;
     if (c.kind == CH_ROPE && (a.rope.d % 8 || !aligned16(a.rope.qkv))) return -1;
     if (c.kind == CH_CONVERT && (c.H % 4 || c.ldi % 4 || c.ldo % 4 || !aligned16(c.in))) return -1;
-    if (c.kind == CH_REDUCE && (c.src != s - 1 || s == 0 || a.s[c.src].kind != CH_GEMM)) return -1;
     if (c.kind != CH_GEMM) continue;
     if (ng >= CHAIN_MAX_GEMMS) return -1;
     const ChainGemm& g = p.gemm[s];
     if (!g.W || !g.X || c.K % 8 || !aligned16(g.W) || !aligned16(g.X) || !aligned16(c.out)) return -1;
-    // fp32 outputs whose split tiles the next step completes
-    if ((c.epi != EPI_F32 && c.epi != EPI_ADD_F32) || c.N % 4 || c.ldo % 4) return -1;
-    if (s + 1 >= p.nsteps || a.s[s + 1].kind != CH_REDUCE) return -1;
+    if (c.epi != EPI_F32 && c.epi != EPI_BF16 && c.epi != EPI_ADD_F32) return -1;
     if (!make_tmap_bf16(&maps.w[ng], g.W, c.N, c.K, 128)) return -3;
     if (!make_tmap_bf16(&maps.x[ng], g.X, p.M, c.K, BN, g.ldx)) return -3;
     c.gemm = ng++;
     c.tiles_t = (p.M + BN - 1) / BN;
     c.kb = (c.K + 63) / 64;
     c.units = (long long)((c.N + 127) / 128) * c.tiles_t * c.kb;
-    if (c.units * G >= (1LL << 31) || c.units / c.kb > CHAIN_MAX_TILES) return -2;
+    if (c.units * G >= (1LL << 31) || c.units / c.kb > p.counters_len) return -2;
   }
   cudaError_t e;
   switch (BN) {

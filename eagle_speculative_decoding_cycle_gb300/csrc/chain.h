@@ -9,8 +9,7 @@
 
 namespace eagle {
 
-enum : int { CH_GEMM = 0, CH_RMSNORM = 1, CH_SWIGLU = 2, CH_ROPE = 3, CH_CONVERT = 4, CH_EMBED = 5, CH_CONCAT = 6,
-             CH_REDUCE = 7 };
+enum : int { CH_GEMM = 0, CH_RMSNORM = 1, CH_SWIGLU = 2, CH_ROPE = 3, CH_CONVERT = 4, CH_EMBED = 5, CH_CONCAT = 6 };
 constexpr int CHAIN_MAX_STEPS = 16;
 constexpr int CHAIN_MAX_GEMMS = 4;
 
@@ -23,10 +22,10 @@ constexpr int CHAIN_MAX_GEMMS = 4;
 //  CH_CONVERT  out[r][0:H] (row stride ldo) = in fp32 [r][0:H] (row stride ldi)
 //  CH_EMBED    out fp32 [M][H] = aux[idx[r]] (table of V rows)
 //  CH_CONCAT   out [M][2H] = [aux[idx[r]] ; in[idx2[r]]] (table of V rows; in [*][H])
-//  CH_REDUCE   completes the GEMM step before it (src): a GEMM step writes the tiles one
-//              CTA computes whole; the tiles stream-K splits across CTAs are left as fp32
-//              partial tiles, and this step adds them up in contributor order (onto the old
-//              values for EPI_ADD_F32) into the GEMM's output. Every GEMM step is followed by one.
+//
+// A GEMM step splits its (tile, k-block) units stream-K over the CTAs; the last contributor
+// to a split tile (per-tile ticket) sums the partial tiles in contributor order and writes
+// the tile, so every step's output is complete when the CTAs pass its barrier.
 struct ChainStep {
   int kind;
   int gemm;               // filled by chain_run: tensor-map pair index
@@ -40,7 +39,6 @@ struct ChainStep {
   const int* idx;
   const int* idx2;
   float eps;
-  int src;                // CH_REDUCE: the GEMM step it completes (the one just before)
 };
 
 struct ChainRope {
@@ -61,6 +59,7 @@ struct ChainArgs {
   ChainStep s[CHAIN_MAX_STEPS];
   ChainRope rope;
   float* partials;        // stream-K partial tiles, 2 per CTA
+  int* counters;          // per-tile arrival tickets, zero between launches
   unsigned* bar;          // [2] barrier arrivals and exit tickets, zero between launches
   int* err;
 };
@@ -81,6 +80,8 @@ struct ChainProgram {
   ChainArgs args{};
   ChainGemm gemm[CHAIN_MAX_STEPS]{};
   float* partials = nullptr;
+  int* counters = nullptr;
+  int counters_len = 0;
   unsigned* bar = nullptr;
   int* err = nullptr;
 
@@ -88,17 +89,12 @@ struct ChainProgram {
     ChainStep& s = args.s[nsteps++];
     s = ChainStep{};
     s.kind = kind;
-    s.src = -1;
     return s;
   }
-  // a projection (fp32 output) and the step that completes its split tiles
   void add_gemm(const void* W, int N, int K, const void* X, int epi, void* out, int ldo) {
-    const int g = nsteps;
-    gemm[g] = ChainGemm{W, X, 0};
+    gemm[nsteps] = ChainGemm{W, X, 0};
     ChainStep& s = add(CH_GEMM);
     s.N = N; s.K = K; s.epi = epi; s.out = out; s.ldo = ldo;
-    ChainStep& r = add(CH_REDUCE);
-    r.src = g;
   }
 };
 

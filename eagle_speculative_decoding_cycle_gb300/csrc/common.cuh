@@ -171,6 +171,18 @@ EAGLE_DEV void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint3
       : "memory");
 }
 
+// Orders this thread's earlier generic-proxy memory accesses with its later async-proxy
+// ones (bulk / tensor copies).
+EAGLE_DEV void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+// Contiguous bulk copy global -> shared memory (16-byte aligned addresses and size),
+// completion signalled on `bar` (complete_tx).
+EAGLE_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Bring one 2D tile of a tensor into L2 without touching shared memory.
 EAGLE_DEV void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

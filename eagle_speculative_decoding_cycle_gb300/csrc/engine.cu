@@ -330,6 +330,8 @@ ChainProgram chain_prog(eagle_ctx* ctx, int M) {
   ChainProgram p;
   p.M = M;
   p.partials = ctx->gemm_part;
+  p.counters = ctx->gemm_cnt;
+  p.counters_len = ctx->gemm_cnt_len;
   p.bar = ctx->chain_bar;
   p.err = ctx->dev_err;
   return p;
@@ -348,7 +350,6 @@ double chain_step_bytes(const ChainStep& s, const ChainProgram& p, int M) {
     case CH_CONVERT: return (double)M * s.H * (4 + 2);
     case CH_EMBED: return (double)M * s.H * (2 + 4);
     case CH_CONCAT: return (double)M * 2 * s.H * (2 + 2);
-    case CH_REDUCE: return 0.0;   // scratch traffic, not part of the layer's algorithmic bytes
   }
   return 0.0;
 }

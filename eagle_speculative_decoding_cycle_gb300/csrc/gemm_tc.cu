@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tfull = bars + 2 * C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* fixbar = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(smem_u32(tempty + b), 128);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(fixbar), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -138,38 +140,43 @@ __global__ void __launch_bounds__(192, 1)
       // The first ring of weight tiles does not depend on the previous kernel: issue it
       // before waiting for that kernel, then add the activation halves of those stages
       // once its outputs are visible.
+      // unit coordinates (k-block, weight tile, token tile), advanced without division
+      const long long tile0 = u_begin / a.kb;
+      const int k0 = (int)(u_begin - tile0 * a.kb), tn0 = (int)(tile0 / a.tiles_t),
+                tt0 = (int)(tile0 - (long long)tn0 * a.tiles_t);
+      int pk = k0, ptn = tn0, ptt = tt0;
+      auto advance = [&](int& k, int& tn, int& tt) {
+        if (++k == a.kb) { k = 0; if (++tt == a.tiles_t) { tt = 0; ++tn; } }
+      };
       const int n_pre = (int)min((long long)C::STAGES, u_end - u_begin);
       for (int i = 0; i < n_pre; ++i) {
-        const long long u = u_begin + i;
-        const long long tile = u / a.kb;
         const uint32_t fb = smem_u32(full + i);
         mbar_expect_tx(fb, C::STAGE);
-        tma_load_2d(smem_u32(smem + i * C::STAGE), &tmW, (int)(u - tile * a.kb) * 64, (int)(tile / a.tiles_t) * 128,
-                    fb, pol_w);
+        tma_load_2d(smem_u32(smem + i * C::STAGE), &tmW, pk * 64, ptn * 128, fb, pol_w);
         issued |= 1u << i;
+        advance(pk, ptn, ptt);
       }
       pdl_wait();
-      for (int i = 0; i < n_pre; ++i) {
-        const long long u = u_begin + i;
-        const long long tile = u / a.kb;
-        tma_load_2d(smem_u32(smem + i * C::STAGE) + C::A_BYTES, &tmX, (int)(u - tile * a.kb) * 64,
-                    (int)(tile % a.tiles_t) * BN, smem_u32(full + i), pol_x);
+      {
+        int bk = k0, btn = tn0, btt = tt0;
+        for (int i = 0; i < n_pre; ++i) {
+          tma_load_2d(smem_u32(smem + i * C::STAGE) + C::A_BYTES, &tmX, bk * 64, btt * BN, smem_u32(full + i), pol_x);
+          advance(bk, btn, btt);
+        }
       }
       stage = n_pre % C::STAGES;
       phase = (n_pre == C::STAGES) ? 1u : 0u;
       for (long long u = u_begin + n_pre; u < u_end; ++u) {
-        const long long tile = u / a.kb;
-        const int kb = (int)(u - tile * a.kb);
-        const int tn = (int)(tile / a.tiles_t), tt = (int)(tile % a.tiles_t);
         if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, abort_flag, a.err)) break;
         const uint32_t fb = smem_u32(full + stage);
         mbar_expect_tx(fb, C::STAGE);
         const uint32_t sa = smem_u32(smem + stage * C::STAGE);
-        tma_load_2d(sa, &tmW, kb * 64, tn * 128, fb, pol_w);
-        tma_load_2d(sa + C::A_BYTES, &tmX, kb * 64, tt * BN, fb, pol_x);
+        tma_load_2d(sa, &tmW, pk * 64, ptn * 128, fb, pol_w);
+        tma_load_2d(sa + C::A_BYTES, &tmX, pk * 64, ptt * BN, fb, pol_x);
         issued |= 1u << stage;
         parity = (parity & ~(1u << stage)) | (phase << stage);
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        advance(pk, ptn, ptt);
       }
       if (*abort_flag) {
         for (int s = 0; s < C::STAGES; ++s)
@@ -268,32 +275,65 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         if (bcast[1]) {
           __threadfence();
-          // Sum the contributors' rows in contributor order, two contributors' loads in
-          // flight together. Every contributor after the first began its range inside this
-          // tile (slot 0); the first holds it in slot 1 when its range began earlier.
+          // every contributor after the first began its range inside this tile (slot 0); the
+          // first holds it in slot 1 when its range began earlier
           const int s_first = ((long long)cf * U / G < tile * a.kb) ? 1 : 0;
-          for (int c0 = 0; c0 < BN; c0 += C::CH) {
-            float v[C::CH];
-#pragma unroll
-            for (int i = 0; i < C::CH; ++i) v[i] = 0.f;
-            for (int cc = cf; cc <= cl; cc += 2) {
-              const bool two = cc + 1 <= cl;
-              const float* p0 = a.partials + (size_t)(cc * 2 + (cc == cf ? s_first : 0)) * BN * 128 + c0 * 128 + row;
-              const float* p1 = a.partials + (size_t)((cc + 1) * 2) * BN * 128 + c0 * 128 + row;
-              float x0[C::CH], x1[C::CH];
-#pragma unroll
-              for (int i = 0; i < C::CH; ++i) {
-                x0[i] = __ldcg(p0 + i * 128);
-                x1[i] = two ? __ldcg(p1 + i * 128) : 0.f;
+          const int ncon = cl - cf + 1;
+          constexpr uint32_t PART = (uint32_t)BN * 128 * 4;
+          if (seg_end == u_end && (uint32_t)ncon * PART <= (uint32_t)(C::STAGES * C::STAGE)) {
+            // The CTA's last tile: the ring is idle (every stage consumed), so the partials
+            // come in as bulk copies, all in flight at once, and are summed from shared
+            // memory in contributor order.
+            if (leader) {
+              fence_proxy_async_all();
+              mbar_expect_tx(smem_u32(fixbar), (uint32_t)ncon * PART);
+              for (int q = 0; q < ncon; ++q) {
+                const int cc = cf + q;
+                bulk_load(smem_u32(smem + (size_t)q * PART),
+                          a.partials + (size_t)(cc * 2 + (q == 0 ? s_first : 0)) * BN * 128, PART,
+                          smem_u32(fixbar));
               }
+              bcast[0] = mbar_wait(smem_u32(fixbar), 0, abort_flag, a.err) ? 1 : 0;
+            }
+            named_bar_sync(1, 128);
+            const float* sp = reinterpret_cast<const float*>(smem);
+            if (bcast[0]) {
+              for (int c0 = 0; c0 < BN; c0 += C::CH) {
+                float v[C::CH];
 #pragma unroll
-              for (int i = 0; i < C::CH; ++i) v[i] += x0[i];
-              if (two) {
+                for (int i = 0; i < C::CH; ++i) v[i] = 0.f;
+                for (int q = 0; q < ncon; ++q)
 #pragma unroll
-                for (int i = 0; i < C::CH; ++i) v[i] += x1[i];
+                  for (int i = 0; i < C::CH; ++i) v[i] += sp[(size_t)q * BN * 128 + (c0 + i) * 128 + row];
+                epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
               }
             }
-            epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+          } else {
+            // Sum the contributors' rows in contributor order, two contributors' loads in
+            // flight together.
+            for (int c0 = 0; c0 < BN; c0 += C::CH) {
+              float v[C::CH];
+#pragma unroll
+              for (int i = 0; i < C::CH; ++i) v[i] = 0.f;
+              for (int cc = cf; cc <= cl; cc += 2) {
+                const bool two = cc + 1 <= cl;
+                const float* p0 = a.partials + (size_t)(cc * 2 + (cc == cf ? s_first : 0)) * BN * 128 + c0 * 128 + row;
+                const float* p1 = a.partials + (size_t)((cc + 1) * 2) * BN * 128 + c0 * 128 + row;
+                float x0[C::CH], x1[C::CH];
+#pragma unroll
+                for (int i = 0; i < C::CH; ++i) {
+                  x0[i] = __ldcg(p0 + i * 128);
+                  x1[i] = two ? __ldcg(p1 + i * 128) : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < C::CH; ++i) v[i] += x0[i];
+                if (two) {
+#pragma unroll
+                  for (int i = 0; i < C::CH; ++i) v[i] += x1[i];
+                }
+              }
+              epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+            }
           }
           if (leader) a.counters[tile] = 0;
         }
