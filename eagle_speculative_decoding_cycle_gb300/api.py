@@ -188,9 +188,11 @@ def gemm(W: torch.Tensor, X: torch.Tensor, epi: int = 0, out: Optional[torch.Ten
     lib = L.lib()
     N, K = W.shape
     M = X.shape[0]
+    if epi == 4:            # SwiGLU: W holds [gate; up], the output has half as many features
+        N //= 2
     if out is None:
-        out = torch.zeros(M, N, dtype=torch.bfloat16 if epi == 1 else torch.float32, device=X.device)
-    nb = lib.eagle_op_gemm_scratch_bytes(M, N)
+        out = torch.zeros(M, N, dtype=torch.bfloat16 if epi in (1, 4) else torch.float32, device=X.device)
+    nb = lib.eagle_op_gemm_scratch_bytes(M, 2 * N if epi == 4 else N)
     scratch = torch.zeros(max(nb, 1), dtype=torch.uint8, device=X.device)
     rc = lib.eagle_op_gemm(_dtype_code(W), _stream(stream), W.data_ptr(), N, K, X.data_ptr(), M, epi,
                            out.data_ptr(), out.stride(0), scratch.data_ptr(), nb)

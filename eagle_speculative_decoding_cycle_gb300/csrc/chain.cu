@@ -210,9 +210,8 @@ __device__ __noinline__ void row_rmsnorm(const ChainStep& st, int M, int cta, in
   }
 }
 
-// 4 consecutive features per item (F % 4 == 0, so rows of gu stay 16-byte aligned), two
+// 4 consecutive features per item (F % 4 == 0, so rows of gu stay 16-byte aligned), four
 // items in flight per thread.
-EAGLE_DEV float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 __device__ __noinline__ void row_swiglu(const ChainStep& st, int M, int t0, int stride) {
   const float* gu = reinterpret_cast<const float*>(st.in);
@@ -346,10 +345,13 @@ __device__ __noinline__ void row_rope(const ChainRope& p, int M, int t0, int str
         const float4 a = x0[u], b = x1[u];
         __nv_bfloat16* dst = h < p.nq ? q + ((size_t)r[u] * p.nq + h) * p.d
                                       : kc + ((size_t)(seq[u] * p.nkv + (h - p.nq)) * p.cap + slot[u]) * p.d;
-        store4(dst + e, a.x * c.x - b.x * sn.x, a.y * c.y - b.y * sn.y, a.z * c.z - b.z * sn.z,
-               a.w * c.w - b.w * sn.w);
-        store4(dst + e + half, b.x * c.x + a.x * sn.x, b.y * c.y + a.y * sn.y, b.z * c.z + a.z * sn.z,
-               b.w * c.w + a.w * sn.w);
+        float l0, l1, l2, l3, h0, h1, h2, h3;
+        rope_pair(a.x, b.x, c.x, sn.x, l0, h0);
+        rope_pair(a.y, b.y, c.y, sn.y, l1, h1);
+        rope_pair(a.z, b.z, c.z, sn.z, l2, h2);
+        rope_pair(a.w, b.w, c.w, sn.w, l3, h3);
+        store4(dst + e, l0, l1, l2, l3);
+        store4(dst + e + half, h0, h1, h2, h3);
       } else {
         if (!slot_ok) continue;
         const int jj = j[u] - rot;

@@ -38,6 +38,16 @@ EAGLE_DEV void latch_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// ---- shared element-wise arithmetic (one definition, so fused and separate kernels agree
+// bit for bit) --------------------------------------------------------------------------------
+// Rotate-half RoPE of the pair (a = x[i], b = x[i + d/2]) by the angle with cosine c, sine s.
+__device__ __forceinline__ void rope_pair(float a, float b, float c, float s, float& lo, float& hi) {
+  lo = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+  hi = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s));
+}
+// SwiGLU gate: silu(g) * u.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.f, expf(-g))), u); }
+
 // ---- element traits ---------------------------------------------------------------------
 template <typename T> struct Elem;
 template <> struct Elem<float> {

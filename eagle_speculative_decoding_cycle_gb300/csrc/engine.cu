@@ -143,6 +143,7 @@ struct eagle_ctx {
   float *attn_po, *attn_pml; size_t attn_pfloats;
   unsigned* chain_bar;                  // grid-barrier words of the layer-chain kernel
   int use_chain = 0;                    // bf16: run each layer as chain launches (EAGLE_CHAIN=1 turns them on)
+  int fuse_epi = 0;                     // bf16: RoPE/KV write and SwiGLU in the GEMM epilogues (EAGLE_FUSE_EPI=1: on)
   float *rope_cos, *rope_sin;
   void *kc, *vc, *dkc, *dvc;
   int* prompt_copy;   // unused placeholder
@@ -226,18 +227,19 @@ int fail(eagle_ctx* c, int code, const std::string& msg) {
 
 // ---- building blocks -------------------------------------------------------------------------
 int gemm(eagle_ctx* ctx, const void* W, int N, int K, const void* X, int M, int epi, void* out, int ldo,
-         const HeadParams* head = nullptr) {
+         const HeadParams* head = nullptr, const QkvEpi* qkv = nullptr) {
   const Dims& z = ctx->z;
   if (z.dt == DT_BF16) {
     const bool prof = ctx->prof_on && 2 * (ctx->prof_n + 1) <= (int)ctx->prof_ev.size();
     if (prof) cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n], ctx->st);
     const int r = gemm_bf16(ctx->st, W, N, K, X, M, epi, out, ldo, ctx->gemm_part, ctx->gemm_cnt, ctx->gemm_cnt_len,
-                            ctx->dev_err, head);
+                            ctx->dev_err, head, true, qkv);
     if (prof) {
       cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n + 1], ctx->st);
-      // algorithmic bytes: weight + activation in + output (fp32, or bf16 / head records)
-      const double ob = epi == EPI_HEAD ? 0.0 : (double)M * N * (epi == EPI_BF16 ? 2 : 4) * (epi == EPI_ADD_F32 ? 2 : 1);
-      ctx->prof_bytes[ctx->prof_n] = (double)N * K * 2 + (double)M * K * 2 + ob;
+      // algorithmic bytes: weight + activation in + output (fp32, bf16, none for the head)
+      const bool b16 = epi == EPI_BF16 || epi == EPI_SWIGLU || epi == EPI_QKV;
+      const double ob = epi == EPI_HEAD ? 0.0 : (double)M * N * (b16 ? 2 : 4) * (epi == EPI_ADD_F32 ? 2 : 1);
+      ctx->prof_bytes[ctx->prof_n] = (double)N * K * 2 * (epi == EPI_SWIGLU ? 2 : 1) + (double)M * K * 2 + ob;
       ++ctx->prof_n;
     }
     return r;
@@ -306,15 +308,26 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
                   void* vcache, int cap, int rows_per_seq, const int* pos, const int* slot, const int* seq, int mode,
                   int tree_T, const uint64_t* mask, int mask_words) {
   const Dims& z = ctx->z;
-  CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_F32, ctx->qkv, z.QKV));
-  CK(rope_store(ctx->st, z.dt, ctx->qkv, R, z.nq, z.nkv, z.d, pos, slot, seq, ctx->rope_cos, ctx->rope_sin, ctx->qb,
-                kcache, vcache, cap, ctx->dev_err, cap));
+  if (z.dt == DT_BF16 && ctx->fuse_epi && 128 % z.d == 0) {
+    // RoPE, the q output and the KV-cache write in the projection's epilogue
+    const QkvEpi q{pos, slot, seq, ctx->rope_cos, ctx->rope_sin, ctx->qb, kcache, vcache, z.nq, z.nkv, z.d, cap};
+    CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_QKV, nullptr, 0, nullptr, &q));
+  } else {
+    CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_F32, ctx->qkv, z.QKV));
+    CK(rope_store(ctx->st, z.dt, ctx->qkv, R, z.nq, z.nkv, z.d, pos, slot, seq, ctx->rope_cos, ctx->rope_sin,
+                  ctx->qb, kcache, vcache, cap, ctx->dev_err, cap));
+  }
   int r = attend(ctx, kcache, vcache, cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words);
   if (r) return r;
   CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
   CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
-  CK(gemm(ctx, lw.wgu, 2 * z.F, z.H, ctx->ain, R, EPI_F32, ctx->gu, 2 * z.F));
-  CK(swiglu_rows(ctx->st, z.dt, ctx->gu, z.F, R, ctx->hb));
+  if (z.dt == DT_BF16 && ctx->fuse_epi && z.F % 64 == 0) {
+    // gate and up rows of each 64 features share one tile; SwiGLU in the epilogue
+    CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_SWIGLU, ctx->hb, z.F));
+  } else {
+    CK(gemm(ctx, lw.wgu, 2 * z.F, z.H, ctx->ain, R, EPI_F32, ctx->gu, 2 * z.F));
+    CK(swiglu_rows(ctx->st, z.dt, ctx->gu, z.F, R, ctx->hb));
+  }
   CK(gemm(ctx, lw.wd, z.H, z.F, ctx->hb, R, EPI_ADD_F32, ctx->x, z.H));
   return 0;
 }
@@ -781,6 +794,7 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
   ctx->w.layers = ctx->layers.data();
   ctx->st = reinterpret_cast<cudaStream_t>(stream);
   if (getenv("EAGLE_CHAIN")) ctx->use_chain = strcmp(getenv("EAGLE_CHAIN"), "0") != 0;
+  if (getenv("EAGLE_FUSE_EPI")) ctx->fuse_epi = strcmp(getenv("EAGLE_FUSE_EPI"), "0") != 0;
   Carver c;
   c.base = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(workspace), 256));
   carve(c, ctx, z);

@@ -44,11 +44,97 @@ struct GemmArgs {
   int* counters;
   int* err;
   HeadParams head;
+  QkvEpi qkv;
 };
 
-template <int CH>
+// Epilogue variants, one kernel instantiation each: generic (store / residual add / fused LM
+// head, chosen by a.epi), SwiGLU of [gate; up] tile pairs, RoPE + KV-cache write of QKV.
+enum { MODE_GENERIC = 0, MODE_QKV = 1, MODE_SWIGLU = 2 };
+
+template <int CH, int MODE>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int BN, int row, int c0,
                                           const float* v, float* staging, int ew, int lane) {
+  if constexpr (MODE == MODE_SWIGLU) {
+    // accumulator rows 0-63: gate features tn*64.., rows 64-127: the matching up features
+    if (row >= 64) {
+#pragma unroll
+      for (int i = 0; i < CH; ++i) staging[i * 64 + (row - 64)] = v[i];
+    }
+    named_bar_sync(2, 128);
+    const int f = tn * 64 + row;
+    if (row < 64 && f < a.N) {
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const int j = tt * BN + c0 + i;
+        if (j < a.M) o[(size_t)j * a.ldo + f] = __float2bfloat16_rn(silu_mul(v[i], staging[i * 64 + row]));
+      }
+    }
+    named_bar_sync(2, 128);
+    return;
+  }
+  if constexpr (MODE == MODE_QKV) {
+    const QkvEpi& q = a.qkv;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) staging[i * 128 + row] = v[i];
+    named_bar_sync(2, 128);
+    const int f = tn * 128 + row;
+    if (f < a.N) {
+      const int d = q.d, half = d >> 1;
+      const int h = f / d, e = f - h * d;
+      const bool lo_half = e < half;
+      const int prow = lo_half ? row + half : row - half;
+      __nv_bfloat16* qo = reinterpret_cast<__nv_bfloat16*>(q.q);
+      __nv_bfloat16* ko = reinterpret_cast<__nv_bfloat16*>(q.kc);
+      __nv_bfloat16* vo = reinterpret_cast<__nv_bfloat16*>(q.vc);
+      const bool roped = h < q.nq + q.nkv;
+      const int eh = lo_half ? e : e - half;
+      // eight columns at a time: their token metadata and cos/sin entries are loaded
+      // together, then rotated and stored
+#pragma unroll
+      for (int i0 = 0; i0 < CH; i0 += 8) {
+        int sl[8], sq[8];
+        float cs[8], sn[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int j = min(tt * BN + c0 + i0 + i, a.M - 1);
+          sl[i] = q.slot[j];
+          sq[i] = q.seq[j];
+          if (roped) {
+            const int ci = q.pos[j] * half + eh;
+            cs[i] = q.cos[ci];
+            sn[i] = q.sin[ci];
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int j = tt * BN + c0 + i0 + i;
+          if (j >= a.M) break;
+          const float x = v[i0 + i];
+          const int slot = sl[i];
+          const bool slot_ok = slot >= 0 && slot < q.cap;
+          if (roped) {
+            const float y = staging[(i0 + i) * 128 + prow];
+            float lo, hi;
+            if (lo_half) rope_pair(x, y, cs[i], sn[i], lo, hi);
+            else rope_pair(y, x, cs[i], sn[i], lo, hi);
+            const float r = lo_half ? lo : hi;
+            if (h < q.nq) {
+              qo[((size_t)j * q.nq + h) * d + e] = __float2bfloat16_rn(r);
+            } else if (slot_ok) {
+              ko[((size_t)(sq[i] * q.nkv + (h - q.nq)) * q.cap + slot) * d + e] = __float2bfloat16_rn(r);
+            } else if (e == 0) {
+              latch_error(a.err, DEVERR_CAPACITY);
+            }
+          } else if (slot_ok) {
+            vo[((size_t)(sq[i] * q.nkv + (h - q.nq - q.nkv)) * q.cap + slot) * d + e] = __float2bfloat16_rn(x);
+          }
+        }
+      }
+    }
+    named_bar_sync(2, 128);
+    return;
+  }
   const int f = tn * 128 + row;
   if (a.epi == EPI_ADD_F32) {
     if (f < a.N) {
@@ -86,7 +172,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int
   }
 }
 
-template <int BN>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const GemmArgs a) {
@@ -145,6 +231,15 @@ __global__ void __launch_bounds__(192, 1)
       const int k0 = (int)(u_begin - tile0 * a.kb), tn0 = (int)(tile0 / a.tiles_t),
                 tt0 = (int)(tile0 - (long long)tn0 * a.tiles_t);
       int pk = k0, ptn = tn0, ptt = tt0;
+      // weight tile (128 rows x 64 k); SwiGLU: 64 gate rows + the matching 64 up rows
+      auto load_w = [&](uint32_t dst, int k, int tn, uint32_t bar) {
+        if constexpr (MODE == MODE_SWIGLU) {
+          tma_load_2d(dst, &tmW, k * 64, tn * 64, bar, pol_w);
+          tma_load_2d(dst + C::A_BYTES / 2, &tmW, k * 64, a.N + tn * 64, bar, pol_w);
+        } else {
+          tma_load_2d(dst, &tmW, k * 64, tn * 128, bar, pol_w);
+        }
+      };
       auto advance = [&](int& k, int& tn, int& tt) {
         if (++k == a.kb) { k = 0; if (++tt == a.tiles_t) { tt = 0; ++tn; } }
       };
@@ -152,7 +247,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int i = 0; i < n_pre; ++i) {
         const uint32_t fb = smem_u32(full + i);
         mbar_expect_tx(fb, C::STAGE);
-        tma_load_2d(smem_u32(smem + i * C::STAGE), &tmW, pk * 64, ptn * 128, fb, pol_w);
+        load_w(smem_u32(smem + i * C::STAGE), pk, ptn, fb);
         issued |= 1u << i;
         advance(pk, ptn, ptt);
       }
@@ -171,7 +266,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t fb = smem_u32(full + stage);
         mbar_expect_tx(fb, C::STAGE);
         const uint32_t sa = smem_u32(smem + stage * C::STAGE);
-        tma_load_2d(sa, &tmW, pk * 64, ptn * 128, fb, pol_w);
+        load_w(sa, pk, ptn, fb);
         tma_load_2d(sa + C::A_BYTES, &tmX, pk * 64, ptt * BN, fb, pol_x);
         issued |= 1u << stage;
         parity = (parity & ~(1u << stage)) | (phase << stage);
@@ -244,7 +339,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int c0 = 0; c0 < BN; c0 += C::CH) {
           float v[C::CH];
           if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
-          epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+          epi_chunk<C::CH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(tempty + acc));
@@ -305,7 +400,7 @@ __global__ void __launch_bounds__(192, 1)
                 for (int q = 0; q < ncon; ++q)
 #pragma unroll
                   for (int i = 0; i < C::CH; ++i) v[i] += sp[(size_t)q * BN * 128 + (c0 + i) * 128 + row];
-                epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+                epi_chunk<C::CH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
               }
             }
           } else {
@@ -332,7 +427,7 @@ __global__ void __launch_bounds__(192, 1)
                   for (int i = 0; i < C::CH; ++i) v[i] += x1[i];
                 }
               }
-              epi_chunk<C::CH>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+              epi_chunk<C::CH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
             }
           }
           if (leader) a.counters[tile] = 0;
@@ -418,13 +513,14 @@ int gemm_bn_for(int M) {
 
 size_t gemm_bf16_scratch_bytes() { return (size_t)num_sms_cap() * 2 * 256 * 128 * sizeof(float); }
 
-template <int BN>
+template <int BN, int MODE>
 static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int tiles_n,
                              cudaStream_t st) {
   using C = TcCfg<BN>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_bf16_tc<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -434,32 +530,48 @@ static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmA
   int G = num_sms();
   if (G > num_sms_cap()) G = num_sms_cap();
   if ((long long)G > a.units) G = (int)a.units;
-  launch_k(gemm_bf16_tc<BN>, G, 192, C::SMEM, st, mw, mx, a);
+  launch_k(gemm_bf16_tc<BN, MODE>, G, 192, C::SMEM, st, mw, mx, a);
   return cudaGetLastError();
+}
+
+template <int BN>
+static cudaError_t launch_mode(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int tiles_n,
+                               cudaStream_t st) {
+  if (a.epi == EPI_SWIGLU) return launch_bn<BN, MODE_SWIGLU>(mw, mx, a, tiles_n, st);
+  if (a.epi == EPI_QKV) return launch_bn<BN, MODE_QKV>(mw, mx, a, tiles_n, st);
+  return launch_bn<BN, MODE_GENERIC>(mw, mx, a, tiles_n, st);
 }
 
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
               int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head,
-              bool cache_maps) {
+              bool cache_maps, const QkvEpi* qkv) {
   if (M <= 0 || N <= 0 || K <= 0 || (K % 8) != 0 || !W || !X) return -1;
   if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(X)) & 15) return -1;
+  if (epi == EPI_SWIGLU && N % 64) return -1;
+  if (epi == EPI_QKV && (!qkv || qkv->d < 2 || qkv->d % 2 || 128 % qkv->d || N != (qkv->nq + 2 * qkv->nkv) * qkv->d))
+    return -1;
   const int BN = gemm_bn_for(M);
-  const int tiles_n = (N + 127) / 128;
+  const int tiles_n = epi == EPI_SWIGLU ? N / 64 : (N + 127) / 128;
   if ((long long)tiles_n * ((M + BN - 1) / BN) > counters_len) return -2;
   CUtensorMap mw, mx;
-  if (!make_map(&mw, W, N, K, 128, cache_maps)) return -3;
+  if (epi == EPI_SWIGLU) {
+    if (!make_map(&mw, W, 2LL * N, K, 64, cache_maps)) return -3;
+  } else if (!make_map(&mw, W, N, K, 128, cache_maps)) {
+    return -3;
+  }
   if (!make_map(&mx, X, M, K, BN, cache_maps)) return -3;
   GemmArgs a{};
   a.M = M; a.N = N; a.K = K; a.epi = epi; a.out = out; a.ldo = ldo;
   a.partials = partials; a.counters = counters; a.err = err;
   if (head) a.head = *head;
+  if (qkv) a.qkv = *qkv;
   cudaError_t e;
   switch (BN) {
-    case 16: e = launch_bn<16>(mw, mx, a, tiles_n, st); break;
-    case 32: e = launch_bn<32>(mw, mx, a, tiles_n, st); break;
-    case 64: e = launch_bn<64>(mw, mx, a, tiles_n, st); break;
-    case 128: e = launch_bn<128>(mw, mx, a, tiles_n, st); break;
-    default: e = launch_bn<256>(mw, mx, a, tiles_n, st); break;
+    case 16: e = launch_mode<16>(mw, mx, a, tiles_n, st); break;
+    case 32: e = launch_mode<32>(mw, mx, a, tiles_n, st); break;
+    case 64: e = launch_mode<64>(mw, mx, a, tiles_n, st); break;
+    case 128: e = launch_mode<128>(mw, mx, a, tiles_n, st); break;
+    default: e = launch_mode<256>(mw, mx, a, tiles_n, st); break;
   }
   return e == cudaSuccess ? 0 : -4;
 }

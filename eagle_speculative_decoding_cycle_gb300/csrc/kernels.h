@@ -30,7 +30,22 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_ADD_F32 = 2, EPI_HEAD = 3 };
+enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_ADD_F32 = 2, EPI_HEAD = 3, EPI_SWIGLU = 4, EPI_QKV = 5 };
+
+// EPI_QKV: the fused [q | k | v] projection's epilogue applies rotate-half RoPE to the q and
+// k heads (pairs inside one 128-row tile: head_dim divides 128), writes q to its buffer
+// [R][nq][d] and k, v into the cache at each row's slot (storage bf16).
+struct QkvEpi {
+  const int* pos;
+  const int* slot;
+  const int* seq;
+  const float* cos;       // [positions][d / 2]
+  const float* sin;
+  void* q;
+  void* kc;               // [(seq * nkv + h) * cap + slot][d]
+  void* vc;
+  int nq, nkv, d, cap;
+};
 enum { DT_F32 = 0, DT_BF16 = 1 };
 
 inline int num_sms_cap() { return 192; }
@@ -41,7 +56,8 @@ size_t gemm_bf16_scratch_bytes();
 // bf16 tcgen05 GEMM, Y[M][N] = X[M][K] W[N][K]^T. Returns 0 or a negative code.
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
               int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head,
-              bool cache_maps = true);
+              bool cache_maps = true, const QkvEpi* qkv = nullptr);
+// EPI_SWIGLU: W is [2N][K] ([gate; up]), out bf16 [M][ldo] = silu(X Wg^T) * (X Wu^T); N % 64 == 0.
 // Tensor map of a bf16 row-major [rows][K] matrix (row stride ld elements, 0 = K): boxes of
 // 64 (K) x box_rows, 128-byte swizzle. Cached by (ptr, rows, K, box_rows, ld).
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, long long K, int box_rows, long long ld = 0);

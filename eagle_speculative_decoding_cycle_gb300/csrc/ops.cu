@@ -117,10 +117,10 @@ __global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int
   const float* sr = rsn + (size_t)pos * half;
   T* dst = h < nq ? q_out + ((size_t)r * nq + h) * d : kc + ((size_t)(seq * nkv + (h - nq)) * cap + slot) * d;
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    const float a = src[i], b = src[i + half];
-    const float c = cr[i], s = sr[i];
-    dst[i] = Elem<T>::from_f(a * c - b * s);
-    dst[i + half] = Elem<T>::from_f(b * c + a * s);
+    float lo, hi;
+    rope_pair(src[i], src[i + half], cr[i], sr[i], lo, hi);
+    dst[i] = Elem<T>::from_f(lo);
+    dst[i + half] = Elem<T>::from_f(hi);
   }
 }
 
@@ -151,10 +151,7 @@ __global__ void swiglu_k(const float* gu, int F, T* out) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = i0 + j;
-    if (i < F) {
-      const float a = g[i];
-      out[(size_t)r * F + i] = Elem<T>::from_f(a / (1.f + expf(-a)) * g[F + i]);
-    }
+    if (i < F) out[(size_t)r * F + i] = Elem<T>::from_f(silu_mul(g[i], g[F + i]));
   }
 }
 

@@ -35,11 +35,12 @@ int eagle_op_gemm(int dtype, void* stream, const void* W, int N, int K, const vo
     if (epi != EPI_F32 && epi != EPI_ADD_F32) return EAGLE_EINVAL;
     return gemm_f32(st, (const float*)W, N, K, (const float*)X, M, epi, (float*)out, ldo) == 0 ? EAGLE_OK : EAGLE_ECUDA;
   }
-  if (dtype != EAGLE_DTYPE_BF16 || epi < 0 || epi > 2 || K % 8) return EAGLE_EINVAL;
-  if (!scratch || scratch_bytes < eagle_op_gemm_scratch_bytes(M, N)) return EAGLE_ECAPACITY;
+  if (dtype != EAGLE_DTYPE_BF16 || epi < 0 || epi == EPI_HEAD || epi > EPI_SWIGLU || K % 8) return EAGLE_EINVAL;
+  const int tiles_N = epi == EPI_SWIGLU ? 2 * N : N;   // SwiGLU: W has 2N rows, tiles of 64 + 64
+  if (!scratch || scratch_bytes < eagle_op_gemm_scratch_bytes(M, tiles_N)) return EAGLE_ECAPACITY;
   float* part = reinterpret_cast<float*>(scratch);
   int* cnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(scratch) + al(gemm_bf16_scratch_bytes()));
-  const int r = gemm_bf16(st, W, N, K, X, M, epi, out, ldo, part, cnt, tiles_for(M, N), nullptr, nullptr);
+  const int r = gemm_bf16(st, W, N, K, X, M, epi, out, ldo, part, cnt, tiles_for(M, tiles_N), nullptr, nullptr);
   return r == 0 ? EAGLE_OK : (r == -4 ? EAGLE_ECUDA : EAGLE_EINVAL);
 }
 

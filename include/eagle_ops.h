@@ -22,9 +22,11 @@ extern "C" {
  * target and drafter projection and the LM head). dtype EAGLE_DTYPE_BF16: tcgen05
  * tensor-core kernel, X and W bf16 row-major with K a multiple of 8 and 16-byte
  * aligned bases; dtype EAGLE_DTYPE_F32: fp32 FFMA kernel. epi: 0 = store fp32 Y,
- * 1 = store bf16 Y (bf16 only), 2 = Y += result (fp32 residual update). out has row
- * stride ldo elements. Scratch holds split-tile partial sums and per-tile tickets; it
- * must be zero-filled before the first call and is left zeroed by every call. */
+ * 1 = store bf16 Y (bf16 only), 2 = Y += result (fp32 residual update), 4 = SwiGLU
+ * (bf16 only, N % 64 == 0): W holds 2N rows [Wgate; Wup] and out (bf16, [M][N]) receives
+ * silu(X Wgate^T) * (X Wup^T); size its scratch with eagle_op_gemm_scratch_bytes(M, 2N).
+ * out has row stride ldo elements. Scratch holds split-tile partial sums and per-tile
+ * tickets; it must be zero-filled before the first call and is left zeroed by every call. */
 size_t eagle_op_gemm_scratch_bytes(int M, int N);
 int eagle_op_gemm(int dtype, void* stream, const void* W, int N, int K, const void* X, int M, int epi,
                   void* out, int ldo, void* scratch, size_t scratch_bytes);

@@ -22,16 +22,18 @@ def _built():
     __graft_entry__.build()
 
 
-def _run(wl, weights, prompts, chain: bool, max_batch=1):
-    old = os.environ.get("EAGLE_CHAIN")
+def _run(wl, weights, prompts, chain: bool, max_batch=1, fuse: bool = True):
+    saved = {k: os.environ.get(k) for k in ("EAGLE_CHAIN", "EAGLE_FUSE_EPI")}
     os.environ["EAGLE_CHAIN"] = "1" if chain else "0"
+    os.environ["EAGLE_FUSE_EPI"] = "1" if fuse else "0"
     try:
         eng = api.Engine(wl, weights, max_batch=max_batch)
     finally:
-        if old is None:
-            del os.environ["EAGLE_CHAIN"]
-        else:
-            os.environ["EAGLE_CHAIN"] = old
+        for k, v in saved.items():
+            if v is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = v
     eng.prefill([p.to(DEV) for p in prompts])
     eng.sync()
     st = eng.dump(L.DUMP_STATE)
@@ -89,3 +91,19 @@ def test_chain_prefill_many_rows():
     assert np.max(np.abs(a["feat0"].numpy() - b["feat0"].numpy())) < 5e-2
     assert a["root"].tolist() == b["root"].tolist()
     assert np.allclose(a["cand_logc"].numpy(), b["cand_logc"].numpy(), atol=3e-2)
+
+
+@pytest.mark.parametrize("name", ["small-bf16-3L-H320", "small-bf16-eagle3-gqa"])
+def test_fused_epilogues_match_separate_kernels(name):
+    """RoPE/KV-write and SwiGLU in the GEMM epilogues against the separate row kernels: the
+    same fp32 values go through the same arithmetic, so every output is bit-identical."""
+    wl = {w.name: w for w in (synth.SMALL_BF16, synth.SMALL_BF16_E3)}[name]
+    weights = {k: v.to(DEV) for k, v in synth.make_weights(wl, "cpu").items()}
+    prompts = synth.make_prompts(wl)[:1]
+    a = _run(wl, weights, prompts, chain=False, fuse=True)
+    b = _run(wl, weights, prompts, chain=False, fuse=False)
+    assert torch.equal(a["feat0"], b["feat0"])
+    assert a["root"].tolist() == b["root"].tolist()
+    assert torch.equal(a["cand_logc"], b["cand_logc"]) and torch.equal(a["cand_tok"], b["cand_tok"])
+    assert torch.equal(a["tree"], b["tree"]) and torch.equal(a["logits"], b["logits"])
+    assert a["out"].tolist() == b["out"].tolist() and a["cnt"].tolist() == b["cnt"].tolist()

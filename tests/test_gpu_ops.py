@@ -300,3 +300,19 @@ def test_attention_split_kv_long_context(nq, nkv, T, ctx):
     assert np.max(np.abs(split - want)) < 2e-2
     assert np.max(np.abs(single - want)) < 2e-2
     assert np.max(np.abs(split - single)) < 2e-2
+
+
+@pytest.mark.parametrize("M,F,K", [(61, 11008 // 4, 1024), (10, 832, 320), (1, 640, 256), (130, 704, 264)])
+def test_gemm_bf16_swiglu_epilogue(M, F, K):
+    """Gate/up projection with SwiGLU in the epilogue: bf16(silu(X Wg^T) * (X Wu^T))."""
+    g = torch.Generator().manual_seed(F + M)
+    X = _rand((M, K), g, torch.bfloat16)
+    W = _rand((2 * F, K), g, torch.bfloat16, 0.05)
+    out = torch.zeros(M, F, dtype=torch.bfloat16, device=DEV)
+    api.gemm(W.to(DEV), X.to(DEV), epi=4, out=out)
+    x, w = X.double().numpy(), W.double().numpy()
+    gate, up = x @ w[:F].T, x @ w[F:].T
+    want = gate / (1 + np.exp(-gate)) * up
+    mag = (np.abs(x) @ np.abs(w[:F]).T) * (np.abs(x) @ np.abs(w[F:]).T)
+    got = out.cpu().double().numpy()
+    assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -8 + 2e-3 * mag + 1e-6)
