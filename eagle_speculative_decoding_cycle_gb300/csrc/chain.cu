@@ -33,35 +33,6 @@
 namespace eagle {
 
 EAGLE_DEV void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
-EAGLE_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-EAGLE_DEV void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-EAGLE_DEV unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-EAGLE_DEV bool err_raised(const int* err) { return *reinterpret_cast<const volatile int*>(err) != 0; }
-
-// Bounded wait until bar >= target. Gives up (false) on the CTA's abort flag, on an error
-// latched by another CTA, or after the time limit (then latches a timeout).
-EAGLE_DEV bool grid_wait(const unsigned* bar, unsigned target, volatile int* abort_flag, int* err) {
-  if (ld_acquire_u32(bar) >= target) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t spins = 1;; ++spins) {
-    if (ld_acquire_u32(bar) >= target) return true;
-    if (*abort_flag || ((spins & 255u) == 0 && err_raised(err))) { *abort_flag = 1; return false; }
-    if (globaltimer() - t0 > EAGLE_WAIT_LIMIT_NS) {
-      *abort_flag = 1;
-      latch_error(err, DEVERR_MBAR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 // A step with fewer units than CTAs is split over its first U CTAs only, so that every
 // CTA taking part holds at least one unit (the split-tile tickets count contributors).
 EAGLE_DEV int step_ctas(long long U, int G) { return U < (long long)G ? (int)U : G; }

@@ -22,7 +22,8 @@ constexpr int kNoallocMaxCtas = 192;
 constexpr int kNoallocMaxTiles = 8192;
 
 // Split-tile partial sums, [cta][2 slots][32 columns][128 rows] fp32 (6 MiB), and the
-// per-tile tickets that decide which CTA finishes a split tile (32 KiB).
+// per-tile counters through which a split tile's later contributors hand their partial
+// sums to the CTA that finishes it (32 KiB).
 static __device__ __align__(256) float g_noalloc_partials[kNoallocMaxCtas * 2 * kNoallocMaxRows * 128];
 static __device__ __align__(256) int g_noalloc_tickets[kNoallocMaxTiles];
 

@@ -11,8 +11,13 @@
 // Work split: stream-K. The (tile, k-block) units of the whole GEMM are cut into
 // gridDim.x equal contiguous ranges, one per persistent CTA, so every SM streams the
 // same number of weight bytes whatever the shape. A tile split across CTAs is finished
-// by the last contributor to arrive (atomic ticket, no waiting): it sums the fp32
-// partials in contributor order, so results do not depend on timing.
+// by its first contributor, for which it is the last segment of its range: the later
+// contributors reach the tile at the start of their ranges, publish fp32 partials and
+// count themselves in on a per-tile counter; the owner waits (bounded) for that count
+// and adds the partials to its own accumulator in contributor order, so results do not
+// depend on timing and the owner never writes its own partial. Every CTA of the grid is
+// resident at once (one CTA per SM, at most one per SM launched), so the wait always
+// ends.
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM owner,
 // warps 2-5 = epilogue (TMEM -> registers -> global / fused LM-head reduction).
@@ -319,7 +324,6 @@ __global__ void __launch_bounds__(192, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const bool leader = (ew == 0 && lane == 0);
-    const long long first_tile = u_begin / a.kb;
     int acc = 0;
     uint32_t acc_phase = 0;
     long long u = u_begin;
@@ -344,92 +348,82 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(tempty + acc));
       } else {
-        // partial tile [BN tokens][128 features]: a warp's stores cover whole 128-byte lines
-        const int slot = (tile == first_tile) ? 0 : 1;
-        float* part = a.partials + (size_t)(cta * 2 + slot) * BN * 128;
-        for (int c0 = 0; c0 < BN; c0 += C::CH) {
-          float v[C::CH];
-          if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
-#pragma unroll
-          for (int i = 0; i < C::CH; ++i) part[(c0 + i) * 128 + row] = v[i];
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(tempty + acc));
-        // publish the partial: every thread fences, the CTA synchronises, one thread
-        // takes the ticket between gpu-scope fences
-        __threadfence();
-        named_bar_sync(1, 128);
+        // Split tile. Its first contributor cf (whose range holds the tile's first k-block;
+        // for it the tile is its last segment) owns the result; each later contributor (for
+        // which the tile is its first segment) publishes a partial [BN tokens][128 features]
+        // and counts itself in. The owner waits for the count, then adds the partials to
+        // its own accumulator in contributor order.
         const int cf = cta_of_unit(tile * a.kb, U, G);
         const int cl = cta_of_unit((tile + 1) * a.kb - 1, U, G);
-        if (leader) {
+        const int nother = cl - cf;
+        constexpr uint32_t PART = (uint32_t)BN * 128 * 4;
+        if (u != tile * a.kb) {
+          float* part = a.partials + (size_t)(cta * 2) * BN * 128;
+          for (int c0 = 0; c0 < BN; c0 += C::CH) {
+            float v[C::CH];
+            if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
+#pragma unroll
+            for (int i = 0; i < C::CH; ++i) part[(c0 + i) * 128 + row] = v[i];
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(tempty + acc));
           __threadfence();
-          const int old = atomicAdd(a.counters + tile, 1);
-          bcast[1] = (old == cl - cf) ? 1 : 0;
-          __threadfence();
-        }
-        named_bar_sync(1, 128);
-        if (bcast[1]) {
-          __threadfence();
-          // every contributor after the first began its range inside this tile (slot 0); the
-          // first holds it in slot 1 when its range began earlier
-          const int s_first = ((long long)cf * U / G < tile * a.kb) ? 1 : 0;
-          const int ncon = cl - cf + 1;
-          constexpr uint32_t PART = (uint32_t)BN * 128 * 4;
-          if (seg_end == u_end && (uint32_t)ncon * PART <= (uint32_t)(C::STAGES * C::STAGE)) {
-            // The CTA's last tile: the ring is idle (every stage consumed), so the partials
-            // come in as bulk copies, all in flight at once, and are summed from shared
-            // memory in contributor order.
-            if (leader) {
+          named_bar_sync(1, 128);
+          if (leader) red_release_add(reinterpret_cast<unsigned*>(a.counters + tile), 1u);
+        } else {
+          // the ring is idle (this is the CTA's last segment): with room, the partials come
+          // in as bulk copies, all in flight at once
+          const bool bulk = (uint32_t)nother * PART <= (uint32_t)(C::STAGES * C::STAGE);
+          if (leader) {
+            bool ok = grid_wait(reinterpret_cast<const unsigned*>(a.counters + tile), (unsigned)nother,
+                                abort_flag, a.err, false);
+            if (ok && bulk && nother > 0) {
+              fence_acq_rel_gpu();
               fence_proxy_async_all();
-              mbar_expect_tx(smem_u32(fixbar), (uint32_t)ncon * PART);
-              for (int q = 0; q < ncon; ++q) {
-                const int cc = cf + q;
-                bulk_load(smem_u32(smem + (size_t)q * PART),
-                          a.partials + (size_t)(cc * 2 + (q == 0 ? s_first : 0)) * BN * 128, PART,
-                          smem_u32(fixbar));
-              }
-              bcast[0] = mbar_wait(smem_u32(fixbar), 0, abort_flag, a.err) ? 1 : 0;
+              mbar_expect_tx(smem_u32(fixbar), (uint32_t)nother * PART);
+              for (int q = 0; q < nother; ++q)
+                bulk_load(smem_u32(smem + (size_t)q * PART), a.partials + (size_t)((cf + 1 + q) * 2) * BN * 128,
+                          PART, smem_u32(fixbar));
+              ok = mbar_wait(smem_u32(fixbar), 0, abort_flag, a.err);
             }
-            named_bar_sync(1, 128);
+            bcast[0] = ok ? 1 : 0;
+          }
+          named_bar_sync(1, 128);
+          if (bcast[0]) {
+            if (!bulk) __threadfence();
             const float* sp = reinterpret_cast<const float*>(smem);
-            if (bcast[0]) {
-              for (int c0 = 0; c0 < BN; c0 += C::CH) {
-                float v[C::CH];
-#pragma unroll
-                for (int i = 0; i < C::CH; ++i) v[i] = 0.f;
-                for (int q = 0; q < ncon; ++q)
-#pragma unroll
-                  for (int i = 0; i < C::CH; ++i) v[i] += sp[(size_t)q * BN * 128 + (c0 + i) * 128 + row];
-                epi_chunk<C::CH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
-              }
-            }
-          } else {
-            // Sum the contributors' rows in contributor order, two contributors' loads in
-            // flight together.
             for (int c0 = 0; c0 < BN; c0 += C::CH) {
               float v[C::CH];
+              if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
+              if (bulk) {
+                for (int q = 0; q < nother; ++q)
 #pragma unroll
-              for (int i = 0; i < C::CH; ++i) v[i] = 0.f;
-              for (int cc = cf; cc <= cl; cc += 2) {
-                const bool two = cc + 1 <= cl;
-                const float* p0 = a.partials + (size_t)(cc * 2 + (cc == cf ? s_first : 0)) * BN * 128 + c0 * 128 + row;
-                const float* p1 = a.partials + (size_t)((cc + 1) * 2) * BN * 128 + c0 * 128 + row;
-                float x0[C::CH], x1[C::CH];
+                  for (int i = 0; i < C::CH; ++i) v[i] += sp[(size_t)q * BN * 128 + (c0 + i) * 128 + row];
+              } else {
+                // two contributors' loads in flight together
+                for (int cc = cf + 1; cc <= cl; cc += 2) {
+                  const bool two = cc + 1 <= cl;
+                  const float* p0 = a.partials + (size_t)(cc * 2) * BN * 128 + c0 * 128 + row;
+                  const float* p1 = a.partials + (size_t)((cc + 1) * 2) * BN * 128 + c0 * 128 + row;
+                  float x0[C::CH], x1[C::CH];
 #pragma unroll
-                for (int i = 0; i < C::CH; ++i) {
-                  x0[i] = __ldcg(p0 + i * 128);
-                  x1[i] = two ? __ldcg(p1 + i * 128) : 0.f;
-                }
+                  for (int i = 0; i < C::CH; ++i) {
+                    x0[i] = __ldcg(p0 + i * 128);
+                    x1[i] = two ? __ldcg(p1 + i * 128) : 0.f;
+                  }
 #pragma unroll
-                for (int i = 0; i < C::CH; ++i) v[i] += x0[i];
-                if (two) {
+                  for (int i = 0; i < C::CH; ++i) v[i] += x0[i];
+                  if (two) {
 #pragma unroll
-                  for (int i = 0; i < C::CH; ++i) v[i] += x1[i];
+                    for (int i = 0; i < C::CH; ++i) v[i] += x1[i];
+                  }
                 }
               }
               epi_chunk<C::CH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
             }
           }
+          tc_fence_before();
+          mbar_arrive(smem_u32(tempty + acc));
           if (leader) a.counters[tile] = 0;
         }
         named_bar_sync(1, 128);

@@ -26,7 +26,9 @@ extern "C" {
  * (bf16 only, N % 64 == 0): W holds 2N rows [Wgate; Wup] and out (bf16, [M][N]) receives
  * silu(X Wgate^T) * (X Wup^T); size its scratch with eagle_op_gemm_scratch_bytes(M, 2N).
  * out has row stride ldo elements. Scratch holds split-tile partial sums and per-tile
- * tickets; it must be zero-filled before the first call and is left zeroed by every call. */
+ * counters; it must be zero-filled before the first call and is left zeroed by every call.
+ * The kernel's CTAs hand partial sums to one another, so no other work may hold SMs for
+ * the whole of a call (kernels on other streams that finish on their own are fine). */
 size_t eagle_op_gemm_scratch_bytes(int M, int N);
 int eagle_op_gemm(int dtype, void* stream, const void* W, int N, int K, const void* X, int M, int epi,
                   void* out, int ldo, void* scratch, size_t scratch_bytes);
