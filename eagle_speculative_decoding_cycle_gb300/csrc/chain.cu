@@ -206,8 +206,8 @@ __device__ __noinline__ void row_swiglu(const ChainStep& st, int M, int t0, int 
     for (int q = 0; q < SB; ++q) {
       if (i0 + q * stride < n) {
         __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + off[q]);
-        o[0] = __floats2bfloat162_rn(silu_mul(g[q].x, u[q].x), silu_mul(g[q].y, u[q].y));
-        o[1] = __floats2bfloat162_rn(silu_mul(g[q].z, u[q].z), silu_mul(g[q].w, u[q].w));
+        o[0] = __floats2bfloat162_rn(silu_mul_bf16(g[q].x, u[q].x), silu_mul_bf16(g[q].y, u[q].y));
+        o[1] = __floats2bfloat162_rn(silu_mul_bf16(g[q].z, u[q].z), silu_mul_bf16(g[q].w, u[q].w));
       }
     }
   }

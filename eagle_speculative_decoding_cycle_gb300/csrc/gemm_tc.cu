@@ -60,80 +60,94 @@ template <int CH, int MODE>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int BN, int row, int c0,
                                           const float* v, float* staging, int ew, int lane) {
   if constexpr (MODE == MODE_SWIGLU) {
-    // accumulator rows 0-63: gate features tn*64.., rows 64-127: the matching up features
-    if (row >= 64) {
+    // accumulator rows 0-63: gate features tn*64.., rows 64-127: the matching up features.
+    // Through shared memory every thread then takes one gate/up pair for half the columns.
 #pragma unroll
-      for (int i = 0; i < CH; ++i) staging[i * 64 + (row - 64)] = v[i];
-    }
+    for (int i = 0; i < CH; ++i) staging[i * 128 + row] = v[i];
     named_bar_sync(2, 128);
-    const int f = tn * 64 + row;
-    if (row < 64 && f < a.N) {
+    const int r = row & 63, c_lo = (row >> 6) * (CH / 2);
+    const int f = tn * 64 + r;
+    if (f < a.N) {
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out);
 #pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        const int j = tt * BN + c0 + i;
-        if (j < a.M) o[(size_t)j * a.ldo + f] = __float2bfloat16_rn(silu_mul(v[i], staging[i * 64 + row]));
+      for (int i = 0; i < CH / 2; ++i) {
+        const int c = c_lo + i;
+        const int j = tt * BN + c0 + c;
+        if (j < a.M)
+          o[(size_t)j * a.ldo + f] = __float2bfloat16_rn(silu_mul_bf16(staging[c * 128 + r], staging[c * 128 + 64 + r]));
       }
     }
     named_bar_sync(2, 128);
     return;
   }
   if constexpr (MODE == MODE_QKV) {
+    // 16-column chunks. Shared memory holds the chunk's values [16][128], the cos/sin rows
+    // of its positions [16][d/2] each, and the tile's per-column slot / sequence / position.
+    // The code stays short (rolled loops): it runs cold at the end of the kernel.
+    static_assert(CH == 16, "the QKV epilogue works on 16-column chunks");
     const QkvEpi& q = a.qkv;
+    int* meta = reinterpret_cast<int*>(staging + 32 * 128);
+    float* css = staging + CH * 128;
+    float* sns = css + CH * 64;
+    const int d = q.d, half = d >> 1, hs = __ffs(half) - 1;
+    if (c0 == 0) {
+      for (int t = row; t < BN; t += 128) {
+        const int j = min(tt * BN + t, a.M - 1);
+        meta[t] = q.slot[j];
+        meta[256 + t] = q.seq[j];
+        meta[512 + t] = q.pos[j];
+      }
+      named_bar_sync(2, 128);
+    }
 #pragma unroll
     for (int i = 0; i < CH; ++i) staging[i * 128 + row] = v[i];
+#pragma unroll
+    for (int k = 0; k < CH * 64 / 128; ++k) {
+      const int idx = k * 128 + row;
+      if (idx < (CH << hs)) {
+        const int ci = meta[512 + c0 + (idx >> hs)] * half + (idx & (half - 1));
+        css[idx] = q.cos[ci];
+        sns[idx] = q.sin[ci];
+      }
+    }
     named_bar_sync(2, 128);
     const int f = tn * 128 + row;
     if (f < a.N) {
-      const int d = q.d, half = d >> 1;
-      const int h = f / d, e = f - h * d;
+      const int h = f >> (hs + 1), e = f & (d - 1);
       const bool lo_half = e < half;
       const int prow = lo_half ? row + half : row - half;
-      __nv_bfloat16* qo = reinterpret_cast<__nv_bfloat16*>(q.q);
-      __nv_bfloat16* ko = reinterpret_cast<__nv_bfloat16*>(q.kc);
-      __nv_bfloat16* vo = reinterpret_cast<__nv_bfloat16*>(q.vc);
-      const bool roped = h < q.nq + q.nkv;
-      const int eh = lo_half ? e : e - half;
-      // eight columns at a time: their token metadata and cos/sin entries are loaded
-      // together, then rotated and stored
-#pragma unroll
-      for (int i0 = 0; i0 < CH; i0 += 8) {
-        int sl[8], sq[8];
-        float cs[8], sn[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int j = min(tt * BN + c0 + i0 + i, a.M - 1);
-          sl[i] = q.slot[j];
-          sq[i] = q.seq[j];
-          if (roped) {
-            const int ci = q.pos[j] * half + eh;
-            cs[i] = q.cos[ci];
-            sn[i] = q.sin[ci];
+      const int eh = e & (half - 1);
+      const int jn = min(CH, a.M - (tt * BN + c0));
+      if (h < q.nq + q.nkv) {
+        __nv_bfloat16* qo = reinterpret_cast<__nv_bfloat16*>(q.q);
+        __nv_bfloat16* ko = reinterpret_cast<__nv_bfloat16*>(q.kc);
+#pragma unroll 4
+        for (int i = 0; i < jn; ++i) {
+          const int j = tt * BN + c0 + i;
+          const float x = staging[i * 128 + row], y = staging[i * 128 + prow];
+          const float c = css[(i << hs) + eh], sn = sns[(i << hs) + eh];
+          float lo, hi;
+          if (lo_half) rope_pair(x, y, c, sn, lo, hi);
+          else rope_pair(y, x, c, sn, lo, hi);
+          const __nv_bfloat16 r = __float2bfloat16_rn(lo_half ? lo : hi);
+          if (h < q.nq) {
+            qo[((size_t)j * q.nq + h) * d + e] = r;
+          } else {
+            const int slot = meta[c0 + i];
+            if (slot >= 0 && slot < q.cap)
+              ko[((size_t)(meta[256 + c0 + i] * q.nkv + (h - q.nq)) * q.cap + slot) * d + e] = r;
+            else if (e == 0)
+              latch_error(a.err, DEVERR_CAPACITY);
           }
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int j = tt * BN + c0 + i0 + i;
-          if (j >= a.M) break;
-          const float x = v[i0 + i];
-          const int slot = sl[i];
-          const bool slot_ok = slot >= 0 && slot < q.cap;
-          if (roped) {
-            const float y = staging[(i0 + i) * 128 + prow];
-            float lo, hi;
-            if (lo_half) rope_pair(x, y, cs[i], sn[i], lo, hi);
-            else rope_pair(y, x, cs[i], sn[i], lo, hi);
-            const float r = lo_half ? lo : hi;
-            if (h < q.nq) {
-              qo[((size_t)j * q.nq + h) * d + e] = __float2bfloat16_rn(r);
-            } else if (slot_ok) {
-              ko[((size_t)(sq[i] * q.nkv + (h - q.nq)) * q.cap + slot) * d + e] = __float2bfloat16_rn(r);
-            } else if (e == 0) {
-              latch_error(a.err, DEVERR_CAPACITY);
-            }
-          } else if (slot_ok) {
-            vo[((size_t)(sq[i] * q.nkv + (h - q.nq - q.nkv)) * q.cap + slot) * d + e] = __float2bfloat16_rn(x);
-          }
+      } else {
+        __nv_bfloat16* vo = reinterpret_cast<__nv_bfloat16*>(q.vc);
+#pragma unroll 4
+        for (int i = 0; i < jn; ++i) {
+          const int slot = meta[c0 + i];
+          if (slot >= 0 && slot < q.cap)
+            vo[((size_t)(meta[256 + c0 + i] * q.nkv + (h - q.nq - q.nkv)) * q.cap + slot) * d + e] =
+                __float2bfloat16_rn(staging[i * 128 + row]);
         }
       }
     }
@@ -320,6 +334,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     pdl_wait();
+    // epilogue chunk width (accumulator columns per TMEM load)
+    constexpr int ECH = (MODE == MODE_QKV) ? 16 : C::CH;
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -340,10 +356,10 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (whole) {
-        for (int c0 = 0; c0 < BN; c0 += C::CH) {
-          float v[C::CH];
-          if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
-          epi_chunk<C::CH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+        for (int c0 = 0; c0 < BN; c0 += ECH) {
+          float v[ECH];
+          if constexpr (ECH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
+          epi_chunk<ECH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(tempty + acc));
@@ -359,11 +375,11 @@ __global__ void __launch_bounds__(192, 1)
         constexpr uint32_t PART = (uint32_t)BN * 128 * 4;
         if (u != tile * a.kb) {
           float* part = a.partials + (size_t)(cta * 2) * BN * 128;
-          for (int c0 = 0; c0 < BN; c0 += C::CH) {
-            float v[C::CH];
-            if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
+          for (int c0 = 0; c0 < BN; c0 += ECH) {
+            float v[ECH];
+            if constexpr (ECH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
 #pragma unroll
-            for (int i = 0; i < C::CH; ++i) part[(c0 + i) * 128 + row] = v[i];
+            for (int i = 0; i < ECH; ++i) part[(c0 + i) * 128 + row] = v[i];
           }
           tc_fence_before();
           mbar_arrive(smem_u32(tempty + acc));
@@ -392,34 +408,34 @@ __global__ void __launch_bounds__(192, 1)
           if (bcast[0]) {
             if (!bulk) __threadfence();
             const float* sp = reinterpret_cast<const float*>(smem);
-            for (int c0 = 0; c0 < BN; c0 += C::CH) {
-              float v[C::CH];
-              if constexpr (C::CH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
+            for (int c0 = 0; c0 < BN; c0 += ECH) {
+              float v[ECH];
+              if constexpr (ECH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
               if (bulk) {
                 for (int q = 0; q < nother; ++q)
 #pragma unroll
-                  for (int i = 0; i < C::CH; ++i) v[i] += sp[(size_t)q * BN * 128 + (c0 + i) * 128 + row];
+                  for (int i = 0; i < ECH; ++i) v[i] += sp[(size_t)q * BN * 128 + (c0 + i) * 128 + row];
               } else {
                 // two contributors' loads in flight together
                 for (int cc = cf + 1; cc <= cl; cc += 2) {
                   const bool two = cc + 1 <= cl;
                   const float* p0 = a.partials + (size_t)(cc * 2) * BN * 128 + c0 * 128 + row;
                   const float* p1 = a.partials + (size_t)((cc + 1) * 2) * BN * 128 + c0 * 128 + row;
-                  float x0[C::CH], x1[C::CH];
+                  float x0[ECH], x1[ECH];
 #pragma unroll
-                  for (int i = 0; i < C::CH; ++i) {
+                  for (int i = 0; i < ECH; ++i) {
                     x0[i] = __ldcg(p0 + i * 128);
                     x1[i] = two ? __ldcg(p1 + i * 128) : 0.f;
                   }
 #pragma unroll
-                  for (int i = 0; i < C::CH; ++i) v[i] += x0[i];
+                  for (int i = 0; i < ECH; ++i) v[i] += x0[i];
                   if (two) {
 #pragma unroll
-                    for (int i = 0; i < C::CH; ++i) v[i] += x1[i];
+                    for (int i = 0; i < ECH; ++i) v[i] += x1[i];
                   }
                 }
               }
-              epi_chunk<C::CH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
+              epi_chunk<ECH, MODE>(a, tn, tt, BN, row, c0, v, staging, ew, lane);
             }
           }
           tc_fence_before();

@@ -3,6 +3,7 @@
 // plain row conversions / gathers. All are memory-bound and use coalesced row loops.
 #include "common.cuh"
 #include "kernels.h"
+#include <type_traits>
 
 namespace eagle {
 
@@ -151,7 +152,10 @@ __global__ void swiglu_k(const float* gu, int F, T* out) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = i0 + j;
-    if (i < F) out[(size_t)r * F + i] = Elem<T>::from_f(silu_mul(g[i], g[F + i]));
+    if (i < F) {
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) out[(size_t)r * F + i] = Elem<T>::from_f(silu_mul_bf16(g[i], g[F + i]));
+      else out[(size_t)r * F + i] = Elem<T>::from_f(silu_mul(g[i], g[F + i]));
+    }
   }
 }
 

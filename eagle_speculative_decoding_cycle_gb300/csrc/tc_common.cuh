@@ -17,7 +17,7 @@ struct TcCfg {
   static constexpr int STAGES = (196608 / STAGE) > 12 ? 12 : (196608 / STAGE);
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int CH = BN < 32 ? BN : 32;
-  static constexpr int STAGING = 32 * 128 * 4;
+  static constexpr int STAGING = 32 * 128 * 4 + 3 * 256 * 4;   // epilogue values + per-column metadata
   static constexpr int SMEM = 1024 + STAGES * STAGE + STAGING + 512;
 };
 
