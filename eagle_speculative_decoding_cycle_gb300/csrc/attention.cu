@@ -213,9 +213,12 @@ __device__ __forceinline__ bool visible(const AttnArgs& a, const RowVis& rv, int
   return (rv.mw[t >> 6] >> (t & 63)) & 1ull;
 }
 
+// Everything before the query loads reads data older than the preceding kernel (the rows'
+// sequence, slot, mask and context length, and in tree mode the context keys below
+// ctx_len, which that kernel never writes), so it runs before waiting on that kernel: the
+// first key tile of a tree-mode CTA is already in flight when the queries arrive.
 template <int D>
 __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
-  PDL_ENTRY();
   constexpr int LD = D + 8;                      // padded smem row (bf16 elements)
   extern __shared__ __align__(16) uint8_t attn_smem[];
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(attn_smem);              // [2][64][LD]
@@ -256,21 +259,6 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   setup_row(qv_a, va, row_a, head_a);
   setup_row(qv_b, vb, row_b, head_b);
 
-  // Q fragments (bf16 pairs), zero for rows past the block
-  uint32_t qf[D / 16][4];
-  {
-    const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* pa = qp + ((size_t)row_a * a.nq + head_a) * D;
-    const __nv_bfloat16* pb = qp + ((size_t)row_b * a.nq + head_b) * D;
-    const int c = (lane & 3) * 2;
-#pragma unroll
-    for (int kt = 0; kt < D / 16; ++kt) {
-      qf[kt][0] = va.valid ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + c) : 0u;
-      qf[kt][1] = vb.valid ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + c) : 0u;
-      qf[kt][2] = va.valid ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + 8 + c) : 0u;
-      qf[kt][3] = vb.valid ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + 8 + c) : 0u;
-    }
-  }
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -292,7 +280,25 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
     cp_async_commit();
   };
 
-  if (t_begin < t_end) load_tile(t_begin, 0);
+  const bool early = a.mode == 1 && t_begin < t_end && (t_begin + 1) * MT_KEYS <= ctx;
+  if (early) load_tile(t_begin, 0);
+  PDL_ENTRY();
+  // Q fragments (bf16 pairs), zero for rows past the block
+  uint32_t qf[D / 16][4];
+  {
+    const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* pa = qp + ((size_t)row_a * a.nq + head_a) * D;
+    const __nv_bfloat16* pb = qp + ((size_t)row_b * a.nq + head_b) * D;
+    const int c = (lane & 3) * 2;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; ++kt) {
+      qf[kt][0] = va.valid ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + c) : 0u;
+      qf[kt][1] = vb.valid ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + c) : 0u;
+      qf[kt][2] = va.valid ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + 8 + c) : 0u;
+      qf[kt][3] = vb.valid ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + 8 + c) : 0u;
+    }
+  }
+  if (!early && t_begin < t_end) load_tile(t_begin, 0);
   for (int t = t_begin; t < t_end; ++t) {
     const int buf = (t - t_begin) & 1;
     if (t + 1 < t_end) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
@@ -407,27 +413,46 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   }
 }
 
-// out[r][h] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), splits in order.
+// out[r][h] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), splits in order. One warp per
+// (row, head): lane s holds split s's (m, l); every split's partial output is loaded before
+// the in-order sums, so the kernel costs two dependent loads instead of one per split.
+constexpr int MAX_SPLITS = 16;
 template <int D>
 __global__ void attn_combine_k(AttnArgs a, int splits) {
   PDL_ENTRY();
   const int qi = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (qi >= a.R * a.nq) return;
-  float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, a.part_ml[((size_t)s * a.R * a.nq + qi) * 2]);
+  const size_t stride = (size_t)a.R * a.nq;
+  float ms = -INFINITY, ls = 0.f;
+  if (lane < splits) {
+    ms = a.part_ml[((size_t)lane * stride + qi) * 2];
+    ls = a.part_ml[((size_t)lane * stride + qi) * 2 + 1];
+  }
+  float x[MAX_SPLITS][D / 32];
+#pragma unroll
+  for (int sp = 0; sp < MAX_SPLITS; ++sp)
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i)
+      x[sp][i] = sp < splits ? a.part_o[((size_t)sp * stride + qi) * D + lane + 32 * i] : 0.f;
+  float M = ms;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
   float L = 0.f;
   float acc[D / 32];
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const size_t si = (size_t)s * a.R * a.nq + qi;
-    const float ms = a.part_ml[si * 2], ls = a.part_ml[si * 2 + 1];
-    if (ms == -INFINITY) continue;
-    const float w = exp2f(ms - M);
-    L += ls * w;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) acc[i] += a.part_o[si * D + lane + 32 * i] * w;
+  for (int sp = 0; sp < MAX_SPLITS; ++sp) {
+    const float ws = __shfl_sync(0xffffffffu, w, sp);
+    const float lw = __shfl_sync(0xffffffffu, ls * w, sp);
+    const float msp = __shfl_sync(0xffffffffu, ms, sp);
+    if (sp < splits && msp != -INFINITY) {
+      L += lw;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) acc[i] += x[sp][i] * ws;
+    }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out);
@@ -458,7 +483,7 @@ static int launch_mma(cudaStream_t st, const AttnArgs& a) {
   // double the time of this latency-bound kernel)
   int splits = per_sm * sms / base;
   const int max_tiles = (a.cap + MT_KEYS - 1) / MT_KEYS;
-  splits = std::min(std::min(splits, 16), max_tiles);
+  splits = std::min(std::min(splits, MAX_SPLITS), max_tiles);
   while (splits > 1 && (size_t)splits * a.R * a.nq * D > a.part_floats) --splits;
   if (!a.part_o || !a.part_ml) splits = 1;
   if (splits < 1) splits = 1;

@@ -91,37 +91,61 @@ int rmsnorm_rows(cudaStream_t st, int dtype_in, const void* x, int ldx, const vo
 }
 
 // Rotate-half RoPE on q and k (angle table precomputed on the host in double precision);
-// q written to q_out, k and v into the cache at the row's slot. One block per (row, head)
-// of the fused [q | k | v] projection output, one thread per rotation pair.
+// q written to q_out, k and v into the cache at the row's slot. One block per row and group
+// of RS_HEADS heads of the fused [q | k | v] projection output; a thread takes RS_ITEMS
+// (head, rotation pair) items, loading all of them before it stores.
+constexpr int RS_HEADS = 8, RS_THREADS = 128, RS_ITEMS = 4;
+
 template <typename T>
 __global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int* row_pos, const int* row_slot,
                              const int* row_seq, const float* rc, const float* rsn, T* q_out, T* kc, T* vc, int cap,
                              int* err, int slot_limit) {
   PDL_ENTRY();
-  const int r = blockIdx.x, h = blockIdx.y;
-  const int half = d / 2;
+  const int r = blockIdx.x, h0 = blockIdx.y * RS_HEADS;
+  const int H = nq + 2 * nkv, half = d / 2;
   const int slot = row_slot[r];
   const bool slot_ok = slot >= 0 && slot < cap && slot < slot_limit;
-  if (!slot_ok) {
-    if (h == 0 && threadIdx.x == 0) latch_error(err, DEVERR_CAPACITY);
-    if (h >= nq) return;
-  }
-  const float* src = qkv + (size_t)r * (nq + 2 * nkv) * d + (size_t)h * d;
-  const int seq = row_seq[r];
-  if (h >= nq + nkv) {   // value head: plain copy
-    T* v = vc + ((size_t)(seq * nkv + (h - nq - nkv)) * cap + slot) * d;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) v[i] = Elem<T>::from_f(src[i]);
-    return;
-  }
-  const int pos = row_pos[r];
-  const float* cr = rc + (size_t)pos * half;
-  const float* sr = rsn + (size_t)pos * half;
-  T* dst = h < nq ? q_out + ((size_t)r * nq + h) * d : kc + ((size_t)(seq * nkv + (h - nq)) * cap + slot) * d;
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    float lo, hi;
-    rope_pair(src[i], src[i + half], cr[i], sr[i], lo, hi);
-    dst[i] = Elem<T>::from_f(lo);
-    dst[i + half] = Elem<T>::from_f(hi);
+  if (!slot_ok && blockIdx.y == 0 && threadIdx.x == 0) latch_error(err, DEVERR_CAPACITY);
+  const int seq = row_seq[r], pos = row_pos[r];
+  const float* src = qkv + (size_t)r * H * d;
+  const int n = min(RS_HEADS, H - h0) * half;   // (head, pair) items of this block
+  for (int base = 0; base < n; base += RS_ITEMS * RS_THREADS) {
+    // all loads of the thread's items first, then the rotations and stores
+    float xa[RS_ITEMS], xb[RS_ITEMS], cs[RS_ITEMS], sn[RS_ITEMS];
+#pragma unroll
+    for (int k = 0; k < RS_ITEMS; ++k) {
+      const int it = base + k * RS_THREADS + threadIdx.x;
+      const int hl = it / half, i = it - hl * half, h = h0 + hl;
+      xa[k] = xb[k] = cs[k] = sn[k] = 0.f;
+      if (it < n) {
+        xa[k] = src[(size_t)h * d + i];
+        xb[k] = src[(size_t)h * d + i + half];
+        if (h < nq + nkv) {
+          cs[k] = rc[(size_t)pos * half + i];
+          sn[k] = rsn[(size_t)pos * half + i];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < RS_ITEMS; ++k) {
+      const int it = base + k * RS_THREADS + threadIdx.x;
+      const int hl = it / half, i = it - hl * half, h = h0 + hl;
+      if (it >= n) continue;
+      if (h >= nq + nkv) {   // value head: plain copy
+        if (slot_ok) {
+          T* v = vc + ((size_t)(seq * nkv + (h - nq - nkv)) * cap + slot) * d;
+          v[i] = Elem<T>::from_f(xa[k]);
+          v[i + half] = Elem<T>::from_f(xb[k]);
+        }
+        continue;
+      }
+      if (h >= nq && !slot_ok) continue;
+      float lo, hi;
+      rope_pair(xa[k], xb[k], cs[k], sn[k], lo, hi);
+      T* dst = h < nq ? q_out + ((size_t)r * nq + h) * d : kc + ((size_t)(seq * nkv + (h - nq)) * cap + slot) * d;
+      dst[i] = Elem<T>::from_f(lo);
+      dst[i + half] = Elem<T>::from_f(hi);
+    }
   }
 }
 
@@ -130,8 +154,10 @@ int rope_store(cudaStream_t st, int dtype, const float* qkv, int R, int nq, int 
                const float* rope_sin, void* q_out, void* kcache, void* vcache, int cap, int* err,
                int slot_limit) {
   if (R <= 0) return 0;
-  dim3 grid(R, nq + 2 * nkv);
-  const int threads = d / 2 < 32 ? 32 : (d / 2 > 128 ? 128 : d / 2);
+  // blocks of RS_HEADS heads of one row: a 7B verify pass (61 rows x 96 heads) is one wave
+  // of resident blocks, so the next kernel can be scheduled while this one runs
+  dim3 grid(R, (nq + 2 * nkv + RS_HEADS - 1) / RS_HEADS);
+  const int threads = RS_THREADS;
   if (dtype == DT_F32)
     launch_k(rope_store_k<float>, grid, threads, 0, st, qkv, nq, nkv, d, row_pos, row_slot, row_seq, rope_cos, rope_sin,
                                                   (float*)q_out, (float*)kcache, (float*)vcache, cap, err, slot_limit);
