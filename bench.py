@@ -457,14 +457,29 @@ def run_gemm_probe(args):
     for _ in range(3):
         call()
     torch.cuda.synchronize()
+    # back-to-back launches replayed from a CUDA graph, so the host-side call overhead
+    # (tensor-map encode, argument checks) is not timed; inputs are larger than L2 for the
+    # verify-pass shapes, so consecutive launches stream the weight from HBM
+    reps = 10
+    gs = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gs):
+        st = gs.cuda_stream
+        graph.capture_begin()
+        for _ in range(reps):
+            call()
+        graph.capture_end()
     ts = []
-    for _ in range(args.steps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        call()
-        e1.record()
+    with torch.cuda.stream(gs):
+        graph.replay()
         torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1))
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(gs)
+            graph.replay()
+            e1.record(gs)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / reps)
     byt = N * K * 2 + M * K * 2 + M * N * 4
     us = statistics.median(ts) * 1e3
     hbm, src = peaks()
