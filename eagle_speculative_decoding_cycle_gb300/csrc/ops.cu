@@ -17,7 +17,20 @@ __global__ void embed_k(const T* E, int V, int H, const int* tok, float* x, int*
     t = 0;
   }
   const T* e = E + (size_t)t * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) x[(size_t)r * H + i] = Elem<T>::to_f(e[i]);
+  float* o = x + (size_t)r * H;
+  for (int base = 0; base < H; base += 4 * blockDim.x) {
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      v[k] = i < H ? Elem<T>::to_f(e[i]) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      if (i < H) o[i] = v[k];
+    }
+  }
 }
 
 int embed_rows(cudaStream_t st, int dtype, const void* E, int V, int H, const int* tok, int R, float* x,
@@ -193,7 +206,11 @@ int swiglu_rows(cudaStream_t st, int dtype, const float* gu, int F, int R, void*
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-// EAGLE-1 drafter input row: [E[tok]; feature] (2H).
+// EAGLE-1 drafter input row: [E[tok]; feature] (2H). Rows whose length and bases allow it
+// move in 16-byte words, and every thread issues all its loads before its stores (a
+// strided element loop paid one memory round trip per iteration).
+constexpr int ROW_UNROLL = 4;
+
 template <typename T>
 __global__ void concat_k(const T* E, int V, int H, const int* tok, const T* feat, const int* feat_row, T* out,
                          int* err) {
@@ -207,9 +224,40 @@ __global__ void concat_k(const T* E, int V, int H, const int* tok, const T* feat
   const T* e = E + (size_t)t * H;
   const T* f = feat + (size_t)feat_row[r] * H;
   T* o = out + (size_t)r * 2 * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    o[i] = e[i];
-    o[H + i] = f[i];
+  constexpr int VW = 16 / sizeof(T);
+  if (H % VW == 0 && ((reinterpret_cast<uintptr_t>(e) | reinterpret_cast<uintptr_t>(f) |
+                       reinterpret_cast<uintptr_t>(o)) & 15) == 0) {
+    const int n = H / VW;
+    const uint4* ev = reinterpret_cast<const uint4*>(e);
+    const uint4* fv = reinterpret_cast<const uint4*>(f);
+    uint4* ov = reinterpret_cast<uint4*>(o);
+    for (int base = 0; base < n; base += ROW_UNROLL * blockDim.x) {
+      uint4 a[ROW_UNROLL], b[ROW_UNROLL];
+#pragma unroll
+      for (int k = 0; k < ROW_UNROLL; ++k) {
+        const int i = base + k * blockDim.x + threadIdx.x;
+        if (i < n) { a[k] = ev[i]; b[k] = fv[i]; }
+      }
+#pragma unroll
+      for (int k = 0; k < ROW_UNROLL; ++k) {
+        const int i = base + k * blockDim.x + threadIdx.x;
+        if (i < n) { ov[i] = a[k]; ov[n + i] = b[k]; }
+      }
+    }
+    return;
+  }
+  for (int base = 0; base < H; base += ROW_UNROLL * blockDim.x) {
+    T a[ROW_UNROLL], b[ROW_UNROLL];
+#pragma unroll
+    for (int k = 0; k < ROW_UNROLL; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      if (i < H) { a[k] = e[i]; b[k] = f[i]; }
+    }
+#pragma unroll
+    for (int k = 0; k < ROW_UNROLL; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      if (i < H) { o[i] = a[k]; o[H + i] = b[k]; }
+    }
   }
 }
 
@@ -224,18 +272,48 @@ int concat_emb_feat(cudaStream_t st, int dtype, const void* E, int V, int H, con
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// Row conversions fp32 <-> storage type, ROW_UNROLL elements per thread and pass with
+// all loads issued before the stores.
 template <typename T>
 __global__ void convert_k(const float* x, int H, T* out, int ldo) {
   PDL_ENTRY();
   const int r = blockIdx.x;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) out[(size_t)r * ldo + i] = Elem<T>::from_f(x[(size_t)r * H + i]);
+  const float* xr = x + (size_t)r * H;
+  T* o = out + (size_t)r * ldo;
+  for (int base = 0; base < H; base += ROW_UNROLL * blockDim.x) {
+    float v[ROW_UNROLL];
+#pragma unroll
+    for (int k = 0; k < ROW_UNROLL; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      v[k] = i < H ? xr[i] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < ROW_UNROLL; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      if (i < H) o[i] = Elem<T>::from_f(v[k]);
+    }
+  }
 }
 
 template <typename T>
 __global__ void widen_k(const T* x, int ldx, int H, float* out) {
   PDL_ENTRY();
   const int r = blockIdx.x;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) out[(size_t)r * H + i] = Elem<T>::to_f(x[(size_t)r * ldx + i]);
+  const T* xr = x + (size_t)r * ldx;
+  float* o = out + (size_t)r * H;
+  for (int base = 0; base < H; base += ROW_UNROLL * blockDim.x) {
+    float v[ROW_UNROLL];
+#pragma unroll
+    for (int k = 0; k < ROW_UNROLL; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      v[k] = i < H ? Elem<T>::to_f(xr[i]) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < ROW_UNROLL; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      if (i < H) o[i] = v[k];
+    }
+  }
 }
 
 int widen_rows(cudaStream_t st, int dtype, const void* x, int ldx, int H, int R, float* out) {
