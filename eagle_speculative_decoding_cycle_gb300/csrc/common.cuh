@@ -89,6 +89,25 @@ EAGLE_DEV bool rank_before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+// Order-preserving 32-bit key of a float (larger value, larger key; -0 and +0 map to one
+// key) and its inverse, so that a warp takes a maximum with one redux.sync instead of a
+// shuffle butterfly.
+EAGLE_DEV uint32_t f2key(float v) {
+  const uint32_t b = __float_as_uint(v + 0.f);   // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+EAGLE_DEV float key2f(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); }
+
+// The warp's best (value, id) of one candidate per lane in the rank_before order: the
+// largest value, then the smallest id among the lanes that hold it. Empty lanes carry
+// (-inf, 0x7fffffff).
+EAGLE_DEV void warp_best(float v, int id, float& bv, int& bi) {
+  const uint32_t kv = f2key(v);
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, kv);
+  bi = (int)__reduce_min_sync(0xffffffffu, kv == kmax ? (uint32_t)id : 0xffffffffu);
+  bv = key2f(kmax);
+}
+
 // ---- Philox4x32-10 (Salmon et al., SC'11) ---------------------------------------------------
 struct u32x4 { uint32_t x, y, z, w; };
 

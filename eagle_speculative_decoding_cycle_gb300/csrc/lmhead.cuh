@@ -82,7 +82,7 @@ EAGLE_DEV void head_tile_row(const float* vals, int tile, int row, const HeadPar
     rv[q] = rank_ok ? (p.gumbel ? sv[q] + gumbel_noise(p, row, id) : sv[q]) : -INFINITY;
     rid[q] = rank_ok ? id : 0x7fffffff;
   }
-  mx = warp_max(mx);
+  mx = key2f(__reduce_max_sync(0xffffffffu, f2key(mx)));
   float se = 0.f;
   if (mx != -INFINITY) {
 #pragma unroll
@@ -102,12 +102,7 @@ EAGLE_DEV void head_tile_row(const float* vals, int tile, int row, const HeadPar
 #pragma unroll
     for (int q = 1; q < 4; ++q)
       if (rank_before(rv[q], rid[q], bv, bi)) { bv = rv[q]; bi = rid[q]; }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (rank_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
+    warp_best(bv, bi, bv, bi);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       if (rid[q] == bi) { rv[q] = -INFINITY; rid[q] = 0x7fffffff; }
@@ -165,8 +160,8 @@ EAGLE_DEV void head_merge_fold(const HeadParams& p, int row, int t0, int stride,
   }
 }
 
-// Warp reduction of the lanes' sorted lists and (max, sum-exp) pairs, in a fixed
-// butterfly order: lane 0 receives the K best (out_v, out_i) and the combined pair. Each
+// Warp reduction of the lanes' sorted lists and (max, sum-exp) pairs (the pairs in a fixed
+// butterfly order): lane 0 receives the K best (out_v, out_i) and the combined pair. Each
 // round takes the best list head over the lanes and pops it from its owner's list.
 EAGLE_DEV void head_merge_warp(int K, float* lv, int* li, float& M, float& S, int lane, float* out_v, int* out_i) {
 #pragma unroll
@@ -178,15 +173,10 @@ EAGLE_DEV void head_merge_warp(int K, float* lv, int* li, float& M, float& S, in
     M = mn;
   }
   for (int k = 0; k < K; ++k) {
-    float bv = lv[0];
-    int bi = li[0];
-    const int mine = bi;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (rank_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
+    float bv;
+    int bi;
+    const int mine = li[0];
+    warp_best(lv[0], li[0], bv, bi);
     if (mine == bi && bi != 0x7fffffff) {
 #pragma unroll
       for (int j = 0; j < 15; ++j) { lv[j] = lv[j + 1]; li[j] = li[j + 1]; }

@@ -74,6 +74,8 @@ int tree_start(cudaStream_t st, const CycleDev& c) {
 }
 
 // Expansion at depth d: pick the k best depth-d nodes and lay out their drafter rows.
+constexpr int TS_QMAX = 8;   // candidates per lane (k * k <= 256)
+
 __global__ void tree_select_k(CycleDev c, int d) {
   PDL_ENTRY();
   const int b = blockIdx.x, lane = threadIdx.x;
@@ -81,22 +83,21 @@ __global__ void tree_select_k(CycleDev c, int d) {
   const int k = c.k;
   const int lo = (d == 1) ? 0 : k + (d - 2) * k * k;
   const int cnt = (d == 1) ? k : k * k;
+  // the candidates' path values, loaded once (k <= 16: at most 256 candidates)
+  float cv[TS_QMAX];
+#pragma unroll
+  for (int q = 0; q < TS_QMAX; ++q) cv[q] = lane + 32 * q < cnt ? c.node_logv[base + lo + lane + 32 * q] : -INFINITY;
   uint32_t taken = 0;   // bit q: candidate lo + lane + 32 q already selected
   for (int r = 0; r < k; ++r) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int q = 0; lane + 32 * q < cnt; ++q) {
-      if ((taken >> q) & 1) continue;
-      const int g = lo + lane + 32 * q;
-      const float v = c.node_logv[base + g];
-      if (rank_before(v, g, bv, bi)) { bv = v; bi = g; }
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (rank_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    for (int q = 0; q < TS_QMAX; ++q) {
+      if (lane + 32 * q >= cnt || ((taken >> q) & 1)) continue;
+      const int g = lo + lane + 32 * q;
+      if (rank_before(cv[q], g, bv, bi)) { bv = cv[q]; bi = g; }
     }
+    warp_best(bv, bi, bv, bi);
     if (bi != 0x7fffffff && ((bi - lo) & 31) == lane) taken |= 1u << ((bi - lo) >> 5);
     if (lane == 0) {
       c.exp_node[(b * c.D + (d - 1)) * k + r] = bi;
@@ -139,7 +140,7 @@ __global__ void tree_select_k(CycleDev c, int d) {
 }
 
 int tree_select(cudaStream_t st, const CycleDev& c, int d) {
-  if (c.k > 32 || c.k * c.k > 32 * 32) return -1;
+  if (c.k > 16) return -1;
   launch_k(tree_select_k, c.B, 32, 0, st, c, d);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
