@@ -177,7 +177,9 @@ int tree_add(cudaStream_t st, const CycleDev& c, int d, const HeadOut& h) {
 }
 
 // Global top-m rerank and flattening.
-__global__ void tree_finalize_k(CycleDev c) {
+constexpr int TF_THREADS = 256;
+
+__global__ void __launch_bounds__(TF_THREADS) tree_finalize_k(CycleDev c) {
   PDL_ENTRY();
   extern __shared__ uint8_t sm[];
   const int NG = c.NG;
@@ -195,19 +197,43 @@ __global__ void tree_finalize_k(CycleDev c) {
     row_of[i] = rank < c.m ? 1 : 0;
   }
   __syncthreads();
-  // flattened row = 1 + number of kept nodes with a smaller generation index
-  for (int i = threadIdx.x; i < NG; i += blockDim.x) {
-    int before = 0;
-    for (int j = 0; j < i; ++j) before += (row_of[j] != 0 && row_of[j] != -1) ? 1 : 0;
-    key[i] = (uint64_t)(row_of[i] ? 1 + before : 0);
+  // flattened row = 1 + number of kept nodes with a smaller generation index: each thread
+  // counts a contiguous run of nodes, an exclusive block scan gives its runs' offsets
+  {
+    __shared__ int s_warp[TF_THREADS / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = (NG + TF_THREADS - 1) / TF_THREADS;
+    const int i0 = min(NG, threadIdx.x * per), i1 = min(NG, i0 + per);
+    int cnt = 0;
+    for (int i = i0; i < i1; ++i) cnt += row_of[i];
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int run = incl - cnt;
+    for (int w = 0; w < warp; ++w) run += s_warp[w];
+    for (int i = i0; i < i1; ++i) {
+      const int kept = row_of[i];
+      key[i] = (uint64_t)(kept ? 1 + run : 0);
+      run += kept;
+    }
   }
   __syncthreads();
+  const int T1 = c.T1;
+  // the tree rows' parent and token, kept in shared memory for the mask and child walks
+  int* s_par = row_of + NG;
+  int* s_tok = s_par + T1;
   for (int i = threadIdx.x; i < NG; i += blockDim.x) row_of[i] = key[i] ? (int)key[i] : -1;
+  for (int r = threadIdx.x; r < T1; r += blockDim.x) { s_par[r] = -1; s_tok[r] = -1; }
   __syncthreads();
   const int ctx = c.ctx_len[b];
-  const int T1 = c.T1;
   const int rb = b * T1;
   if (threadIdx.x == 0) {
+    s_tok[0] = c.root_tok[b];
     c.tree_tok[rb] = c.root_tok[b];
     c.tree_pos[rb] = ctx;
     c.tree_slot[rb] = ctx;
@@ -225,7 +251,10 @@ __global__ void tree_finalize_k(CycleDev c) {
       pr = row_of[p];
       if (pr < 0) { latch_error(c.err, DEVERR_BOUNDS); pr = 0; }
     }
-    c.tree_tok[rb + r] = c.node_tok[base + i];
+    const int tok = c.node_tok[base + i];
+    s_par[r] = pr;
+    s_tok[r] = tok;
+    c.tree_tok[rb + r] = tok;
     c.tree_pos[rb + r] = ctx + c.node_depth[base + i];
     c.tree_slot[rb + r] = ctx + r;
     c.tree_seq[rb + r] = b;
@@ -233,26 +262,36 @@ __global__ void tree_finalize_k(CycleDev c) {
     c.tree_node[rb + r] = i;
   }
   __syncthreads();
+  // ancestry masks built in registers (T1 <= 256: at most four words), written once
   for (int r = threadIdx.x; r < T1; r += blockDim.x) {
-    uint64_t* mw = c.tmask + (size_t)(rb + r) * c.tmask_words;
-    for (int w = 0; w < c.tmask_words; ++w) mw[w] = 0ull;
+    uint64_t m0 = 0ull, m1 = 0ull, m2 = 0ull, m3 = 0ull;
     int a = r, guard = 0;
     while (a >= 0 && guard++ <= T1) {
-      mw[a >> 6] |= 1ull << (a & 63);
-      a = c.tree_parent[rb + a];
+      const uint64_t bit = 1ull << (a & 63);
+      const int w = a >> 6;
+      m0 |= w == 0 ? bit : 0ull;
+      m1 |= w == 1 ? bit : 0ull;
+      m2 |= w == 2 ? bit : 0ull;
+      m3 |= w == 3 ? bit : 0ull;
+      a = s_par[a];
     }
+    uint64_t* mw = c.tmask + (size_t)(rb + r) * c.tmask_words;
+    mw[0] = m0;
+    if (c.tmask_words > 1) mw[1] = m1;
+    if (c.tmask_words > 2) mw[2] = m2;
+    if (c.tmask_words > 3) mw[3] = m3;
     int n = 0;
     int* kids = c.tree_kids + (size_t)(rb + r) * c.k;
     for (int x = r + 1; x < T1 && n < c.k; ++x)
-      if (c.tree_parent[rb + x] == r) kids[n++] = c.tree_tok[rb + x];
+      if (s_par[x] == r) kids[n++] = s_tok[x];
     for (; n < c.k; ++n) kids[n] = -1;
   }
 }
 
 int tree_finalize(cudaStream_t st, const CycleDev& c) {
-  if (c.m > c.NG) return -1;
-  const size_t sm = (size_t)c.NG * (sizeof(uint64_t) + sizeof(int));
-  launch_k(tree_finalize_k, c.B, 256, sm, st, c);
+  if (c.m > c.NG || c.T1 > 256 || c.tmask_words > 4) return -1;
+  const size_t sm = (size_t)c.NG * (sizeof(uint64_t) + sizeof(int)) + (size_t)2 * c.T1 * sizeof(int);
+  launch_k(tree_finalize_k, c.B, TF_THREADS, sm, st, c);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
