@@ -25,7 +25,7 @@ def _stream(stream: Optional[torch.cuda.Stream]) -> int:
 
 
 def configs(w: Workload, max_batch: Optional[int] = None, max_ctx: Optional[int] = None,
-            prefill_chunk: int = 512):
+            prefill_chunk: int = 512, kv_block: Optional[int] = None):
     m = w.model
     mc = L.ModelCfg(m.n_layers, m.hidden, m.n_heads, m.n_kv_heads, m.head_dim, m.ffn, m.vocab,
                     m.rope_theta, m.rms_eps, L.DTYPE_F32 if m.dtype == "f32" else L.DTYPE_BF16)
@@ -34,7 +34,7 @@ def configs(w: Workload, max_batch: Optional[int] = None, max_ctx: Optional[int]
     tc = L.TreeCfg(t.topk, t.depth, t.m, t.temperature, w.seed, t.planted_p, t.planted_conf)
     if max_ctx is None:
         max_ctx = w.prompt_len[1] + w.new_tokens + 4 * (t.depth + 1) + 16
-    lim = L.Limits(max_batch or w.batch, max_ctx, 0, prefill_chunk)
+    lim = L.Limits(max_batch or w.batch, max_ctx, w.kv_block if kv_block is None else kv_block, prefill_chunk)
     return mc, dc, tc, lim
 
 
@@ -43,12 +43,12 @@ class Engine:
 
     def __init__(self, w: Workload, weights: Dict[str, torch.Tensor], max_batch: Optional[int] = None,
                  max_ctx: Optional[int] = None, prefill_chunk: int = 512,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 stream: Optional[torch.cuda.Stream] = None, kv_block: Optional[int] = None):
         self.lib = L.lib()
         self.w = w
         self.weights = weights
         self.stream = stream
-        self.mc, self.dc, self.tc, self.lim = configs(w, max_batch, max_ctx, prefill_chunk)
+        self.mc, self.dc, self.tc, self.lim = configs(w, max_batch, max_ctx, prefill_chunk, kv_block)
         nb = self.lib.eagle_workspace_bytes(C.byref(self.mc), C.byref(self.dc), C.byref(self.tc), C.byref(self.lim))
         if nb == 0:
             raise L.EagleError(L.EAGLE_EINVAL, "invalid configuration")
@@ -119,6 +119,13 @@ class Engine:
         k, v, cap = C.c_void_p(), C.c_void_p(), C.c_int()
         self._check(self.lib.eagle_kv_view(self.h, C.byref(k), C.byref(v), C.byref(cap)), "eagle_kv_view")
         return k.value, v.value, cap.value
+
+    def kv_table(self):
+        """Paged target KV: (device pointer of the int32 block table [max_batch][tab_w], tab_w,
+        pool blocks per layer, block size)."""
+        t, tw, nb, bs = C.c_void_p(), C.c_int(), C.c_int(), C.c_int()
+        self._check(self.lib.eagle_kv_table(self.h, C.byref(t), C.byref(tw), C.byref(nb), C.byref(bs)), "eagle_kv_table")
+        return t.value, tw.value, nb.value, bs.value
 
     def dump_raw(self, what: int) -> torch.Tensor:
         n = self.lib.eagle_dump_bytes(self.h, what)

@@ -77,41 +77,43 @@ int accept_walk(cudaStream_t st, const CycleDev& c, const HeadOut& h, int* out_t
 // element positions and reads all L sources before writing any target, so overlapping
 // source/target slots cannot race.
 template <typename T>
-__global__ void compact_k(T* kc, T* vc, int layers, int B, int nkv, int cap, int d, const int* n_old,
-                          const int* acc_len, const int* acc_path, int Dmax) {
+__global__ void compact_k(T* kc, T* vc, int layers, size_t layer_elems, int B, int nkv, int cap, int d,
+                          const int* n_old, const int* acc_len, const int* acc_path, int Dmax, KvPage page) {
   PDL_ENTRY();
   const int layer = blockIdx.x;
   const int bh = blockIdx.y;
-  const int b = bh / nkv;
+  const int b = bh / nkv, h = bh - b * nkv;
   const int L = acc_len[b];
   if (L <= 0) return;
   const int n = n_old[b];
-  const size_t base = (((size_t)layer * B * nkv) + bh) * (size_t)cap * d;
+  T* kl = kc + (size_t)layer * layer_elems;
+  T* vl = vc + (size_t)layer * layer_elems;
   T tk[8], tv[8];
   for (int e = threadIdx.x; e < d; e += blockDim.x) {
     for (int j = 0; j < L && j < 8; ++j) {
-      const size_t s = base + (size_t)(n + acc_path[b * Dmax + j]) * d + e;
-      tk[j] = kc[s];
-      tv[j] = vc[s];
+      const size_t s = kv_row(page, b, nkv, h, cap, n + acc_path[b * Dmax + j]) * d + e;
+      tk[j] = kl[s];
+      tv[j] = vl[s];
     }
     for (int j = 0; j < L && j < 8; ++j) {
-      const size_t t = base + (size_t)(n + 1 + j) * d + e;
-      kc[t] = tk[j];
-      vc[t] = tv[j];
+      const size_t t = kv_row(page, b, nkv, h, cap, n + 1 + j) * d + e;
+      kl[t] = tk[j];
+      vl[t] = tv[j];
     }
   }
 }
 
-int compact_kv(cudaStream_t st, int dtype, void* kc, void* vc, int layers, int B, int nkv, int cap, int d,
-               const int* n_old, const int* acc_len, const int* acc_path, int Dmax) {
+int compact_kv(cudaStream_t st, int dtype, void* kc, void* vc, int layers, size_t layer_elems, int B, int nkv,
+               int cap, int d, const int* n_old, const int* acc_len, const int* acc_path, int Dmax,
+               const KvPage& page) {
   if (Dmax > 8) return -1;
   dim3 grid(layers, B * nkv);
   if (dtype == DT_F32)
-    launch_k(compact_k<float>, grid, 128, 0, st, (float*)kc, (float*)vc, layers, B, nkv, cap, d, n_old, acc_len,
-                                           acc_path, Dmax);
+    launch_k(compact_k<float>, grid, 128, 0, st, (float*)kc, (float*)vc, layers, layer_elems, B, nkv, cap, d, n_old,
+             acc_len, acc_path, Dmax, page);
   else
-    launch_k(compact_k<__nv_bfloat16>, grid, 128, 0, st, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, layers, B, nkv, cap,
-                                                   d, n_old, acc_len, acc_path, Dmax);
+    launch_k(compact_k<__nv_bfloat16>, grid, 128, 0, st, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, layers, layer_elems, B,
+             nkv, cap, d, n_old, acc_len, acc_path, Dmax, page);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -41,8 +41,8 @@ __global__ void __launch_bounds__(128) attn_simt_k(AttnArgs a) {
   const int d = a.d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const T* qp = reinterpret_cast<const T*>(a.q);
-  const T* kc = reinterpret_cast<const T*>(a.kcache) + (size_t)(seq * a.nkv + kvh) * a.cap * d;
-  const T* vc = reinterpret_cast<const T*>(a.vcache) + (size_t)(seq * a.nkv + kvh) * a.cap * d;
+  const T* kc = reinterpret_cast<const T*>(a.kcache);
+  const T* vc = reinterpret_cast<const T*>(a.vcache);
   const int ctx = a.ctx_len[seq];
 
   // load the query vectors: qv = (row - r0) * G + g
@@ -72,8 +72,9 @@ __global__ void __launch_bounds__(128) attn_simt_k(AttnArgs a) {
       const int kk = i / d, c = i % d;
       const int s = t0 + kk;
       const bool in = s < kend;
-      sk[kk][c] = in ? Elem<T>::to_f(kc[(size_t)s * d + c]) : 0.f;
-      sv[kk][c] = in ? Elem<T>::to_f(vc[(size_t)s * d + c]) : 0.f;
+      const size_t ro = in ? kv_row(a.page, seq, a.nkv, kvh, a.cap, s) * d + c : 0;
+      sk[kk][c] = in ? Elem<T>::to_f(kc[ro]) : 0.f;
+      sv[kk][c] = in ? Elem<T>::to_f(vc[ro]) : 0.f;
     }
     __syncthreads();
     const int s = t0 + lane;
@@ -235,8 +236,8 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   const int seq = a.row_seq[r0];
   const int ctx = a.ctx_len[seq];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.kcache) + (size_t)(seq * a.nkv + kvh) * a.cap * D;
-  const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.vcache) + (size_t)(seq * a.nkv + kvh) * a.cap * D;
+  const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.kcache);
+  const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.vcache);
 
   int kend = 0;
   for (int r = r0; r < r1; ++r) kend = max(kend, a.mode == 0 ? a.row_slot[r] + 1 : ctx + a.tree_T);
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
       const int kr = i / CH, c = i % CH;
       const int key = t * MT_KEYS + kr;
       const bool in = key < kend;
-      const size_t goff = (size_t)(in ? key : 0) * D + c * 8;
+      const size_t goff = kv_row(a.page, seq, a.nkv, kvh, a.cap, in ? key : 0) * D + c * 8;
       const uint32_t dk = smem_u32(sK + (buf * MT_KEYS + kr) * LD + c * 8);
       const uint32_t dv = smem_u32(sV + (buf * MT_KEYS + kr) * LD + c * 8);
       cp_async16(dk, kc + goff, in ? 16 : 0);

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "kernels.h"
+
 namespace eagle {
 
 struct CycleDev {
@@ -73,8 +75,10 @@ int tree_select(cudaStream_t st, const CycleDev& c, int d);
 int tree_add(cudaStream_t st, const CycleDev& c, int d, const HeadOut& h);
 int tree_finalize(cudaStream_t st, const CycleDev& c);
 int accept_walk(cudaStream_t st, const CycleDev& c, const HeadOut& h, int* out_tokens, int* out_count);
-int compact_kv(cudaStream_t st, int dtype, void* kc, void* vc, int layers, int B, int nkv, int cap, int d,
-               const int* n_old, const int* acc_len, const int* acc_path, int Dmax);
+// accepted tree slots n + acc_path[j] -> n + 1 + j, every layer (layer_elems apart)
+int compact_kv(cudaStream_t st, int dtype, void* kc, void* vc, int layers, size_t layer_elems, int B, int nkv,
+               int cap, int d, const int* n_old, const int* acc_len, const int* acc_path, int Dmax,
+               const KvPage& page);
 // drafter update rows after acceptance: rows b*(D+1)+j, j = 0..D
 int update_rows(cudaStream_t st, const CycleDev& c, int* row_tok, int* row_pos, int* row_slot, int* row_seq,
                 int* row_featsrc);

@@ -46,6 +46,10 @@ struct Carver {
 struct Dims {
   int L, H, F, V, nq, nkv, d, QKV, A, B, k, D, m, T1, NG, cap, dcap, P, Rt, Rd, R, Rh, KIN, fsrc_rows, dmw, tmw,
       rope_pos, kind, esz, dt, max_ctx, n_tiles, Kh;
+  // target KV cache: kvb_log2 = 0 contiguous, else blocks of 2^kvb_log2 slots, tab_w blocks
+  // per sequence in the block table, nblk blocks in the pool; kv_layer_elems per layer
+  int kvb_log2, tab_w, nblk;
+  size_t kv_layer_elems;
 };
 
 bool derive(const eagle_model_cfg* mc, const eagle_drafter_cfg* dc, const eagle_tree_cfg* tc,
@@ -76,7 +80,9 @@ bool derive(const eagle_model_cfg* mc, const eagle_drafter_cfg* dc, const eagle_
   if (tc->planted_p < 0.f || tc->planted_p > 1.f || tc->planted_conf <= 0.f || tc->planted_conf >= 1.f) {
     why = "planted_p must be in [0,1] and planted_conf in (0,1)"; return false; }
   if (lim->max_batch < 1 || lim->max_ctx < 2) { why = "max_batch >= 1 and max_ctx >= 2 required"; return false; }
-  if (lim->kv_block != 0) { why = "paged KV (kv_block > 0) is not implemented in this build"; return false; }
+  if (lim->kv_block < 0 || (lim->kv_block != 0 && (lim->kv_block < 8 || lim->kv_block > 256 ||
+                                                    (lim->kv_block & (lim->kv_block - 1))))) {
+    why = "kv_block must be 0 (contiguous KV) or a power of two in 8..256"; return false; }
   z.B = lim->max_batch;
   z.max_ctx = lim->max_ctx;
   z.T1 = z.m + 1;
@@ -95,6 +101,17 @@ bool derive(const eagle_model_cfg* mc, const eagle_drafter_cfg* dc, const eagle_
   z.rope_pos = std::max(z.cap, z.dcap) + 8;
   z.n_tiles = (z.V + 127) / 128;
   z.Kh = std::max(z.k, 2);
+  z.kvb_log2 = 0;
+  while (lim->kv_block > 0 && (1 << z.kvb_log2) < lim->kv_block) ++z.kvb_log2;
+  if (z.kvb_log2 > 0) {
+    z.tab_w = (z.cap + lim->kv_block - 1) >> z.kvb_log2;
+    z.nblk = z.B * z.tab_w;
+    z.kv_layer_elems = (size_t)z.nblk * z.nkv * ((size_t)1 << z.kvb_log2) * z.d;
+  } else {
+    z.tab_w = 0;
+    z.nblk = 0;
+    z.kv_layer_elems = (size_t)z.B * z.nkv * z.cap * z.d;
+  }
   return true;
 }
 
@@ -146,6 +163,9 @@ struct eagle_ctx {
   int fuse_epi = 0;                     // bf16: RoPE/KV write and SwiGLU in the GEMM epilogues (EAGLE_FUSE_EPI=1: on)
   float *rope_cos, *rope_sin;
   void *kc, *vc, *dkc, *dvc;
+  int* kv_table;      // paged target KV: [B][tab_w] physical block per logical block, -1 = none
+  int* kv_next;       // next free block of the pool (one device counter)
+  KvPage page;        // the target cache's addressing (table == nullptr: contiguous)
   int* prompt_copy;   // unused placeholder
   CycleDev cd;
 };
@@ -206,10 +226,13 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
     x->attn_pml = c.take<float>((size_t)16 * rs * z.nq * 2);
   }
   x->chain_bar = c.take<unsigned>(4);
+  x->kv_table = c.take<int>(std::max(1, z.nblk));
+  x->kv_next = c.take<int>(4);
   x->rope_cos = c.take<float>((size_t)z.rope_pos * (z.d / 2));
   x->rope_sin = c.take<float>((size_t)z.rope_pos * (z.d / 2));
-  x->kc = c.take<uint8_t>((size_t)z.L * B * z.nkv * z.cap * z.d * es);
-  x->vc = c.take<uint8_t>((size_t)z.L * B * z.nkv * z.cap * z.d * es);
+  x->kc = c.take<uint8_t>((size_t)z.L * z.kv_layer_elems * es);
+  x->vc = c.take<uint8_t>((size_t)z.L * z.kv_layer_elems * es);
+  x->page = KvPage{z.kvb_log2 ? x->kv_table : nullptr, z.tab_w, z.kvb_log2};
   x->dkc = c.take<uint8_t>((size_t)B * z.nkv * z.dcap * z.d * es);
   x->dvc = c.take<uint8_t>((size_t)B * z.nkv * z.dcap * z.d * es);
 }
@@ -290,13 +313,14 @@ int lm_head(eagle_ctx* ctx, const void* X, int M, HeadParams& p, float* logits_b
 // Self-attention of one layer over R rows (q in ctx->qb, keys/values already in the cache)
 // into ctx->att.
 int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_per_seq, const int* slot,
-           const int* seq, int mode, int tree_T, const uint64_t* mask, int mask_words) {
+           const int* seq, int mode, int tree_T, const uint64_t* mask, int mask_words, const KvPage& page) {
   const Dims& z = ctx->z;
   AttnArgs a{};
   a.q = ctx->qb; a.kcache = kcache; a.vcache = vcache; a.out = ctx->att;
   a.R = R; a.nq = z.nq; a.nkv = z.nkv; a.d = z.d; a.cap = cap; a.rows_per_seq = rows_per_seq;
   a.row_seq = seq; a.row_slot = slot; a.ctx_len = ctx->ctx_len; a.mode = mode; a.tree_T = tree_T;
   a.mask = mask; a.mask_words = mask_words; a.scale = 1.f / sqrtf((float)z.d);
+  a.page = page;
   a.part_o = ctx->attn_po; a.part_ml = ctx->attn_pml; a.part_floats = ctx->attn_pfloats;
   CK(attention(ctx->st, z.dt, a));
   return 0;
@@ -306,18 +330,19 @@ int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_
 // [R][kin]; x: fp32 residual.
 int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const void* attn_in, int kin, void* kcache,
                   void* vcache, int cap, int rows_per_seq, const int* pos, const int* slot, const int* seq, int mode,
-                  int tree_T, const uint64_t* mask, int mask_words) {
+                  int tree_T, const uint64_t* mask, int mask_words, const KvPage& page) {
   const Dims& z = ctx->z;
-  if (z.dt == DT_BF16 && ctx->fuse_epi && 128 % z.d == 0) {
+  // the fused epilogue writes a contiguous cache only
+  if (z.dt == DT_BF16 && ctx->fuse_epi && 128 % z.d == 0 && !page.table) {
     // RoPE, the q output and the KV-cache write in the projection's epilogue
     const QkvEpi q{pos, slot, seq, ctx->rope_cos, ctx->rope_sin, ctx->qb, kcache, vcache, z.nq, z.nkv, z.d, cap};
     CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_QKV, nullptr, 0, nullptr, &q));
   } else {
     CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_F32, ctx->qkv, z.QKV));
     CK(rope_store(ctx->st, z.dt, ctx->qkv, R, z.nq, z.nkv, z.d, pos, slot, seq, ctx->rope_cos, ctx->rope_sin,
-                  ctx->qb, kcache, vcache, cap, ctx->dev_err, cap));
+                  ctx->qb, kcache, vcache, cap, ctx->dev_err, cap, page));
   }
-  int r = attend(ctx, kcache, vcache, cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words);
+  int r = attend(ctx, kcache, vcache, cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words, page);
   if (r) return r;
   CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
   CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
@@ -336,7 +361,7 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
 // The chain's vectorised row ops need head_dim % 8 == 0, ffn % 4 == 0 (bf16 sizes are
 // already multiples of 8) and rows of at most 5120 features; other shapes run per-op.
 bool chained(const eagle_ctx* ctx) {
-  return ctx->z.dt == DT_BF16 && ctx->use_chain && ctx->z.d % 8 == 0 && ctx->z.F % 4 == 0 && ctx->z.H <= 5120;
+  return ctx->z.dt == DT_BF16 && ctx->use_chain && !ctx->page.table && ctx->z.d % 8 == 0 && ctx->z.F % 4 == 0 && ctx->z.H <= 5120;
 }
 
 ChainProgram chain_prog(eagle_ctx* ctx, int M) {
@@ -420,7 +445,7 @@ int target_forward_chain(eagle_ctx* ctx, int R, const int* tok, const int* pos, 
                          int rows_per_seq, int mode, int tree_T, const uint64_t* mask, int mask_words, void* feat_out,
                          void* caps_out, size_t caps_ld, size_t caps_row0) {
   const Dims& z = ctx->z;
-  const size_t lstride = (size_t)z.B * z.nkv * z.cap * z.d * z.esz;
+  const size_t lstride = z.kv_layer_elems * z.esz;
   auto kc = [&](int l) { return (void*)((uint8_t*)ctx->kc + l * lstride); };
   auto vc = [&](int l) { return (void*)((uint8_t*)ctx->vc + l * lstride); };
   ChainProgram p = chain_prog(ctx, R);
@@ -431,7 +456,7 @@ int target_forward_chain(eagle_ctx* ctx, int R, const int* tok, const int* pos, 
   int r = run_chain(ctx, p);
   if (r) return r;
   for (int l = 0; l < z.L; ++l) {
-    r = attend(ctx, kc(l), vc(l), z.cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words);
+    r = attend(ctx, kc(l), vc(l), z.cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words, ctx->page);
     if (r) return r;
     p = chain_prog(ctx, R);
     add_post(p, ctx, ctx->layers[l]);
@@ -462,12 +487,12 @@ int target_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const 
     return target_forward_chain(ctx, R, tok, pos, slot, seq, rows_per_seq, mode, tree_T, mask, mask_words, feat_out,
                                 caps_out, caps_ld, caps_row0);
   CK(embed_rows(ctx->st, z.dt, ctx->w.embed, z.V, z.H, tok, R, ctx->x, ctx->dev_err));
-  const size_t lstride = (size_t)z.B * z.nkv * z.cap * z.d * z.esz;
+  const size_t lstride = z.kv_layer_elems * z.esz;
   for (int l = 0; l < z.L; ++l) {
     const eagle_layer_weights& lw = ctx->layers[l];
     CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
     int r = layer_forward(ctx, lw, R, ctx->ain, z.H, (uint8_t*)ctx->kc + l * lstride, (uint8_t*)ctx->vc + l * lstride,
-                          z.cap, rows_per_seq, pos, slot, seq, mode, tree_T, mask, mask_words);
+                          z.cap, rows_per_seq, pos, slot, seq, mode, tree_T, mask, mask_words, ctx->page);
     if (r) return r;
     if (z.kind == 3 && caps_out) {
       for (int j = 0; j < 3; ++j)
@@ -529,7 +554,8 @@ int drafter_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const
     add_qkv(p, ctx, lw, kin, ctx->dkc, ctx->dvc, z.dcap, pos, slot, seq);
     int r = run_chain(ctx, p);
     if (r) return r;
-    r = attend(ctx, ctx->dkc, ctx->dvc, z.dcap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words);
+    r = attend(ctx, ctx->dkc, ctx->dvc, z.dcap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words,
+               KvPage{nullptr, 0, 0});
     if (r) return r;
     p = chain_prog(ctx, R);
     add_post(p, ctx, lw);
@@ -537,7 +563,7 @@ int drafter_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const
     return run_chain(ctx, p);
   }
   int r = layer_forward(ctx, lw, R, ctx->ain, kin, ctx->dkc, ctx->dvc, z.dcap, rows_per_seq, pos, slot, seq, mode,
-                        tree_T, mask, mask_words);
+                        tree_T, mask, mask_words, KvPage{nullptr, 0, 0});
   if (r) return r;
   CK(convert_rows(ctx->st, z.dt, ctx->x, z.H, R, ctx->dout, z.H));
   return 0;
@@ -579,12 +605,52 @@ __global__ void drow_out_k(int* out, int B, int k, int fsrc_rows, int d) {
   if (i < B * k) out[i] = (i / k) * fsrc_rows + 1 + (d - 1) * k + (i % k);
 }
 
+// ---- paged target KV: block assignment ---------------------------------------------------------
+// Every table entry -1 and the pool's counter 0 (at prefill, which starts the sequences anew).
+__global__ void kv_reset_k(int* table, int n, int* next) {
+  PDL_ENTRY();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) table[i] = -1;
+  if (i == 0) *next = 0;
+}
+
+// Sequences b0 .. b0 + nb - 1 get pool blocks for their slots [lo, lo + span), lo = lo_dev[b]
+// (or lo_const): one thread walks them in order, so placement is deterministic. The pool holds
+// every sequence's worst case, so it runs dry only on a host-side capacity bug (latched).
+__global__ void kv_reserve_k(int* table, int tab_w, int bs_log2, int* next, int nblk, int b0, int nb,
+                             const int* lo_dev, int lo_const, int span, int* err) {
+  PDL_ENTRY();
+  if (blockIdx.x || threadIdx.x) return;
+  int nx = *next;
+  for (int b = b0; b < b0 + nb; ++b) {
+    const int lo = lo_dev ? lo_dev[b] : lo_const;
+    if (span <= 0 || lo < 0) continue;
+    const int j0 = lo >> bs_log2, j1 = min((lo + span - 1) >> bs_log2, tab_w - 1);
+    for (int j = j0; j <= j1; ++j) {
+      int* e = table + (size_t)b * tab_w + j;
+      if (*e >= 0) continue;
+      if (nx >= nblk) { latch_error(err, DEVERR_CAPACITY); break; }
+      *e = nx++;
+    }
+  }
+  *next = nx;
+}
+
+int kv_reserve(eagle_ctx* ctx, int b0, int nb, const int* lo_dev, int lo_const, int span) {
+  const Dims& z = ctx->z;
+  if (!ctx->page.table) return 0;
+  launch_k(kv_reserve_k, 1, 32, 0, ctx->st, ctx->kv_table, z.tab_w, z.kvb_log2, ctx->kv_next, z.nblk, b0, nb, lo_dev,
+           lo_const, span, ctx->dev_err);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
 // ---- the cycle -------------------------------------------------------------------------------
 int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   const Dims& z = ctx->z;
   const int B = ctx->batch;
   CycleDev& c = ctx->cd;
   const size_t rb = (size_t)z.H * z.esz;
+  CK(kv_reserve(ctx, 0, B, ctx->ctx_len, 0, z.T1));   // the tree rows' slots [ctx, ctx + m + 1)
   CK(tree_start(ctx->st, c));
   for (int d = 1; d < z.D; ++d) {
     CK(tree_select(ctx->st, c, d));
@@ -631,8 +697,8 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   hv.top_id = ctx->v_id; hv.top_val = ctx->v_val; hv.lse = ctx->v_lse; hv.spec_logit = ctx->v_spec;
   hv.K = p.K; hv.S = sampling ? z.k : 1;
   CK(accept_walk(ctx->st, c, hv, out_tokens, out_count));
-  CK(compact_kv(ctx->st, z.dt, ctx->kc, ctx->vc, z.L, z.B, z.nkv, z.cap, z.d, ctx->n_old, ctx->acc_len, ctx->acc_path,
-                z.D));
+  CK(compact_kv(ctx->st, z.dt, ctx->kc, ctx->vc, z.L, z.kv_layer_elems, z.B, z.nkv, z.cap, z.d, ctx->n_old,
+                ctx->acc_len, ctx->acc_path, z.D, ctx->page));
   // drafter update over the committed positions
   const int RU = B * (z.D + 1);
   CK(update_rows(ctx->st, c, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, ctx->row_feat));
@@ -853,6 +919,12 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
   ctx->cd.ref = d_ref;
   ctx->cd.ref_len = ctx->ref_len;
   CycleDev& c = ctx->cd;
+  if (ctx->page.table) {
+    // the sequences start anew: empty block table, then blocks for every prompt slot
+    launch_k(kv_reset_k, (z.nblk + 255) / 256, 256, 0, ctx->st, ctx->kv_table, z.nblk, ctx->kv_next);
+    if (cudaGetLastError() != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "kv table reset failed");
+    for (int b = 0; b < batch; ++b) CK(kv_reserve(ctx, b, 1, nullptr, 0, h_lens[b]));
+  }
   const size_t rb = (size_t)z.H * z.esz;
   bool uniform = true;
   for (int b = 1; b < batch; ++b) uniform = uniform && h_lens[b] == h_lens[0];
@@ -981,6 +1053,7 @@ int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens, float
   CycleDev& c = ctx->cd;
   const bool sampling = ctx->tc.temperature > 0.f;
   for (int s = 0; s < n_steps; ++s) {
+    CK(kv_reserve(ctx, 0, B, ctx->ctx_len, 0, 1));
     CK(plain_rows(ctx->st, c, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq));
     int r = target_forward(ctx, B, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, 1, 0, 0, nullptr, 0,
                            ctx->feat_t, nullptr, 0, 0);
@@ -1121,6 +1194,16 @@ int eagle_kv_view(const eagle_ctx* ctx, void** k, void** v, int* cap) {
   if (k) *k = ctx->kc;
   if (v) *v = ctx->vc;
   if (cap) *cap = ctx->z.cap;
+  return EAGLE_OK;
+}
+
+int eagle_kv_table(const eagle_ctx* ctx, const int32_t** table, int* tab_w, int* n_blocks, int* block) {
+  if (!ctx) return EAGLE_EINVAL;
+  if (!ctx->page.table) return EAGLE_EUNSUPPORTED;
+  if (table) *table = ctx->kv_table;
+  if (tab_w) *tab_w = ctx->z.tab_w;
+  if (n_blocks) *n_blocks = ctx->z.nblk;
+  if (block) *block = 1 << ctx->z.kvb_log2;
   return EAGLE_OK;
 }
 

@@ -71,6 +71,24 @@ int head_partials_from_logits(cudaStream_t st, const float* logits, int ld, cons
 int head_merge(cudaStream_t st, const HeadParams& p);
 size_t head_part_bytes(int vocab, int rows, int K);
 
+// ---- KV-cache addressing ----------------------------------------------------------------------
+// Contiguous cache (table == nullptr): one layer is [seq][nkv][cap][d]. Paged cache: one layer
+// is a pool of blocks of 2^bs_log2 token slots, [block][nkv][slot in block][d], and
+// table[seq * tab_w + j] is the physical block that holds the sequence's slots
+// [j << bs_log2, (j + 1) << bs_log2) (-1 = not assigned yet).
+struct KvPage {
+  const int* table;
+  int tab_w;
+  int bs_log2;
+};
+// Row (in units of d elements) of key/value head h of sequence seq at slot.
+__host__ __device__ inline size_t kv_row(const KvPage& p, int seq, int nkv, int h, int cap, int slot) {
+  if (!p.table) return ((size_t)seq * nkv + h) * (size_t)cap + (size_t)slot;
+  int blk = p.table[(size_t)seq * p.tab_w + (slot >> p.bs_log2)];
+  if (blk < 0) blk = 0;   // unassigned: writers check first; a read stays inside the pool
+  return (((size_t)blk * nkv + h) << p.bs_log2) + (size_t)(slot & ((1 << p.bs_log2) - 1));
+}
+
 // ---- element-wise / row ops (dtype = DT_F32 or DT_BF16 storage) --------------------------
 int embed_rows(cudaStream_t st, int dtype, const void* E, int V, int H, const int* tok, int R, float* x,
                int* err);
@@ -78,7 +96,8 @@ int rmsnorm_rows(cudaStream_t st, int dtype_in, const void* x, int ldx, const vo
                  int R, int dtype_out, void* out, int ldo);
 int rope_store(cudaStream_t st, int dtype, const float* qkv, int R, int nq, int nkv, int d,
                const int* row_pos, const int* row_slot, const int* row_seq, const float* rope_cos,
-               const float* rope_sin, void* q_out, void* kcache, void* vcache, int cap, int* err, int slot_limit);
+               const float* rope_sin, void* q_out, void* kcache, void* vcache, int cap, int* err, int slot_limit,
+               const KvPage& page = KvPage{nullptr, 0, 0});
 int swiglu_rows(cudaStream_t st, int dtype, const float* gu, int F, int R, void* out);
 int concat_emb_feat(cudaStream_t st, int dtype, const void* E, int V, int H, const int* tok,
                     const void* feat, const int* feat_row, int R, void* out, int* err);
@@ -90,8 +109,9 @@ int widen_rows(cudaStream_t st, int dtype, const void* x, int ldx, int H, int R,
 // ---- attention -----------------------------------------------------------------------------
 struct AttnArgs {
   const void* q;        // [R][nq][d]
-  const void* kcache;   // this layer: [(seq * nkv + h) * cap + slot][d]
+  const void* kcache;   // this layer: row kv_row(page, seq, nkv, h, cap, slot) of d elements
   const void* vcache;
+  KvPage page;          // table == nullptr: contiguous [(seq * nkv + h) * cap + slot][d]
   void* out;            // [R][nq][d]
   int R, nq, nkv, d, cap;
   int rows_per_seq;     // rows of one sequence are contiguous; a row block never straddles two

@@ -112,12 +112,14 @@ constexpr int RS_HEADS = 8, RS_THREADS = 128, RS_ITEMS = 4;
 template <typename T>
 __global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int* row_pos, const int* row_slot,
                              const int* row_seq, const float* rc, const float* rsn, T* q_out, T* kc, T* vc, int cap,
-                             int* err, int slot_limit) {
+                             int* err, int slot_limit, KvPage page) {
   PDL_ENTRY();
   const int r = blockIdx.x, h0 = blockIdx.y * RS_HEADS;
   const int H = nq + 2 * nkv, half = d / 2;
   const int slot = row_slot[r];
-  const bool slot_ok = slot >= 0 && slot < cap && slot < slot_limit;
+  // a paged cache must hold a block for the slot (assigned before the step that writes it)
+  const bool slot_ok = slot >= 0 && slot < cap && slot < slot_limit &&
+                       (!page.table || page.table[(size_t)row_seq[r] * page.tab_w + (slot >> page.bs_log2)] >= 0);
   if (!slot_ok && blockIdx.y == 0 && threadIdx.x == 0) latch_error(err, DEVERR_CAPACITY);
   const int seq = row_seq[r], pos = row_pos[r];
   const float* src = qkv + (size_t)r * H * d;
@@ -146,7 +148,7 @@ __global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int
       if (it >= n) continue;
       if (h >= nq + nkv) {   // value head: plain copy
         if (slot_ok) {
-          T* v = vc + ((size_t)(seq * nkv + (h - nq - nkv)) * cap + slot) * d;
+          T* v = vc + kv_row(page, seq, nkv, h - nq - nkv, cap, slot) * d;
           v[i] = Elem<T>::from_f(xa[k]);
           v[i + half] = Elem<T>::from_f(xb[k]);
         }
@@ -155,7 +157,7 @@ __global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int
       if (h >= nq && !slot_ok) continue;
       float lo, hi;
       rope_pair(xa[k], xb[k], cs[k], sn[k], lo, hi);
-      T* dst = h < nq ? q_out + ((size_t)r * nq + h) * d : kc + ((size_t)(seq * nkv + (h - nq)) * cap + slot) * d;
+      T* dst = h < nq ? q_out + ((size_t)r * nq + h) * d : kc + kv_row(page, seq, nkv, h - nq, cap, slot) * d;
       dst[i] = Elem<T>::from_f(lo);
       dst[i + half] = Elem<T>::from_f(hi);
     }
@@ -165,7 +167,7 @@ __global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int
 int rope_store(cudaStream_t st, int dtype, const float* qkv, int R, int nq, int nkv, int d,
                const int* row_pos, const int* row_slot, const int* row_seq, const float* rope_cos,
                const float* rope_sin, void* q_out, void* kcache, void* vcache, int cap, int* err,
-               int slot_limit) {
+               int slot_limit, const KvPage& page) {
   if (R <= 0) return 0;
   // blocks of RS_HEADS heads of one row: a 7B verify pass (61 rows x 96 heads) is one wave
   // of resident blocks, so the next kernel can be scheduled while this one runs
@@ -173,11 +175,11 @@ int rope_store(cudaStream_t st, int dtype, const float* qkv, int R, int nq, int 
   const int threads = RS_THREADS;
   if (dtype == DT_F32)
     launch_k(rope_store_k<float>, grid, threads, 0, st, qkv, nq, nkv, d, row_pos, row_slot, row_seq, rope_cos, rope_sin,
-                                                  (float*)q_out, (float*)kcache, (float*)vcache, cap, err, slot_limit);
+                                                  (float*)q_out, (float*)kcache, (float*)vcache, cap, err, slot_limit, page);
   else
     launch_k(rope_store_k<__nv_bfloat16>, grid, threads, 0, st, qkv, nq, nkv, d, row_pos, row_slot, row_seq, rope_cos,
                                                           rope_sin, (__nv_bfloat16*)q_out, (__nv_bfloat16*)kcache,
-                                                          (__nv_bfloat16*)vcache, cap, err, slot_limit);
+                                                          (__nv_bfloat16*)vcache, cap, err, slot_limit, page);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -209,7 +209,8 @@ int eagle_op_compact(int dtype, void* stream, void* kcache, void* vcache, int la
       Dmax > 8)
     return EAGLE_EINVAL;
   const int r = compact_kv(reinterpret_cast<cudaStream_t>(stream), dtype == EAGLE_DTYPE_F32 ? DT_F32 : DT_BF16, kcache,
-                           vcache, layers, B, nkv, cap, d, n_old, acc_len, acc_path, Dmax);
+                           vcache, layers, (size_t)B * nkv * cap * d, B, nkv, cap, d, n_old, acc_len, acc_path,
+                           Dmax, KvPage{nullptr, 0, 0});
   return r == 0 ? EAGLE_OK : EAGLE_ECUDA;
 }
 

@@ -88,7 +88,9 @@ typedef struct {
 typedef struct {
   int max_batch;      /* sequences per context */
   int max_ctx;        /* KV entries per sequence (prompt + generated) */
-  int kv_block;       /* 0 = contiguous KV (only mode of this build) */
+  int kv_block;       /* 0 = contiguous target KV; 8..256 (a power of two) = paged target KV
+                         in blocks of kv_block slots, assigned from a pool as sequences grow
+                         (the drafter's one-layer cache stays contiguous) */
   int prefill_chunk;  /* prompt rows per prefill pass (0 = 512) */
 } eagle_limits;
 
@@ -183,9 +185,15 @@ int eagle_debug_dump(eagle_ctx* ctx, int what, void* dst, size_t bytes);
 enum { EAGLE_DEBUG_LOGITS = 1 };
 int eagle_set_debug(eagle_ctx* ctx, int flags);
 
-/* Device pointers of the target KV cache, layout [layer][batch][kv_head][slot][head_dim]
- * with `cap` slots per sequence (storage type); for tests and tools. */
+/* Device pointers of the target KV cache (storage type); for tests and tools. Contiguous
+ * (kv_block = 0): layout [layer][batch][kv_head][slot][head_dim] with `cap` slots per sequence.
+ * Paged: each layer is a pool [block][kv_head][slot in block][head_dim]; see eagle_kv_table. */
 int eagle_kv_view(const eagle_ctx* ctx, void** k, void** v, int* cap);
+
+/* Paged target KV: the device block table [batch][*tab_w] (int32, physical block of each
+ * sequence's slots [j * kv_block, (j + 1) * kv_block), -1 = unassigned), the pool's blocks per
+ * layer and the block size. EAGLE_EUNSUPPORTED for a contiguous cache. */
+int eagle_kv_table(const eagle_ctx* ctx, const int32_t** table, int* tab_w, int* n_blocks, int* block);
 
 /* Per-launch timing of the tensor-core GEMMs inside real cycles (graph replay off):
  * eagle_profile_begin arms CUDA events (host-created, no device allocation) around the

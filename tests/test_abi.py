@@ -58,11 +58,30 @@ def test_workspace_rejects_bad_configs(lib):
                    lambda mc, dc, tc, lim: setattr(mc, "n_kv_heads", 3),
                    lambda mc, dc, tc, lim: setattr(mc, "head_dim", 256),
                    lambda mc, dc, tc, lim: setattr(dc, "kind", 2),
-                   lambda mc, dc, tc, lim: setattr(lim, "kv_block", 16),
+                   lambda mc, dc, tc, lim: setattr(lim, "kv_block", 12),
+                   lambda mc, dc, tc, lim: setattr(lim, "kv_block", 4),
+                   lambda mc, dc, tc, lim: setattr(lim, "kv_block", 512),
+                   lambda mc, dc, tc, lim: setattr(lim, "kv_block", -16),
                    lambda mc, dc, tc, lim: setattr(tc, "planted_conf", 1.0)):
         mc, dc, tc, lim = _cfg(w)
         mutate(mc, dc, tc, lim)
         assert lib.eagle_workspace_bytes(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(lim)) == 0
+
+
+def test_paged_kv_workspace(lib):
+    """kv_block = 16 (the batch-64 configuration's paged cache) is accepted; the pool holds
+    every sequence's worst case, so it costs at most one block per sequence more than the
+    contiguous cache."""
+    w = synth.LLAMA31_8B_BS64
+    assert w.kv_block == 16
+    mc, dc, tc, lim = _cfg(w)
+    paged = lib.eagle_workspace_bytes(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(lim))
+    lim.kv_block = 0
+    contiguous = lib.eagle_workspace_bytes(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(lim))
+    assert paged > 0 and contiguous > 0
+    m = w.model
+    block_bytes = 2 * m.n_layers * m.n_kv_heads * 16 * m.head_dim * 2
+    assert contiguous <= paged <= contiguous + lim.max_batch * (block_bytes + 64) + (1 << 20)
 
 
 def test_create_rejects_without_touching_gpu(lib):
