@@ -152,6 +152,8 @@ def oracle_sample(wl: synth.Workload, weights_gpu, steps: int, warmup: int, budg
     from oracle.cycle import OracleSeq, build_model, plain_decode
     L = wl.model.n_layers
     wl1 = wl.replace(model=dataclasses.replace(wl.model, n_layers=1), new_tokens=64)
+    if wl.drafter.kind == 3:   # the fused features come from the one remaining layer
+        wl1 = wl1.replace(drafter=dataclasses.replace(wl.drafter, fuse_layers=(0, 0, 0)))
     keep = ["embed", "lm_head", "final_norm"] + [k for k in weights_gpu if k.startswith("layers.0.") or
                                                  k.startswith("draft.")]
     W = {k: weights_gpu[k].to("cpu", torch.float64).numpy() for k in keep}
@@ -190,7 +192,8 @@ def oracle_sample(wl: synth.Workload, weights_gpu, steps: int, warmup: int, budg
             "cycles": done, "s_per_cycle": t_total / done, "tau": committed / done,
             "sample": (f"{done} oracle cycle(s) of {wl.name} shapes (prompt {len(prompt)}, k{wl.tree.topk} "
                        f"D{wl.tree.depth} m{wl.tree.m}, planted p={wl.tree.planted_p}) with the target "
-                       f"truncated to 1 of {L} layers; each cycle's target-forward time scaled x{L}; "
+                       f"truncated to 1 of {L} layers{' (EAGLE-3 features all from it)' if wl.drafter.kind == 3 else ''}; "
+                       f"each cycle's target-forward time scaled x{L}; "
                        f"numpy fp64 on {cores} host cores")}
 
 
@@ -301,6 +304,14 @@ def run_ours(args, ws, rank, local):
             eng.cycle()
         n_launch, gemm_ms, gemm_bytes = eng.profile_end()
         eng.sync()
+        # verify-pass time in cycles that carry only the two events around it (per-launch
+        # events would break the programmatic dependent launches between kernels)
+        eng.profile_begin(0)
+        for _ in range(max(3, args.prof_steps)):
+            eng.cycle()
+        eng.profile_end()
+        n_verify, verify_ms = eng.profile_verify()
+        eng.sync()
     clk = clocks.stop()
     # end to end through the public API with host buffers: prompt + reference H2D from pinned
     # memory, prefill, then K cycles each followed by a D2H read of the committed tokens
@@ -367,6 +378,15 @@ def run_ours(args, ws, rank, local):
                                    f"{args.prof_steps} cycles (eager launches on the engine stream)",
                          "bytes_per_launch_avg": gemm_bytes / max(n_launch, 1),
                          "us_per_launch_avg": gemm_ms * 1e3 / max(n_launch, 1)},
+            "verify_pass": {
+                "what": "the target's tree-attention verify pass (all layers over the m+1 tree rows, then the "
+                        "fused LM-head epilogue), CUDA events around it inside the profiled eager cycles",
+                "passes": n_verify,
+                "us": verify_ms * 1e3 / max(n_verify, 1),
+                "algorithmic_bytes": byt["verify"],
+                "gbs": byt["verify"] / (verify_ms / max(n_verify, 1) / 1e3) / 1e9 if verify_ms > 0 else None,
+                "frac_of_hbm_peak": (byt["verify"] / (verify_ms / max(n_verify, 1) / 1e3) / 1e9 / hbm_peak)
+                if verify_ms > 0 else None},
             "clocks": clk,
             "e2e": {"value": e2e_tok_all / e2e_s, "unit": UNIT,
                     "h2d_bytes_per_step": (prompt.numel() * 4 + R.numel() * 4) / K,

@@ -115,6 +115,12 @@ class Engine:
         self._check(self.lib.eagle_profile_end(self.h, C.byref(n), C.byref(ms), C.byref(by)), "eagle_profile_end")
         return n.value, ms.value, by.value
 
+    def profile_verify(self):
+        """(verify passes timed, their total device ms) of the last profiled cycles."""
+        n, ms = C.c_int(), C.c_double()
+        self._check(self.lib.eagle_profile_verify(self.h, C.byref(n), C.byref(ms)), "eagle_profile_verify")
+        return n.value, ms.value
+
     def kv_view(self):
         k, v, cap = C.c_void_p(), C.c_void_p(), C.c_int()
         self._check(self.lib.eagle_kv_view(self.h, C.byref(k), C.byref(v), C.byref(cap)), "eagle_kv_view")

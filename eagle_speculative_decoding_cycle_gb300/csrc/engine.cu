@@ -142,6 +142,9 @@ struct eagle_ctx {
   std::vector<cudaEvent_t> prof_ev;
   std::vector<double> prof_bytes;
   int prof_on = 0, prof_n = 0;
+  std::vector<cudaEvent_t> ver_ev;      // profiled cycles: events around each verify pass
+  int ver_n = 0, ver_done = 0;          // passes recorded / timed by eagle_profile_end
+  double ver_ms = 0.0;
   // buffers
   int* dev_err;
   int *ctx_len, *n_old, *root_tok, *committed, *on_track, *root_plant, *acc_len, *bonus, *acc_path, *root_row, *iota;
@@ -670,7 +673,9 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
     CK(tree_add(ctx->st, c, d, head_out(ctx, z.k, 1)));
   }
   CK(tree_finalize(ctx->st, c));
-  // verify
+  // verify (target forward over the tree rows, then the LM head epilogue)
+  const bool vprof = ctx->prof_on && 2 * (ctx->ver_n + 1) <= (int)ctx->ver_ev.size();
+  if (vprof) cudaEventRecord(ctx->ver_ev[2 * ctx->ver_n], ctx->st);
   const int RT = B * z.T1;
   int r = target_forward(ctx, RT, ctx->tree_tok, ctx->tree_pos, ctx->tree_slot, ctx->tree_seq, z.T1, 1, z.T1,
                          ctx->tmask, z.tmw, ctx->feat_t, ctx->caps, (size_t)z.Rt, 0);
@@ -693,6 +698,7 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   p.spec_logit = ctx->v_spec;
   r = lm_head(ctx, ctx->feat_t, RT, p, ctx->v_logits, (ctx->debug & EAGLE_DEBUG_LOGITS) != 0);
   if (r) return r;
+  if (vprof) cudaEventRecord(ctx->ver_ev[2 * ctx->ver_n++ + 1], ctx->st);
   HeadOut hv;
   hv.top_id = ctx->v_id; hv.top_val = ctx->v_val; hv.lse = ctx->v_lse; hv.spec_logit = ctx->v_spec;
   hv.K = p.K; hv.S = sampling ? z.k : 1;
@@ -1086,7 +1092,7 @@ int eagle_set_graph(eagle_ctx* ctx, int enable) {
 }
 
 int eagle_profile_begin(eagle_ctx* ctx, int max_launches) {
-  if (!ctx || max_launches < 1) return EAGLE_EINVAL;
+  if (!ctx || max_launches < 0) return EAGLE_EINVAL;
   if (ctx->graph_enabled) return fail(ctx, EAGLE_EINVAL, "GEMM profiling runs with graph replay off");
   for (auto e : ctx->prof_ev) cudaEventDestroy(e);
   ctx->prof_ev.assign(2 * (size_t)max_launches, nullptr);
@@ -1094,6 +1100,13 @@ int eagle_profile_begin(eagle_ctx* ctx, int max_launches) {
     if (cudaEventCreate(&e) != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "event creation failed");
   ctx->prof_bytes.assign(max_launches, 0.0);
   ctx->prof_n = 0;
+  for (auto e : ctx->ver_ev) cudaEventDestroy(e);
+  ctx->ver_ev.assign(2 * 64, nullptr);
+  for (auto& e : ctx->ver_ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "event creation failed");
+  ctx->ver_n = 0;
+  ctx->ver_done = 0;
+  ctx->ver_ms = 0.0;
   ctx->prof_on = 1;
   return EAGLE_OK;
 }
@@ -1115,6 +1128,24 @@ int eagle_profile_end(eagle_ctx* ctx, int* launches, double* total_ms, double* t
   if (total_bytes) *total_bytes = bytes;
   for (auto e : ctx->prof_ev) cudaEventDestroy(e);
   ctx->prof_ev.clear();
+  double vms = 0;
+  for (int i = 0; i < ctx->ver_n; ++i) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, ctx->ver_ev[2 * i], ctx->ver_ev[2 * i + 1]) != cudaSuccess)
+      return fail(ctx, EAGLE_ECUDA, "event timing failed");
+    vms += t;
+  }
+  ctx->ver_done = ctx->ver_n;
+  ctx->ver_ms = vms;
+  for (auto e : ctx->ver_ev) cudaEventDestroy(e);
+  ctx->ver_ev.clear();
+  return EAGLE_OK;
+}
+
+int eagle_profile_verify(const eagle_ctx* ctx, int* passes, double* total_ms) {
+  if (!ctx) return EAGLE_EINVAL;
+  if (passes) *passes = ctx->ver_done;
+  if (total_ms) *total_ms = ctx->ver_ms;
   return EAGLE_OK;
 }
 

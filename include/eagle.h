@@ -197,11 +197,18 @@ int eagle_kv_table(const eagle_ctx* ctx, const int32_t** table, int* tab_w, int*
 
 /* Per-launch timing of the tensor-core GEMMs inside real cycles (graph replay off):
  * eagle_profile_begin arms CUDA events (host-created, no device allocation) around the
- * next max_launches GEMM launches; eagle_profile_end synchronises and returns the number
- * of launches timed, their summed device time (ms) and their algorithmic bytes (weight
- * + activation input + output). */
+ * next max_launches GEMM launches (0: none, only the verify passes below are timed);
+ * eagle_profile_end synchronises and returns the number of launches timed, their summed
+ * device time (ms) and their algorithmic bytes (weight + activation input + output).
+ * Events between launches stop the next kernel from starting before the previous one
+ * ends, so time the verify pass in a window with max_launches = 0. */
 int eagle_profile_begin(eagle_ctx* ctx, int max_launches);
 int eagle_profile_end(eagle_ctx* ctx, int* launches, double* total_ms, double* total_bytes);
+
+/* The verify passes (target forward over the tree rows + LM-head epilogue) of the cycles
+ * run between eagle_profile_begin and eagle_profile_end (at most 64 are timed): how many
+ * and their summed device time (CUDA events on the context's stream). */
+int eagle_profile_verify(const eagle_ctx* ctx, int* passes, double* total_ms);
 
 const char* eagle_last_error(const eagle_ctx* ctx);
 void eagle_destroy(eagle_ctx* ctx);
