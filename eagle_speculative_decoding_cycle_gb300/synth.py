@@ -63,6 +63,10 @@ class TreeShape:
     temperature: float = 0.0       # 0 = greedy
     planted_p: float = 0.0         # probability of planting the reference token per depth
     planted_conf: float = 0.9      # confidence given to a planted token
+    # static (EAGLE-1) tree: node i = (parent node or -1 for the root, rank among its
+    # parent's drafted children); empty = the EAGLE-2 dynamic tree. m must equal its size.
+    static_parent: Tuple[int, ...] = ()
+    static_rank: Tuple[int, ...] = ()
 
     @property
     def n_gen(self) -> int:

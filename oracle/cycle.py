@@ -43,7 +43,7 @@ import numpy as np
 from . import philox
 from .accept import argmax_lowest, compact, enumerate_walk, greedy_walk, sample_walk
 from .model import KV, Model, logsumexp
-from .tree import FlatTree, NodeTable, flatten, rerank, select_expand, topk_ids
+from .tree import FlatTree, NodeTable, flatten, rerank, select_expand, static_plan, topk_ids
 
 F32 = np.float32
 
@@ -156,8 +156,13 @@ class OracleSeq:
             table.add(tok, -1, lc)
         feat_of: Dict[int, np.ndarray] = {}
         slot_of: Dict[int, int] = {}
+        static = len(t.static_parent) > 0
+        if static:
+            gen, rows = static_plan(t.static_parent, t.static_rank, k, D)
+            if len(gen) != t.m:
+                raise ValueError("a static tree must have m nodes")
         for d in range(1, D):
-            E = select_expand(table, d, k)
+            E = rows[d] if static else select_expand(table, d, k)
             R = len(E)
             feats = np.stack([self.root_feat if table.parent[v] < 0 else feat_of[table.parent[v]] for v in E])
             toks = np.array([table.token[v] for v in E])
@@ -178,7 +183,7 @@ class OracleSeq:
                 ids, lcs = self._candidates(out[r], self._planted_token(path_tokens), self.cycle_idx, d + 1)
                 for tok, lc in zip(ids, lcs):
                     table.add(tok, v, lc)
-        kept = rerank(table, t.m)
+        kept = sorted(gen) if static else rerank(table, t.m)
         flat = flatten(table, kept, self.committed[-1])
         rows = len(flat.token)
         pos = n + flat.depth

@@ -24,6 +24,16 @@ drafter's top-k tokens by (logit desc, token id asc); expansion picks nodes by
 generation index asc); generation indices run depth-major, children of the
 r-th expanded node (in selection order) in their top-k rank order.
 
+Static tree (EAGLE-1): the tree has the same shape every cycle, decided in
+advance ("EAGLE: Feature-Level Drafting", section "EAGLE-2 and dynamic draft
+trees"; "EAGLE-2" page, section "Why This Exists"). Reading, as the pages give no
+shape: a topology of nodes (parent, rank), rank r naming the drafter's r-th best
+child of the parent (depth-1 nodes: the root's r-th candidate). The same machinery
+draws it: at each depth the k expansion rows are the topology's nodes that have
+children, in topology order, then (to keep k rows per depth) the lowest-index
+other nodes of that depth; the kept set is the topology's nodes, with no rerank.
+A chain is the topology with one rank-0 child per depth.
+
 Test infrastructure: only tests, the smoke check and the bench's CPU baseline
 use this package.
 """
@@ -150,6 +160,73 @@ def grow_generic(children_of, depth: int, expand: int, budget: int) -> Tuple[Nod
             for tok, c in children_of(path):
                 t.add(tok, p, np.log(F32(c), dtype=F32))
     return t, rerank(t, budget)
+
+
+def static_plan(parent: Sequence[int], rank: Sequence[int], k: int, depth: int):
+    """Generation indices of a static topology's nodes and the k expansion rows per depth.
+
+    parent[i] (-1 = child of the root, else an earlier node) and rank[i] (< k) describe
+    node i. Returns (gen, rows): gen[i] = generation index of node i; rows[d] = the k
+    generation indices expanded at depth d = 1 .. depth - 1. Generation indices follow
+    the drafter's order: depth-1 nodes are 0..k-1 by rank; the children of the r-th row
+    expanded at depth d start at k + (d - 1) k^2 + r k, in rank order."""
+    n = len(parent)
+    dep = [0] * n
+    for i in range(n):
+        if parent[i] >= i:
+            raise ValueError("parents must precede their children")
+        if not 0 <= rank[i] < k:
+            raise ValueError("rank out of range")
+        dep[i] = 1 if parent[i] < 0 else dep[parent[i]] + 1
+        if dep[i] > depth:
+            raise ValueError("node deeper than the draft depth")
+    gen = [-1] * n
+    for i in range(n):
+        if dep[i] == 1:
+            gen[i] = rank[i]
+    rows = {}
+    for d in range(1, depth):
+        expanded = [i for i in range(n) if dep[i] == d and any(parent[j] == i for j in range(n))]
+        if len(expanded) > k:
+            raise ValueError("more than k nodes with children at one depth")
+        row_gen = [gen[i] for i in expanded]
+        lo = 0 if d == 1 else k + (d - 2) * k * k
+        cnt = k if d == 1 else k * k
+        for g in range(lo, lo + cnt):
+            if len(row_gen) == k:
+                break
+            if g not in row_gen:
+                row_gen.append(g)
+        rows[d] = row_gen
+        base = k + (d - 1) * k * k
+        for r, i in enumerate(expanded):
+            for j in range(n):
+                if parent[j] == i:
+                    gen[j] = base + r * k + rank[j]
+    if len(set(gen)) != n:
+        raise ValueError("two nodes share a parent and a rank")
+    return gen, rows
+
+
+def grow_static(children_of, parent: Sequence[int], rank: Sequence[int], k: int,
+                depth: int) -> Tuple[NodeTable, List[int]]:
+    """The static policy with a callable drafter (children_of as in grow_generic, returning
+    at least k children): expand the planned rows, keep the topology's nodes."""
+    gen, rows = static_plan(parent, rank, k, depth)
+    t = NodeTable()
+    for tok, c in children_of(())[:k]:
+        t.add(tok, -1, np.log(F32(c), dtype=F32))
+    for d in range(1, depth):
+        for p in rows[d]:
+            path = tuple(t.token[j] for j in t.path(p))
+            for tok, c in children_of(path)[:k]:
+                t.add(tok, p, np.log(F32(c), dtype=F32))
+    return t, sorted(gen)
+
+
+def chain_topology(depth: int):
+    """A chain: one rank-0 child per depth."""
+    return [i - 1 for i in range(depth)], [0] * depth
 
 
 def is_ancestor_closed(t: NodeTable, kept: Sequence[int]) -> bool:

@@ -40,6 +40,27 @@ def test_greedy_speculative_equals_plain(wl, planted):
         assert max(o.accept_lengths) >= 2          # deep paths were exercised
 
 
+# static trees for the tiny model (k = 4, D = 4): a chain, and an m = 16 two-branch shape
+_TINY_CHAIN = synth.TINY.replace(tree=dataclasses.replace(synth.TINY.tree, m=4, static_parent=(-1, 0, 1, 2),
+                                                         static_rank=(0, 0, 0, 0)))
+_TINY_STATIC = synth.TINY.replace(tree=dataclasses.replace(
+    synth.TINY.tree, m=16,
+    static_parent=(-1, -1, -1, 0, 0, 0, 1, 1, 2, 3, 3, 4, 6, 9, 9, 10),
+    static_rank=(0, 1, 2, 0, 1, 2, 0, 1, 0, 0, 1, 0, 0, 0, 1, 0)))
+
+
+@pytest.mark.parametrize("wl", [_TINY_CHAIN, _TINY_STATIC])
+def test_greedy_speculative_equals_plain_static_tree(wl):
+    """The static (EAGLE-1) tree keeps the output lossless and verifies exactly its shape."""
+    M, prompt = _setup(wl)
+    N = wl.new_tokens
+    R = plain_decode(M, wl, prompt, N + wl.tree.depth + 2)
+    o = OracleSeq(M, wl)
+    o.prefill(prompt, R)
+    assert o.generate(N) == R[:N]
+    assert max(o.accept_lengths) >= 2
+
+
 def _f64(wl):
     return wl.replace(model=dataclasses.replace(wl.model, dtype="f64"))
 

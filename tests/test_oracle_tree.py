@@ -6,8 +6,8 @@ import numpy as np
 import pytest
 
 from conftest import golden_lines
-from oracle.tree import (NodeTable, flatten, grow_generic, is_ancestor_closed, rerank,
-                         select_expand, topk_ids)
+from oracle.tree import (NodeTable, chain_topology, flatten, grow_generic, grow_static, is_ancestor_closed,
+                         rerank, select_expand, static_plan, topk_ids)
 
 
 def _worked():
@@ -193,3 +193,87 @@ def test_topk_ids_ties_and_exclusion():
     v = np.array([1.0, 3.0, 3.0, 2.0, 3.0])
     assert list(topk_ids(v, 3)) == [1, 2, 4]
     assert list(topk_ids(v, 3, exclude=[2])) == [1, 4, 3]
+
+
+# ---- static (EAGLE-1) trees ------------------------------------------------------------------
+def _hash_drafter(vocab=50, k=4, seed=7):
+    """Deterministic toy drafter: the children of a path are the k tokens with the largest
+    pseudo-random score for (path, token), with those scores as confidences."""
+    def children_of(path):
+        rng = np.random.default_rng(abs(hash((seed,) + tuple(path))) % (2 ** 32))
+        sc = rng.random(vocab)
+        ids = sorted(range(vocab), key=lambda t: (-sc[t], t))[:k]
+        tot = sum(sc[t] for t in ids) + 1.0
+        return [(t, sc[t] / tot) for t in ids]
+    return children_of
+
+
+def test_static_chain_follows_the_top1_path():
+    """A chain topology keeps exactly the drafter's greedy (rank-0) path."""
+    children_of = _hash_drafter()
+    for D in (1, 3, 5):
+        parent, rank = chain_topology(D)
+        t, kept = grow_static(children_of, parent, rank, k=4, depth=D)
+        path, want = (), []
+        for _ in range(D):
+            tok = children_of(path)[0][0]
+            want.append(tok)
+            path = path + (tok,)
+        got = [t.token[i] for i in kept]          # generation order = depth order for a chain
+        assert got == want
+        assert [t.depth[i] for i in kept] == list(range(1, D + 1))
+
+
+def test_static_full_two_level_tree_equals_dynamic_keep_all():
+    """Depth 2 with every depth-1 node expanded: the static policy keeps the same nodes as
+    the dynamic one with the budget equal to all generated nodes."""
+    k = 3
+    children_of = _hash_drafter(k=k)
+    parent = [-1] * k
+    rank = list(range(k))
+    for p in range(k):
+        for r in range(k):
+            parent.append(p)
+            rank.append(r)
+    ts, kept_s = grow_static(children_of, parent, rank, k=k, depth=2)
+    td, kept_d = grow_generic(children_of, depth=2, expand=k, budget=k + k * k)
+    assert ts.token == td.token and ts.parent == td.parent
+    assert sorted(kept_s) == sorted(kept_d)
+
+
+def test_static_kept_nodes_realise_the_topology():
+    """Every kept node is its parent's rank-th child (children of a node in rank order), its
+    depth is the topology's, and the kept set is ancestor-closed."""
+    k, D = 3, 4
+    children_of = _hash_drafter(k=k, seed=11)
+    parent = [-1, -1, -1, 0, 0, 1, 3, 3, 5, 6]
+    rank = [0, 1, 2, 0, 2, 1, 0, 1, 2, 0]
+    gen, rows = static_plan(parent, rank, k, D)
+    t, kept = grow_static(children_of, parent, rank, k=k, depth=D)
+    assert kept == sorted(gen) and len(set(kept)) == len(parent)
+    assert is_ancestor_closed(t, kept)
+    for i, g in enumerate(gen):
+        p = -1 if parent[i] < 0 else gen[parent[i]]
+        assert t.parent[g] == p
+        sib = [j for j in range(len(t)) if t.parent[j] == p]
+        assert sib.index(g) == rank[i]
+        a, dd = i, 0
+        while a >= 0:
+            a, dd = parent[a], dd + 1
+        assert t.depth[g] == dd
+    for d, r in rows.items():
+        assert len(r) == k and len(set(r)) == k
+        assert all(t.depth[g] == d for g in r)
+
+
+def test_static_plan_rejects_bad_topologies():
+    with pytest.raises(ValueError):
+        static_plan([-1, 0], [0, 3], 3, 3)           # rank >= k
+    with pytest.raises(ValueError):
+        static_plan([-1, 0, 1, 2], [0, 0, 0, 0], 3, 3)  # deeper than D
+    with pytest.raises(ValueError):
+        static_plan([1, -1], [0, 0], 3, 3)            # parent after child
+    with pytest.raises(ValueError):
+        static_plan([-1, -1], [0, 0], 3, 3)           # same parent and rank twice
+    with pytest.raises(ValueError, match="more than k"):   # three expanded depth-2 nodes, k = 2
+        static_plan([-1, -1, 0, 0, 1, 2, 3, 4], [0, 1, 0, 1, 0, 0, 0, 0], 2, 3)
