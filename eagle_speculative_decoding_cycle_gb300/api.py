@@ -71,6 +71,8 @@ class Engine:
         L.check(rc, "eagle_create")
         self.h = h
         self.batch = self.lim.max_batch
+        if w.tree.static_parent:
+            self.set_static_tree(w.tree.static_parent, w.tree.static_rank)
         self._ref = None
         self._tokens = None
 
@@ -120,6 +122,14 @@ class Engine:
         n, ms = C.c_int(), C.c_double()
         self._check(self.lib.eagle_profile_verify(self.h, C.byref(n), C.byref(ms)), "eagle_profile_verify")
         return n.value, ms.value
+
+    def set_static_tree(self, parent: Sequence[int], rank: Sequence[int]) -> None:
+        """Static (EAGLE-1) tree of len(parent) == m nodes; an empty topology restores the
+        dynamic tree."""
+        n = len(parent)
+        pa = (C.c_int32 * max(n, 1))(*parent)
+        ra = (C.c_int32 * max(n, 1))(*rank)
+        self._check(self.lib.eagle_set_static_tree(self.h, n, pa, ra), "eagle_set_static_tree")
 
     def kv_view(self):
         k, v, cap = C.c_void_p(), C.c_void_p(), C.c_int()

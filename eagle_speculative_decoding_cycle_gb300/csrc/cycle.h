@@ -13,6 +13,11 @@ struct CycleDev {
   int B, k, D, m, T1, NG, V;
   int dmask_words, tmask_words;
   int fsrc_rows;            // 1 + (D - 1) * k feature rows per sequence (row 0 = root feature)
+  // tree policy: 0 = EAGLE-2 dynamic (expand by path value, rerank the top m); 1 = static
+  // (EAGLE-1): the expansion rows and the kept nodes are fixed in advance
+  int policy;
+  const int* static_exp;    // [D - 1][k] generation index expanded by row r at depth d
+  const int* static_keep;   // [NG] 1 = node kept (exactly m of them)
   // per-sequence state
   int* ctx_len;             // [B] target (and drafter) KV length n
   int* n_old;               // [B] n at the start of the running cycle

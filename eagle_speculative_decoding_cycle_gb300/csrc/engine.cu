@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <string>
+#include <algorithm>
 #include <vector>
 
 #include "../../include/eagle.h"
@@ -166,6 +167,9 @@ struct eagle_ctx {
   int fuse_epi = 0;                     // bf16: RoPE/KV write and SwiGLU in the GEMM epilogues (EAGLE_FUSE_EPI=1: on)
   float *rope_cos, *rope_sin;
   void *kc, *vc, *dkc, *dvc;
+  int *static_exp, *static_keep;        // static tree: [D-1][k] expansion rows, [NG] kept flags
+  int static_on = 0;
+  std::vector<int> h_static_exp, h_static_keep;
   int* kv_table;      // paged target KV: [B][tab_w] physical block per logical block, -1 = none
   int* kv_next;       // next free block of the pool (one device counter)
   KvPage page;        // the target cache's addressing (table == nullptr: contiguous)
@@ -229,6 +233,8 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
     x->attn_pml = c.take<float>((size_t)16 * rs * z.nq * 2);
   }
   x->chain_bar = c.take<unsigned>(4);
+  x->static_exp = c.take<int>(std::max(1, (z.D - 1) * z.k));
+  x->static_keep = c.take<int>(z.NG);
   x->kv_table = c.take<int>(std::max(1, z.nblk));
   x->kv_next = c.take<int>(4);
   x->rope_cos = c.take<float>((size_t)z.rope_pos * (z.d / 2));
@@ -593,6 +599,9 @@ void fill_cd(eagle_ctx* ctx) {
   c.tree_parent = ctx->tree_parent; c.tree_node = ctx->tree_node; c.tree_kids = ctx->tree_kids; c.tmask = ctx->tmask;
   c.acc_len = ctx->acc_len; c.acc_path = ctx->acc_path; c.bonus = ctx->bonus; c.margin = ctx->margin;
   c.err = ctx->dev_err;
+  c.policy = ctx->static_on;
+  c.static_exp = ctx->static_exp;
+  c.static_keep = ctx->static_keep;
 }
 
 __global__ void iota_k(int* p, int n) {
@@ -1225,6 +1234,69 @@ int eagle_kv_view(const eagle_ctx* ctx, void** k, void** v, int* cap) {
   if (k) *k = ctx->kc;
   if (v) *v = ctx->vc;
   if (cap) *cap = ctx->z.cap;
+  return EAGLE_OK;
+}
+
+// Static (EAGLE-1) tree: node i = (parent[i], rank[i]), parent -1 = the root, rank r = the
+// drafter's r-th best child. Generation indices follow the drafter's order (depth-1 nodes
+// 0..k-1 by rank; the children of the r-th row expanded at depth d start at
+// k + (d-1) k^2 + r k); the k rows expanded at depth d are the topology's nodes with
+// children in topology order, then the lowest-index other nodes of that depth.
+int eagle_set_static_tree(eagle_ctx* ctx, int n, const int32_t* parent, const int32_t* rank) {
+  if (!ctx) return EAGLE_EINVAL;
+  const Dims& z = ctx->z;
+  if (n == 0) {
+    ctx->static_on = 0;
+  } else {
+    if (n != z.m || !parent || !rank) return fail(ctx, EAGLE_EINVAL, "a static tree needs m nodes (parent, rank)");
+    std::vector<int> dep(n), gen(n, -1), cnt_exp(z.D + 1, 0);
+    for (int i = 0; i < n; ++i) {
+      if (parent[i] >= i || parent[i] < -1) return fail(ctx, EAGLE_EINVAL, "parents must precede their children");
+      if (rank[i] < 0 || rank[i] >= z.k) return fail(ctx, EAGLE_EINVAL, "rank out of range");
+      dep[i] = parent[i] < 0 ? 1 : dep[parent[i]] + 1;
+      if (dep[i] > z.D) return fail(ctx, EAGLE_EINVAL, "node deeper than the draft depth");
+      if (dep[i] == 1) gen[i] = rank[i];
+    }
+    std::vector<int> exp((size_t)std::max(1, (z.D - 1) * z.k), 0);
+    for (int d = 1; d < z.D; ++d) {
+      std::vector<int> rows, expanded;
+      for (int i = 0; i < n; ++i) {
+        if (dep[i] != d) continue;
+        bool has_child = false;
+        for (int j = i + 1; j < n && !has_child; ++j) has_child = parent[j] == i;
+        if (has_child) expanded.push_back(i);
+      }
+      if ((int)expanded.size() > z.k) return fail(ctx, EAGLE_EINVAL, "more than k nodes with children at one depth");
+      for (int i : expanded) rows.push_back(gen[i]);
+      const int lo = d == 1 ? 0 : z.k + (d - 2) * z.k * z.k;
+      const int cnt = d == 1 ? z.k : z.k * z.k;
+      for (int g = lo; g < lo + cnt && (int)rows.size() < z.k; ++g)
+        if (std::find(rows.begin(), rows.end(), g) == rows.end()) rows.push_back(g);
+      for (int r = 0; r < z.k; ++r) exp[(size_t)(d - 1) * z.k + r] = rows[r];
+      const int base = z.k + (d - 1) * z.k * z.k;
+      for (size_t r = 0; r < expanded.size(); ++r)
+        for (int j = 0; j < n; ++j)
+          if (parent[j] == expanded[r]) gen[j] = base + (int)r * z.k + rank[j];
+    }
+    std::vector<int> keep(z.NG, 0);
+    for (int i = 0; i < n; ++i) {
+      if (gen[i] < 0 || gen[i] >= z.NG || keep[gen[i]]) return fail(ctx, EAGLE_EINVAL, "two nodes share a parent and a rank");
+      keep[gen[i]] = 1;
+    }
+    ctx->h_static_exp = exp;
+    ctx->h_static_keep = keep;
+    if (cudaMemcpyAsync(ctx->static_exp, ctx->h_static_exp.data(), exp.size() * sizeof(int), cudaMemcpyHostToDevice,
+                        ctx->st) != cudaSuccess ||
+        cudaMemcpyAsync(ctx->static_keep, ctx->h_static_keep.data(), keep.size() * sizeof(int),
+                        cudaMemcpyHostToDevice, ctx->st) != cudaSuccess ||
+        cudaStreamSynchronize(ctx->st) != cudaSuccess)
+      return fail(ctx, EAGLE_ECUDA, "static tree upload failed");
+    ctx->static_on = 1;
+  }
+  ctx->cd.policy = ctx->static_on;
+  ctx->cd.static_exp = ctx->static_exp;
+  ctx->cd.static_keep = ctx->static_keep;
+  if (ctx->graph) { cudaGraphExecDestroy(ctx->graph); ctx->graph = nullptr; }   // the policy is a kernel argument
   return EAGLE_OK;
 }
 

@@ -83,6 +83,14 @@ __global__ void tree_select_k(CycleDev c, int d) {
   const int k = c.k;
   const int lo = (d == 1) ? 0 : k + (d - 2) * k * k;
   const int cnt = (d == 1) ? k : k * k;
+  if (c.policy == 1) {
+    // static tree: the rows expanded at this depth are fixed
+    if (lane < k) {
+      const int g = c.static_exp[(d - 1) * k + lane];
+      c.exp_node[(b * c.D + (d - 1)) * k + lane] = g;
+      c.node_rank[base + g] = lane;
+    }
+  } else {
   // the candidates' path values, loaded once (k <= 16: at most 256 candidates)
   float cv[TS_QMAX];
 #pragma unroll
@@ -103,6 +111,7 @@ __global__ void tree_select_k(CycleDev c, int d) {
       c.exp_node[(b * c.D + (d - 1)) * k + r] = bi;
       c.node_rank[base + bi] = r;
     }
+  }
   }
   __syncwarp();
   __threadfence_block();
@@ -191,6 +200,10 @@ __global__ void __launch_bounds__(TF_THREADS) tree_finalize_k(CycleDev c) {
     key[i] = ((uint64_t)(~f32_order_key(c.node_logv[base + i])) << 32) | (uint32_t)i;
   __syncthreads();
   for (int i = threadIdx.x; i < NG; i += blockDim.x) {
+    if (c.policy == 1) {   // static tree: the kept nodes are fixed
+      row_of[i] = c.static_keep[i] ? 1 : 0;
+      continue;
+    }
     const uint64_t ki = key[i];
     int rank = 0;
     for (int j = 0; j < NG; ++j) rank += key[j] < ki;

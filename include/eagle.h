@@ -185,6 +185,15 @@ int eagle_debug_dump(eagle_ctx* ctx, int what, void* dst, size_t bytes);
 enum { EAGLE_DEBUG_LOGITS = 1 };
 int eagle_set_debug(eagle_ctx* ctx, int flags);
 
+/* Static (EAGLE-1) tree policy: the same tree shape every cycle, fixed in advance, instead
+ * of the EAGLE-2 dynamic tree. Host arrays of n = m nodes: parent[i] (-1 = a child of the
+ * root, else an earlier node) and rank[i] in [0, k) (the drafter's rank[i]-th best child of
+ * that parent). At most k nodes of one depth may have children; depth <= the draft depth.
+ * The drafter still expands k rows per depth (the topology's nodes with children, then
+ * others of that depth), and the verify pass scores exactly the topology. n = 0 restores
+ * the dynamic tree. Synchronises the context's stream once (upload of two small tables). */
+int eagle_set_static_tree(eagle_ctx* ctx, int n, const int32_t* parent, const int32_t* rank);
+
 /* Device pointers of the target KV cache (storage type); for tests and tools. Contiguous
  * (kv_block = 0): layout [layer][batch][kv_head][slot][head_dim] with `cap` slots per sequence.
  * Paged: each layer is a pool [block][kv_head][slot in block][head_dim]; see eagle_kv_table. */

@@ -17,7 +17,7 @@ from eagle_speculative_decoding_cycle_gb300 import api, synth
 from oracle import philox
 from oracle.accept import greedy_walk, sample_walk
 from oracle.cycle import OracleSeq, build_model, plain_decode
-from oracle.tree import NodeTable, flatten, rerank, select_expand
+from oracle.tree import NodeTable, flatten, rerank, select_expand, static_plan
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -49,18 +49,21 @@ def gpu_table(eng, b=0):
 
 
 def check_tree_policy(eng, wl, b=0):
-    """Oracle policy on the GPU's path values reproduces the GPU's expansion, rerank,
-    flattening and mask."""
+    """Oracle policy on the GPU's path values reproduces the GPU's expansion, rerank (or, for
+    a static tree, the planned rows and kept set), flattening and mask."""
     k, D, m = wl.tree.topk, wl.tree.depth, wl.tree.m
     t = gpu_table(eng, b)
+    static = bool(wl.tree.static_parent)
+    if static:
+        gen, rows = static_plan(wl.tree.static_parent, wl.tree.static_rank, k, D)
     # expansion order: children of the r-th selected depth-d node occupy block r
     for d in range(1, D):
-        sel = select_expand(NodeTable(t.token, t.parent, t.depth, t.logv), d, k)
+        sel = rows[d] if static else select_expand(NodeTable(t.token, t.parent, t.depth, t.logv), d, k)
         base = k + (d - 1) * k * k
         for r, v in enumerate(sel):
             assert all(t.parent[base + r * k + i] == v for i in range(k))
     st = eng.dump(L.DUMP_STATE)
-    ft = flatten(t, rerank(t, m), int(eng.dump(L.DUMP_TREE)[0][b, 0]))
+    ft = flatten(t, sorted(gen) if static else rerank(t, m), int(eng.dump(L.DUMP_TREE)[0][b, 0]))
     tok, pos, par, node, mask = eng.dump(L.DUMP_TREE)
     assert tok[b].tolist() == ft.token.tolist()
     assert par[b].tolist() == ft.parent.tolist()
@@ -137,6 +140,54 @@ def test_tiny_fp32_lockstep_and_lossless():
     assert st["tree_match"] == st["cycles"]     # same trees every cycle
     assert st["max_logit_err"] < 1e-4 and st["max_feat_err"] < 1e-4
     assert max(st["accepted"]) >= 2
+
+
+# static (EAGLE-1) trees on the tiny model (k = 4, D = 4): a chain, and a 16-node shape
+TINY_CHAIN = synth.TINY.replace(tree=synth.TreeShape(topk=4, depth=4, m=4, planted_p=0.8,
+                                                     static_parent=(-1, 0, 1, 2), static_rank=(0, 0, 0, 0)))
+TINY_STATIC = synth.TINY.replace(tree=synth.TreeShape(
+    topk=4, depth=4, m=16, planted_p=0.8,
+    static_parent=(-1, -1, -1, 0, 0, 0, 1, 1, 2, 3, 3, 4, 6, 9, 9, 10),
+    static_rank=(0, 1, 2, 0, 1, 2, 0, 1, 0, 0, 1, 0, 0, 0, 1, 0)))
+
+
+@pytest.mark.parametrize("wl", [TINY_CHAIN, TINY_STATIC], ids=["chain", "static16"])
+def test_tiny_fp32_static_tree_lockstep_and_lossless(wl):
+    """The static policy: every cycle the GPU expands the planned rows and verifies exactly
+    the topology (checked against the oracle's plan on the GPU's own node table), the
+    floats match the oracle in lock step, and greedy output stays lossless."""
+    got, R, st = run_lockstep(wl)
+    N = wl.new_tokens
+    assert got[:N] == R[:N]
+    assert st["tree_match"] == st["cycles"]
+    assert st["max_logit_err"] < 1e-4 and st["max_feat_err"] < 1e-4
+    assert max(st["accepted"]) >= 2
+
+
+def test_static_tree_can_be_switched_off():
+    """set_static_tree with an empty topology restores the dynamic policy: the run then
+    equals a context created without a static tree."""
+    wl = TINY_STATIC
+    weights, M, prompt, R, eng = setup(wl)
+    dyn = synth.TINY.replace(tree=synth.TreeShape(topk=4, depth=4, m=16, planted_p=0.8))
+    eng2 = api.Engine(dyn, {k: v.to(DEV) for k, v in weights.items()})
+    eng.set_static_tree([], [])
+    ref = torch.tensor([R], dtype=torch.int32, device=DEV)
+    outs = []
+    for e in (eng, eng2):
+        e.prefill([prompt.to(DEV)], ref)
+        out = torch.zeros(1, 5, dtype=torch.int32, device=DEV)
+        cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+        seq = []
+        for _ in range(4):
+            e.cycle(out, cnt)
+            e.sync()
+            seq.append((out.cpu().clone(), cnt.cpu().clone(), [x.clone() for x in e.dump(L.DUMP_TREE)]))
+        outs.append(seq)
+        e.close()
+    for (oa, ca, ta), (ob, cb, tb) in zip(*outs):
+        assert torch.equal(oa, ob) and torch.equal(ca, cb)
+        assert all(torch.equal(x, y) for x, y in zip(ta, tb))
 
 
 def test_tiny_fp32_plain_decode_matches_oracle():
