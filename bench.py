@@ -197,6 +197,34 @@ def oracle_sample(wl: synth.Workload, weights_gpu, steps: int, warmup: int, budg
                        f"numpy fp64 on {cores} host cores")}
 
 
+def static_tree(kind: str, tree: synth.TreeShape) -> synth.TreeShape:
+    """A static (EAGLE-1 style) tree for the workload's k and D, decided before any context
+    is seen. "static-chain": one rank-0 child per depth (m = D). "static-prior": the m nodes
+    with the largest prior acceptance, the prior of a node being the product over its path
+    of a fixed per-rank weight (0.6, 0.15, 0.08, 0.05, 0.03, then 0.02), subject to at most
+    k expanded nodes per depth (nodes are taken best-first, each after its parent)."""
+    k, D, m = tree.topk, tree.depth, tree.m
+    if kind == "static-chain":
+        return dataclasses.replace(tree, m=D, static_parent=tuple(range(-1, D - 1)), static_rank=(0,) * D)
+    w = [0.6, 0.15, 0.08, 0.05, 0.03] + [0.02] * max(0, k - 5)
+    parent, rank, score, depth = [], [], [], []
+    expanded = {d: set() for d in range(1, D + 1)}
+    frontier = [(w[r], -1, r, 1) for r in range(k)]
+    while len(parent) < m and frontier:
+        frontier.sort(key=lambda x: -x[0])
+        sc, p, r, d = frontier.pop(0)
+        if p >= 0 and p not in expanded[d - 1] and len(expanded[d - 1]) >= k:
+            continue
+        if p >= 0:
+            expanded[d - 1].add(p)
+        parent.append(p)
+        rank.append(r)
+        i = len(parent) - 1
+        if d < D:
+            frontier += [(sc * w[c], i, c, d + 1) for c in range(k)]
+    return dataclasses.replace(tree, m=len(parent), static_parent=tuple(parent), static_rank=tuple(rank))
+
+
 # ---------------------------------------------------------------------------------------------
 def run_ours(args, ws, rank, local):
     from eagle_speculative_decoding_cycle_gb300 import _lib as L
@@ -210,6 +238,8 @@ def run_ours(args, ws, rank, local):
     wl = synth.WORKLOADS[args.workload]
     if args.planted_p is not None:
         wl = wl.replace(tree=dataclasses.replace(wl.tree, planted_p=args.planted_p))
+    if args.tree != "dynamic":
+        wl = wl.replace(tree=static_tree(args.tree, wl.tree))
     t = wl.tree
     D = t.depth
     weights = synth.make_weights(wl, device=str(dev))
@@ -355,7 +385,8 @@ def run_ours(args, ws, rank, local):
             "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init N(0,0.02) weights, uniform prompt ids)",
             "config": {"workload": wl.name, "batch": wl.batch, "prompt": len(prompt),
-                       "tree": f"k{t.topk} D{t.depth} m{t.m}", "planted_p": t.planted_p,
+                       "tree": f"k{t.topk} D{t.depth} m{t.m}" + ("" if args.tree == "dynamic" else f" {args.tree}"),
+                       "planted_p": t.planted_p,
                        "temperature": t.temperature, "parallelism": "replicas" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2 (13+ GB of weights streamed per cycle); no flush needed",
                        "graph_replay": True},
@@ -532,6 +563,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=synth.LLAMA2_7B.name, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--planted-p", type=float, default=None)
+    ap.add_argument("--tree", default="dynamic", choices=["dynamic", "static-chain", "static-prior"],
+                    help="tree policy: EAGLE-2 dynamic (default) or a static EAGLE-1 style shape")
     ap.add_argument("--prof-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=2)
