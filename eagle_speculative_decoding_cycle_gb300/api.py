@@ -123,6 +123,16 @@ class Engine:
         self._check(self.lib.eagle_profile_verify(self.h, C.byref(n), C.byref(ms)), "eagle_profile_verify")
         return n.value, ms.value
 
+    def ttt_forward(self, tokens: torch.Tensor, steps: int) -> torch.Tensor:
+        """EAGLE-3 training-time-test forward over one sequence (int32 CUDA tensor): the mean
+        token cross-entropy of each of `steps` self-fed drafter steps (float32 CUDA [steps]).
+        Reuses sequence 0's caches; prefill again before cycling."""
+        x = tokens.to(torch.int32).contiguous()
+        loss = torch.zeros(steps, dtype=torch.float32, device=x.device)
+        self._check(self.lib.eagle_ttt_forward(self.h, x.data_ptr(), int(x.numel()), steps, loss.data_ptr()),
+                    "eagle_ttt_forward")
+        return loss
+
     def set_static_tree(self, parent: Sequence[int], rank: Sequence[int]) -> None:
         """Static (EAGLE-1) tree of len(parent) == m nodes; an empty topology restores the
         dynamic tree."""

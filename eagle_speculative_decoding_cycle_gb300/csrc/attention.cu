@@ -5,6 +5,9 @@
 // section "The Mask Preserves Tree Semantics in One Target Pass", Figure 7). Row
 // visibility of a key slot s:
 //   causal mode: s <= row_slot (prefill, the drafter's context rows, plain decoding);
+//   training-time-test mode (the EAGLE-3 multi-step drafter pass), n = ctx_len: a row at
+//     slot < n is causal; a row at slot n(j-1) + t (step j >= 2 of source t) sees slots
+//     0..t and its own source's earlier steps n(i-1) + t, i = 2..j;
 //   tree mode:   s < ctx_len, or s - ctx_len < T and bit (s - ctx_len) of the row's
 //                ancestry bitmask is set (verify pass, drafter expansion rows).
 // One CTA handles one KV head and a block of rows (all query heads of the GQA group),
@@ -22,6 +25,14 @@ constexpr int AT_WARPS = 4;
 constexpr int QV = QPW * AT_WARPS;
 constexpr int KT = 32;            // keys per tile
 constexpr int DMAX = 128;
+
+// training-time-test visibility of key slot `key` for a row at `slot`, n = sequence length
+__device__ __forceinline__ bool ttt_visible(int slot, int key, int n) {
+  if (slot < n) return key <= slot;
+  const int t = slot % n;
+  return key < n ? key <= t : ((key - n) % n == t && key <= slot);
+}
+
 
 template <typename T>
 __global__ void __launch_bounds__(128) attn_simt_k(AttnArgs a) {
@@ -53,7 +64,7 @@ __global__ void __launch_bounds__(128) attn_simt_k(AttnArgs a) {
   }
   int kend = 0;
   for (int r = r0; r < r1; ++r) {
-    const int e = a.mode == 0 ? a.row_slot[r] + 1 : ctx + a.tree_T;
+    const int e = a.mode == 1 ? ctx + a.tree_T : a.row_slot[r] + 1;
     kend = max(kend, e);
   }
   kend = min(kend, a.cap);
@@ -86,6 +97,8 @@ __global__ void __launch_bounds__(128) attn_simt_k(AttnArgs a) {
       bool vis;
       if (a.mode == 0) {
         vis = s <= a.row_slot[r];
+      } else if (a.mode == 2) {
+        vis = ttt_visible(a.row_slot[r], s, ctx);
       } else {
         const int t = s - ctx;
         vis = s < ctx || (t >= 0 && t < a.tree_T &&
@@ -208,6 +221,7 @@ struct RowVis {
 __device__ __forceinline__ bool visible(const AttnArgs& a, const RowVis& rv, int ctx, int key) {
   if (!rv.valid) return false;
   if (a.mode == 0) return key <= rv.slot;
+  if (a.mode == 2) return ttt_visible(rv.slot, key, ctx);
   if (key < ctx) return true;
   const int t = key - ctx;
   if (t >= a.tree_T) return false;
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.vcache);
 
   int kend = 0;
-  for (int r = r0; r < r1; ++r) kend = max(kend, a.mode == 0 ? a.row_slot[r] + 1 : ctx + a.tree_T);
+  for (int r = r0; r < r1; ++r) kend = max(kend, a.mode == 1 ? ctx + a.tree_T : a.row_slot[r] + 1);
   kend = min(kend, a.cap);
   const int n_tiles = (kend + MT_KEYS - 1) / MT_KEYS;
   const int tps = (n_tiles + splits - 1) / splits;

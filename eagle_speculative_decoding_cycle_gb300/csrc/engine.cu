@@ -170,6 +170,8 @@ struct eagle_ctx {
   int *static_exp, *static_keep;        // static tree: [D-1][k] expansion rows, [NG] kept flags
   int static_on = 0;
   std::vector<int> h_static_exp, h_static_keep;
+  int* ttt_tgt;       // training-time test: the target token of each row
+  float* ttt_acc;     // training-time test: running loss sum
   int* kv_table;      // paged target KV: [B][tab_w] physical block per logical block, -1 = none
   int* kv_next;       // next free block of the pool (one device counter)
   KvPage page;        // the target cache's addressing (table == nullptr: contiguous)
@@ -233,6 +235,8 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
     x->attn_pml = c.take<float>((size_t)16 * rs * z.nq * 2);
   }
   x->chain_bar = c.take<unsigned>(4);
+  x->ttt_tgt = c.take<int>(std::max(z.Rd, z.Rt));
+  x->ttt_acc = c.take<float>(4);
   x->static_exp = c.take<int>(std::max(1, (z.D - 1) * z.k));
   x->static_keep = c.take<int>(z.NG);
   x->kv_table = c.take<int>(std::max(1, z.nblk));
@@ -656,6 +660,48 @@ int kv_reserve(eagle_ctx* ctx, int b0, int nb, const int* lo_dev, int lo_const, 
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// ---- training-time-test forward (EAGLE-3 multi-step drafter pass) ------------------------------
+// Rows of pass s over a sequence of n tokens: s = 0 the target's causal pass (token x_t at
+// position t, slot t); s >= 1 drafter step s, sources t = 0 .. R-1: token x_{t+s} at position
+// t+s-1, slot t (s = 1) or n(s-1)+t, target token x_{t+s+1}. The sequence length goes to
+// ctx_len[0] (the mode-2 attention reads it).
+__global__ void ttt_rows_k(const int* x, int n, int s, int R, int* tok, int* pos, int* slot, int* seq, int* tgt,
+                           int* ctx_len) {
+  PDL_ENTRY();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t == 0) ctx_len[0] = n;
+  if (t >= R) return;
+  if (s == 0) {
+    tok[t] = x[t]; pos[t] = t; slot[t] = t; seq[t] = 0;
+    return;
+  }
+  tok[t] = x[t + s];
+  pos[t] = t + s - 1;
+  slot[t] = s == 1 ? t : n * (s - 1) + t;
+  seq[t] = 0;
+  tgt[t] = x[t + s + 1];
+}
+
+// acc[0] += sum over rows of (lse - logit of the target), in a fixed order; one block.
+__global__ void ttt_loss_acc_k(const float* lse, const float* tgt_logit, int rows, float* acc, int reset) {
+  PDL_ENTRY();
+  __shared__ float red[256];
+  float v = 0.f;
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) v += lse[i] - tgt_logit[i];
+  red[threadIdx.x] = v;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) acc[0] = (reset ? 0.f : acc[0]) + red[0];
+}
+
+__global__ void ttt_loss_fin_k(const float* acc, int rows, float* out) {
+  PDL_ENTRY();
+  if (threadIdx.x == 0 && blockIdx.x == 0) out[0] = acc[0] / (float)rows;
+}
+
 // ---- the cycle -------------------------------------------------------------------------------
 int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   const Dims& z = ctx->z;
@@ -898,6 +944,8 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
     return EAGLE_ECUDA;
   }
   launch_k(iota_k, (std::max(z.B, z.R) + 127) / 128, 128, 0, ctx->st, ctx->iota, std::max(z.B, z.R));
+  if (ctx->page.table)   // no blocks assigned yet (zero would name block 0)
+    launch_k(kv_reset_k, (z.nblk + 255) / 256, 256, 0, ctx->st, ctx->kv_table, z.nblk, ctx->kv_next);
   if (cudaStreamSynchronize(ctx->st) != cudaSuccess) { delete ctx; return EAGLE_ECUDA; }
   ctx->batch = z.B;
   fill_cd(ctx);
@@ -1297,6 +1345,65 @@ int eagle_set_static_tree(eagle_ctx* ctx, int n, const int32_t* parent, const in
   ctx->cd.static_exp = ctx->static_exp;
   ctx->cd.static_keep = ctx->static_keep;
   if (ctx->graph) { cudaGraphExecDestroy(ctx->graph); ctx->graph = nullptr; }   // the policy is a kernel argument
+  return EAGLE_OK;
+}
+
+// EAGLE-3 training-time-test forward over one sequence (device int32 x[n]): the target's
+// causal pass, then `steps` drafter steps (step 1 causal over sources 0..n-3, later steps
+// self-fed with the TTT mask), each scored by its mean token cross-entropy into d_loss[step].
+// Uses sequence 0's caches: run eagle_prefill again before cycling.
+int eagle_ttt_forward(eagle_ctx* ctx, const int32_t* d_tokens, int n, int steps, float* d_loss) {
+  if (!ctx) return EAGLE_EINVAL;
+  const Dims& z = ctx->z;
+  if (!d_tokens || !d_loss || steps < 1 || n < steps + 3) return fail(ctx, EAGLE_EINVAL, "bad training-time-test arguments");
+  if (n > z.P || n - 2 > z.Rd || (size_t)n * steps > (size_t)z.dcap || n > z.cap)
+    return fail(ctx, EAGLE_ECAPACITY, "sequence too long for the training-time test in this context");
+  if (ctx->graph) { cudaGraphExecDestroy(ctx->graph); ctx->graph = nullptr; }
+  ctx->host_ctx_bound = z.max_ctx;   // the cycle state is gone until the next prefill
+  const size_t rb = (size_t)z.H * z.esz;
+  // target pass (causal), features of every position
+  CK(kv_reserve(ctx, 0, 1, nullptr, 0, n));
+  launch_k(ttt_rows_k, (n + 127) / 128, 128, 0, ctx->st, d_tokens, n, 0, n, ctx->row_tok, ctx->row_pos,
+           ctx->row_slot, ctx->row_seq, ctx->ttt_tgt, ctx->ctx_len);
+  int r = target_forward(ctx, n, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, n, 0, 0, nullptr, 0,
+                         ctx->feat_t, ctx->pre_feat, (size_t)z.max_ctx, 0);
+  if (r) return r;
+  for (int s = 1; s <= steps; ++s) {
+    const int R = s == 1 ? n - 2 : n - 1 - s;
+    launch_k(ttt_rows_k, (R + 127) / 128, 128, 0, ctx->st, d_tokens, n, s, R, ctx->row_tok, ctx->row_pos,
+             ctx->row_slot, ctx->row_seq, ctx->ttt_tgt, ctx->ctx_len);
+    if (s == 1) {
+      if (z.kind == 1) {
+        r = drafter_forward(ctx, R, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, R, 2, 0, nullptr, 0,
+                            ctx->feat_t, ctx->iota);
+      } else {
+        r = fuse_rows(ctx, ctx->pre_feat, (size_t)z.max_ctx, nullptr, R);
+        if (r) return r;
+        r = drafter_forward(ctx, R, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, R, 2, 0, nullptr, 0,
+                            ctx->gbuf, nullptr);
+      }
+    } else {
+      // the previous step's output a (rows 0..R-1 of dout) in place of g; the drafter reads
+      // its feature rows before it writes dout
+      r = drafter_forward(ctx, R, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, R, 2, 0, nullptr, 0,
+                          ctx->dout, z.kind == 1 ? ctx->iota : nullptr);
+    }
+    if (r) return r;
+    // token loss through the shared LM head, in chunks of the head's row capacity
+    for (int r0 = 0; r0 < R; r0 += z.Rh) {
+      const int rows = std::min(z.Rh, R - r0);
+      HeadParams p = head_params(ctx, rows, 1);
+      p.specials = ctx->ttt_tgt + r0;
+      p.S = 1;
+      p.lse_excl = 0;
+      r = lm_head(ctx, (const uint8_t*)ctx->dout + (size_t)r0 * rb, rows, p);
+      if (r) return r;
+      launch_k(ttt_loss_acc_k, 1, 256, 0, ctx->st, (const float*)ctx->h_lse, (const float*)ctx->h_spec, rows,
+               ctx->ttt_acc, r0 == 0 ? 1 : 0);
+    }
+    launch_k(ttt_loss_fin_k, 1, 32, 0, ctx->st, (const float*)ctx->ttt_acc, R, d_loss + (s - 1));
+    if (cudaGetLastError() != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "training-time-test launch failed");
+  }
   return EAGLE_OK;
 }
 

@@ -118,7 +118,8 @@ struct AttnArgs {
   const int* row_seq;   // [R]
   const int* row_slot;  // [R]  slot of the row's own key
   const int* ctx_len;   // [B] slots [0, ctx_len) are visible to every row of the sequence
-  int mode;             // 0 = causal (slot <= row_slot), 1 = tree (ctx + mask bits over slots ctx..ctx+T)
+  int mode;             // 0 = causal (slot <= row_slot), 1 = tree (ctx + mask bits over slots ctx..ctx+T),
+                        // 2 = training-time test (n = ctx_len; see attention.cu)
   int tree_T;
   const uint64_t* mask; // [R][mask_words]
   int mask_words;

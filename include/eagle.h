@@ -185,6 +185,16 @@ int eagle_debug_dump(eagle_ctx* ctx, int what, void* dst, size_t bytes);
 enum { EAGLE_DEBUG_LOGITS = 1 };
 int eagle_set_debug(eagle_ctx* ctx, int flags);
 
+/* EAGLE-3 training-time-test forward (forward and loss only, no training), over one
+ * sequence d_tokens (device int32 [n]): the target's causal pass gives every position's
+ * drafter feature; drafter step 1 runs causally over sources t = 0..n-3 ([g_t; emb(x_{t+1})]
+ * at position t); step s >= 2 feeds each source's previous output a back with x_{t+s}, at
+ * position t+s-1, seeing the causal context up to t and its own earlier steps. d_loss
+ * (device float [steps]) receives each step's mean cross-entropy of x_{t+s+1}. Requires
+ * steps + 3 <= n <= prefill_chunk and n * steps within the drafter cache. It reuses sequence
+ * 0's caches, so call eagle_prefill before the next eagle_cycle. */
+int eagle_ttt_forward(eagle_ctx* ctx, const int32_t* d_tokens, int n, int steps, float* d_loss);
+
 /* Static (EAGLE-1) tree policy: the same tree shape every cycle, fixed in advance, instead
  * of the EAGLE-2 dynamic tree. Host arrays of n = m nodes: parent[i] (-1 = a child of the
  * root, else an earlier node) and rank[i] in [0, k) (the drafter's rank[i]-th best child of
