@@ -538,6 +538,93 @@ def run_gemm_probe(args):
                       "frac": byt / us / 1e3 / hbm, "peak_source": src}))
 
 
+def run_plan_budget(args):
+    """Measure the inputs of the batch-aware budget planner on this GPU and plan (k, m) per
+    batch size: for k in (4, 8, 10) the expected committed tokens of the m best nodes (1 +
+    the sum of their path values, averaged over planted cycles) and the drafter's share of a
+    cycle; the verify-pass time at batch 1, 4, 16 and 64 (k10, m60)."""
+    from eagle_speculative_decoding_cycle_gb300 import _lib as L
+    from eagle_speculative_decoding_cycle_gb300 import api
+    from eagle_speculative_decoding_cycle_gb300.build import build
+    build()
+    dev = torch.device("cuda:0")
+    base = synth.WORKLOADS[args.workload]
+    weights = synth.make_weights(base, device=str(dev))
+    stream = torch.cuda.Stream(device=dev)
+    prompt = synth.make_prompts(base)[0].to(dev)
+    D = base.tree.depth
+    n_cyc = 12
+    cands = []
+    for k in (4, 8, 10):
+        t = dataclasses.replace(base.tree, topk=k, m=min(60, k + (D - 1) * k * k))
+        wl = base.replace(tree=t)
+        eng = api.Engine(wl, weights, max_ctx=len(prompt) + 6 * (n_cyc + 8) * (D + 1) + 64, stream=stream)
+        with torch.cuda.stream(stream):
+            eng.prefill([prompt])
+            first = int(eng.dump(L.DUMP_STATE)["root_tok"][0])
+            plain = torch.zeros(1, (n_cyc + 6) * (D + 1), dtype=torch.int32, device=dev)
+            eng.decode_plain(plain.shape[1], plain)
+            eng.sync()
+            ref = torch.cat([torch.tensor([[first]], dtype=torch.int32, device=dev), plain], 1).contiguous()
+            eng.prefill([prompt], ref)
+            curve = np.zeros(t.n_gen)
+            for i in range(n_cyc + 2):
+                eng.cycle()
+                eng.sync()
+                if i >= 2:
+                    logv = eng.dump(L.DUMP_NODES)[3][0].double().numpy()
+                    curve += np.cumsum(np.sort(np.exp(logv))[::-1])
+            curve = 1.0 + curve / n_cyc
+            eng.prefill([prompt], ref)
+            eng.set_graph(True)
+            for _ in range(3):
+                eng.cycle()
+            eng.sync()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n_cyc):
+                eng.cycle()
+            e1.record(stream)
+            eng.sync()
+            cycle_us = e0.elapsed_time(e1) * 1e3 / n_cyc
+            eng.set_graph(False)
+            eng.profile_begin(0)
+            for _ in range(3):
+                eng.cycle()
+            eng.profile_end()
+            nv, vms = eng.profile_verify()
+        eng.close()
+        draft_us = max(0.0, cycle_us - vms * 1e3 / max(nv, 1))
+        cands.append((k, draft_us, [float(x) for x in curve[:min(t.n_gen, 255)]]))
+    rows, vus = [], []
+    for B in (1, 4, 16, 64):
+        wl = base.replace(batch=B)
+        prompts = [prompt] * B
+        eng = api.Engine(wl, weights, max_batch=B, max_ctx=len(prompt) + 12 * (D + 1) + 64, stream=stream)
+        with torch.cuda.stream(stream):
+            eng.prefill(prompts)
+            eng.cycle()
+            eng.sync()
+            eng.profile_begin(0)
+            for _ in range(3):
+                eng.cycle()
+            eng.profile_end()
+            nv, vms = eng.profile_verify()
+        eng.close()
+        rows.append(B * (base.tree.m + 1))
+        vus.append(vms * 1e3 / max(nv, 1))
+    plans = {}
+    for B in (1, 4, 16, 64):
+        k, m, rate = api.plan_budget(cands, rows, vus, B)
+        plans[B] = {"k": k, "m": m, "committed_tok_per_s": rate * 1e6}
+    print(json.dumps({"plan_budget": {
+        "workload": base.name, "verify_rows": rows, "verify_us": vus,
+        "draft_us": {c[0]: c[1] for c in cands},
+        "expected_tokens_at_m": {c[0]: {m: round(c[2][m - 1], 3) for m in (1, 4, 8, 16, 32, 60) if m <= len(c[2])}
+                                 for c in cands},
+        "plan": plans}}))
+
+
 def run_reference(args, ws, rank, local):
     if rank != 0:
         return None
@@ -573,6 +660,8 @@ def main():
                     help="only time one projection GEMM of this shape (for ncu and tuning)")
     ap.add_argument("--ncu-region", action="store_true",
                     help="only run a short NVTX-marked region for an ncu launch list")
+    ap.add_argument("--plan-budget", action="store_true",
+                    help="measure the budget planner's inputs on this GPU and plan (k, m) per batch size")
     ap.add_argument("--layers", type=int, default=0,
                     help="with --ncu-region: truncate the target to this many layers (small profiling case)")
     args = ap.parse_args()
@@ -582,6 +671,9 @@ def main():
         return
     if args.gemm_shape:
         run_gemm_probe(args)
+        return
+    if args.plan_budget:
+        run_plan_budget(args)
         return
     ws, rank, local = dist_setup()
     if args.impl == "reference":

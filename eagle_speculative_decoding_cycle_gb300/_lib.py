@@ -27,7 +27,7 @@ EXPORTED = [
     "eagle_set_graph", "eagle_cycle_kernel_launches", "eagle_status_sync", "eagle_dump_bytes", "eagle_debug_dump", "eagle_set_debug",
     "eagle_kv_view", "eagle_kv_table", "eagle_set_static_tree", "eagle_ttt_forward", "eagle_profile_begin", "eagle_profile_end", "eagle_profile_verify", "eagle_last_error", "eagle_destroy",
     "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_gemm_noalloc", "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
-    "eagle_op_attention_scratch_bytes", "eagle_op_attention", "eagle_op_tree_scratch_bytes", "eagle_op_tree_build", "eagle_op_compact",
+    "eagle_op_attention_scratch_bytes", "eagle_op_attention", "eagle_plan_budget", "eagle_op_tree_scratch_bytes", "eagle_op_tree_build", "eagle_op_compact",
 ]
 
 
@@ -82,6 +82,8 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_kv_view": (i32, [vp, P(vp), P(vp), P(i32)]),
         "eagle_kv_table": (i32, [vp, P(vp), P(i32), P(i32), P(i32)]),
         "eagle_set_static_tree": (i32, [vp, i32, P(i32), P(i32)]),
+        "eagle_plan_budget": (i32, [i32, P(i32), P(C.c_float), P(i32), P(C.c_float), i32, P(i32), P(C.c_float), i32,
+                                  P(i32), P(i32), P(C.c_float)]),
         "eagle_ttt_forward": (i32, [vp, vp, i32, i32, vp]),
         "eagle_profile_begin": (i32, [vp, i32]),
         "eagle_profile_end": (i32, [vp, P(i32), P(C.c_double), P(C.c_double)]),

@@ -311,3 +311,22 @@ def compact(kcache, vcache, n_old, acc_len, acc_path, stream: Optional[torch.cud
                               nkv, cap, d, n_old.data_ptr(), acc_len.data_ptr(), acc_path.data_ptr(),
                               acc_path.shape[1])
     L.check(rc, "eagle_op_compact")
+
+
+def plan_budget(candidates, rows_pts: Sequence[int], verify_us: Sequence[float], batch: int):
+    """Batch-aware draft budget (eagle_plan_budget). candidates: list of (k, draft_us,
+    exp_tokens) with exp_tokens[m-1] the expected committed tokens of an m-node tree.
+    Returns (k, m, tokens per microsecond)."""
+    lib = L.lib()
+    n_k = len(candidates)
+    ks = (C.c_int32 * n_k)(*[c[0] for c in candidates])
+    dr = (C.c_float * n_k)(*[c[1] for c in candidates])
+    mm = (C.c_int32 * n_k)(*[len(c[2]) for c in candidates])
+    flat = [float(v) for c in candidates for v in c[2]]
+    ex = (C.c_float * max(1, len(flat)))(*flat)
+    rp = (C.c_int32 * len(rows_pts))(*rows_pts)
+    vu = (C.c_float * len(verify_us))(*verify_us)
+    bk, bm, rate = C.c_int32(), C.c_int32(), C.c_float()
+    L.check(lib.eagle_plan_budget(n_k, ks, dr, mm, ex, len(rows_pts), rp, vu, batch, C.byref(bk), C.byref(bm),
+                                  C.byref(rate)), "eagle_plan_budget")
+    return bk.value, bm.value, rate.value

@@ -103,6 +103,23 @@ int eagle_op_tree_build(void* stream, int B, int k, int depth, int m, const int3
 int eagle_op_compact(int dtype, void* stream, void* kcache, void* vcache, int layers, int B, int nkv, int cap,
                      int d, const int32_t* n_old, const int32_t* acc_len, const int32_t* acc_path, int Dmax);
 
+/* Batch-aware draft budget (host arithmetic only, no device work). For each candidate k
+ * (k_values[j], n_k of them) the caller supplies draft_us[j], the measured drafter cost of a
+ * cycle, and exp_tokens[off_j + m - 1] for m = 1..m_max[j] (off_j = sum of the earlier
+ * m_max), the expected committed tokens per sequence of a tree of m nodes: 1 + the sum of
+ * the m largest path values, averaged over real cycles (a node's path value estimates its
+ * acceptance: "EAGLE-2: Context-Aware Dynamic Draft Trees", "Path Value Ranks Prefixes").
+ * rows_pts / verify_us (n_points, rows strictly increasing) are measured verify-pass times
+ * against verify rows; between points the time is interpolated linearly, beyond the last
+ * it grows with the last slope (flat before the first; a single point is flat up to it and
+ * proportional past it). Returns in best_k / best_m the choice maximising
+ * batch * exp_tokens / (draft_us + verify(batch * (m + 1))) and that rate (tokens per
+ * microsecond, nullable). Ties keep the earlier k and the smaller m. EAGLE_EINVAL on bad
+ * arguments. */
+int eagle_plan_budget(int n_k, const int32_t* k_values, const float* draft_us, const int32_t* m_max,
+                      const float* exp_tokens, int n_points, const int32_t* rows_pts, const float* verify_us,
+                      int batch, int32_t* best_k, int32_t* best_m, float* tokens_per_us);
+
 #ifdef __cplusplus
 }
 #endif
