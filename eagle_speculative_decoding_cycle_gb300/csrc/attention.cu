@@ -213,26 +213,41 @@ __device__ __forceinline__ void split_bf16(float lo, float hi, uint32_t& h, uint
   l = *reinterpret_cast<const uint32_t*>(&lv);
 }
 
+// a row's visibility data: validity, own slot, and (tree mode) the 64 mask bits of the
+// current key tile, bit i <-> key tile_base + i
 struct RowVis {
   int valid, slot;
-  uint64_t mw[4];
+  uint64_t win;
 };
 
-__device__ __forceinline__ bool visible(const AttnArgs& a, const RowVis& rv, int ctx, int key) {
+// Bits [base, base + 64) of a row's tree mask (4 words in shared memory); bits below 0 and
+// past the words read as 0.
+__device__ __forceinline__ uint64_t mask_window(const uint64_t* mw, int base) {
+  if (base <= -64 || base >= 256) return 0ull;
+  if (base < 0) return mw[0] << (-base);
+  const int w = base >> 6, sh = base & 63;
+  const uint64_t lo = mw[w] >> sh;
+  const uint64_t hi = (sh && w < 3) ? mw[w + 1] << (64 - sh) : 0ull;
+  return lo | hi;
+}
+
+template <bool TTT>
+__device__ __forceinline__ bool visible(const AttnArgs& a, const RowVis& rv, int ctx, int key, int kb) {
   if (!rv.valid) return false;
+  if constexpr (TTT) return ttt_visible(rv.slot, key, ctx);
   if (a.mode == 0) return key <= rv.slot;
-  if (a.mode == 2) return ttt_visible(rv.slot, key, ctx);
   if (key < ctx) return true;
-  const int t = key - ctx;
-  if (t >= a.tree_T) return false;
-  return (rv.mw[t >> 6] >> (t & 63)) & 1ull;
+  if (key - ctx >= a.tree_T) return false;
+  return (rv.win >> (key - kb)) & 1ull;
 }
 
 // Everything before the query loads reads data older than the preceding kernel (the rows'
 // sequence, slot, mask and context length, and in tree mode the context keys below
 // ctx_len, which that kernel never writes), so it runs before waiting on that kernel: the
 // first key tile of a tree-mode CTA is already in flight when the queries arrive.
-template <int D>
+// KIND: 0 = contiguous cache, 1 = paged cache, 2 = training-time-test mask (contiguous);
+// one instantiation each, so the cycle's contiguous kernel carries neither of the others.
+template <int D, int KIND>
 __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   constexpr int LD = D + 8;                      // padded smem row (bf16 elements)
   extern __shared__ __align__(16) uint8_t attn_smem[];
@@ -268,7 +283,7 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
     head = kvh * G + qv % G;
     v.valid = row < r1;
     v.slot = v.valid ? a.row_slot[row] : -1;
-    for (int w = 0; w < 4; ++w) v.mw[w] = (v.valid && a.mode == 1 && w < a.mask_words) ? a.mask[(size_t)row * a.mask_words + w] : 0ull;
+    v.win = 0ull;
   };
   int row_a, head_a, row_b, head_b;
   setup_row(qv_a, va, row_a, head_a);
@@ -280,13 +295,19 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
   const float sl2 = a.scale * 1.4426950408889634f;
 
+  // contiguous cache: one (sequence, head) run of rows; paged: rows through the block table
+  const size_t head_row0 = KIND == 1 ? 0 : ((size_t)seq * a.nkv + kvh) * (size_t)a.cap;
   auto load_tile = [&](int t, int buf) {
     constexpr int CH = D / 8;   // 16-byte chunks per row
     for (int i = threadIdx.x; i < MT_KEYS * CH; i += 128) {
       const int kr = i / CH, c = i % CH;
       const int key = t * MT_KEYS + kr;
       const bool in = key < kend;
-      const size_t goff = kv_row(a.page, seq, a.nkv, kvh, a.cap, in ? key : 0) * D + c * 8;
+      const int kk = in ? key : 0;
+      size_t grow;
+      if constexpr (KIND == 1) grow = kv_row(a.page, seq, a.nkv, kvh, a.cap, kk);
+      else grow = head_row0 + kk;
+      const size_t goff = grow * D + c * 8;
       const uint32_t dk = smem_u32(sK + (buf * MT_KEYS + kr) * LD + c * 8);
       const uint32_t dv = smem_u32(sV + (buf * MT_KEYS + kr) * LD + c * 8);
       cp_async16(dk, kc + goff, in ? 16 : 0);
@@ -295,6 +316,14 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
     cp_async_commit();
   };
 
+  // the block's rows' tree masks, [row in block][4 words]
+  __shared__ uint64_t s_mask[MT_QV][4];
+  if (a.mode == 1) {
+    for (int i = threadIdx.x; i < RB * 4; i += 128) {
+      const int rr = i >> 2, w = i & 3, row = r0 + rr;
+      s_mask[rr][w] = (row < r1 && w < a.mask_words) ? a.mask[(size_t)row * a.mask_words + w] : 0ull;
+    }
+  }
   const bool early = a.mode == 1 && t_begin < t_end && (t_begin + 1) * MT_KEYS <= ctx;
   if (early) load_tile(t_begin, 0);
   PDL_ENTRY();
@@ -319,6 +348,11 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
     if (t + 1 < t_end) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
     else cp_async_wait<0>();
     __syncthreads();
+    const int kb = t * MT_KEYS;
+    if (a.mode == 1 && kb + MT_KEYS > ctx) {   // the tile reaches the tree rows' keys
+      va.win = va.valid ? mask_window(s_mask[row_a - r0], kb - ctx) : 0ull;
+      vb.win = vb.valid ? mask_window(s_mask[row_b - r0], kb - ctx) : 0ull;
+    }
     const __nv_bfloat16* K = sK + buf * MT_KEYS * LD;
     const __nv_bfloat16* Vt = sV + buf * MT_KEYS * LD;
     float s[8][4];
@@ -340,8 +374,8 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = t * MT_KEYS + nt * 8 + (lane & 3) * 2 + e;
-        s[nt][e] = visible(a, va, ctx, key) ? s[nt][e] * sl2 : -INFINITY;
-        s[nt][2 + e] = visible(a, vb, ctx, key) ? s[nt][2 + e] * sl2 : -INFINITY;
+        s[nt][e] = visible<KIND == 2>(a, va, ctx, key, kb) ? s[nt][e] * sl2 : -INFINITY;
+        s[nt][2 + e] = visible<KIND == 2>(a, vb, ctx, key, kb) ? s[nt][2 + e] * sl2 : -INFINITY;
         mx_a = fmaxf(mx_a, s[nt][e]);
         mx_b = fmaxf(mx_b, s[nt][2 + e]);
       }
@@ -490,8 +524,11 @@ static int launch_mma(cudaStream_t st, const AttnArgs& a) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(attn_mma_k<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_mma_k<D>, 128, smem) != cudaSuccess || per_sm < 1)
+    cudaFuncSetAttribute(attn_mma_k<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(attn_mma_k<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(attn_mma_k<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_mma_k<D, 0>, 128, smem) != cudaSuccess ||
+        per_sm < 1)
       per_sm = 1;
   }
   // as many key splits as one wave of resident CTAs holds (a second, partial wave would
@@ -502,7 +539,12 @@ static int launch_mma(cudaStream_t st, const AttnArgs& a) {
   while (splits > 1 && (size_t)splits * a.R * a.nq * D > a.part_floats) --splits;
   if (!a.part_o || !a.part_ml) splits = 1;
   if (splits < 1) splits = 1;
-  launch_k(attn_mma_k<D>, dim3(a.nkv, nseq * nb, splits), 128, smem, st, a, splits);
+  // the training-time-test mask is its own instantiation, so the cycle's kernel stays lean
+  const dim3 grid(a.nkv, nseq * nb, splits);
+  if (a.mode == 2 && !a.page.table) launch_k(attn_mma_k<D, 2>, grid, 128, smem, st, a, splits);
+  else if (a.mode == 2) return -1;   // the training-time test runs on the contiguous drafter cache
+  else if (a.page.table) launch_k(attn_mma_k<D, 1>, grid, 128, smem, st, a, splits);
+  else launch_k(attn_mma_k<D, 0>, grid, 128, smem, st, a, splits);
   if (splits > 1) launch_k(attn_combine_k<D>, (a.R * a.nq + 3) / 4, 128, 0, st, a, splits);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
