@@ -41,7 +41,8 @@ struct GemmArgs {
   int M, N, K;
   int tiles_t;        // token tiles
   int kb;             // 64-wide k-blocks
-  long long units;    // tiles_n * tiles_t * kb
+  long long units;    // units of one slice: tiles_n * (tiles_t / slices) * kb
+  int slices;         // 1, or tiles_t: CTA c then works on token tile c % tiles_t only
   int epi;
   void* out;
   int ldo;
@@ -211,9 +212,17 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Units are (weight tile, k-block) steps. With several token tiles, the CTAs form slices:
+  // slice c % S takes token tile c % S, and stream-K runs over the weight tiles' units within
+  // each slice, so the S CTAs of a group read the same weight boxes at the same time (one DRAM
+  // read, the rest from L2) instead of re-streaming the weight for every token tile.
+  const int S = a.slices, cta = blockIdx.x;
+  const int slice = cta % S, G = gridDim.x / S, cs = cta / S;   // G: CTAs per slice, cs: index in it
   const long long U = a.units;
-  const int G = gridDim.x, cta = blockIdx.x;
-  const long long u_begin = (long long)cta * U / G, u_end = (long long)(cta + 1) * U / G;
+  const long long u_begin = (long long)cs * U / G, u_end = (long long)(cs + 1) * U / G;
+  // slice-local tile -> (weight tile, token tile)
+  auto tile_tn = [&](long long lt) { return (int)(S > 1 ? lt : lt / a.tiles_t); };
+  auto tile_tt = [&](long long lt) { return S > 1 ? slice : (int)(lt % a.tiles_t); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -247,8 +256,7 @@ __global__ void __launch_bounds__(192, 1)
       // once its outputs are visible.
       // unit coordinates (k-block, weight tile, token tile), advanced without division
       const long long tile0 = u_begin / a.kb;
-      const int k0 = (int)(u_begin - tile0 * a.kb), tn0 = (int)(tile0 / a.tiles_t),
-                tt0 = (int)(tile0 - (long long)tn0 * a.tiles_t);
+      const int k0 = (int)(u_begin - tile0 * a.kb), tn0 = tile_tn(tile0), tt0 = tile_tt(tile0);
       int pk = k0, ptn = tn0, ptt = tt0;
       // weight tile (128 rows x 64 k); SwiGLU: 64 gate rows + the matching 64 up rows
       auto load_w = [&](uint32_t dst, int k, int tn, uint32_t bar) {
@@ -260,7 +268,11 @@ __global__ void __launch_bounds__(192, 1)
         }
       };
       auto advance = [&](int& k, int& tn, int& tt) {
-        if (++k == a.kb) { k = 0; if (++tt == a.tiles_t) { tt = 0; ++tn; } }
+        if (++k == a.kb) {
+          k = 0;
+          if (S > 1) ++tn;
+          else if (++tt == a.tiles_t) { tt = 0; ++tn; }
+        }
       };
       const int n_pre = (int)min((long long)C::STAGES, u_end - u_begin);
       for (int i = 0; i < n_pre; ++i) {
@@ -344,10 +356,11 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     long long u = u_begin;
     while (u < u_end) {
-      const long long tile = u / a.kb;
+      const long long tile = u / a.kb;   // slice-local
       const long long seg_end = min(u_end, (tile + 1) * a.kb);
       const bool whole = (u == tile * a.kb) && (seg_end == (tile + 1) * a.kb);
-      const int tn = (int)(tile / a.tiles_t), tt = (int)(tile % a.tiles_t);
+      const int tn = tile_tn(tile), tt = tile_tt(tile);
+      const long long gtile = (long long)tn * a.tiles_t + tt;   // counter index
       if (leader) bcast[0] = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag, a.err) ? 1 : 0;
       named_bar_sync(1, 128);
       const int ok = bcast[0];
@@ -369,6 +382,7 @@ __global__ void __launch_bounds__(192, 1)
         // which the tile is its first segment) publishes a partial [BN tokens][128 features]
         // and counts itself in. The owner waits for the count, then adds the partials to
         // its own accumulator in contributor order.
+        // contributors as slice indices; CTA of slice index i: i * S + slice
         const int cf = cta_of_unit(tile * a.kb, U, G);
         const int cl = cta_of_unit((tile + 1) * a.kb - 1, U, G);
         const int nother = cl - cf;
@@ -385,21 +399,21 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive(smem_u32(tempty + acc));
           __threadfence();
           named_bar_sync(1, 128);
-          if (leader) red_release_add(reinterpret_cast<unsigned*>(a.counters + tile), 1u);
+          if (leader) red_release_add(reinterpret_cast<unsigned*>(a.counters + gtile), 1u);
         } else {
           // the ring is idle (this is the CTA's last segment): with room, the partials come
           // in as bulk copies, all in flight at once
           const bool bulk = (uint32_t)nother * PART <= (uint32_t)(C::STAGES * C::STAGE);
           if (leader) {
-            bool ok = grid_wait(reinterpret_cast<const unsigned*>(a.counters + tile), (unsigned)nother,
+            bool ok = grid_wait(reinterpret_cast<const unsigned*>(a.counters + gtile), (unsigned)nother,
                                 abort_flag, a.err, false);
             if (ok && bulk && nother > 0) {
               fence_acq_rel_gpu();
               fence_proxy_async_all();
               mbar_expect_tx(smem_u32(fixbar), (uint32_t)nother * PART);
               for (int q = 0; q < nother; ++q)
-                bulk_load(smem_u32(smem + (size_t)q * PART), a.partials + (size_t)((cf + 1 + q) * 2) * BN * 128,
-                          PART, smem_u32(fixbar));
+                bulk_load(smem_u32(smem + (size_t)q * PART),
+                          a.partials + (size_t)(((cf + 1 + q) * S + slice) * 2) * BN * 128, PART, smem_u32(fixbar));
               ok = mbar_wait(smem_u32(fixbar), 0, abort_flag, a.err);
             }
             bcast[0] = ok ? 1 : 0;
@@ -419,8 +433,8 @@ __global__ void __launch_bounds__(192, 1)
                 // two contributors' loads in flight together
                 for (int cc = cf + 1; cc <= cl; cc += 2) {
                   const bool two = cc + 1 <= cl;
-                  const float* p0 = a.partials + (size_t)(cc * 2) * BN * 128 + c0 * 128 + row;
-                  const float* p1 = a.partials + (size_t)((cc + 1) * 2) * BN * 128 + c0 * 128 + row;
+                  const float* p0 = a.partials + (size_t)((cc * S + slice) * 2) * BN * 128 + c0 * 128 + row;
+                  const float* p1 = a.partials + (size_t)(((cc + 1) * S + slice) * 2) * BN * 128 + c0 * 128 + row;
                   float x0[ECH], x1[ECH];
 #pragma unroll
                   for (int i = 0; i < ECH; ++i) {
@@ -440,7 +454,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_before();
           mbar_arrive(smem_u32(tempty + acc));
-          if (leader) a.counters[tile] = 0;
+          if (leader) a.counters[gtile] = 0;
         }
         named_bar_sync(1, 128);
       }
@@ -536,10 +550,14 @@ static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmA
   }
   a.tiles_t = (a.M + BN - 1) / BN;
   a.kb = (a.K + 63) / 64;
-  a.units = (long long)tiles_n * a.tiles_t * a.kb;
   int G = num_sms();
   if (G > num_sms_cap()) G = num_sms_cap();
-  if ((long long)G > a.units) G = (int)a.units;
+  // several token tiles: one slice of CTAs per token tile (see the kernel)
+  a.slices = (a.tiles_t > 1 && a.tiles_t <= G) ? a.tiles_t : 1;
+  a.units = (long long)tiles_n * (a.tiles_t / a.slices) * a.kb;
+  long long per_slice = G / a.slices;
+  if (per_slice > a.units) per_slice = a.units;
+  G = (int)per_slice * a.slices;
   launch_k(gemm_bf16_tc<BN, MODE>, G, 192, C::SMEM, st, mw, mx, a);
   return cudaGetLastError();
 }

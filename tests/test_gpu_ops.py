@@ -36,7 +36,9 @@ def _ref_mm(X, W):
 
 
 GEMM_SHAPES = [(1, 128, 64), (7, 300, 200), (61, 640, 320), (61, 12288 // 4, 4096 // 4), (16, 1000, 256),
-               (17, 4096, 1024), (100, 257, 136), (200, 384, 512), (300, 520, 264), (61, 4096, 11008)]
+               (17, 4096, 1024), (100, 257, 136), (200, 384, 512), (300, 520, 264), (61, 4096, 11008),
+               # several 256-row token tiles: the CTAs split into one slice per token tile
+               (1088, 1536, 1024), (600, 4096, 4096), (1300, 640, 2048), (1025, 384, 520)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -49,7 +51,7 @@ def test_gemm_bf16_matches_oracle(M, N, K):
     assert np.all(np.abs(Y - ref) <= 1e-3 * mag + 1e-6), np.max(np.abs(Y - ref) / (mag + 1e-9))
 
 
-@pytest.mark.parametrize("M,N,K", [(61, 640, 320), (5, 4096, 4096), (130, 520, 264)])
+@pytest.mark.parametrize("M,N,K", [(61, 640, 320), (5, 4096, 4096), (130, 520, 264), (700, 512, 768)])
 def test_gemm_bf16_epilogues(M, N, K):
     g = torch.Generator().manual_seed(11)
     X = _rand((M, K), g, torch.bfloat16)
