@@ -44,22 +44,24 @@ def peaks():
         return 6800.0, "fallback (6.8 TB/s)"
 
 
-def algorithmic_bytes(w: synth.Workload, ctx: int) -> dict:
-    """Bytes one cycle must move at batch 1 (bf16 weights and KV), split by phase:
-    verify = all target layer weights + LM head + ctx KV read + tree KV write;
-    drafter = (depth - 1) expansions + 1 update, each FC + one layer + LM head (+ KV)."""
+def algorithmic_bytes(w: synth.Workload, ctx: float, batch: int = 1) -> dict:
+    """Bytes one cycle over `batch` sequences of mean context `ctx` must move (bf16 weights
+    and KV), split by phase: verify = all target layer weights + LM head, read once for the
+    batch, + each sequence's ctx KV read and tree KV write; drafter = (depth - 1) expansions
+    + 1 update, each FC + one layer + LM head (+ each sequence's drafter KV)."""
     m, t = w.model, w.tree
     H, F, V, d = m.hidden, m.ffn, m.vocab, m.head_dim
     qkv = m.qkv_out
     layer = (qkv * H + H * m.n_heads * d + 3 * H * F) * 2
     lm = V * H * 2
     kv_tok = 2 * m.n_layers * m.n_kv_heads * d * 2
-    verify = m.n_layers * layer + lm + ctx * kv_tok + (t.m + 1) * kv_tok
+    verify = int(m.n_layers * layer + lm + batch * (ctx + t.m + 1) * kv_tok)
     fc_in = 2 * H if w.drafter.kind == 1 else 3 * H
     dlayer = ((qkv * (H if w.drafter.kind == 1 else 2 * H)) + H * m.n_heads * d + 3 * H * F) * 2
-    dstep = H * fc_in * 2 + dlayer + lm + ctx * 2 * m.n_kv_heads * d * 2
+    dstep = int(H * fc_in * 2 + dlayer + lm + batch * ctx * 2 * m.n_kv_heads * d * 2)
     drafter = t.depth * dstep
-    return {"verify": verify, "drafter": drafter, "cycle": verify + drafter}
+    return {"verify": verify, "drafter": drafter, "cycle": verify + drafter,
+            "verify_weights": m.n_layers * layer + lm}
 
 
 class ClockSampler:
@@ -244,69 +246,73 @@ def run_ours(args, ws, rank, local):
     D = t.depth
     weights = synth.make_weights(wl, device=str(dev))
     torch.cuda.synchronize()
-    prompt = synth.make_prompts(wl)[0]
+    prompts = synth.make_prompts(wl)
+    B = len(prompts)
     K, W = args.steps, args.warmup
     n_ref = (W + K + args.prof_steps + 8) * (D + 1) + D + 2
     n_plain = 64
-    max_ctx = len(prompt) + 2 * n_ref + (W + K + args.prof_steps + 8) * (D + 1) + 64
+    max_ctx = max(len(p) for p in prompts) + 2 * n_ref + (W + K + args.prof_steps + 8) * (D + 1) + 64
     stream = torch.cuda.Stream(device=dev)
-    eng = api.Engine(wl, weights, max_ctx=max_ctx, stream=stream)
-    prompt_d = prompt.to(dev)
-    out_d = torch.zeros(1, D + 1, dtype=torch.int32, device=dev)
-    cnt_d = torch.zeros(1, dtype=torch.int32, device=dev)
+    eng = api.Engine(wl, weights, max_batch=B, max_ctx=max_ctx, stream=stream)
+    prompts_d = [p.to(dev) for p in prompts]
+    out_d = torch.zeros(B, D + 1, dtype=torch.int32, device=dev)
+    cnt_d = torch.zeros(B, dtype=torch.int32, device=dev)
+
+    def run_cycles(n, got):
+        for _ in range(n):
+            eng.cycle(out_d, cnt_d)
+            eng.sync()
+            o, c = out_d.cpu(), cnt_d.cpu()
+            for b in range(B):
+                got[b] += o[b, :int(c[b])].tolist()
+
     with torch.cuda.stream(stream):
-        # plain decoding: the speedup baseline
-        eng.prefill([prompt_d])
-        plain = torch.zeros(1, n_plain, dtype=torch.int32, device=dev)
+        # plain decoding (one token per sequence per step): the speedup baseline
+        eng.prefill(prompts_d)
+        plain = torch.zeros(B, n_plain, dtype=torch.int32, device=dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         eng.decode_plain(n_plain, plain)
         e1.record(stream)
         eng.sync()
-        plain_ms_per_tok = e0.elapsed_time(e1) / n_plain
-        # the planted reference: the target's own greedy continuation as the planted verify
+        plain_ms_per_step = e0.elapsed_time(e1) / n_plain
+        # the planted reference: each sequence's greedy continuation as the planted verify
         # pass computes it. Start from speculative decoding with planting off, then rerun
         # the planted cycles with the previous run's committed tokens as reference until the
-        # committed sequence reproduces itself (near-tie argmax decisions depend on the
+        # committed sequences reproduce themselves (near-tie argmax decisions depend on the
         # summation order, which depends on the tree, so an outside reference drifts).
-        eng.prefill([prompt_d])
-        ref = [int(eng.dump(L.DUMP_STATE)["root_tok"][0])]
-        while len(ref) < n_ref:
-            eng.cycle(out_d, cnt_d)
-            eng.sync()
-            ref += out_d[0, :int(cnt_d[0])].tolist()
+        eng.prefill(prompts_d)
+        ref = [[int(x)] for x in eng.dump(L.DUMP_STATE)["root_tok"][:B].tolist()]
+        while min(len(r) for r in ref) < n_ref:
+            run_cycles(1, ref)
         n_cyc = W + K + args.prof_steps + 4
         ref_iters = 0
         # under sampling the committed tokens follow the draws, so the reference cannot be
         # a fixed point beyond the first non-greedy draw (planting then goes inert)
         for ref_iters in range(1, 12 if t.temperature == 0.0 else 2):
-            rb = torch.tensor([ref[:n_ref]], dtype=torch.int32, device=dev)
-            eng.prefill([prompt_d], rb)
-            got = [ref[0]]
-            for _ in range(n_cyc):
-                eng.cycle(out_d, cnt_d)
-                eng.sync()
-                got += out_d[0, :int(cnt_d[0])].tolist()
-            stable = got == ref[:len(got)]
-            while len(got) < n_ref:          # extend with the verify pass's greedy tokens
-                eng.cycle(out_d, cnt_d)
-                eng.sync()
-                got += out_d[0, :int(cnt_d[0])].tolist()
-            ref = got[:n_ref]
+            rb = torch.tensor([r[:n_ref] for r in ref], dtype=torch.int32, device=dev)
+            eng.prefill(prompts_d, rb)
+            got = [[r[0]] for r in ref]
+            run_cycles(n_cyc, got)
+            stable = all(g == r[:len(g)] for g, r in zip(got, ref))
+            while min(len(g) for g in got) < n_ref:     # extend with the verify pass's greedy tokens
+                run_cycles(1, got)
+            ref = [g[:n_ref] for g in got]
             if stable:
                 break
-    R = torch.tensor([ref], dtype=torch.int32, device=dev)
+    R = torch.tensor(ref, dtype=torch.int32, device=dev)
     ref_buf = R.clone()
     # speculative cycles, graph replay
     clocks = ClockSampler(local)
     with torch.cuda.stream(stream):
         eng.set_graph(True)
-        eng.prefill([prompt_d], ref_buf)
+        eng.prefill(prompts_d, ref_buf)
         for _ in range(W):
             eng.cycle()
         eng.sync()
-        c0 = int(eng.dump(L.DUMP_STATE)["committed"][0])
-        ctx0 = int(eng.dump(L.DUMP_STATE)["ctx_len"][0])
+        st0 = eng.dump(L.DUMP_STATE)
+        c0 = st0["committed"][:B].long()
+        ctx0 = float(st0["ctx_len"][:B].double().mean())
         barrier(ws)
         torch.cuda.synchronize(dev)
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -318,14 +324,14 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize(dev)
         barrier(ws)
         st = eng.dump(L.DUMP_STATE)
-        committed = int(st["committed"][0]) - c0
-        ctx1 = int(st["ctx_len"][0])
-        on_track = int(st["on_track"][0])
+        committed = int((st["committed"][:B].long() - c0).sum())
+        ctx1 = float(st["ctx_len"][:B].double().mean())
+        on_track = int(st["on_track"][:B].min())
     ms_local = s0.elapsed_time(s1)
     # per-launch GEMM timing inside real cycles (eager launches, events around each GEMM)
     with torch.cuda.stream(stream):
         eng.set_graph(False)
-        eng.prefill([prompt_d], ref_buf)
+        eng.prefill(prompts_d, ref_buf)
         for _ in range(2):
             eng.cycle()
         eng.sync()
@@ -345,28 +351,30 @@ def run_ours(args, ws, rank, local):
     clk = clocks.stop()
     # end to end through the public API with host buffers: prompt + reference H2D from pinned
     # memory, prefill, then K cycles each followed by a D2H read of the committed tokens
-    prompt_h = prompt.pin_memory()
+    lens = [len(p) for p in prompts]
+    prompt_h = torch.cat(prompts).pin_memory()
+    prompt_all = torch.empty(prompt_h.shape, dtype=torch.int32, device=dev)
     ref_h = R.cpu().pin_memory()
-    out_h = torch.zeros(1, D + 1, dtype=torch.int32).pin_memory()
-    cnt_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    out_h = torch.zeros(B, D + 1, dtype=torch.int32).pin_memory()
+    cnt_h = torch.zeros(B, dtype=torch.int32).pin_memory()
     with torch.cuda.stream(stream):
         eng.set_graph(True)
-        eng.prefill([prompt_d], ref_buf)       # capture the graph with these output buffers
+        eng.prefill(prompts_d, ref_buf)        # capture the graph with these output buffers
         eng.cycle(out_d, cnt_d)
         eng.sync()
         torch.cuda.synchronize(dev)
         barrier(ws)
         t0 = time.perf_counter()
-        prompt_d.copy_(prompt_h, non_blocking=True)
+        prompt_all.copy_(prompt_h, non_blocking=True)
         ref_buf.copy_(ref_h, non_blocking=True)
-        eng.prefill([prompt_d], ref_buf)
-        e2e_tok = 1
+        eng.prefill(list(torch.split(prompt_all, lens)), ref_buf)
+        e2e_tok = B
         for _ in range(K):
             eng.cycle(out_d, cnt_d)
             out_h.copy_(out_d, non_blocking=True)
             cnt_h.copy_(cnt_d, non_blocking=True)
             stream.synchronize()
-            e2e_tok += int(cnt_h[0])
+            e2e_tok += int(cnt_h.sum())
         e2e_s = time.perf_counter() - t0
         eng.sync()
     e2e_s = barrier_max(ws, e2e_s, dev)
@@ -375,7 +383,7 @@ def run_ours(args, ws, rank, local):
     ms = barrier_max(ws, ms_local, dev)
     committed_all = barrier_sum(ws, committed, dev)
     hbm_peak, peak_src = peaks()
-    byt = algorithmic_bytes(wl, (ctx0 + ctx1) // 2)
+    byt = algorithmic_bytes(wl, (ctx0 + ctx1) / 2, B)
     cycle_s = ms / 1e3 / K
     gemm_gbs = gemm_bytes / (gemm_ms / 1e3) / 1e9 if gemm_ms > 0 else None
     res = None
@@ -384,19 +392,20 @@ def run_ours(args, ws, rank, local):
             "metric": METRIC, "value": committed_all / (ms / 1e3), "unit": UNIT, "n_gpus": ws, "steps": K,
             "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init N(0,0.02) weights, uniform prompt ids)",
-            "config": {"workload": wl.name, "batch": wl.batch, "prompt": len(prompt),
+            "config": {"workload": wl.name, "batch": B,
+                       "prompt": lens[0] if B == 1 else f"{min(lens)}-{max(lens)} tokens, {sum(lens)} in all",
                        "tree": f"k{t.topk} D{t.depth} m{t.m}" + ("" if args.tree == "dynamic" else f" {args.tree}"),
                        "planted_p": t.planted_p,
                        "temperature": t.temperature, "parallelism": "replicas" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2 (13+ GB of weights streamed per cycle); no flush needed",
                        "graph_replay": True},
             "cycle_us": cycle_s * 1e6,
-            "tau": committed / K,
-            "tree_tok_s": ws * wl.batch * (t.m + 1) / cycle_s,
+            "tau": committed / K / B,
+            "tree_tok_s": ws * B * (t.m + 1) / cycle_s,
             "hbm_gbs": byt["cycle"] / cycle_s / 1e9,
             "algorithmic_bytes_per_cycle": byt,
-            "plain_decode": {"ms_per_token": plain_ms_per_tok, "tok_s": 1e3 / plain_ms_per_tok},
-            "speedup_vs_plain": (committed / K) / cycle_s / (1e3 / plain_ms_per_tok),
+            "plain_decode": {"ms_per_step": plain_ms_per_step, "tok_s": B * 1e3 / plain_ms_per_step},
+            "speedup_vs_plain": (committed / K) / cycle_s / (B * 1e3 / plain_ms_per_step),
             "on_track": on_track,
             "reference": f"planted reference = the planted verify pass's own greedy continuation (fixed point "
                          f"reached after {ref_iters} rerun(s)); on_track = 1 if the timed cycles never left it",
@@ -417,11 +426,14 @@ def run_ours(args, ws, rank, local):
                 "algorithmic_bytes": byt["verify"],
                 "gbs": byt["verify"] / (verify_ms / max(n_verify, 1) / 1e3) / 1e9 if verify_ms > 0 else None,
                 "frac_of_hbm_peak": (byt["verify"] / (verify_ms / max(n_verify, 1) / 1e3) / 1e9 / hbm_peak)
-                if verify_ms > 0 else None},
+                if verify_ms > 0 else None,
+                # projections + LM head only (2 flops per weight per row); attention excluded
+                "weight_tflops": (byt["verify_weights"] * B * (t.m + 1) / (verify_ms / max(n_verify, 1) / 1e3)
+                                  / 1e12) if verify_ms > 0 else None},
             "clocks": clk,
             "e2e": {"value": e2e_tok_all / e2e_s, "unit": UNIT,
-                    "h2d_bytes_per_step": (prompt.numel() * 4 + R.numel() * 4) / K,
-                    "d2h_bytes_per_step": (D + 1) * 4 + 4,
+                    "h2d_bytes_per_step": (prompt_h.numel() * 4 + R.numel() * 4) / K,
+                    "d2h_bytes_per_step": B * ((D + 1) * 4 + 4),
                     "what": "public API with host buffers: pinned H2D of prompt + reference, prefill, then K "
                             "cycles each with a D2H read of its committed tokens and a host sync"},
             "gpu_launches": graph_launches * K if graph_launches else None,
