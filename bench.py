@@ -473,27 +473,29 @@ def run_ncu_region(args):
         wl = wl.replace(model=dataclasses.replace(wl.model, n_layers=args.layers))
     D = wl.tree.depth
     weights = synth.make_weights(wl, device=str(dev))
-    prompt = synth.make_prompts(wl)[0].to(dev)
+    prompts = [p.to(dev) for p in synth.make_prompts(wl)]
+    B = len(prompts)
     n_plain = (args.steps + 4) * (D + 1) + D + 2
-    eng = api.Engine(wl, weights, max_ctx=len(prompt) + n_plain + (args.steps + 8) * (D + 1) + 64)
-    eng.prefill([prompt])
-    first = int(eng.dump(L.DUMP_STATE)["root_tok"][0])
-    plain = torch.zeros(1, n_plain, dtype=torch.int32, device=dev)
+    eng = api.Engine(wl, weights, max_batch=B,
+                     max_ctx=max(len(p) for p in prompts) + n_plain + (args.steps + 8) * (D + 1) + 64)
+    eng.prefill(prompts)
+    first = eng.dump(L.DUMP_STATE)["root_tok"][:B].to(dev).to(torch.int32)
+    plain = torch.zeros(B, n_plain, dtype=torch.int32, device=dev)
     eng.decode_plain(n_plain, plain)
-    R = torch.cat([torch.tensor([first], dtype=torch.int32, device=dev), plain[0]]).view(1, -1).contiguous()
-    eng.prefill([prompt], R)
+    R = torch.cat([first.view(B, 1), plain], 1).contiguous()
+    eng.prefill(prompts, R)
     eng.cycle()
     eng.sync()
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("profiled")
     for _ in range(args.steps):
         eng.cycle()
-    out = torch.zeros(1, 2, dtype=torch.int32, device=dev)
+    out = torch.zeros(B, 2, dtype=torch.int32, device=dev)
     eng.decode_plain(2, out)
     eng.sync()
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
-    print(json.dumps({"ncu_region": True, "workload": wl.name, "cycles": args.steps, "plain_steps": 2}))
+    print(json.dumps({"ncu_region": True, "workload": wl.name, "batch": B, "cycles": args.steps, "plain_steps": 2}))
 
 
 def run_gemm_probe(args):

@@ -343,12 +343,15 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
     }
   }
   if (!early && t_begin < t_end) load_tile(t_begin, 0);
+  const bool warp_live = warp * 16 < (r1 - r0) * G;
   for (int t = t_begin; t < t_end; ++t) {
     const int buf = (t - t_begin) & 1;
     if (t + 1 < t_end) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
     else cp_async_wait<0>();
     __syncthreads();
     const int kb = t * MT_KEYS;
+    // a warp whose 16 query vectors are all past the block's rows only helps load the tiles
+    if (!warp_live) { __syncthreads(); continue; }
     if (a.mode == 1 && kb + MT_KEYS > ctx) {   // the tile reaches the tree rows' keys
       va.win = va.valid ? mask_window(s_mask[row_a - r0], kb - ctx) : 0ull;
       vb.win = vb.valid ? mask_window(s_mask[row_b - r0], kb - ctx) : 0ull;

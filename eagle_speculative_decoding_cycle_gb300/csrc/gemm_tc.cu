@@ -181,13 +181,29 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int
       }
     }
   } else {
+    // LM head: each warp transposes its 32 vocabulary rows x CH columns through shared
+    // memory (column stride 129 floats: the column reads are free of bank conflicts) and
+    // each lane reduces one column's 32 entries; the warp holding vocabulary rows 0..31
+    // combines the four quarter records of its column in quarter order.
+    constexpr int LDS = 129;
+    const int quarter = row >> 5;
 #pragma unroll
-    for (int i = 0; i < CH; ++i) staging[i * 128 + row] = v[i];
+    for (int i = 0; i < CH; ++i) staging[i * LDS + row] = v[i];
+    __syncwarp();
+    const int j = tt * BN + c0 + lane;
+    const bool live = lane < CH && j < a.M;
+    const int id0 = tn * 128 + quarter * 32;
+    float r[32];
+    uint32_t rank_ok = 0;
+    float mx = -INFINITY, se = 0.f;
+    if (live) head_quarter_load(staging + lane * LDS + quarter * 32, id0, j, a.head, r, rank_ok, mx, se);
+    named_bar_sync(2, 128);                  // all columns read: the staging area is free
+    const int RS = 2 + 2 * a.head.K;
+    float* xq = staging + lane * RS;         // quarter q's record of this column: xq + q * 32 * RS
+    if (live) head_quarter_select(r, rank_ok, id0, a.head.K, mx, se, xq + quarter * 32 * RS);
     named_bar_sync(2, 128);
-    for (int i = ew; i < CH; i += 4) {
-      const int j = tt * BN + c0 + i;
-      if (j < a.M) head_tile_row(staging + i * 128, tn, j, a.head, lane);
-    }
+    if (quarter == 0 && live)
+      head_quarter_merge(xq, xq + 32 * RS, xq + 64 * RS, xq + 96 * RS, a.head.K, tn, j, a.head);
     named_bar_sync(2, 128);
   }
 }

@@ -113,6 +113,104 @@ EAGLE_DEV void head_tile_row(const float* vals, int tile, int row, const HeadPar
   }
 }
 
+// The same record built by one thread from 32 consecutive vocabulary entries of one row
+// (ids id0 .. id0 + 31, unit stride in shared memory): the tensor-core epilogue gives each
+// lane one token column and each warp one quarter of the 128-entry tile, so the reduction
+// needs no cross-lane step. head_quarter_load reads the entries into registers (max and sum
+// of exp over the entries in the lse, ranking values); head_quarter_select then takes the K
+// kept entries in K rounds, each the best remaining entry in the rank_before order (the
+// scan runs in id order and keeps the first of equal values), and writes the quarter's
+// record [m, s, (value, id) x K] (id -1: empty) to shared memory. head_quarter_merge
+// combines the four quarter records of a row in quarter order into the tile's record.
+EAGLE_DEV void head_quarter_load(const float* vals, int id0, int row, const HeadParams& p, float (&r)[32],
+                                 uint32_t& rank_ok, float& mx, float& se) {
+  uint32_t special = 0;
+  if (p.specials) {
+    for (int s = 0; s < p.S; ++s) {
+      const int sid = p.specials[row * p.S + s];
+      const int o = sid - id0;
+      if (o >= 0 && o < 32 && sid < p.vocab) {
+        special |= 1u << o;
+        p.spec_logit[row * p.S + s] = vals[o];
+      }
+    }
+  }
+  const uint32_t valid = (p.vocab - id0 >= 32) ? 0xffffffffu : ((1u << max(0, p.vocab - id0)) - 1u);
+  const uint32_t in_lse = p.lse_excl ? (valid & ~special) : valid;
+  rank_ok = valid & ~special;
+  mx = -INFINITY;
+#pragma unroll
+  for (int v = 0; v < 32; ++v) {
+    r[v] = vals[v] * p.inv_t;
+    if ((in_lse >> v) & 1u) mx = fmaxf(mx, r[v]);
+  }
+  se = 0.f;
+  if (mx != -INFINITY) {
+#pragma unroll
+    for (int v = 0; v < 32; ++v)
+      if ((in_lse >> v) & 1u) se += expf(r[v] - mx);
+  }
+  if (p.gumbel) {
+#pragma unroll
+    for (int v = 0; v < 32; ++v)
+      if ((rank_ok >> v) & 1u) r[v] += gumbel_noise(p, row, id0 + v);
+  }
+}
+
+EAGLE_DEV void head_quarter_select(const float (&r)[32], uint32_t avail, int id0, int K, float mx, float se,
+                                   float* dst) {
+  dst[0] = mx;
+  dst[1] = se;
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int bvi = -1;
+#pragma unroll
+    for (int v = 0; v < 32; ++v)
+      if (((avail >> v) & 1u) && (bvi < 0 || r[v] > bv)) { bv = r[v]; bvi = v; }
+    if (bvi >= 0) avail &= ~(1u << bvi);
+    dst[2 + 2 * k] = bvi >= 0 ? bv : -INFINITY;
+    dst[3 + 2 * k] = __int_as_float(bvi >= 0 ? id0 + bvi : -1);
+  }
+}
+
+// q0 .. q3: the four quarter records of the row, in quarter order.
+EAGLE_DEV void head_quarter_merge(const float* q0, const float* q1, const float* q2, const float* q3, int K,
+                                  int tile, int row, const HeadParams& p) {
+  const float* qs[4] = {q0, q1, q2, q3};
+  float M = -INFINITY, S = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float m2 = qs[q][0], s2 = qs[q][1];
+    if (m2 != -INFINITY) {
+      if (m2 > M) { S = S * expf(M - m2) + s2; M = m2; }
+      else S += s2 * expf(m2 - M);
+    }
+  }
+  float* rec = p.part + ((size_t)tile * p.n_rows + row) * (2 + 2 * K);
+  rec[0] = M;
+  rec[1] = S;
+  int h0 = 0, h1 = 0, h2 = 0, h3 = 0;     // next entry of each quarter's sorted list
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff, bq = -1;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int h = q == 0 ? h0 : q == 1 ? h1 : q == 2 ? h2 : h3;
+      if (h < K) {
+        const float cv = qs[q][2 + 2 * h];
+        const int ci = __float_as_int(qs[q][3 + 2 * h]);
+        if (ci >= 0 && (bq < 0 || rank_before(cv, ci, bv, bi))) { bv = cv; bi = ci; bq = q; }
+      }
+    }
+    h0 += bq == 0;
+    h1 += bq == 1;
+    h2 += bq == 2;
+    h3 += bq == 3;
+    rec[2 + 2 * k] = bq >= 0 ? bv : -INFINITY;
+    rec[3 + 2 * k] = __int_as_float(bq >= 0 ? bi : -1);
+  }
+}
+
 // Merge: each thread folds the records of tiles t0, t0 + stride, ... into its sorted
 // list (lv, li; K entries, the rest -inf) and its (max, sum-exp) pair. A thread's first
 // record is taken as is (records are sorted); later ones are inserted.
