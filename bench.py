@@ -552,6 +552,71 @@ def run_gemm_probe(args):
                       "frac": byt / us / 1e3 / hbm, "peak_source": src}))
 
 
+def run_attn_probe(args):
+    """The tree-mode attention kernel in isolation (contiguous cache larger than L2), timed
+    with CUDA events over graph-replayed launches: B sequences of CTX context keys, ROWS tree
+    rows each (a chain: row i sees rows 0..i), Llama-3.1-8B head geometry (32 query heads,
+    8 KV heads, head dim 128)."""
+    from eagle_speculative_decoding_cycle_gb300 import _lib as L
+    from eagle_speculative_decoding_cycle_gb300 import api
+    from eagle_speculative_decoding_cycle_gb300.build import build
+    build()
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev).manual_seed(0)
+    B, CTX, T = args.attn_shape
+    nq, nkv, d = 32, 8, 128
+    cap = CTX + T + 16
+    R = B * T
+    kc = torch.randn(B, nkv, cap, d, generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn(B, nkv, cap, d, generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn(R, nq, d, generator=g, device=dev).to(torch.bfloat16)
+    row_seq = torch.arange(R, device=dev, dtype=torch.int32) // T
+    row_slot = (CTX + torch.arange(R, device=dev, dtype=torch.int32) % T).to(torch.int32)
+    ctx_len = torch.full((B,), CTX, dtype=torch.int32, device=dev)
+    mw = (T + 63) // 64
+    bits = torch.zeros(T, mw * 64, dtype=torch.bool)
+    for i in range(T):
+        bits[i, :i + 1] = True
+    words = torch.zeros(T, mw, dtype=torch.int64)
+    for w in range(mw):
+        for b in range(64):
+            words[:, w] |= bits[:, w * 64 + b].to(torch.int64) << b
+    mask = words.repeat(B, 1).to(dev)
+    gs = torch.cuda.Stream()
+
+    def call():
+        api.attention(q, kc, vc, row_seq, row_slot, ctx_len, T, 1, tree_T=T, mask=mask, stream=gs)
+
+    with torch.cuda.stream(gs):
+        for _ in range(3):
+            call()
+    torch.cuda.synchronize()
+    reps = 10
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gs):
+        graph.capture_begin()
+        for _ in range(reps):
+            call()
+        graph.capture_end()
+    ts = []
+    with torch.cuda.stream(gs):
+        graph.replay()
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(gs)
+            graph.replay()
+            e1.record(gs)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / reps)
+    byt = B * nkv * (CTX + T) * d * 2 * 2 + 2 * R * nq * d * 2
+    us = statistics.median(ts) * 1e3
+    hbm, src = peaks()
+    print(json.dumps({"attention": {"batch": B, "ctx": CTX, "tree_rows": T, "nq": nq, "nkv": nkv, "d": d},
+                      "us_median": us, "us_min": min(ts) * 1e3, "gbs": byt / us / 1e3, "frac": byt / us / 1e3 / hbm,
+                      "peak_source": src}))
+
+
 def run_plan_budget(args):
     """Measure the inputs of the batch-aware budget planner on this GPU and plan (k, m) per
     batch size: for k in (4, 8, 10) the expected committed tokens of the m best nodes (1 +
@@ -674,6 +739,8 @@ def main():
                     help="only time one projection GEMM of this shape (for ncu and tuning)")
     ap.add_argument("--ncu-region", action="store_true",
                     help="only run a short NVTX-marked region for an ncu launch list")
+    ap.add_argument("--attn-shape", type=int, nargs=3, default=None, metavar=("B", "CTX", "ROWS"),
+                    help="time the tree-mode attention kernel alone (8B head geometry, contiguous cache)")
     ap.add_argument("--plan-budget", action="store_true",
                     help="measure the budget planner's inputs on this GPU and plan (k, m) per batch size")
     ap.add_argument("--layers", type=int, default=0,
@@ -685,6 +752,9 @@ def main():
         return
     if args.gemm_shape:
         run_gemm_probe(args)
+        return
+    if args.attn_shape:
+        run_attn_probe(args)
         return
     if args.plan_budget:
         run_plan_budget(args)
