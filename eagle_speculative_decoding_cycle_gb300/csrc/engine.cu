@@ -164,7 +164,11 @@ struct eagle_ctx {
   float *attn_po, *attn_pml; size_t attn_pfloats;
   unsigned* chain_bar;                  // grid-barrier words of the layer-chain kernel
   int use_chain = 0;                    // bf16: run each layer as chain launches (EAGLE_CHAIN=1 turns them on)
-  int fuse_epi = 0;                     // bf16: RoPE/KV write and SwiGLU in the GEMM epilogues (EAGLE_FUSE_EPI=1: on)
+  // bf16 fused epilogues: -1 (default) SwiGLU in the gate/up epilogue from 128 rows on, where
+  // the separate SwiGLU pass costs more than the epilogue work; 1 (EAGLE_FUSE_EPI=1) also
+  // RoPE/KV write in the QKV epilogue, at every row count; 0 (EAGLE_FUSE_EPI=0) none. Both
+  // epilogues agree bit for bit with the row kernels they replace.
+  int fuse_epi = -1;
   float *rope_cos, *rope_sin;
   void *kc, *vc, *dkc, *dvc;
   int *static_exp, *static_keep;        // static tree: [D-1][k] expansion rows, [NG] kept flags
@@ -346,7 +350,7 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
                   int tree_T, const uint64_t* mask, int mask_words, const KvPage& page) {
   const Dims& z = ctx->z;
   // the fused epilogue writes a contiguous cache only
-  if (z.dt == DT_BF16 && ctx->fuse_epi && 128 % z.d == 0 && !page.table) {
+  if (z.dt == DT_BF16 && ctx->fuse_epi > 0 && 128 % z.d == 0 && !page.table) {
     // RoPE, the q output and the KV-cache write in the projection's epilogue
     const QkvEpi q{pos, slot, seq, ctx->rope_cos, ctx->rope_sin, ctx->qb, kcache, vcache, z.nq, z.nkv, z.d, cap};
     CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_QKV, nullptr, 0, nullptr, &q));
@@ -359,7 +363,7 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   if (r) return r;
   CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
   CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
-  if (z.dt == DT_BF16 && ctx->fuse_epi && z.F % 64 == 0) {
+  if (z.dt == DT_BF16 && (ctx->fuse_epi > 0 || (ctx->fuse_epi < 0 && R >= 128)) && z.F % 64 == 0) {
     // gate and up rows of each 64 features share one tile; SwiGLU in the epilogue
     CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_SWIGLU, ctx->hb, z.F));
   } else {
