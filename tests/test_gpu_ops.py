@@ -86,7 +86,9 @@ def test_gemm_f32_matches_oracle(M, N, K):
 
 
 @pytest.mark.parametrize("dtype,V,H,M,K", [(torch.bfloat16, 32000, 512, 61, 2), (torch.bfloat16, 1000, 320, 10, 5),
-                                           (torch.float32, 1024, 256, 17, 4), (torch.bfloat16, 5000, 256, 3, 10)])
+                                           (torch.float32, 1024, 256, 17, 4), (torch.bfloat16, 5000, 256, 3, 10),
+                                           # several 256-row token tiles, the largest K, a ragged last tile
+                                           (torch.bfloat16, 3000, 256, 300, 16), (torch.bfloat16, 2056, 512, 600, 3)])
 def test_lm_head_topk_and_lse(dtype, V, H, M, K):
     """Fused head vs the oracle's top-k / log-sum-exp on the same logits (the GPU GEMM's
     own fp32 logits, so index results must agree bit for bit)."""
@@ -100,6 +102,24 @@ def test_lm_head_topk_and_lse(dtype, V, H, M, K):
         want = topk_ids(logits[r].astype(np.float32), K)
         assert list(ids[r]) == list(want)
         assert np.array_equal(vals[r], logits[r][want].astype(np.float32))
+        assert abs(lse[r] - logsumexp(logits[r])) < 1e-4
+
+
+@pytest.mark.parametrize("M,K", [(7, 8), (260, 16)])
+def test_lm_head_equal_logits_rank_by_id(M, K):
+    """Vocabulary rows repeat every 50 ids, so every logit value occurs 20 times across
+    tiles and quarters of a tile: the kept entries must be the lowest ids of the best
+    values, in value then id order (the oracle's top-k rule)."""
+    g = torch.Generator().manual_seed(21)
+    V, H = 1000, 256
+    X = _rand((M, H), g, torch.bfloat16).to(DEV)
+    W = _rand((50, H), g, torch.bfloat16, 0.05).repeat(V // 50, 1).contiguous().to(DEV)
+    logits = api.gemm(W, X).cpu().double().numpy()
+    ids, vals, lse, _ = api.lm_head(W, X, K)
+    ids, lse = ids.cpu().numpy(), lse.cpu().numpy()
+    for r in range(M):
+        want = topk_ids(logits[r].astype(np.float32), K)
+        assert list(ids[r]) == list(want)
         assert abs(lse[r] - logsumexp(logits[r])) < 1e-4
 
 
