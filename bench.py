@@ -108,14 +108,18 @@ class ClockSampler:
                 if any(r[3].replace(".", "").isdigit() for r in rows) else None}
 
 
-def dist_setup():
+def dist_setup(backend: str = ""):
+    """Rank, world size and local GPU from the torchrun environment; for N > 1 a process
+    group for the timing reductions: NCCL on GPUs, gloo where no GPU is present."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
     return ws, rank, local
 
 
