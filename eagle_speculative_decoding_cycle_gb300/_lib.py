@@ -28,6 +28,7 @@ EXPORTED = [
     "eagle_kv_view", "eagle_kv_table", "eagle_set_static_tree", "eagle_ttt_forward", "eagle_profile_begin", "eagle_profile_end", "eagle_profile_verify", "eagle_last_error", "eagle_destroy",
     "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_gemm_noalloc", "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
     "eagle_op_attention_scratch_bytes", "eagle_op_attention", "eagle_plan_budget", "eagle_op_tree_scratch_bytes", "eagle_op_tree_build", "eagle_op_compact",
+    "eagle_op_wait_probe",
 ]
 
 
@@ -102,6 +103,7 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_op_tree_scratch_bytes": (sz, [i32, i32, i32, i32]),
         "eagle_op_tree_build": (i32, [vp, i32, i32, i32, i32] + [vp] * 15 + [sz]),
         "eagle_op_compact": (i32, [i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32]),
+        "eagle_op_wait_probe": (i32, [vp, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)

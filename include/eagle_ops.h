@@ -120,6 +120,17 @@ int eagle_plan_budget(int n_k, const int32_t* k_values, const float* draft_us, c
                       const float* exp_tokens, int n_points, const int32_t* rows_pts, const float* verify_us,
                       int batch, int32_t* best_k, int32_t* best_m, float* tokens_per_us);
 
+/* Failure-detection probe. Runs one of the library's bounded device waits on a condition
+ * that nothing satisfies and returns once it gives up: kind 0 waits on a shared-memory
+ * mbarrier phase that nobody completes (the wait of the TMA / tensor-core pipelines),
+ * kind 1 waits until the device word *d_counter (caller-owned, zero, nullable for kind 0)
+ * reaches 1 (the wait of the split-tile owner and the layer chain). Each wait stops after
+ * the library's limit of 2 s of %globaltimer and atomically latches 1 (timeout) into *d_err
+ * if it is still 0; *d_result receives 1 if the wait was satisfied, 0 if it gave up. Launches
+ * one CTA on `stream` and returns without synchronising; EAGLE_EINVAL on a bad kind or a
+ * null pointer. */
+int eagle_op_wait_probe(void* stream, int kind, const unsigned* d_counter, int* d_err, int* d_result);
+
 #ifdef __cplusplus
 }
 #endif
