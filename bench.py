@@ -238,9 +238,12 @@ def run_ours(args, ws, rank, local):
     from eagle_speculative_decoding_cycle_gb300.build import build
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    if rank == 0 or ws > 1:
+    # rank 0 compiles (if the sources changed); the other ranks then find its library
+    if rank == 0:
         build()
     barrier(ws)
+    if rank != 0:
+        build()
     wl = synth.WORKLOADS[args.workload]
     if args.planted_p is not None:
         wl = wl.replace(tree=dataclasses.replace(wl.tree, planted_p=args.planted_p))
