@@ -96,6 +96,34 @@ def test_create_rejects_without_touching_gpu(lib):
     assert rc == L.EAGLE_EINVAL
 
 
+def test_injected_create_fault_fails_on_the_host(lib, monkeypatch):
+    """EAGLE_FAULT=create makes a create call that passed every argument check fail with
+    EAGLE_ECUDA before its first CUDA call (placeholder pointers are never dereferenced)."""
+    mc, dc, tc, lim = _cfg(synth.TINY)
+    fake = C.c_void_p(256)
+    layers = (L.LayerWeights * mc.n_layers)()
+    for lw in layers:
+        for name, _ in L.LayerWeights._fields_:
+            setattr(lw, name, fake)
+    w = L.Weights()
+    for name in ("embed", "lm_head", "final_norm", "fc", "norm_g", "norm_e"):
+        setattr(w, name, fake)
+    w.layers = layers
+    for name, _ in L.LayerWeights._fields_:
+        setattr(w.draft, name, fake)
+    need = lib.eagle_workspace_bytes(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(lim))
+    assert need > 0
+    monkeypatch.setenv("EAGLE_FAULT", "create")
+    h = C.c_void_p()
+    rc = lib.eagle_create(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(w), C.byref(lim), fake, need, None,
+                          C.byref(h))
+    assert rc == L.EAGLE_ECUDA and not h.value
+    # a workspace one byte short is refused first, fault or not
+    rc = lib.eagle_create(C.byref(mc), C.byref(dc), C.byref(tc), C.byref(w), C.byref(lim), fake, need - 1, None,
+                          C.byref(h))
+    assert rc == L.EAGLE_ECAPACITY and not h.value
+
+
 def test_op_scratch_sizes(lib):
     assert lib.eagle_op_gemm_scratch_bytes(61, 12288) > 0
     assert lib.eagle_op_gemm_scratch_bytes(0, 10) == 0
