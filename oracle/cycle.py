@@ -131,6 +131,10 @@ class OracleSeq:
 
     # -- prefill ---------------------------------------------------------------
     def prefill(self, prompt: Sequence[int], R: Optional[Sequence[int]] = None):
+        """Prefill (the EAGLE-2 page, table "Putting It Together", before step 1): the target
+        over the prompt gives the first committed token and the features; the drafter runs
+        over the prompt positions and its last output gives the root's depth-1 candidates.
+        R: the reference continuation for planted mode, or None."""
         prompt = np.asarray(prompt, dtype=np.int64)
         n = len(prompt)
         self.R = None if R is None else np.asarray(R, dtype=np.int64)
@@ -149,6 +153,10 @@ class OracleSeq:
 
     # -- one cycle -------------------------------------------------------------
     def draft_and_verify(self) -> Plan:
+        """Steps 1-3 of one cycle: grow the draft tree (EAGLE-2 page, "Path Value Ranks
+        Prefixes, Not Isolated Tokens": expand the top-k nodes by path value per depth),
+        keep the top-m, flatten with the ancestry mask, and run the target once over the
+        tree rows ("The Mask Preserves Tree Semantics in One Target Pass")."""
         t, n = self.t, self.n
         k, D = t.topk, t.depth
         table = NodeTable()
@@ -218,6 +226,9 @@ class OracleSeq:
         return sample_walk(flat, p_child, uni, bonus, dtype=np.float64)
 
     def commit(self, plan: Plan, path: List[int], bonus: int) -> List[int]:
+        """Steps 4-5: copy the accepted rows' KV into their final slots, commit the path and
+        the bonus token, and run the drafter over the committed rows (features of the root
+        and the path) to get the next root's candidates. Returns the committed tokens."""
         n, flat = self.n, plan.flat
         L = len(path)
         compact(self.kv.k, self.kv.v, n, path)
@@ -240,6 +251,7 @@ class OracleSeq:
         return new_tokens
 
     def cycle(self) -> List[int]:
+        """One draft-and-verify cycle: tree, verify, acceptance walk, commit."""
         plan = self.draft_and_verify()
         path, bonus = self.decide(plan)
         return self.commit(plan, path, bonus)
@@ -303,4 +315,5 @@ def plain_decode(model: Model, wl, prompt: Sequence[int], steps: int, seq: int =
 
 
 def build_model(weights_np: Dict[str, np.ndarray], wl) -> Model:
+    """The oracle model of a workload from float32 copies of its weights."""
     return Model(weights_np, wl.model, wl.drafter.kind, wl.drafter.fuse_layers)

@@ -40,10 +40,12 @@ def bf16_round(x) -> np.ndarray:
 
 
 def f32_round(x) -> np.ndarray:
+    """Round to float32 and back (a rounding point of the fp32 model)."""
     return np.asarray(x, dtype=np.float32).astype(np.float64)
 
 
 def no_round(x) -> np.ndarray:
+    """No rounding: float64 as is."""
     return np.asarray(x, dtype=np.float64)
 
 
@@ -54,11 +56,14 @@ def quantizer(dtype: str):
 
 
 def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of the last axis: x / sqrt(mean(x^2) + eps) * g (Llama-style target layers,
+    "EAGLE 三代" page §2.3)."""
     x = np.asarray(x, dtype=np.float64)
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * g
 
 
 def silu(x: np.ndarray) -> np.ndarray:
+    """SiLU, x * sigmoid(x), the SwiGLU MLP's gate activation."""
     return x / (1.0 + np.exp(-x))
 
 
@@ -76,6 +81,8 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
 
 
 def logsumexp(v: np.ndarray, axis=-1) -> np.ndarray:
+    """log sum exp along `axis`, shifted by the maximum (the softmax normaliser behind each
+    draft confidence log c = logit - lse)."""
     mx = np.max(v, axis=axis, keepdims=True)
     return (mx + np.log(np.sum(np.exp(v - mx), axis=axis, keepdims=True))).squeeze(axis)
 
@@ -195,6 +202,8 @@ class Model:
         return f, capl
 
     def logits(self, f: np.ndarray) -> np.ndarray:
+        """The shared LM head over features f ("EAGLE: Feature-Level Drafting", "The big idea:
+        draft at the feature level": one matrix, then softmax)."""
         return mm(f, self.W["lm_head"])
 
     # -- drafter ------------------------------------------------------------------

@@ -52,6 +52,7 @@ def philox4x32_10(ctr, key):
 
 
 def key_of(seed: int):
+    """The Philox4x32 key (two 32-bit words, low word first) of a 64-bit seed."""
     return np.array([seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF], dtype=np.uint64)
 
 

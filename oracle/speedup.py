@@ -17,8 +17,10 @@ use this package.
 
 
 def expected_tokens(alpha: float, k: int) -> float:
+    """1 + alpha + ... + alpha^k: expected committed tokens per verify pass of a k-draft chain."""
     return sum(alpha ** i for i in range(k + 1))
 
 
 def speedup(alpha: float, k: int, draft_cost: float) -> float:
+    """expected_tokens / (1 + k * draft_cost), draft_cost = one draft pass relative to one target pass."""
     return expected_tokens(alpha, k) / (1.0 + k * draft_cost)

@@ -122,6 +122,10 @@ class FlatTree:
 
 
 def flatten(t: NodeTable, kept: Sequence[int], root_token: int) -> FlatTree:
+    """The verify rows of a kept node set: the root at row 0, then the kept nodes in generation
+    order (parents before children), each with its token, parent row, depth and ancestry mask
+    (self, its ancestors and the root; EAGLE-2 page, "The Mask Preserves Tree Semantics in One
+    Target Pass")."""
     order = sorted(kept)                      # generation order: parents precede children
     row_of = {node: r + 1 for r, node in enumerate(order)}
     n = len(order) + 1
@@ -230,5 +234,7 @@ def chain_topology(depth: int):
 
 
 def is_ancestor_closed(t: NodeTable, kept: Sequence[int]) -> bool:
+    """Every kept node's parent is kept or is the root (the closure the EAGLE lesson states for
+    the top-m rerank)."""
     s = set(kept)
     return all(t.parent[i] < 0 or t.parent[i] in s for i in kept)
