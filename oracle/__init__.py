@@ -14,8 +14,9 @@ compaction), cycle (prefill, cycle, plain decode, planted mode), speedup (the
 tokens-per-step model).
 
 Parity status: every function is pinned by a test against what the pages or
-mathematics fix (tests/test_oracle_*.py), except the drafter's numeric values
-beyond its layer math: the drafter wiring (feature pre/post norm, concat order,
-EAGLE-3 combination) is a reading of the pages and has no external value to be
-pinned against -- parity unpinned for those wiring choices.
+mathematics fix (tests/test_oracle_*.py). The drafter's wiring (which feature and
+which token feed a drafter position, which target layers EAGLE-3 fuses, and the
+substitution of the drafter's own output below the root) is pinned by constructed
+weights that reduce the drafter to an identity on one input, so its candidates follow
+from the target alone (tests/test_oracle_wiring.py).
 """
