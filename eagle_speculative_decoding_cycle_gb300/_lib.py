@@ -17,8 +17,8 @@ EAGLE_OK, EAGLE_EINVAL, EAGLE_ECAPACITY, EAGLE_ECUDA, EAGLE_EDEVICE, EAGLE_ETIME
 STATUS_NAMES = {0: "EAGLE_OK", -1: "EAGLE_EINVAL", -2: "EAGLE_ECAPACITY", -3: "EAGLE_ECUDA",
                 -4: "EAGLE_EDEVICE", -5: "EAGLE_ETIMEOUT", -6: "EAGLE_EUNSUPPORTED"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
-DUMP_STATE, DUMP_CAND, DUMP_NODES, DUMP_TREE, DUMP_ACCEPT, DUMP_VERIFY_HEAD, DUMP_VERIFY_LOGITS, DUMP_FEATURES = \
-    range(8)
+DUMP_STATE, DUMP_CAND, DUMP_NODES, DUMP_TREE, DUMP_ACCEPT, DUMP_VERIFY_HEAD, DUMP_VERIFY_LOGITS, DUMP_FEATURES, \
+    DUMP_TTT = range(9)
 DEBUG_LOGITS = 1
 
 # every symbol the headers declare (checked by the CPU test suite)
@@ -26,7 +26,8 @@ EXPORTED = [
     "eagle_workspace_bytes", "eagle_create", "eagle_prefill", "eagle_cycle", "eagle_decode_plain",
     "eagle_set_graph", "eagle_cycle_kernel_launches", "eagle_status_sync", "eagle_dump_bytes", "eagle_debug_dump", "eagle_set_debug",
     "eagle_kv_view", "eagle_kv_table", "eagle_set_static_tree", "eagle_ttt_forward", "eagle_profile_begin", "eagle_profile_end", "eagle_profile_verify", "eagle_last_error", "eagle_destroy",
-    "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_gemm_noalloc", "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
+    "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_gemm_noalloc", "eagle_op_gemm_noalloc_status",
+    "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
     "eagle_op_attention_scratch_bytes", "eagle_op_attention", "eagle_plan_budget", "eagle_op_tree_scratch_bytes", "eagle_op_tree_build", "eagle_op_compact",
     "eagle_op_wait_probe",
 ]
@@ -94,6 +95,7 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_op_gemm_scratch_bytes": (sz, [i32, i32]),
         "eagle_op_gemm": (i32, [i32, vp, vp, i32, i32, vp, i32, i32, vp, i32, vp, sz]),
         "eagle_op_gemm_noalloc": (i32, [vp, vp, i32, i32, vp, i32, i32, vp, i32]),
+        "eagle_op_gemm_noalloc_status": (i32, [vp]),
         "eagle_op_lm_head_scratch_bytes": (sz, [i32, i32, i32, i32]),
         "eagle_op_lm_head": (i32, [i32, vp, vp, i32, i32, vp, i32, i32, f32, i32, i32, vp, i32, vp, vp, vp, u32,
                                    u64, i32, vp, vp, vp, vp, sz]),

@@ -196,6 +196,12 @@ class Engine:
         if what == L.DUMP_FEATURES:
             dt = torch.float32 if self.w.model.dtype == "f32" else torch.bfloat16
             return raw.view(dt).view(B * T1, self.w.model.hidden)
+        if what == L.DUMP_TTT:
+            H = self.w.model.hidden
+            es = 4 if self.w.model.dtype == "f32" else 2
+            R = raw.numel() // (H * es + 4)
+            dt = torch.float32 if es == 4 else torch.bfloat16
+            return raw[:R * H * es].view(dt).view(R, H), f32(R * H * es, raw.numel())
         raise ValueError(what)
 
     def close(self) -> None:

@@ -47,7 +47,7 @@ __device__ __forceinline__ void rope_pair(float a, float b, float c, float s, fl
 }
 // SwiGLU gate: silu(g) * u.
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.f, expf(-g))), u); }
-// bf16 paths (row kernel, GEMM epilogue, layer chain): the same product with the fast
+// bf16 paths (row kernel, GEMM epilogue): the same product with the fast
 // exponential and divide; their relative error (~1e-6) is far below bf16 rounding. For
 // g < -87 the denominator overflows and the result is 0, the limit of silu.
 __device__ __forceinline__ float silu_mul_bf16(float g, float u) {

@@ -18,7 +18,6 @@
 #include "../../include/eagle.h"
 #include "common.cuh"
 #include "cycle.h"
-#include "chain.h"
 #include "kernels.h"
 #include "lmhead.cuh"
 
@@ -162,8 +161,6 @@ struct eagle_ctx {
   float *v_val, *v_lse, *v_spec, *v_logits; int* v_id;       // verify head (kept for the cycle's dump)
   float* gemm_part; int* gemm_cnt; int gemm_cnt_len;
   float *attn_po, *attn_pml; size_t attn_pfloats;
-  unsigned* chain_bar;                  // grid-barrier words of the layer-chain kernel
-  int use_chain = 0;                    // bf16: run each layer as chain launches (EAGLE_CHAIN=1 turns them on)
   // bf16 fused epilogues: -1 (default) SwiGLU in the gate/up epilogue from 128 rows on, where
   // the separate SwiGLU pass costs more than the epilogue work; 1 (EAGLE_FUSE_EPI=1) also
   // RoPE/KV write in the QKV epilogue, at every row count; 0 (EAGLE_FUSE_EPI=0) none. Both
@@ -176,6 +173,8 @@ struct eagle_ctx {
   std::vector<int> h_static_exp, h_static_keep;
   int* ttt_tgt;       // training-time test: the target token of each row
   float* ttt_acc;     // training-time test: running loss sum
+  float* ttt_ce;      // training-time test: the last step's per-row cross-entropy
+  int ttt_rows = 0;   // rows of the last training-time-test step (0: none run yet)
   int* kv_table;      // paged target KV: [B][tab_w] physical block per logical block, -1 = none
   int* kv_next;       // next free block of the pool (one device counter)
   KvPage page;        // the target cache's addressing (table == nullptr: contiguous)
@@ -238,9 +237,9 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
     x->attn_po = c.take<float>(x->attn_pfloats);
     x->attn_pml = c.take<float>((size_t)16 * rs * z.nq * 2);
   }
-  x->chain_bar = c.take<unsigned>(4);
   x->ttt_tgt = c.take<int>(std::max(z.Rd, z.Rt));
   x->ttt_acc = c.take<float>(4);
+  x->ttt_ce = c.take<float>(std::max(z.Rd, z.Rt));
   x->static_exp = c.take<int>(std::max(1, (z.D - 1) * z.k));
   x->static_keep = c.take<int>(z.NG);
   x->kv_table = c.take<int>(std::max(1, z.nblk));
@@ -374,135 +373,12 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   return 0;
 }
 
-// ---- layer chains (bf16): each launch runs the steps between two attentions ---------------------
-// The chain's vectorised row ops need head_dim % 8 == 0, ffn % 4 == 0 (bf16 sizes are
-// already multiples of 8) and rows of at most 5120 features; other shapes run per-op.
-bool chained(const eagle_ctx* ctx) {
-  return ctx->z.dt == DT_BF16 && ctx->use_chain && !ctx->page.table && ctx->z.d % 8 == 0 && ctx->z.F % 4 == 0 && ctx->z.H <= 5120;
-}
-
-ChainProgram chain_prog(eagle_ctx* ctx, int M) {
-  ChainProgram p;
-  p.M = M;
-  p.partials = ctx->gemm_part;
-  p.counters = ctx->gemm_cnt;
-  p.counters_len = ctx->gemm_cnt_len;
-  p.bar = ctx->chain_bar;
-  p.err = ctx->dev_err;
-  return p;
-}
-
-// Bytes a chain step must move (weights, activations read and written).
-double chain_step_bytes(const ChainStep& s, const ChainProgram& p, int M) {
-  switch (s.kind) {
-    case CH_GEMM: {
-      const double ob = (double)M * s.N * (s.epi == EPI_BF16 ? 2 : 4) * (s.epi == EPI_ADD_F32 ? 2 : 1);
-      return (double)s.N * s.K * 2 + (double)M * s.K * 2 + ob;
-    }
-    case CH_RMSNORM: return (double)M * s.H * ((s.in_bf16 ? 2 : 4) + 2) + s.H * 2.0;
-    case CH_SWIGLU: return (double)M * s.H * (8 + 2);
-    case CH_ROPE: return (double)M * (p.args.rope.nq + 2 * p.args.rope.nkv) * p.args.rope.d * (4 + 2);
-    case CH_CONVERT: return (double)M * s.H * (4 + 2);
-    case CH_EMBED: return (double)M * s.H * (2 + 4);
-    case CH_CONCAT: return (double)M * 2 * s.H * (2 + 2);
-  }
-  return 0.0;
-}
-
-int run_chain(eagle_ctx* ctx, ChainProgram& p) {
-  const bool prof = ctx->prof_on && 2 * (ctx->prof_n + 1) <= (int)ctx->prof_ev.size();
-  if (prof) cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n], ctx->st);
-  const int r = chain_run(ctx->st, p);
-  if (r) return fail(ctx, EAGLE_ECUDA, "layer chain launch failed (" + std::to_string(r) + ")");
-  if (prof) {
-    cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n + 1], ctx->st);
-    double b = 0.0;
-    for (int s = 0; s < p.nsteps; ++s) b += chain_step_bytes(p.args.s[s], p, p.M);
-    ctx->prof_bytes[ctx->prof_n] = b;
-    ++ctx->prof_n;
-  }
-  return 0;
-}
-
-void add_rmsnorm(ChainProgram& p, const void* in, int in_bf16, int ldi, const void* g, int H, float eps, void* out,
-                 int ldo) {
-  ChainStep& s = p.add(CH_RMSNORM);
-  s.in = in; s.in_bf16 = in_bf16; s.ldi = ldi; s.aux = g; s.H = H; s.eps = eps; s.out = out; s.ldo = ldo;
-}
-
-void add_convert(ChainProgram& p, const float* in, int H, void* out, int ldo) {
-  ChainStep& s = p.add(CH_CONVERT);
-  s.in = in; s.ldi = H; s.H = H; s.out = out; s.ldo = ldo;
-}
-
-// QKV projection of ain [R][kin] and the rotary embedding / KV-cache write.
-void add_qkv(ChainProgram& p, eagle_ctx* ctx, const eagle_layer_weights& lw, int kin, void* kcache, void* vcache,
-             int cap, const int* pos, const int* slot, const int* seq) {
-  const Dims& z = ctx->z;
-  p.add_gemm(lw.wqkv, z.QKV, kin, ctx->ain, EPI_F32, ctx->qkv, z.QKV);
-  p.add(CH_ROPE);
-  ChainRope& r = p.args.rope;
-  r.qkv = ctx->qkv; r.nq = z.nq; r.nkv = z.nkv; r.d = z.d; r.cap = cap;
-  r.pos = pos; r.slot = slot; r.seq = seq; r.cos = ctx->rope_cos; r.sin = ctx->rope_sin;
-  r.q = ctx->qb; r.kc = kcache; r.vc = vcache;
-}
-
-// Output projection (+ residual), MLP RMSNorm, gate/up, SwiGLU, down (+ residual).
-void add_post(ChainProgram& p, eagle_ctx* ctx, const eagle_layer_weights& lw) {
-  const Dims& z = ctx->z;
-  p.add_gemm(lw.wo, z.H, z.A, ctx->att, EPI_ADD_F32, ctx->x, z.H);
-  add_rmsnorm(p, ctx->x, 0, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, ctx->ain, z.H);
-  p.add_gemm(lw.wgu, 2 * z.F, z.H, ctx->ain, EPI_F32, ctx->gu, 2 * z.F);
-  ChainStep& sw = p.add(CH_SWIGLU);
-  sw.in = ctx->gu; sw.H = z.F; sw.out = ctx->hb;
-  p.add_gemm(lw.wd, z.H, z.F, ctx->hb, EPI_ADD_F32, ctx->x, z.H);
-}
-
-int target_forward_chain(eagle_ctx* ctx, int R, const int* tok, const int* pos, const int* slot, const int* seq,
-                         int rows_per_seq, int mode, int tree_T, const uint64_t* mask, int mask_words, void* feat_out,
-                         void* caps_out, size_t caps_ld, size_t caps_row0) {
-  const Dims& z = ctx->z;
-  const size_t lstride = z.kv_layer_elems * z.esz;
-  auto kc = [&](int l) { return (void*)((uint8_t*)ctx->kc + l * lstride); };
-  auto vc = [&](int l) { return (void*)((uint8_t*)ctx->vc + l * lstride); };
-  ChainProgram p = chain_prog(ctx, R);
-  ChainStep& e = p.add(CH_EMBED);
-  e.aux = ctx->w.embed; e.V = z.V; e.H = z.H; e.idx = tok; e.out = ctx->x;
-  add_rmsnorm(p, ctx->x, 0, z.H, ctx->layers[0].attn_norm, z.H, ctx->mc.rms_eps, ctx->ain, z.H);
-  add_qkv(p, ctx, ctx->layers[0], z.H, kc(0), vc(0), z.cap, pos, slot, seq);
-  int r = run_chain(ctx, p);
-  if (r) return r;
-  for (int l = 0; l < z.L; ++l) {
-    r = attend(ctx, kc(l), vc(l), z.cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words, ctx->page);
-    if (r) return r;
-    p = chain_prog(ctx, R);
-    add_post(p, ctx, ctx->layers[l]);
-    if (z.kind == 3 && caps_out) {
-      for (int j = 0; j < 3; ++j)
-        if (ctx->dc.fuse_layers[j] == l)
-          add_convert(p, ctx->x, z.H, (uint8_t*)caps_out + ((size_t)j * caps_ld + caps_row0) * z.H * z.esz, z.H);
-    }
-    if (l + 1 < z.L) {
-      add_rmsnorm(p, ctx->x, 0, z.H, ctx->layers[l + 1].attn_norm, z.H, ctx->mc.rms_eps, ctx->ain, z.H);
-      add_qkv(p, ctx, ctx->layers[l + 1], z.H, kc(l + 1), vc(l + 1), z.cap, pos, slot, seq);
-    } else {
-      add_rmsnorm(p, ctx->x, 0, z.H, ctx->w.final_norm, z.H, ctx->mc.rms_eps, feat_out, z.H);
-    }
-    r = run_chain(ctx, p);
-    if (r) return r;
-  }
-  return 0;
-}
-
 // Target forward over R rows: features (rounded final-norm output) into feat_out [R][H],
 // EAGLE-3 captures into caps_out [3][caps_ld][H] (rows at offset caps_row0).
 int target_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const int* slot, const int* seq,
                    int rows_per_seq, int mode, int tree_T, const uint64_t* mask, int mask_words, void* feat_out,
                    void* caps_out, size_t caps_ld, size_t caps_row0) {
   const Dims& z = ctx->z;
-  if (chained(ctx))
-    return target_forward_chain(ctx, R, tok, pos, slot, seq, rows_per_seq, mode, tree_T, mask, mask_words, feat_out,
-                                caps_out, caps_ld, caps_row0);
   CK(embed_rows(ctx->st, z.dt, ctx->w.embed, z.V, z.H, tok, R, ctx->x, ctx->dev_err));
   const size_t lstride = z.kv_layer_elems * z.esz;
   for (int l = 0; l < z.L; ++l) {
@@ -542,42 +418,21 @@ int drafter_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const
   const Dims& z = ctx->z;
   const eagle_layer_weights& lw = ctx->w.draft;
   const size_t rb = (size_t)z.H * z.esz;
-  const bool ch = chained(ctx);
-  ChainProgram p = chain_prog(ctx, R);
   int kin;
   if (z.kind == 1) {
-    if (ch) {
-      ChainStep& c = p.add(CH_CONCAT);
-      c.aux = ctx->w.embed; c.V = z.V; c.H = z.H; c.idx = tok; c.in = feat; c.idx2 = feat_row; c.out = ctx->ain;
-      p.add_gemm(ctx->w.fc, z.H, 2 * z.H, ctx->ain, EPI_F32, ctx->x, z.H);
-      add_rmsnorm(p, ctx->x, 0, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, ctx->ain, z.H);
-    } else {
-      CK(concat_emb_feat(ctx->st, z.dt, ctx->w.embed, z.V, z.H, tok, feat, feat_row, R, ctx->ain, ctx->dev_err));
-      CK(gemm(ctx, ctx->w.fc, z.H, 2 * z.H, ctx->ain, R, EPI_F32, ctx->x, z.H));
-      CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
-    }
+    CK(concat_emb_feat(ctx->st, z.dt, ctx->w.embed, z.V, z.H, tok, feat, feat_row, R, ctx->ain, ctx->dev_err));
+    CK(gemm(ctx, ctx->w.fc, z.H, 2 * z.H, ctx->ain, R, EPI_F32, ctx->x, z.H));
+    CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
     kin = z.H;
   } else {
     if (feat != ctx->gbuf || feat_row)
       CK(gather_rows(ctx->st, rb, feat, rb, feat_row, R, ctx->gbuf, rb));
     CK(widen_rows(ctx->st, z.dt, ctx->gbuf, z.H, z.H, R, ctx->x));
     CK(rmsnorm_rows(ctx->st, z.dt, ctx->gbuf, z.H, ctx->w.norm_g, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, 2 * z.H));
-    CK(gather_rows(ctx->st, rb, ctx->w.embed, rb, tok, R, ctx->ebuf, rb));
+    CK(gather_rows(ctx->st, rb, ctx->w.embed, rb, tok, R, ctx->ebuf, rb, nullptr, z.V, ctx->dev_err));
     CK(rmsnorm_rows(ctx->st, z.dt, ctx->ebuf, z.H, ctx->w.norm_e, z.H, ctx->mc.rms_eps, R, z.dt,
                     (uint8_t*)ctx->ain + rb, 2 * z.H));
     kin = 2 * z.H;
-  }
-  if (ch) {
-    add_qkv(p, ctx, lw, kin, ctx->dkc, ctx->dvc, z.dcap, pos, slot, seq);
-    int r = run_chain(ctx, p);
-    if (r) return r;
-    r = attend(ctx, ctx->dkc, ctx->dvc, z.dcap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words,
-               KvPage{nullptr, 0, 0});
-    if (r) return r;
-    p = chain_prog(ctx, R);
-    add_post(p, ctx, lw);
-    add_convert(p, ctx->x, z.H, ctx->dout, z.H);
-    return run_chain(ctx, p);
   }
   int r = layer_forward(ctx, lw, R, ctx->ain, kin, ctx->dkc, ctx->dvc, z.dcap, rows_per_seq, pos, slot, seq, mode,
                         tree_T, mask, mask_words, KvPage{nullptr, 0, 0});
@@ -686,12 +541,17 @@ __global__ void ttt_rows_k(const int* x, int n, int s, int R, int* tok, int* pos
   tgt[t] = x[t + s + 1];
 }
 
-// acc[0] += sum over rows of (lse - logit of the target), in a fixed order; one block.
-__global__ void ttt_loss_acc_k(const float* lse, const float* tgt_logit, int rows, float* acc, int reset) {
+// ce[i] = lse - logit of the target for each row; acc[0] += their sum, in a fixed order;
+// one block.
+__global__ void ttt_loss_acc_k(const float* lse, const float* tgt_logit, int rows, float* acc, int reset, float* ce) {
   PDL_ENTRY();
   __shared__ float red[256];
   float v = 0.f;
-  for (int i = threadIdx.x; i < rows; i += blockDim.x) v += lse[i] - tgt_logit[i];
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+    const float c = lse[i] - tgt_logit[i];
+    ce[i] = c;
+    v += c;
+  }
   red[threadIdx.x] = v;
   __syncthreads();
   for (int o = blockDim.x / 2; o > 0; o >>= 1) {
@@ -924,7 +784,6 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
   ctx->layers.assign(weights->layers, weights->layers + model->n_layers);
   ctx->w.layers = ctx->layers.data();
   ctx->st = reinterpret_cast<cudaStream_t>(stream);
-  if (getenv("EAGLE_CHAIN")) ctx->use_chain = strcmp(getenv("EAGLE_CHAIN"), "0") != 0;
   if (getenv("EAGLE_FUSE_EPI")) ctx->fuse_epi = strcmp(getenv("EAGLE_FUSE_EPI"), "0") != 0;
   Carver c;
   c.base = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(workspace), 256));
@@ -978,10 +837,6 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
   }
   ctx->batch = batch;
   ctx->ref_len = d_ref ? ref_len : 0;
-  // barrier words of the layer chain start from zero (a launch that gave up on an error
-  // may have left them inconsistent)
-  if (cudaMemsetAsync(ctx->chain_bar, 0, 4 * sizeof(unsigned), ctx->st) != cudaSuccess)
-    return fail(ctx, EAGLE_ECUDA, "memset failed");
   fill_cd(ctx);
   ctx->cd.ref = d_ref;
   ctx->cd.ref_len = ctx->ref_len;
@@ -1239,6 +1094,7 @@ size_t eagle_dump_bytes(const eagle_ctx* ctx, int what) {
     }
     case EAGLE_DUMP_VERIFY_LOGITS: return B * z.T1 * (size_t)z.V * 4;
     case EAGLE_DUMP_FEATURES: return B * z.T1 * (size_t)z.H * z.esz;
+    case EAGLE_DUMP_TTT: return (size_t)ctx->ttt_rows * ((size_t)z.H * z.esz + 4);
   }
   return 0;
 }
@@ -1277,6 +1133,10 @@ int eagle_debug_dump(eagle_ctx* ctx, int what, void* dst, size_t bytes) {
     }
     case EAGLE_DUMP_VERIFY_LOGITS: cp(ctx->v_logits, B * z.T1 * (size_t)z.V * 4); break;
     case EAGLE_DUMP_FEATURES: cp(ctx->feat_t, B * z.T1 * (size_t)z.H * z.esz); break;
+    case EAGLE_DUMP_TTT:
+      cp(ctx->dout, (size_t)ctx->ttt_rows * z.H * z.esz);
+      cp(ctx->ttt_ce, (size_t)ctx->ttt_rows * 4);
+      break;
   }
   return cudaGetLastError() == cudaSuccess ? EAGLE_OK : fail(ctx, EAGLE_ECUDA, "dump copy failed");
 }
@@ -1364,6 +1224,7 @@ int eagle_ttt_forward(eagle_ctx* ctx, const int32_t* d_tokens, int n, int steps,
     return fail(ctx, EAGLE_ECAPACITY, "sequence too long for the training-time test in this context");
   if (ctx->graph) { cudaGraphExecDestroy(ctx->graph); ctx->graph = nullptr; }
   ctx->host_ctx_bound = z.max_ctx;   // the cycle state is gone until the next prefill
+  ctx->ttt_rows = 0;
   const size_t rb = (size_t)z.H * z.esz;
   // target pass (causal), features of every position
   CK(kv_reserve(ctx, 0, 1, nullptr, 0, n));
@@ -1403,8 +1264,9 @@ int eagle_ttt_forward(eagle_ctx* ctx, const int32_t* d_tokens, int n, int steps,
       r = lm_head(ctx, (const uint8_t*)ctx->dout + (size_t)r0 * rb, rows, p);
       if (r) return r;
       launch_k(ttt_loss_acc_k, 1, 256, 0, ctx->st, (const float*)ctx->h_lse, (const float*)ctx->h_spec, rows,
-               ctx->ttt_acc, r0 == 0 ? 1 : 0);
+               ctx->ttt_acc, r0 == 0 ? 1 : 0, ctx->ttt_ce + r0);
     }
+    ctx->ttt_rows = R;
     launch_k(ttt_loss_fin_k, 1, 32, 0, ctx->st, (const float*)ctx->ttt_acc, R, d_loss + (s - 1));
     if (cudaGetLastError() != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "training-time-test launch failed");
   }

@@ -26,12 +26,17 @@ constexpr int kNoallocMaxTiles = 8192;
 // sums to the CTA that finishes it (32 KiB).
 static __device__ __align__(256) float g_noalloc_partials[kNoallocMaxCtas * 2 * kNoallocMaxRows * 128];
 static __device__ __align__(256) int g_noalloc_tickets[kNoallocMaxTiles];
+// Status word: a bounded device wait that gives up (a split tile whose partial sums never
+// arrive) records the timeout here instead of returning silently. It is sticky across
+// calls until eagle_op_gemm_noalloc_status reads and clears it.
+static __device__ __align__(256) int g_noalloc_status[4];
 
 namespace {
 
 struct DeviceScratch {
   float* partials = nullptr;
   int* tickets = nullptr;
+  int* status = nullptr;
   bool ready = false;
 };
 constexpr int kMaxDevices = 64;
@@ -48,10 +53,15 @@ int scratch_for_current_device(DeviceScratch** out) {
   if (!s.ready) {
     void* p = nullptr;
     void* t = nullptr;
+    void* e = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess) return EAGLE_ECUDA;
     if (cudaGetSymbolAddress(&t, g_noalloc_tickets) != cudaSuccess) return EAGLE_ECUDA;
+    if (cudaGetSymbolAddress(&e, g_noalloc_status) != cudaSuccess) return EAGLE_ECUDA;
+    // the status word starts at zero on every device (a blocking clear, once, at set-up)
+    if (cudaMemset(e, 0, sizeof(g_noalloc_status)) != cudaSuccess) return EAGLE_ECUDA;
     s.partials = static_cast<float*>(p);
     s.tickets = static_cast<int*>(t);
+    s.status = static_cast<int*>(e);
     s.ready = true;
   }
   *out = &s;
@@ -76,7 +86,22 @@ extern "C" int eagle_op_gemm_noalloc(void* stream, const void* W, int N, int K, 
   // the tickets must start at zero; a completed call leaves them at zero, but an
   // abandoned one (device timeout) may not, so clear the ones this call uses
   if (cudaMemsetAsync(s->tickets, 0, (size_t)tiles * sizeof(int), st) != cudaSuccess) return EAGLE_ECUDA;
-  const int r = gemm_bf16(st, W, N, K, X, M, epi, out, ldo, s->partials, s->tickets, (int)tiles, nullptr, nullptr,
+  const int r = gemm_bf16(st, W, N, K, X, M, epi, out, ldo, s->partials, s->tickets, (int)tiles, s->status, nullptr,
                           /*cache_maps=*/false);
   return r == 0 ? EAGLE_OK : (r == -4 ? EAGLE_ECUDA : EAGLE_EINVAL);
+}
+
+extern "C" int eagle_op_gemm_noalloc_status(void* stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceScratch* s = nullptr;
+  const int rc = scratch_for_current_device(&s);
+  if (rc != EAGLE_OK) return rc;
+  int h = 0;
+  if (cudaMemcpyAsync(&h, s->status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return EAGLE_ECUDA;
+  if (h == 0) return EAGLE_OK;
+  if (cudaMemsetAsync(s->status, 0, sizeof(int), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return EAGLE_ECUDA;
+  return h == DEVERR_MBAR_TIMEOUT ? EAGLE_ETIMEOUT : EAGLE_EDEVICE;
 }

@@ -28,6 +28,8 @@
 
 #include <cstdio>
 #include <map>
+#include <mutex>
+#include <set>
 #include <tuple>
 
 #include "common.cuh"
@@ -507,8 +509,10 @@ static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long 
                      bool use_cache = true, long long ld = 0) {
   if (ld <= 0) ld = K;
   static std::map<std::tuple<const void*, long long, long long, int, long long>, CUtensorMap> cache;
+  static std::mutex mu;
   auto key = std::make_tuple(ptr, rows, K, box_rows, ld);
   if (use_cache) {
+    std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) { *m = it->second; return true; }
   }
@@ -523,6 +527,7 @@ static bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long 
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   if (!use_cache) return true;
+  std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache[key] = *m;
   return true;
@@ -532,16 +537,39 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, long long K
   return make_map(m, ptr, rows, K, box_rows, true, ld);
 }
 
-static int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+// Host caches kept per device: a process may drive several GPUs, each with its own SM
+// count and its own per-function attributes.
+constexpr int kMaxDevices = 64;
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int n[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!n[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    n[dev] = v;
   }
-  return n;
+  return n[dev];
 }
+
+cudaError_t raise_smem_limit(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::tuple<int, const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(dev, func, bytes);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
+}
+
+static int num_sms() { return device_sm_count(); }
 
 int gemm_bn_for(int M) {
   if (M <= 16) return 16;
@@ -557,13 +585,8 @@ template <int BN, int MODE>
 static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int tiles_n,
                              cudaStream_t st) {
   using C = TcCfg<BN>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_bf16_tc<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemm_bf16_tc<BN, MODE>), C::SMEM);
+  if (e != cudaSuccess) return e;
   a.tiles_t = (a.M + BN - 1) / BN;
   a.kb = (a.K + 63) / 64;
   int G = num_sms();

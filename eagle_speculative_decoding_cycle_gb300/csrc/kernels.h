@@ -49,6 +49,10 @@ struct QkvEpi {
 enum { DT_F32 = 0, DT_BF16 = 1 };
 
 inline int num_sms_cap() { return 192; }
+// SM count of the current device (cached per device).
+int device_sm_count();
+// Raise a kernel's dynamic shared-memory limit on the current device (once per device).
+cudaError_t raise_smem_limit(const void* func, int bytes);
 
 // ---- GEMMs -------------------------------------------------------------------------------
 int gemm_bn_for(int M);
@@ -102,8 +106,10 @@ int swiglu_rows(cudaStream_t st, int dtype, const float* gu, int F, int R, void*
 int concat_emb_feat(cudaStream_t st, int dtype, const void* E, int V, int H, const int* tok,
                     const void* feat, const int* feat_row, int R, void* out, int* err);
 int convert_rows(cudaStream_t st, int dtype, const float* x, int H, int R, void* out, int ldo);
+// dst row (dst_idx ? dst_idx[r] : r) <- src row (idx ? idx[r] : r). With src_rows > 0 a source
+// index outside [0, src_rows) is latched into *err (DEVERR_BOUNDS) and its row skipped.
 int gather_rows(cudaStream_t st, size_t row_bytes, const void* src, size_t src_ld, const int* idx, int R,
-                void* dst, size_t dst_ld, const int* dst_idx = nullptr);
+                void* dst, size_t dst_ld, const int* dst_idx = nullptr, int src_rows = 0, int* err = nullptr);
 int widen_rows(cudaStream_t st, int dtype, const void* x, int ldx, int H, int R, float* out);
 
 // ---- attention -----------------------------------------------------------------------------

@@ -334,10 +334,15 @@ int convert_rows(cudaStream_t st, int dtype, const float* x, int H, int R, void*
 
 // dst row didx[r] <- src row sidx[r] (identity when an index is null); 16-byte words when aligned.
 __global__ void gather_k(const uint8_t* src, size_t src_ld, const int* sidx, size_t row_bytes, uint8_t* dst,
-                         size_t dst_ld, const int* didx) {
+                         size_t dst_ld, const int* didx, int src_rows, int* err) {
   PDL_ENTRY();
   const int r = blockIdx.x;
-  const uint8_t* s = src + (size_t)(sidx ? sidx[r] : r) * src_ld;
+  const int si = sidx ? sidx[r] : r;
+  if (src_rows > 0 && (si < 0 || si >= src_rows)) {   // an index from the caller's data (a token id)
+    if (threadIdx.x == 0) latch_error(err, DEVERR_BOUNDS);
+    return;
+  }
+  const uint8_t* s = src + (size_t)si * src_ld;
   uint8_t* d = dst + (size_t)(didx ? didx[r] : r) * dst_ld;
   if (((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d) | row_bytes) & 15) == 0) {
     for (size_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x)
@@ -348,9 +353,10 @@ __global__ void gather_k(const uint8_t* src, size_t src_ld, const int* sidx, siz
 }
 
 int gather_rows(cudaStream_t st, size_t row_bytes, const void* src, size_t src_ld, const int* idx, int R,
-                void* dst, size_t dst_ld, const int* dst_idx) {
+                void* dst, size_t dst_ld, const int* dst_idx, int src_rows, int* err) {
   if (R <= 0) return 0;
-  launch_k(gather_k, R, 128, 0, st, (const uint8_t*)src, src_ld, idx, row_bytes, (uint8_t*)dst, dst_ld, dst_idx);
+  launch_k(gather_k, R, 128, 0, st, (const uint8_t*)src, src_ld, idx, row_bytes, (uint8_t*)dst, dst_ld, dst_idx,
+           src_rows, err);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

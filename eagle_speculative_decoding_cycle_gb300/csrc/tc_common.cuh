@@ -1,5 +1,4 @@
-// Pieces shared by the tcgen05 weight-streaming kernels (the single GEMM and the layer
-// chain): stage geometry, the shared-memory operand descriptor, and the stream-K split.
+// Pieces of the tcgen05 weight-streaming GEMM: stage geometry, the shared-memory operand descriptor, and the stream-K split.
 #pragma once
 
 #include "common.cuh"

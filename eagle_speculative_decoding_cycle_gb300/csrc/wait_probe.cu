@@ -23,7 +23,7 @@ __global__ void wait_probe_k(int kind, const unsigned* counter, int* err, int* r
     fence_mbar_init();
     ok = mbar_wait(smem_u32(&bar), 0, &abort_flag, err);
   } else {
-    // the split-tile owner's and the layer chain's wait: a counter that nothing increments
+    // the split-tile owner's wait: a counter that nothing increments
     ok = grid_wait(counter, 1u, &abort_flag, err, false);
   }
   *result = ok ? 1 : 0;

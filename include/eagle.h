@@ -168,6 +168,9 @@ int eagle_status_sync(eagle_ctx* ctx);
  *   EAGLE_DUMP_VERIFY_LOGITS: full verify logits [B(m+1)][V] float (only when
  *                      eagle_set_debug(ctx, EAGLE_DEBUG_LOGITS) was set before the cycle)
  *   EAGLE_DUMP_FEATURES: target features of the verify rows [B(m+1)][H] (storage type)
+ *   EAGLE_DUMP_TTT   : after eagle_ttt_forward, its last step's R drafter outputs a
+ *                      [R][H] (storage type), then each row's token cross-entropy [R]
+ *                      float (R = the step's source rows; 0 bytes before any such call)
  * eagle_dump_bytes gives the size of each view. */
 enum {
   EAGLE_DUMP_STATE = 0,
@@ -177,7 +180,8 @@ enum {
   EAGLE_DUMP_ACCEPT = 4,
   EAGLE_DUMP_VERIFY_HEAD = 5,
   EAGLE_DUMP_VERIFY_LOGITS = 6,
-  EAGLE_DUMP_FEATURES = 7
+  EAGLE_DUMP_FEATURES = 7,
+  EAGLE_DUMP_TTT = 8
 };
 size_t eagle_dump_bytes(const eagle_ctx* ctx, int what);
 int eagle_debug_dump(eagle_ctx* ctx, int what, void* dst, size_t bytes);

@@ -45,9 +45,18 @@ int eagle_op_gemm(int dtype, void* stream, const void* W, int N, int K, const vo
  * The first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress)
  * with that device current; make that first call before any stream capture. All calls
  * share the one scratch area and the last call's contents remain in it: calls that may
- * overlap on the GPU (different streams without ordering) race and must not be issued. */
+ * overlap on the GPU (different streams without ordering) race and must not be issued;
+ * graph replays that contain this call must be serialised the same way.
+ * A bounded device wait that gives up leaves `out` incomplete and records a timeout in a
+ * status word that is also a file-scope device array; read it with
+ * eagle_op_gemm_noalloc_status. */
 int eagle_op_gemm_noalloc(void* stream, const void* W, int N, int K, const void* X, int M, int epi, void* out,
                           int ldo);
+
+/* Status of the allocation-free GEMM on the current device: waits for `stream`, reads
+ * the status word that its calls share and clears it. EAGLE_OK when no call since the
+ * last read gave up, EAGLE_ETIMEOUT when one did (its output is incomplete). */
+int eagle_op_gemm_noalloc_status(void* stream);
 
 /* Fused LM head: logits = X[M][H] * W_lm[V][H]^T reduced per row without writing the
  * logits (bf16), or through an fp32 logits buffer inside the scratch (f32). Per row it
@@ -124,7 +133,7 @@ int eagle_plan_budget(int n_k, const int32_t* k_values, const float* draft_us, c
  * that nothing satisfies and returns once it gives up: kind 0 waits on a shared-memory
  * mbarrier phase that nobody completes (the wait of the TMA / tensor-core pipelines),
  * kind 1 waits until the device word *d_counter (caller-owned, zero, nullable for kind 0)
- * reaches 1 (the wait of the split-tile owner and the layer chain). Each wait stops after
+ * reaches 1 (the wait of the split-tile owner). Each wait stops after
  * the library's limit of 2 s of %globaltimer and atomically latches 1 (timeout) into *d_err
  * if it is still 0; *d_result receives 1 if the wait was satisfied, 0 if it gave up. Launches
  * one CTA on `stream` and returns without synchronising; EAGLE_EINVAL on a bad kind or a
