@@ -167,16 +167,37 @@ int attention(cudaStream_t st, int dtype, const AttnArgs& a) {
 }  // namespace eagle
 
 // ------------------------------------------------------------------------------------------------
-// Tensor-core path (bf16): mma.sync m16n8k16 with fp32 accumulation, FlashAttention-style
-// online softmax in the exp2 domain, K/V tiles of 64 keys double-buffered in shared memory
-// by cp.async, and split-KV over the key range with a fixed-order log-sum-exp combine.
-// A CTA covers one KV head and 64 query vectors (rows x the GQA group); warp w owns query
-// vectors 16w .. 16w+15.
+// Tensor-core path (bf16), with a result for each query row that does not depend on which
+// other rows share the launch.
+//
+// A row at logical position P attends to the keys of positions 0..P: positions below the
+// context length are the cache slots of the same number; a tree row's positions from the
+// context length on are its ancestors (the root, ..., itself), one per depth, whose slots
+// are the set bits of its ancestry mask in increasing order (generation order is depth
+// major, so an ancestor always precedes its descendants); a training-time-test row of step
+// j >= 2 and source t reads positions t+1 .. t+j-1 from its own source chain. The softmax
+// over those keys is computed in a fixed decomposition that depends on P alone:
+//   body  -- positions [0, B) with B = min(P + 1 - TAIL_MIN, first non-plain position),
+//            in fixed key splits of `tps` 64-key tiles (split s: tiles s*tps ..), each an
+//            online softmax over its tiles in order on the tensor cores (mma.sync
+//            m16n8k16, fp32 accumulation, P split into bf16 high and residual parts);
+//   tail  -- positions [B, P] (TAIL_MIN keys, or fewer near the start), one FFMA pass in
+//            position order;
+//   merge -- the body splits in order, then the tail, by log-sum-exp weights.
+// The split length `tps` is a function of the cache capacity and the scratch size only, so
+// a verify row and the plain-decoding step at the same position go through the same
+// arithmetic and give bit-identical outputs (greedy speculative decoding then reproduces the
+// GPU's own plain decoding exactly, "EAGLE: Feature-Level Drafting", "Speculative decoding
+// in four moves", item 4).
 // ------------------------------------------------------------------------------------------------
 namespace eagle {
 
-constexpr int MT_KEYS = 64;
-constexpr int MT_QV = 64;
+constexpr int MT_KEYS = 64;       // keys per body tile
+constexpr int MT_QV = 64;         // query vectors per body CTA (rows x the GQA group)
+constexpr int TAIL_MIN = 16;      // the last TAIL_MIN positions of a row form its tail
+constexpr int MAX_SPLITS = 16;
+constexpr int TAIL_WARPS = 8;
+constexpr int TAIL_KPL = 8;       // tail keys per lane: tails of up to 256 keys
 
 __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -199,11 +220,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // (lo, hi) -> bf16 pairs of their high parts and of the residuals x - bf16(x).
 __device__ __forceinline__ void split_bf16(float lo, float hi, uint32_t& h, uint32_t& l) {
   const __nv_bfloat162 hv = __floats2bfloat162_rn(lo, hi);
@@ -213,46 +229,42 @@ __device__ __forceinline__ void split_bf16(float lo, float hi, uint32_t& h, uint
   l = *reinterpret_cast<const uint32_t*>(&lv);
 }
 
-// a row's visibility data: validity, own slot, and (tree mode) the 64 mask bits of the
-// current key tile, bit i <-> key tile_base + i
-struct RowVis {
-  int valid, slot;
-  uint64_t win;
+// A row's logical position P, the end of its plain-slot prefix (positions p < plain_end sit
+// at slot p), and the end of its body.
+struct RowSpan {
+  int P, plain_end, body;
 };
 
-// Bits [base, base + 64) of a row's tree mask (4 words in shared memory); bits below 0 and
-// past the words read as 0.
-__device__ __forceinline__ uint64_t mask_window(const uint64_t* mw, int base) {
-  if (base <= -64 || base >= 256) return 0ull;
-  if (base < 0) return mw[0] << (-base);
-  const int w = base >> 6, sh = base & 63;
-  const uint64_t lo = mw[w] >> sh;
-  const uint64_t hi = (sh && w < 3) ? mw[w + 1] << (64 - sh) : 0ull;
-  return lo | hi;
+__device__ __forceinline__ RowSpan row_span(const AttnArgs& a, int r, int ctx) {
+  RowSpan s;
+  const int slot = a.row_slot[r];
+  if (a.mode == 1) {
+    int c = 0;
+    for (int w = 0; w < a.mask_words; ++w) c += __popcll(a.mask[(size_t)r * a.mask_words + w]);
+    s.P = ctx + c - 1;
+    s.plain_end = ctx;
+  } else if (a.mode == 2 && ctx > 0 && slot >= ctx) {
+    const int t = slot % ctx;
+    s.P = t + slot / ctx;
+    s.plain_end = t + 1;
+  } else {
+    s.P = slot;
+    s.plain_end = slot + 1;
+  }
+  s.body = max(0, min(s.P + 1 - TAIL_MIN, s.plain_end));
+  return s;
 }
 
-template <bool TTT>
-__device__ __forceinline__ bool visible(const AttnArgs& a, const RowVis& rv, int ctx, int key, int kb) {
-  if (!rv.valid) return false;
-  if constexpr (TTT) return ttt_visible(rv.slot, key, ctx);
-  if (a.mode == 0) return key <= rv.slot;
-  if (key < ctx) return true;
-  if (key - ctx >= a.tree_T) return false;
-  return (rv.win >> (key - kb)) & 1ull;
-}
-
-// Everything before the query loads reads data older than the preceding kernel (the rows'
-// sequence, slot, mask and context length, and in tree mode the context keys below
-// ctx_len, which that kernel never writes), so it runs before waiting on that kernel: the
-// first key tile of a tree-mode CTA is already in flight when the queries arrive.
-// KIND: 0 = contiguous cache, 1 = paged cache, 2 = training-time-test mask (contiguous);
-// one instantiation each, so the cycle's contiguous kernel carries neither of the others.
+// Body: CTA (KV head, block of rows, key split). Query vectors qv = (row - r0) * G + g.
+// Writes the split's (m, l, o) of every query vector whose body reaches into the split.
+// KIND: 0 = contiguous cache, 1 = paged cache.
 template <int D, int KIND>
-__global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
+__global__ void __launch_bounds__(128, 3) attn_body_k(AttnArgs a, int tps) {
   constexpr int LD = D + 8;                      // padded smem row (bf16 elements)
   extern __shared__ __align__(16) uint8_t attn_smem[];
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(attn_smem);              // [2][64][LD]
   __nv_bfloat16* sV = sK + 2 * MT_KEYS * LD;                                    // [2][64][LD]
+  __shared__ int s_body[MT_QV];
   const int G = a.nq / a.nkv;
   const int RB = MT_QV / G;
   const int nb = (a.rows_per_seq + RB - 1) / RB;
@@ -262,32 +274,26 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   const int r0 = sidx * a.rows_per_seq + rb * RB;
   const int r1 = min(r0 + RB, min((sidx + 1) * a.rows_per_seq, a.R));
   if (r0 >= r1) return;
+  // Row metadata and context length were written before the preceding kernel started.
   const int seq = a.row_seq[r0];
   const int ctx = a.ctx_len[seq];
+  for (int i = threadIdx.x; i < r1 - r0; i += blockDim.x) s_body[i] = row_span(a, r0 + i, ctx).body;
+  __syncthreads();
+  int bmax = 0;
+  for (int i = 0; i < r1 - r0; ++i) bmax = max(bmax, s_body[i]);
+  bmax = min(bmax, a.cap);
+  const int t_begin = split * tps, t_end = min(t_begin + tps, (bmax + MT_KEYS - 1) / MT_KEYS);
+  if (t_begin >= t_end) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.kcache);
   const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.vcache);
 
-  int kend = 0;
-  for (int r = r0; r < r1; ++r) kend = max(kend, a.mode == 1 ? ctx + a.tree_T : a.row_slot[r] + 1);
-  kend = min(kend, a.cap);
-  const int n_tiles = (kend + MT_KEYS - 1) / MT_KEYS;
-  const int tps = (n_tiles + splits - 1) / splits;
-  const int t_begin = split * tps, t_end = min(n_tiles, t_begin + tps);
-
   // the two query vectors (rows of the mma fragment) this thread holds
   const int qv_a = warp * 16 + (lane >> 2), qv_b = qv_a + 8;
-  RowVis va, vb;
-  auto setup_row = [&](int qv, RowVis& v, int& row, int& head) {
-    row = r0 + qv / G;
-    head = kvh * G + qv % G;
-    v.valid = row < r1;
-    v.slot = v.valid ? a.row_slot[row] : -1;
-    v.win = 0ull;
-  };
-  int row_a, head_a, row_b, head_b;
-  setup_row(qv_a, va, row_a, head_a);
-  setup_row(qv_b, vb, row_b, head_b);
+  const int row_a = r0 + qv_a / G, head_a = kvh * G + qv_a % G;
+  const int row_b = r0 + qv_b / G, head_b = kvh * G + qv_b % G;
+  const bool val_a = row_a < r1, val_b = row_b < r1;
+  const int body_a = val_a ? s_body[row_a - r0] : 0, body_b = val_b ? s_body[row_b - r0] : 0;
 
   float o[D / 8][4];
 #pragma unroll
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
     for (int i = threadIdx.x; i < MT_KEYS * CH; i += 128) {
       const int kr = i / CH, c = i % CH;
       const int key = t * MT_KEYS + kr;
-      const bool in = key < kend;
+      const bool in = key < bmax;
       const int kk = in ? key : 0;
       size_t grow;
       if constexpr (KIND == 1) grow = kv_row(a.page, seq, a.nkv, kvh, a.cap, kk);
@@ -316,46 +322,36 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
     cp_async_commit();
   };
 
-  // the block's rows' tree masks, [row in block][4 words]
-  __shared__ uint64_t s_mask[MT_QV][4];
-  if (a.mode == 1) {
-    for (int i = threadIdx.x; i < RB * 4; i += 128) {
-      const int rr = i >> 2, w = i & 3, row = r0 + rr;
-      s_mask[rr][w] = (row < r1 && w < a.mask_words) ? a.mask[(size_t)row * a.mask_words + w] : 0ull;
-    }
-  }
-  const bool early = a.mode == 1 && t_begin < t_end && (t_begin + 1) * MT_KEYS <= ctx;
+  // Body keys sit below every slot the preceding kernel writes in tree mode (it writes the
+  // tree rows' slots, from ctx on) and in one-row-per-sequence causal launches (it writes
+  // the row's own slot, beyond its body): their first tile is requested before waiting.
+  const bool early = a.mode == 1 || (a.mode == 0 && a.rows_per_seq == 1);
   if (early) load_tile(t_begin, 0);
   PDL_ENTRY();
   // Q fragments (bf16 pairs), zero for rows past the block
   uint32_t qf[D / 16][4];
   {
     const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* pa = qp + ((size_t)row_a * a.nq + head_a) * D;
-    const __nv_bfloat16* pb = qp + ((size_t)row_b * a.nq + head_b) * D;
+    const __nv_bfloat16* pa = qp + ((size_t)(val_a ? row_a : r0) * a.nq + head_a) * D;
+    const __nv_bfloat16* pb = qp + ((size_t)(val_b ? row_b : r0) * a.nq + head_b) * D;
     const int c = (lane & 3) * 2;
 #pragma unroll
     for (int kt = 0; kt < D / 16; ++kt) {
-      qf[kt][0] = va.valid ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + c) : 0u;
-      qf[kt][1] = vb.valid ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + c) : 0u;
-      qf[kt][2] = va.valid ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + 8 + c) : 0u;
-      qf[kt][3] = vb.valid ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + 8 + c) : 0u;
+      qf[kt][0] = val_a ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + c) : 0u;
+      qf[kt][1] = val_b ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + c) : 0u;
+      qf[kt][2] = val_a ? *reinterpret_cast<const uint32_t*>(pa + kt * 16 + 8 + c) : 0u;
+      qf[kt][3] = val_b ? *reinterpret_cast<const uint32_t*>(pb + kt * 16 + 8 + c) : 0u;
     }
   }
-  if (!early && t_begin < t_end) load_tile(t_begin, 0);
+  if (!early) load_tile(t_begin, 0);
   const bool warp_live = warp * 16 < (r1 - r0) * G;
   for (int t = t_begin; t < t_end; ++t) {
     const int buf = (t - t_begin) & 1;
     if (t + 1 < t_end) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
     else cp_async_wait<0>();
     __syncthreads();
-    const int kb = t * MT_KEYS;
     // a warp whose 16 query vectors are all past the block's rows only helps load the tiles
     if (!warp_live) { __syncthreads(); continue; }
-    if (a.mode == 1 && kb + MT_KEYS > ctx) {   // the tile reaches the tree rows' keys
-      va.win = va.valid ? mask_window(s_mask[row_a - r0], kb - ctx) : 0ull;
-      vb.win = vb.valid ? mask_window(s_mask[row_b - r0], kb - ctx) : 0ull;
-    }
     const __nv_bfloat16* K = sK + buf * MT_KEYS * LD;
     const __nv_bfloat16* Vt = sV + buf * MT_KEYS * LD;
     float s[8][4];
@@ -370,15 +366,16 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
         mma_bf16_16816(s[nt], qf[kt], b0, b1);
       }
     }
-    // mask, scale to the exp2 domain, running max
+    // keys past a query vector's body are its tail's or invisible: scaled to the exp2 domain
+    // or -inf, then the running max
     float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = t * MT_KEYS + nt * 8 + (lane & 3) * 2 + e;
-        s[nt][e] = visible<KIND == 2>(a, va, ctx, key, kb) ? s[nt][e] * sl2 : -INFINITY;
-        s[nt][2 + e] = visible<KIND == 2>(a, vb, ctx, key, kb) ? s[nt][2 + e] * sl2 : -INFINITY;
+        s[nt][e] = key < body_a ? s[nt][e] * sl2 : -INFINITY;
+        s[nt][2 + e] = key < body_b ? s[nt][2 + e] * sl2 : -INFINITY;
         mx_a = fmaxf(mx_a, s[nt][e]);
         mx_b = fmaxf(mx_b, s[nt][2 + e]);
       }
@@ -438,128 +435,282 @@ __global__ void __launch_bounds__(128, 3) attn_mma_k(AttnArgs a, int splits) {
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
   const int c = (lane & 3) * 2;
-  if (splits == 1) {
-    __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out);
-    const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+  const bool wr_a = val_a && t_begin * MT_KEYS < body_a, wr_b = val_b && t_begin * MT_KEYS < body_b;
+  const size_t sa = ((size_t)split * a.R + row_a) * a.nq + head_a;
+  const size_t sb = ((size_t)split * a.R + row_b) * a.nq + head_b;
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      if (va.valid)
-        *reinterpret_cast<__nv_bfloat162*>(op + ((size_t)row_a * a.nq + head_a) * D + i * 8 + c) =
-            __floats2bfloat162_rn(o[i][0] * ia, o[i][1] * ia);
-      if (vb.valid)
-        *reinterpret_cast<__nv_bfloat162*>(op + ((size_t)row_b * a.nq + head_b) * D + i * 8 + c) =
-            __floats2bfloat162_rn(o[i][2] * ib, o[i][3] * ib);
-    }
-  } else {
-    const size_t sa = ((size_t)split * a.R + row_a) * a.nq + head_a;
-    const size_t sb = ((size_t)split * a.R + row_b) * a.nq + head_b;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      if (va.valid) *reinterpret_cast<float2*>(a.part_o + sa * D + i * 8 + c) = make_float2(o[i][0], o[i][1]);
-      if (vb.valid) *reinterpret_cast<float2*>(a.part_o + sb * D + i * 8 + c) = make_float2(o[i][2], o[i][3]);
-    }
-    if ((lane & 3) == 0) {
-      if (va.valid) { a.part_ml[sa * 2] = m_a; a.part_ml[sa * 2 + 1] = l_a; }
-      if (vb.valid) { a.part_ml[sb * 2] = m_b; a.part_ml[sb * 2 + 1] = l_b; }
-    }
+  for (int i = 0; i < D / 8; ++i) {
+    if (wr_a) *reinterpret_cast<float2*>(a.part_o + sa * D + i * 8 + c) = make_float2(o[i][0], o[i][1]);
+    if (wr_b) *reinterpret_cast<float2*>(a.part_o + sb * D + i * 8 + c) = make_float2(o[i][2], o[i][3]);
+  }
+  if ((lane & 3) == 0) {
+    if (wr_a) { a.part_ml[sa * 2] = m_a; a.part_ml[sa * 2 + 1] = l_a; }
+    if (wr_b) { a.part_ml[sb * 2] = m_b; a.part_ml[sb * 2 + 1] = l_b; }
   }
 }
 
-// out[r][h] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), splits in order. One warp per
-// (row, head): lane s holds split s's (m, l); every split's partial output is loaded before
-// the in-order sums, so the kernel costs two dependent loads instead of one per split.
-constexpr int MAX_SPLITS = 16;
-template <int D>
-__global__ void attn_combine_k(AttnArgs a, int splits) {
+// Tail + merge: CTA (KV head, block of `rpc` rows of one sequence). Stages the plain slots of
+// the block's tails (positions [min body, max plain tail end)) and, in tree mode, the T tree
+// slots; then each warp takes (row, query head) items: the tail's scores in position order
+// (lane j holds tail keys j, j + 32, ..), their softmax and P.V in position order, and the
+// merge with the body splits. Training-time-test chain keys are read from the cache directly.
+template <int D, int KIND>
+__global__ void __launch_bounds__(TAIL_WARPS * 32) attn_tail_k(AttnArgs a, int tps, int rpc, int nA_cap, int nB,
+                                                              int tail_cap, int* err) {
+  constexpr int LD = D + 8;
+  constexpr int DL = D / 32;                         // output dims per lane
+  extern __shared__ __align__(16) uint8_t attn_smem[];
+  __nv_bfloat16* sAK = reinterpret_cast<__nv_bfloat16*>(attn_smem);
+  __nv_bfloat16* sAV = sAK + (size_t)nA_cap * LD;
+  __nv_bfloat16* sBK = sAV + (size_t)nA_cap * LD;
+  __nv_bfloat16* sBV = sBK + (size_t)nB * LD;
+  uint8_t* wbase = reinterpret_cast<uint8_t*>(sBV + (size_t)nB * LD);
+  __shared__ int s_P[32], s_pe[32], s_body[32];
+  __shared__ int s_lo, s_hi;
+  const int G = a.nq / a.nkv;
+  const int nbt = (a.rows_per_seq + rpc - 1) / rpc;
+  const int kvh = blockIdx.x;
+  const int sidx = blockIdx.y / nbt, rb = blockIdx.y % nbt;
+  const int r0 = sidx * a.rows_per_seq + rb * rpc;
+  const int r1 = min(r0 + rpc, min((sidx + 1) * a.rows_per_seq, a.R));
+  if (r0 >= r1) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seq = a.row_seq[r0];
+  const int ctx = a.ctx_len[seq];
+  if (threadIdx.x < r1 - r0) {
+    const RowSpan rs = row_span(a, r0 + threadIdx.x, ctx);
+    s_P[threadIdx.x] = rs.P;
+    s_pe[threadIdx.x] = rs.plain_end;
+    s_body[threadIdx.x] = rs.body;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int lo = INT32_MAX, hi = 0;
+    for (int i = 0; i < r1 - r0; ++i) {
+      lo = min(lo, s_body[i]);
+      hi = max(hi, min(s_P[i] + 1, s_pe[i]));
+    }
+    if (hi < lo) hi = lo;
+    if (hi - lo > nA_cap) { latch_error(err, DEVERR_BOUNDS); hi = lo; lo = -1; }
+    s_lo = lo;
+    s_hi = hi;
+  }
+  __syncthreads();
+  if (s_lo < 0) return;
+  const int lo = s_lo, nA = s_hi - s_lo;
+  const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.kcache);
+  const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.vcache);
+  auto grow = [&](int slot) -> size_t {
+    if constexpr (KIND == 1) return kv_row(a.page, seq, a.nkv, kvh, a.cap, slot);
+    else return ((size_t)seq * a.nkv + kvh) * (size_t)a.cap + slot;
+  };
+  // Every key was written by a kernel that completed before the body kernel released this
+  // one; only the body's partial results need the dependency wait.
+  {
+    constexpr int CH = D / 8;
+    const int nS = nA + (a.mode == 1 ? nB : 0);
+    for (int i = threadIdx.x; i < nS * CH; i += blockDim.x) {
+      const int k = i / CH, c = i % CH;
+      const bool inA = k < nA;
+      const int slot = inA ? lo + k : ctx + (k - nA);
+      const bool ok = slot >= 0 && slot < a.cap;
+      const size_t g = (ok ? grow(slot) : 0) * D + c * 8;
+      const uint4 kv = ok ? *reinterpret_cast<const uint4*>(kc + g) : make_uint4(0, 0, 0, 0);
+      const uint4 vv = ok ? *reinterpret_cast<const uint4*>(vc + g) : make_uint4(0, 0, 0, 0);
+      __nv_bfloat16* dk = inA ? sAK + (size_t)k * LD : sBK + (size_t)(k - nA) * LD;
+      __nv_bfloat16* dv = inA ? sAV + (size_t)k * LD : sBV + (size_t)(k - nA) * LD;
+      *reinterpret_cast<uint4*>(dk + c * 8) = kv;
+      *reinterpret_cast<uint4*>(dv + c * 8) = vv;
+    }
+  }
   PDL_ENTRY();
-  const int qi = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (qi >= a.R * a.nq) return;
-  const size_t stride = (size_t)a.R * a.nq;
-  float ms = -INFINITY, ls = 0.f;
-  if (lane < splits) {
-    ms = a.part_ml[((size_t)lane * stride + qi) * 2];
-    ls = a.part_ml[((size_t)lane * stride + qi) * 2 + 1];
-  }
-  float x[MAX_SPLITS][D / 32];
-#pragma unroll
-  for (int sp = 0; sp < MAX_SPLITS; ++sp)
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i)
-      x[sp][i] = sp < splits ? a.part_o[((size_t)sp * stride + qi) * D + lane + 32 * i] : 0.f;
-  float M = ms;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
-  float L = 0.f;
-  float acc[D / 32];
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-#pragma unroll
-  for (int sp = 0; sp < MAX_SPLITS; ++sp) {
-    const float ws = __shfl_sync(0xffffffffu, w, sp);
-    const float lw = __shfl_sync(0xffffffffu, ls * w, sp);
-    const float msp = __shfl_sync(0xffffffffu, ms, sp);
-    if (sp < splits && msp != -INFINITY) {
-      L += lw;
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) acc[i] += x[sp][i] * ws;
+  __syncthreads();
+  // per-warp scratch: the query vector (fp32), the tail probabilities, key and value row
+  // pointers; tail_cap is a multiple of 4, so every part starts on a 16-byte boundary
+  const size_t wsz = (size_t)D * 4 + (size_t)tail_cap * (4 + 16);
+  uint8_t* wb = wbase + (size_t)warp * wsz;
+  float* wq = reinterpret_cast<float*>(wb);
+  float* wp = wq + D;
+  const __nv_bfloat16** wk = reinterpret_cast<const __nv_bfloat16**>(wp + tail_cap);
+  const __nv_bfloat16** wv = wk + tail_cap;
+  const float sl2 = a.scale * 1.4426950408889634f;
+  const int n_items = (r1 - r0) * G;
+  for (int it = warp; it < n_items; it += TAIL_WARPS) {
+    const int i = it / G, g = it % G;
+    const int row = r0 + i, head = kvh * G + g;
+    const int P = s_P[i], pe = s_pe[i], body = s_body[i];
+    const int nt = P + 1 - body;
+    if (nt < 1 || nt > tail_cap) {             // a mask or slot the row layout does not allow
+      if (lane == 0) latch_error(err, DEVERR_BOUNDS);
+      continue;
     }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out);
+    {
+      const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)row * a.nq + head) * D;
+      for (int c = lane; c < D; c += 32) wq[c] = __bfloat162float(qp[c]);
+    }
+    // key and value rows of tail position body + j
+    for (int j = lane; j < nt; j += 32) {
+      const int p = body + j;
+      const __nv_bfloat16 *kr, *vr;
+      if (p < pe) {
+        kr = sAK + (size_t)(p - lo) * LD;
+        vr = sAV + (size_t)(p - lo) * LD;
+      } else if (a.mode == 1) {
+        // the (p - ctx)-th set bit of the row's ancestry mask
+        int want = p - ctx, bit = 0;
+        for (int w = 0; w < a.mask_words; ++w) {
+          uint64_t m = a.mask[(size_t)row * a.mask_words + w];
+          const int c = __popcll(m);
+          if (want < c) {
+            for (int q = 0; q < want; ++q) m &= m - 1;
+            bit = w * 64 + __ffsll((long long)m) - 1;
+            break;
+          }
+          want -= c;
+        }
+        if (bit < 0 || bit >= nB) {             // a mask bit past the tree
+          latch_error(err, DEVERR_BOUNDS);
+          bit = 0;
+        }
+        kr = sBK + (size_t)bit * LD;
+        vr = sBV + (size_t)bit * LD;
+      } else {
+        const int t = pe - 1;                      // training-time test: own source chain
+        const size_t gr = grow(ctx * (p - t) + t) * D;
+        kr = kc + gr;
+        vr = vc + gr;
+      }
+      wk[j] = kr;
+      wv[j] = vr;
+    }
+    __syncwarp();
+    // scores, in the exp2 domain
+    float x[TAIL_KPL];
+    float mt = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) op[(size_t)qi * D + lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+    for (int u = 0; u < TAIL_KPL; ++u) {
+      const int j = lane + 32 * u;
+      x[u] = -INFINITY;
+      if (j < nt) {
+        const __nv_bfloat16* kr = wk[j];
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D; c += 8) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(kr + c);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+          const float2 k0 = __bfloat1622float2(h2[0]), k1 = __bfloat1622float2(h2[1]);
+          const float2 k2 = __bfloat1622float2(h2[2]), k3 = __bfloat1622float2(h2[3]);
+          acc0 = fmaf(wq[c], k0.x, acc0);
+          acc1 = fmaf(wq[c + 1], k0.y, acc1);
+          acc2 = fmaf(wq[c + 2], k1.x, acc2);
+          acc3 = fmaf(wq[c + 3], k1.y, acc3);
+          acc0 = fmaf(wq[c + 4], k2.x, acc0);
+          acc1 = fmaf(wq[c + 5], k2.y, acc1);
+          acc2 = fmaf(wq[c + 6], k3.x, acc2);
+          acc3 = fmaf(wq[c + 7], k3.y, acc3);
+        }
+        x[u] = ((acc0 + acc1) + (acc2 + acc3)) * sl2;
+      }
+      mt = fmaxf(mt, x[u]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    float lt = 0.f;
+#pragma unroll
+    for (int u = 0; u < TAIL_KPL; ++u) {
+      const int j = lane + 32 * u;
+      const float pj = j < nt ? exp2f(x[u] - mt) : 0.f;
+      if (j < nt) wp[j] = pj;
+      lt += pj;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+    __syncwarp();
+    float ot[DL];
+#pragma unroll
+    for (int u = 0; u < DL; ++u) ot[u] = 0.f;
+    for (int j = 0; j < nt; ++j) {
+      const float pj = wp[j];
+      const __nv_bfloat16* vr = wv[j];
+#pragma unroll
+      for (int u = 0; u < DL; ++u) ot[u] = fmaf(pj, __bfloat162float(vr[lane + 32 * u]), ot[u]);
+    }
+    // merge: body splits in order, then the tail
+    const int S = body > 0 ? (body + tps * MT_KEYS - 1) / (tps * MT_KEYS) : 0;
+    float M = mt;
+    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, a.part_ml[(((size_t)sp * a.R + row) * a.nq + head) * 2]);
+    float L = 0.f, acc[DL];
+#pragma unroll
+    for (int u = 0; u < DL; ++u) acc[u] = 0.f;
+    for (int sp = 0; sp < S; ++sp) {
+      const size_t q = ((size_t)sp * a.R + row) * a.nq + head;
+      const float w = exp2f(a.part_ml[q * 2] - M);
+      L = fmaf(a.part_ml[q * 2 + 1], w, L);
+#pragma unroll
+      for (int u = 0; u < DL; ++u) acc[u] = fmaf(a.part_o[q * D + lane + 32 * u], w, acc[u]);
+    }
+    const float wt = exp2f(mt - M);
+    L = fmaf(lt, wt, L);
+#pragma unroll
+    for (int u = 0; u < DL; ++u) acc[u] = fmaf(ot[u], wt, acc[u]);
+    __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)row * a.nq + head) * D;
+#pragma unroll
+    for (int u = 0; u < DL; ++u) op[lane + 32 * u] = __float2bfloat16_rn(L > 0.f ? acc[u] / L : 0.f);
+    __syncwarp();
+  }
 }
 
-size_t attention_scratch_floats(int rows, int nq, int d) { return (size_t)16 * rows * nq * (d + 2); }
+size_t attention_scratch_floats(int rows, int nq, int d) { return (size_t)MAX_SPLITS * rows * nq * (d + 2); }
 
 template <int D>
-static int launch_mma(cudaStream_t st, const AttnArgs& a) {
+static int launch_bf16(cudaStream_t st, const AttnArgs& a) {
   const int G = a.nq / a.nkv;
   const int RB = MT_QV / G;
   const int nseq = (a.R + a.rows_per_seq - 1) / a.rows_per_seq;
   const int nb = (a.rows_per_seq + RB - 1) / RB;
-  const int base = a.nkv * nseq * nb;
-  const size_t smem = (size_t)4 * MT_KEYS * (D + 8) * sizeof(__nv_bfloat16);
-  static int sms = 0, per_sm = 1;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(attn_mma_k<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaFuncSetAttribute(attn_mma_k<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaFuncSetAttribute(attn_mma_k<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_mma_k<D, 0>, 128, smem) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-  }
-  // as many key splits as one wave of resident CTAs holds (a second, partial wave would
-  // double the time of this latency-bound kernel)
-  int splits = per_sm * sms / base;
-  const int max_tiles = (a.cap + MT_KEYS - 1) / MT_KEYS;
-  splits = std::min(std::min(splits, MAX_SPLITS), max_tiles);
-  while (splits > 1 && (size_t)splits * a.R * a.nq * D > a.part_floats) --splits;
-  if (!a.part_o || !a.part_ml) splits = 1;
-  if (splits < 1) splits = 1;
-  // the training-time-test mask is its own instantiation, so the cycle's kernel stays lean
-  const dim3 grid(a.nkv, nseq * nb, splits);
-  if (a.mode == 2 && !a.page.table) launch_k(attn_mma_k<D, 2>, grid, 128, smem, st, a, splits);
-  else if (a.mode == 2) return -1;   // the training-time test runs on the contiguous drafter cache
-  else if (a.page.table) launch_k(attn_mma_k<D, 1>, grid, 128, smem, st, a, splits);
-  else launch_k(attn_mma_k<D, 0>, grid, 128, smem, st, a, splits);
-  if (splits > 1) launch_k(attn_combine_k<D>, (a.R * a.nq + 3) / 4, 128, 0, st, a, splits);
+  if (!a.part_o || !a.part_ml) return -1;
+  // fixed key splits: a function of the capacity and the scratch only
+  const int max_tiles = std::max(1, (a.cap + MT_KEYS - 1) / MT_KEYS);
+  const long long fit = (long long)(a.part_floats / ((size_t)a.R * a.nq * D));
+  if (fit < 1) return -1;
+  const int S = (int)std::min<long long>(MAX_SPLITS, fit);
+  const int tps = (max_tiles + S - 1) / S;
+  const int splits = (max_tiles + tps - 1) / tps;
+  const size_t body_smem = (size_t)4 * MT_KEYS * (D + 8) * sizeof(__nv_bfloat16);
+  const bool paged = a.page.table != nullptr;
+  const void* body_fn = paged ? reinterpret_cast<const void*>(attn_body_k<D, 1>)
+                              : reinterpret_cast<const void*>(attn_body_k<D, 0>);
+  if (raise_smem_limit(body_fn, (int)body_smem) != cudaSuccess) return -4;
+  const dim3 bgrid(a.nkv, nseq * nb, splits);
+  if (paged) launch_k(attn_body_k<D, 1>, bgrid, 128, body_smem, st, a, tps);
+  else launch_k(attn_body_k<D, 0>, bgrid, 128, body_smem, st, a, tps);
+  // tail + merge: blocks of rows of one sequence, halved while the grid is under two waves
+  int rpc = std::min(a.rows_per_seq, 32);
+  const int sms = device_sm_count();
+  while (rpc > 4 && (long long)a.nkv * nseq * ((a.rows_per_seq + rpc - 1) / rpc) < 2LL * sms) rpc = (rpc + 1) / 2;
+  const int nA_cap = TAIL_MIN + rpc;
+  const int nB = a.mode == 1 ? a.tree_T : 0;
+  const int tail_cap = (std::max(TAIL_MIN, a.mode == 1 ? a.tree_T : 0) + 3) & ~3;   // a multiple of 4
+  const size_t wsz = (size_t)D * 4 + (size_t)tail_cap * (4 + 16);
+  const size_t tail_smem = (size_t)2 * (nA_cap + nB) * (D + 8) * sizeof(__nv_bfloat16) + TAIL_WARPS * wsz + 16;
+  const void* tail_fn = paged ? reinterpret_cast<const void*>(attn_tail_k<D, 1>)
+                              : reinterpret_cast<const void*>(attn_tail_k<D, 0>);
+  if (raise_smem_limit(tail_fn, (int)tail_smem) != cudaSuccess) return -4;
+  const dim3 tgrid(a.nkv, nseq * ((a.rows_per_seq + rpc - 1) / rpc));
+  if (paged) launch_k(attn_tail_k<D, 1>, tgrid, TAIL_WARPS * 32, tail_smem, st, a, tps, rpc, nA_cap, nB, tail_cap, a.err);
+  else launch_k(attn_tail_k<D, 0>, tgrid, TAIL_WARPS * 32, tail_smem, st, a, tps, rpc, nA_cap, nB, tail_cap, a.err);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int attention_bf16_mma(cudaStream_t st, const AttnArgs& a) {
   const int G = a.nq / a.nkv;
   if (G < 1 || G > MT_QV || MT_QV % G) return -1;
-  if (a.mode == 1 && (a.mask_words > 4 || a.tree_T > 256)) return -1;
+  if (a.mode == 1 && (a.mask_words > 4 || a.tree_T > 256 || a.tree_T < 1)) return -1;
+  if (a.mode == 2 && a.page.table) return -1;   // the training-time test runs on the contiguous drafter cache
   switch (a.d) {
-    case 32: return launch_mma<32>(st, a);
-    case 64: return launch_mma<64>(st, a);
-    case 128: return launch_mma<128>(st, a);
+    case 32: return launch_bf16<32>(st, a);
+    case 64: return launch_bf16<64>(st, a);
+    case 128: return launch_bf16<128>(st, a);
   }
   return -1;
 }

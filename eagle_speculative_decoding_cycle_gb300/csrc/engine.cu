@@ -159,7 +159,7 @@ struct eagle_ctx {
   float* logits;
   float *h_part, *h_val, *h_lse, *h_spec; int* h_id;        // drafter / root / plain heads
   float *v_val, *v_lse, *v_spec, *v_logits; int* v_id;       // verify head (kept for the cycle's dump)
-  float* gemm_part; int* gemm_cnt; int gemm_cnt_len;
+  float* gemm_part; size_t gemm_part_floats; int* gemm_cnt; int gemm_cnt_len;
   float *attn_po, *attn_pml; size_t attn_pfloats;
   // bf16 fused epilogues: -1 (default) SwiGLU in the gate/up epilogue from 128 rows on, where
   // the separate SwiGLU pass costs more than the epilogue work; 1 (EAGLE_FUSE_EPI=1) also
@@ -228,14 +228,17 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
   x->v_id = c.take<int>((size_t)z.B * z.T1 * 2); x->v_val = c.take<float>((size_t)z.B * z.T1 * 2);
   x->v_lse = c.take<float>((size_t)z.B * z.T1); x->v_spec = c.take<float>((size_t)z.B * z.T1 * z.k);
   x->v_logits = c.take<float>((size_t)z.B * z.T1 * z.V);
-  x->gemm_part = c.take<float>(gemm_bf16_scratch_bytes() / sizeof(float));
+  x->gemm_part_floats = gemm_bf16_scratch_bytes(std::max(z.R, z.Rh)) / sizeof(float);
+  x->gemm_part = c.take<float>(x->gemm_part_floats);
   x->gemm_cnt_len = 65536;
   x->gemm_cnt = c.take<int>(x->gemm_cnt_len);
   {
-    const int rs = std::max(std::max(z.B * z.T1, z.B * (z.D + 1)), z.B * z.k);
-    x->attn_pfloats = (size_t)16 * rs * z.nq * z.d;
+    // 16 key splits for the cycle's launches; launches with more rows (prefill chunks) run
+    // fewer, longer splits in the same space
+    const int rs = std::max(std::max(std::max(z.B * z.T1, z.B * (z.D + 1)), z.B * z.k) * 16, z.R);
+    x->attn_pfloats = (size_t)rs * z.nq * z.d;
     x->attn_po = c.take<float>(x->attn_pfloats);
-    x->attn_pml = c.take<float>((size_t)16 * rs * z.nq * 2);
+    x->attn_pml = c.take<float>((size_t)rs * z.nq * 2);
   }
   x->ttt_tgt = c.take<int>(std::max(z.Rd, z.Rt));
   x->ttt_acc = c.take<float>(4);
@@ -271,14 +274,16 @@ int gemm(eagle_ctx* ctx, const void* W, int N, int K, const void* X, int M, int 
   if (z.dt == DT_BF16) {
     const bool prof = ctx->prof_on && 2 * (ctx->prof_n + 1) <= (int)ctx->prof_ev.size();
     if (prof) cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n], ctx->st);
-    const int r = gemm_bf16(ctx->st, W, N, K, X, M, epi, out, ldo, ctx->gemm_part, ctx->gemm_cnt, ctx->gemm_cnt_len,
-                            ctx->dev_err, head, true, qkv);
+    const int r = gemm_bf16(ctx->st, W, N, K, X, M, epi, out, ldo, ctx->gemm_part, ctx->gemm_part_floats,
+                            ctx->gemm_cnt, ctx->gemm_cnt_len, ctx->dev_err, head, true, qkv);
     if (prof) {
       cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n + 1], ctx->st);
       // algorithmic bytes: weight + activation in + output (fp32, bf16, none for the head)
       const bool b16 = epi == EPI_BF16 || epi == EPI_SWIGLU || epi == EPI_QKV;
-      const double ob = epi == EPI_HEAD ? 0.0 : (double)M * N * (b16 ? 2 : 4) * (epi == EPI_ADD_F32 ? 2 : 1);
-      ctx->prof_bytes[ctx->prof_n] = (double)N * K * 2 * (epi == EPI_SWIGLU ? 2 : 1) + (double)M * K * 2 + ob;
+      const bool paired = epi == EPI_SWIGLU || epi == EPI_GU;
+      const double ob = epi == EPI_HEAD ? 0.0
+                                        : (double)M * N * (b16 ? 2 : 4) * (epi == EPI_ADD_F32 || epi == EPI_GU ? 2 : 1);
+      ctx->prof_bytes[ctx->prof_n] = (double)N * K * 2 * (paired ? 2 : 1) + (double)M * K * 2 + ob;
       ++ctx->prof_n;
     }
     return r;
@@ -338,6 +343,7 @@ int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_
   a.mask = mask; a.mask_words = mask_words; a.scale = 1.f / sqrtf((float)z.d);
   a.page = page;
   a.part_o = ctx->attn_po; a.part_ml = ctx->attn_pml; a.part_floats = ctx->attn_pfloats;
+  a.err = ctx->dev_err;
   CK(attention(ctx->st, z.dt, a));
   return 0;
 }
@@ -362,9 +368,15 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   if (r) return r;
   CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
   CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
-  if (z.dt == DT_BF16 && (ctx->fuse_epi > 0 || (ctx->fuse_epi < 0 && R >= 128)) && z.F % 64 == 0) {
-    // gate and up rows of each 64 features share one tile; SwiGLU in the epilogue
-    CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_SWIGLU, ctx->hb, z.F));
+  if (z.dt == DT_BF16 && z.F % 64 == 0) {
+    // gate and up rows of each 64 features share one tile; SwiGLU in the epilogue from 128
+    // rows on, else a separate pass over the stored gate/up values (the same bits either way)
+    if (ctx->fuse_epi > 0 || (ctx->fuse_epi < 0 && R >= 128)) {
+      CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_SWIGLU, ctx->hb, z.F));
+    } else {
+      CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_GU, ctx->gu, 2 * z.F));
+      CK(swiglu_rows(ctx->st, z.dt, ctx->gu, z.F, R, ctx->hb));
+    }
   } else {
     CK(gemm(ctx, lw.wgu, 2 * z.F, z.H, ctx->ain, R, EPI_F32, ctx->gu, 2 * z.F));
     CK(swiglu_rows(ctx->st, z.dt, ctx->gu, z.F, R, ctx->hb));
@@ -1219,7 +1231,8 @@ int eagle_set_static_tree(eagle_ctx* ctx, int n, const int32_t* parent, const in
 int eagle_ttt_forward(eagle_ctx* ctx, const int32_t* d_tokens, int n, int steps, float* d_loss) {
   if (!ctx) return EAGLE_EINVAL;
   const Dims& z = ctx->z;
-  if (!d_tokens || !d_loss || steps < 1 || n < steps + 3) return fail(ctx, EAGLE_EINVAL, "bad training-time-test arguments");
+  if (!d_tokens || !d_loss || steps < 1 || steps > 16 || n < steps + 3)
+    return fail(ctx, EAGLE_EINVAL, "bad training-time-test arguments");
   if (n > z.P || n - 2 > z.Rd || (size_t)n * steps > (size_t)z.dcap || n > z.cap)
     return fail(ctx, EAGLE_ECAPACITY, "sequence too long for the training-time test in this context");
   if (ctx->graph) { cudaGraphExecDestroy(ctx->graph); ctx->graph = nullptr; }

@@ -86,7 +86,8 @@ extern "C" int eagle_op_gemm_noalloc(void* stream, const void* W, int N, int K, 
   // the tickets must start at zero; a completed call leaves them at zero, but an
   // abandoned one (device timeout) may not, so clear the ones this call uses
   if (cudaMemsetAsync(s->tickets, 0, (size_t)tiles * sizeof(int), st) != cudaSuccess) return EAGLE_ECUDA;
-  const int r = gemm_bf16(st, W, N, K, X, M, epi, out, ldo, s->partials, s->tickets, (int)tiles, s->status, nullptr,
+  const int r = gemm_bf16(st, W, N, K, X, M, epi, out, ldo, s->partials,
+                          sizeof(g_noalloc_partials) / sizeof(float), s->tickets, (int)tiles, s->status, nullptr,
                           /*cache_maps=*/false);
   return r == 0 ? EAGLE_OK : (r == -4 ? EAGLE_ECUDA : EAGLE_EINVAL);
 }

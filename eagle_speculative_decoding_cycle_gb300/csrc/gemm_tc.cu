@@ -8,16 +8,22 @@
 // lives in TMEM, double-buffered so the epilogue of one tile overlaps the next tile's
 // main loop.
 //
-// Work split: stream-K. The (tile, k-block) units of the whole GEMM are cut into
-// gridDim.x equal contiguous ranges, one per persistent CTA, so every SM streams the
-// same number of weight bytes whatever the shape. A tile split across CTAs is finished
-// by its first contributor, for which it is the last segment of its range: the later
-// contributors reach the tile at the start of their ranges, publish fp32 partials and
-// count themselves in on a per-tile counter; the owner waits (bounded) for that count
-// and adds the partials to its own accumulator in contributor order, so results do not
-// depend on timing and the owner never writes its own partial. Every CTA of the grid is
-// resident at once (one CTA per SM, at most one per SM launched), so the wait always
-// ends.
+// Work split: stream-K over the (weight tile, k-block) units of one token tile, cut into
+// gridDim.x equal contiguous ranges, one per persistent CTA, so every SM streams the same
+// number of weight bytes whatever the shape. The ranges depend on (N, K, SM count) only,
+// never on the number of tokens M: with several token tiles (M > 256) each CTA runs its
+// range once per token tile, segment by segment (a segment = the range's piece of one
+// weight tile, run for every token tile before the next, so the token tiles re-read its
+// weight boxes from L2). Every output element is therefore summed over the same k-split
+// points in the same order whatever M is, and a token's projection is bit-identical in a
+// 1-row and a 1088-row GEMM. A tile split across CTAs is finished by its first
+// contributor, for which it is the last segment of its range: the later contributors reach
+// the tile at the start of their ranges, publish fp32 partials and count themselves in on
+// a per-(tile, token tile) counter; the owner waits (bounded) for that count and adds the
+// partials to its own accumulator in contributor order, so results do not depend on timing
+// and the owner never writes its own partial. A contributor publishes before it waits on
+// anything and every CTA of the grid is resident at once (one CTA per SM, at most one per
+// SM launched), so the wait always ends.
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM owner,
 // warps 2-5 = epilogue (TMEM -> registers -> global / fused LM-head reduction).
@@ -26,11 +32,12 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <map>
 #include <mutex>
-#include <set>
 #include <tuple>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -43,8 +50,7 @@ struct GemmArgs {
   int M, N, K;
   int tiles_t;        // token tiles
   int kb;             // 64-wide k-blocks
-  long long units;    // units of one slice: tiles_n * (tiles_t / slices) * kb
-  int slices;         // 1, or tiles_t: CTA c then works on token tile c % tiles_t only
+  long long units;    // units of one token tile: tiles_n * kb
   int epi;
   void* out;
   int ldo;
@@ -64,6 +70,20 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int
                                           const float* v, float* staging, int ew, int lane) {
   if constexpr (MODE == MODE_SWIGLU) {
     // accumulator rows 0-63: gate features tn*64.., rows 64-127: the matching up features.
+    if (a.epi == EPI_GU) {
+      // fp32 gate and up values to out [M][2N] (gate at f, up at N + f), for a separate
+      // SwiGLU pass that then sees exactly the values the fused epilogue would
+      const int f = tn * 64 + (row & 63);
+      if (f < a.N) {
+        float* o = reinterpret_cast<float*>(a.out) + (row < 64 ? f : a.N + f);
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+          const int j = tt * BN + c0 + i;
+          if (j < a.M) o[(size_t)j * a.ldo] = v[i];
+        }
+      }
+      return;
+    }
     // Through shared memory every thread then takes one gate/up pair for half the columns.
 #pragma unroll
     for (int i = 0; i < CH; ++i) staging[i * 128 + row] = v[i];
@@ -210,6 +230,35 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int tn, int tt, int
   }
 }
 
+// Walk over a CTA's work: the segments of its unit range [u_begin, u_end) (a segment = the
+// range's piece of one weight tile), each run for token tiles 0..TT-1 in turn.
+struct SegCursor {
+  long long u, s0, s1, end, tile;
+  int tt, TT, kb;
+  __device__ __forceinline__ void init(long long ub, long long ue, int nt, int k) {
+    end = ue; TT = nt; kb = k; tt = 0;
+    u = s0 = ub;
+    tile = ub / kb;
+    s1 = min(ue, (tile + 1) * kb);
+  }
+  __device__ __forceinline__ bool done() const { return s0 >= end; }
+  // the next unit (k-block) in issue order
+  __device__ __forceinline__ void next() {
+    if (++u < s1) return;
+    if (++tt < TT) { u = s0; return; }
+    tt = 0;
+    s0 = s1;
+    u = s0;
+    tile = s0 / kb;
+    s1 = min(end, (tile + 1) * kb);
+  }
+  // the start of the next (segment, token tile) item
+  __device__ __forceinline__ void next_item() {
+    u = s1 - 1;
+    next();
+  }
+};
+
 template <int BN, int MODE>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -230,17 +279,9 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Units are (weight tile, k-block) steps. With several token tiles, the CTAs form slices:
-  // slice c % S takes token tile c % S, and stream-K runs over the weight tiles' units within
-  // each slice, so the S CTAs of a group read the same weight boxes at the same time (one DRAM
-  // read, the rest from L2) instead of re-streaming the weight for every token tile.
-  const int S = a.slices, cta = blockIdx.x;
-  const int slice = cta % S, G = gridDim.x / S, cs = cta / S;   // G: CTAs per slice, cs: index in it
+  const int cta = blockIdx.x, G = gridDim.x, TT = a.tiles_t;
   const long long U = a.units;
-  const long long u_begin = (long long)cs * U / G, u_end = (long long)(cs + 1) * U / G;
-  // slice-local tile -> (weight tile, token tile)
-  auto tile_tn = [&](long long lt) { return (int)(S > 1 ? lt : lt / a.tiles_t); };
-  auto tile_tt = [&](long long lt) { return S > 1 ? slice : (int)(lt % a.tiles_t); };
+  const long long u_begin = (long long)cta * U / G, u_end = (long long)(cta + 1) * U / G;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -269,15 +310,9 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, issued = 0, parity = 0;
-      // The first ring of weight tiles does not depend on the previous kernel: issue it
-      // before waiting for that kernel, then add the activation halves of those stages
-      // once its outputs are visible.
-      // unit coordinates (k-block, weight tile, token tile), advanced without division
-      const long long tile0 = u_begin / a.kb;
-      const int k0 = (int)(u_begin - tile0 * a.kb), tn0 = tile_tn(tile0), tt0 = tile_tt(tile0);
-      int pk = k0, ptn = tn0, ptt = tt0;
       // weight tile (128 rows x 64 k); SwiGLU: 64 gate rows + the matching 64 up rows
-      auto load_w = [&](uint32_t dst, int k, int tn, uint32_t bar) {
+      auto load_w = [&](uint32_t dst, const SegCursor& c, uint32_t bar) {
+        const int k = (int)(c.u - c.tile * a.kb), tn = (int)c.tile;
         if constexpr (MODE == MODE_SWIGLU) {
           tma_load_2d(dst, &tmW, k * 64, tn * 64, bar, pol_w);
           tma_load_2d(dst + C::A_BYTES / 2, &tmW, k * 64, a.N + tn * 64, bar, pol_w);
@@ -285,42 +320,44 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d(dst, &tmW, k * 64, tn * 128, bar, pol_w);
         }
       };
-      auto advance = [&](int& k, int& tn, int& tt) {
-        if (++k == a.kb) {
-          k = 0;
-          if (S > 1) ++tn;
-          else if (++tt == a.tiles_t) { tt = 0; ++tn; }
-        }
+      auto load_x = [&](uint32_t dst, const SegCursor& c, uint32_t bar) {
+        tma_load_2d(dst, &tmX, (int)(c.u - c.tile * a.kb) * 64, c.tt * BN, bar, pol_x);
       };
-      const int n_pre = (int)min((long long)C::STAGES, u_end - u_begin);
-      for (int i = 0; i < n_pre; ++i) {
-        const uint32_t fb = smem_u32(full + i);
-        mbar_expect_tx(fb, C::STAGE);
-        load_w(smem_u32(smem + i * C::STAGE), pk, ptn, fb);
-        issued |= 1u << i;
-        advance(pk, ptn, ptt);
+      // The first ring of weight tiles does not depend on the previous kernel: issue it
+      // before waiting for that kernel, then add the activation halves of those stages
+      // once its outputs are visible.
+      const long long steps = (u_end - u_begin) * TT;
+      const int n_pre = (int)min((long long)C::STAGES, steps);
+      SegCursor cur;
+      cur.init(u_begin, u_end, TT, a.kb);
+      {
+        SegCursor c = cur;
+        for (int i = 0; i < n_pre; ++i) {
+          const uint32_t fb = smem_u32(full + i);
+          mbar_expect_tx(fb, C::STAGE);
+          load_w(smem_u32(smem + i * C::STAGE), c, fb);
+          issued |= 1u << i;
+          c.next();
+        }
       }
       pdl_wait();
-      {
-        int bk = k0, btn = tn0, btt = tt0;
-        for (int i = 0; i < n_pre; ++i) {
-          tma_load_2d(smem_u32(smem + i * C::STAGE) + C::A_BYTES, &tmX, bk * 64, btt * BN, smem_u32(full + i), pol_x);
-          advance(bk, btn, btt);
-        }
+      for (int i = 0; i < n_pre; ++i) {
+        load_x(smem_u32(smem + i * C::STAGE) + C::A_BYTES, cur, smem_u32(full + i));
+        cur.next();
       }
       stage = n_pre % C::STAGES;
       phase = (n_pre == C::STAGES) ? 1u : 0u;
-      for (long long u = u_begin + n_pre; u < u_end; ++u) {
+      for (long long i = n_pre; i < steps; ++i) {
         if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, abort_flag, a.err)) break;
         const uint32_t fb = smem_u32(full + stage);
         mbar_expect_tx(fb, C::STAGE);
         const uint32_t sa = smem_u32(smem + stage * C::STAGE);
-        load_w(sa, pk, ptn, fb);
-        tma_load_2d(sa + C::A_BYTES, &tmX, pk * 64, ptt * BN, fb, pol_x);
+        load_w(sa, cur, fb);
+        load_x(sa + C::A_BYTES, cur, fb);
         issued |= 1u << stage;
         parity = (parity & ~(1u << stage)) | (phase << stage);
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-        advance(pk, ptn, ptt);
+        cur.next();
       }
       if (*abort_flag) {
         for (int s = 0; s < C::STAGES; ++s)
@@ -333,22 +370,21 @@ __global__ void __launch_bounds__(192, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      long long u = u_begin;
-      while (ok && u < u_end) {
-        const long long tile = u / a.kb;
-        const long long seg_end = min(u_end, (tile + 1) * a.kb);
+      SegCursor c;
+      c.init(u_begin, u_end, TT, a.kb);
+      // one item = a segment's units for one token tile, accumulated into one TMEM buffer
+      while (ok && !c.done()) {
         if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-        const long long seg_begin = u;
-        for (; u < seg_end; ++u) {
+        for (long long u = c.s0; u < c.s1; ++u) {
           if (!mbar_wait(smem_u32(full + stage), phase, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::STAGE);
           const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + C::A_BYTES);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            tc_mma_bf16(d, da + 2 * k, db + 2 * k, IDESC, (u != seg_begin || k) ? 1u : 0u);
+            tc_mma_bf16(d, da + 2 * k, db + 2 * k, IDESC, (u != c.s0 || k) ? 1u : 0u);
           tc_commit(smem_u32(empty + stage));
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
@@ -356,6 +392,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_commit(smem_u32(tfull + acc));
         acc ^= 1;
         if (!acc) acc_phase ^= 1;
+        c.next_item();
       }
       if (!ok) {
         tc_commit(smem_u32(drain));
@@ -372,13 +409,14 @@ __global__ void __launch_bounds__(192, 1)
     const bool leader = (ew == 0 && lane == 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    long long u = u_begin;
-    while (u < u_end) {
-      const long long tile = u / a.kb;   // slice-local
-      const long long seg_end = min(u_end, (tile + 1) * a.kb);
-      const bool whole = (u == tile * a.kb) && (seg_end == (tile + 1) * a.kb);
-      const int tn = tile_tn(tile), tt = tile_tt(tile);
-      const long long gtile = (long long)tn * a.tiles_t + tt;   // counter index
+    SegCursor c;
+    c.init(u_begin, u_end, TT, a.kb);
+    while (!c.done()) {
+      const long long tile = c.tile;
+      const int tn = (int)tile, tt = c.tt;
+      const bool whole = (c.s0 == tile * a.kb) && (c.s1 == (tile + 1) * a.kb);
+      const bool last_item = c.s1 == u_end && tt == TT - 1;   // nothing follows in the TMA ring
+      const long long gtile = (long long)tn * TT + tt;        // counter index
       if (leader) bcast[0] = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag, a.err) ? 1 : 0;
       named_bar_sync(1, 128);
       const int ok = bcast[0];
@@ -398,15 +436,15 @@ __global__ void __launch_bounds__(192, 1)
         // Split tile. Its first contributor cf (whose range holds the tile's first k-block;
         // for it the tile is its last segment) owns the result; each later contributor (for
         // which the tile is its first segment) publishes a partial [BN tokens][128 features]
-        // and counts itself in. The owner waits for the count, then adds the partials to
-        // its own accumulator in contributor order.
-        // contributors as slice indices; CTA of slice index i: i * S + slice
+        // into its slot for this token tile and counts itself in. The owner waits for the
+        // count, then adds the partials to its own accumulator in contributor order.
         const int cf = cta_of_unit(tile * a.kb, U, G);
         const int cl = cta_of_unit((tile + 1) * a.kb - 1, U, G);
         const int nother = cl - cf;
         constexpr uint32_t PART = (uint32_t)BN * 128 * 4;
-        if (u != tile * a.kb) {
-          float* part = a.partials + (size_t)(cta * 2) * BN * 128;
+        auto slot = [&](int q) { return a.partials + ((size_t)q * TT + tt) * BN * 128; };
+        if (c.s0 != tile * a.kb) {
+          float* part = slot(cta);
           for (int c0 = 0; c0 < BN; c0 += ECH) {
             float v[ECH];
             if constexpr (ECH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
@@ -419,9 +457,9 @@ __global__ void __launch_bounds__(192, 1)
           named_bar_sync(1, 128);
           if (leader) red_release_add(reinterpret_cast<unsigned*>(a.counters + gtile), 1u);
         } else {
-          // the ring is idle (this is the CTA's last segment): with room, the partials come
-          // in as bulk copies, all in flight at once
-          const bool bulk = (uint32_t)nother * PART <= (uint32_t)(C::STAGES * C::STAGE);
+          // on the CTA's last item the TMA ring is idle: with room, the partials come in as
+          // bulk copies, all in flight at once
+          const bool bulk = last_item && (uint32_t)nother * PART <= (uint32_t)(C::STAGES * C::STAGE);
           if (leader) {
             bool ok = grid_wait(reinterpret_cast<const unsigned*>(a.counters + gtile), (unsigned)nother,
                                 abort_flag, a.err, false);
@@ -430,8 +468,7 @@ __global__ void __launch_bounds__(192, 1)
               fence_proxy_async_all();
               mbar_expect_tx(smem_u32(fixbar), (uint32_t)nother * PART);
               for (int q = 0; q < nother; ++q)
-                bulk_load(smem_u32(smem + (size_t)q * PART),
-                          a.partials + (size_t)(((cf + 1 + q) * S + slice) * 2) * BN * 128, PART, smem_u32(fixbar));
+                bulk_load(smem_u32(smem + (size_t)q * PART), slot(cf + 1 + q), PART, smem_u32(fixbar));
               ok = mbar_wait(smem_u32(fixbar), 0, abort_flag, a.err);
             }
             bcast[0] = ok ? 1 : 0;
@@ -451,8 +488,8 @@ __global__ void __launch_bounds__(192, 1)
                 // two contributors' loads in flight together
                 for (int cc = cf + 1; cc <= cl; cc += 2) {
                   const bool two = cc + 1 <= cl;
-                  const float* p0 = a.partials + (size_t)((cc * S + slice) * 2) * BN * 128 + c0 * 128 + row;
-                  const float* p1 = a.partials + (size_t)(((cc + 1) * S + slice) * 2) * BN * 128 + c0 * 128 + row;
+                  const float* p0 = slot(cc) + c0 * 128 + row;
+                  const float* p1 = slot(two ? cc + 1 : cc) + c0 * 128 + row;
                   float x0[ECH], x1[ECH];
 #pragma unroll
                   for (int i = 0; i < ECH; ++i) {
@@ -476,9 +513,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         named_bar_sync(1, 128);
       }
-      u = seg_end;
       acc ^= 1;
       if (!acc) acc_phase ^= 1;
+      c.next_item();
     }
   }
   tc_fence_before();
@@ -557,15 +594,16 @@ int device_sm_count() {
 
 cudaError_t raise_smem_limit(const void* func, int bytes) {
   static std::mutex mu;
-  static std::set<std::tuple<int, const void*, int>> done;
+  static std::map<std::pair<int, const void*>, int> limit;   // the limit last set, per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_tuple(dev, func, bytes);
-  if (done.count(key)) return cudaSuccess;
+  const auto key = std::make_pair(dev, func);
+  auto it = limit.find(key);
+  if (it != limit.end() && it->second >= bytes) return cudaSuccess;   // only ever raised
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert(key);
+  if (e == cudaSuccess) limit[key] = bytes;
   return e;
 }
 
@@ -579,49 +617,49 @@ int gemm_bn_for(int M) {
   return 256;
 }
 
-size_t gemm_bf16_scratch_bytes() { return (size_t)num_sms_cap() * 2 * 256 * 128 * sizeof(float); }
+// Split-tile partial sums: one slot of BN x 128 floats per (CTA, token tile).
+size_t gemm_bf16_scratch_bytes(int max_rows) {
+  const size_t tt = max_rows > 256 ? (size_t)(max_rows + 255) / 256 : 1;
+  return (size_t)num_sms_cap() * tt * 256 * 128 * sizeof(float);
+}
 
 template <int BN, int MODE>
-static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int tiles_n,
-                             cudaStream_t st) {
+static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int G, cudaStream_t st) {
   using C = TcCfg<BN>;
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemm_bf16_tc<BN, MODE>), C::SMEM);
   if (e != cudaSuccess) return e;
-  a.tiles_t = (a.M + BN - 1) / BN;
-  a.kb = (a.K + 63) / 64;
-  int G = num_sms();
-  if (G > num_sms_cap()) G = num_sms_cap();
-  // several token tiles: one slice of CTAs per token tile (see the kernel)
-  a.slices = (a.tiles_t > 1 && a.tiles_t <= G) ? a.tiles_t : 1;
-  a.units = (long long)tiles_n * (a.tiles_t / a.slices) * a.kb;
-  long long per_slice = G / a.slices;
-  if (per_slice > a.units) per_slice = a.units;
-  G = (int)per_slice * a.slices;
   launch_k(gemm_bf16_tc<BN, MODE>, G, 192, C::SMEM, st, mw, mx, a);
   return cudaGetLastError();
 }
 
 template <int BN>
-static cudaError_t launch_mode(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int tiles_n,
-                               cudaStream_t st) {
-  if (a.epi == EPI_SWIGLU) return launch_bn<BN, MODE_SWIGLU>(mw, mx, a, tiles_n, st);
-  if (a.epi == EPI_QKV) return launch_bn<BN, MODE_QKV>(mw, mx, a, tiles_n, st);
-  return launch_bn<BN, MODE_GENERIC>(mw, mx, a, tiles_n, st);
+static cudaError_t launch_mode(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int G, cudaStream_t st) {
+  if (a.epi == EPI_SWIGLU || a.epi == EPI_GU) return launch_bn<BN, MODE_SWIGLU>(mw, mx, a, G, st);
+  if (a.epi == EPI_QKV) return launch_bn<BN, MODE_QKV>(mw, mx, a, G, st);
+  return launch_bn<BN, MODE_GENERIC>(mw, mx, a, G, st);
 }
 
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
-              int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head,
-              bool cache_maps, const QkvEpi* qkv) {
+              int ldo, float* partials, size_t partial_floats, int* counters, int counters_len, int* err,
+              const HeadParams* head, bool cache_maps, const QkvEpi* qkv) {
   if (M <= 0 || N <= 0 || K <= 0 || (K % 8) != 0 || !W || !X) return -1;
   if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(X)) & 15) return -1;
-  if (epi == EPI_SWIGLU && N % 64) return -1;
+  const bool paired = epi == EPI_SWIGLU || epi == EPI_GU;
+  if (paired && N % 64) return -1;
   if (epi == EPI_QKV && (!qkv || qkv->d < 2 || qkv->d % 2 || 128 % qkv->d || N != (qkv->nq + 2 * qkv->nkv) * qkv->d))
     return -1;
   const int BN = gemm_bn_for(M);
-  const int tiles_n = epi == EPI_SWIGLU ? N / 64 : (N + 127) / 128;
-  if ((long long)tiles_n * ((M + BN - 1) / BN) > counters_len) return -2;
+  const int tiles_n = paired ? N / 64 : (N + 127) / 128;
+  const int tiles_t = (M + BN - 1) / BN;
+  if ((long long)tiles_n * tiles_t > counters_len) return -2;
+  const int kb = (K + 63) / 64;
+  const long long units = (long long)tiles_n * kb;
+  // the stream-K ranges depend on (N, K, SM count) only
+  int G = std::min(num_sms(), num_sms_cap());
+  if (G > units) G = (int)units;
+  if ((size_t)G * tiles_t * BN * 128 > partial_floats) return -2;
   CUtensorMap mw, mx;
-  if (epi == EPI_SWIGLU) {
+  if (paired) {
     if (!make_map(&mw, W, 2LL * N, K, 64, cache_maps)) return -3;
   } else if (!make_map(&mw, W, N, K, 128, cache_maps)) {
     return -3;
@@ -629,16 +667,17 @@ int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M
   if (!make_map(&mx, X, M, K, BN, cache_maps)) return -3;
   GemmArgs a{};
   a.M = M; a.N = N; a.K = K; a.epi = epi; a.out = out; a.ldo = ldo;
+  a.tiles_t = tiles_t; a.kb = kb; a.units = units;
   a.partials = partials; a.counters = counters; a.err = err;
   if (head) a.head = *head;
   if (qkv) a.qkv = *qkv;
   cudaError_t e;
   switch (BN) {
-    case 16: e = launch_mode<16>(mw, mx, a, tiles_n, st); break;
-    case 32: e = launch_mode<32>(mw, mx, a, tiles_n, st); break;
-    case 64: e = launch_mode<64>(mw, mx, a, tiles_n, st); break;
-    case 128: e = launch_mode<128>(mw, mx, a, tiles_n, st); break;
-    default: e = launch_mode<256>(mw, mx, a, tiles_n, st); break;
+    case 16: e = launch_mode<16>(mw, mx, a, G, st); break;
+    case 32: e = launch_mode<32>(mw, mx, a, G, st); break;
+    case 64: e = launch_mode<64>(mw, mx, a, G, st); break;
+    case 128: e = launch_mode<128>(mw, mx, a, G, st); break;
+    default: e = launch_mode<256>(mw, mx, a, G, st); break;
   }
   return e == cudaSuccess ? 0 : -4;
 }

@@ -30,7 +30,10 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_ADD_F32 = 2, EPI_HEAD = 3, EPI_SWIGLU = 4, EPI_QKV = 5 };
+// EPI_GU: the [gate; up] projection in the paired tile layout of EPI_SWIGLU (64 gate + the
+// matching 64 up features per tile), storing fp32 gate and up values to out [M][2N] (gate
+// at f, up at N + f); a separate SwiGLU pass over them then gives the fused epilogue's bits.
+enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_ADD_F32 = 2, EPI_HEAD = 3, EPI_SWIGLU = 4, EPI_QKV = 5, EPI_GU = 6 };
 
 // EPI_QKV: the fused [q | k | v] projection's epilogue applies rotate-half RoPE to the q and
 // k heads (pairs inside one 128-row tile: head_dim divides 128), writes q to its buffer
@@ -51,16 +54,19 @@ enum { DT_F32 = 0, DT_BF16 = 1 };
 inline int num_sms_cap() { return 192; }
 // SM count of the current device (cached per device).
 int device_sm_count();
-// Raise a kernel's dynamic shared-memory limit on the current device (once per device).
+// Raise a kernel's dynamic shared-memory limit on the current device to at least `bytes`
+// (the limit is only ever raised, so launches of any smaller size stay valid).
 cudaError_t raise_smem_limit(const void* func, int bytes);
 
 // ---- GEMMs -------------------------------------------------------------------------------
 int gemm_bn_for(int M);
-size_t gemm_bf16_scratch_bytes();
-// bf16 tcgen05 GEMM, Y[M][N] = X[M][K] W[N][K]^T. Returns 0 or a negative code.
+// partial-sum scratch of GEMMs of up to max_rows rows
+size_t gemm_bf16_scratch_bytes(int max_rows);
+// bf16 tcgen05 GEMM, Y[M][N] = X[M][K] W[N][K]^T. Returns 0 or a negative code (-2: the
+// counters or the partial-sum scratch are too small for this shape).
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
-              int ldo, float* partials, int* counters, int counters_len, int* err, const HeadParams* head,
-              bool cache_maps = true, const QkvEpi* qkv = nullptr);
+              int ldo, float* partials, size_t partial_floats, int* counters, int counters_len, int* err,
+              const HeadParams* head, bool cache_maps = true, const QkvEpi* qkv = nullptr);
 // EPI_SWIGLU: W is [2N][K] ([gate; up]), out bf16 [M][ldo] = silu(X Wg^T) * (X Wu^T); N % 64 == 0.
 // Tensor map of a bf16 row-major [rows][K] matrix (row stride ld elements, 0 = K): boxes of
 // 64 (K) x box_rows, 128-byte swizzle. Cached by (ptr, rows, K, box_rows, ld).
@@ -130,10 +136,12 @@ struct AttnArgs {
   const uint64_t* mask; // [R][mask_words]
   int mask_words;
   float scale;
-  // split-KV scratch for the tensor-core path (bf16): partial outputs and (max, sum) pairs
+  // scratch of the tensor-core path (bf16, required): each key split's partial outputs and
+  // (max, sum) pairs, merged with the row's tail in a fixed order
   float* part_o;        // [splits][R][nq][d]
   float* part_ml;       // [splits][R][nq][2]
-  size_t part_floats;   // capacity of part_o in floats (splits are capped to fit)
+  size_t part_floats;   // capacity of part_o in floats (the number of key splits is capped to fit)
+  int* err;             // device status word for bounds checks (nullable)
 };
 int attention(cudaStream_t st, int dtype, const AttnArgs& a);
 size_t attention_scratch_floats(int rows, int nq, int d);

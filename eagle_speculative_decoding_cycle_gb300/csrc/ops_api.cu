@@ -24,7 +24,7 @@ extern "C" {
 
 size_t eagle_op_gemm_scratch_bytes(int M, int N) {
   if (M <= 0 || N <= 0) return 0;
-  return al(gemm_bf16_scratch_bytes()) + al((size_t)tiles_for(M, N) * sizeof(int));
+  return al(gemm_bf16_scratch_bytes(M)) + al((size_t)tiles_for(M, N) * sizeof(int));
 }
 
 int eagle_op_gemm(int dtype, void* stream, const void* W, int N, int K, const void* X, int M, int epi, void* out,
@@ -39,8 +39,9 @@ int eagle_op_gemm(int dtype, void* stream, const void* W, int N, int K, const vo
   const int tiles_N = epi == EPI_SWIGLU ? 2 * N : N;   // SwiGLU: W has 2N rows, tiles of 64 + 64
   if (!scratch || scratch_bytes < eagle_op_gemm_scratch_bytes(M, tiles_N)) return EAGLE_ECAPACITY;
   float* part = reinterpret_cast<float*>(scratch);
-  int* cnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(scratch) + al(gemm_bf16_scratch_bytes()));
-  const int r = gemm_bf16(st, W, N, K, X, M, epi, out, ldo, part, cnt, tiles_for(M, tiles_N), nullptr, nullptr);
+  int* cnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(scratch) + al(gemm_bf16_scratch_bytes(M)));
+  const int r = gemm_bf16(st, W, N, K, X, M, epi, out, ldo, part, gemm_bf16_scratch_bytes(M) / sizeof(float), cnt,
+                          tiles_for(M, tiles_N), nullptr, nullptr);
   return r == 0 ? EAGLE_OK : (r == -4 ? EAGLE_ECUDA : EAGLE_EINVAL);
 }
 
@@ -76,8 +77,9 @@ int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, co
   } else if (dtype == EAGLE_DTYPE_BF16) {
     if (H % 8) return EAGLE_EINVAL;
     float* part = reinterpret_cast<float*>(s);
-    int* cnt = reinterpret_cast<int*>(s + al(gemm_bf16_scratch_bytes()));
-    const int r = gemm_bf16(st, W_lm, V, H, X, M, EPI_HEAD, nullptr, 0, part, cnt, tiles_for(M, V), nullptr, &p);
+    int* cnt = reinterpret_cast<int*>(s + al(gemm_bf16_scratch_bytes(M)));
+    const int r = gemm_bf16(st, W_lm, V, H, X, M, EPI_HEAD, nullptr, 0, part, gemm_bf16_scratch_bytes(M) / sizeof(float),
+                            cnt, tiles_for(M, V), nullptr, &p);
     if (r) return r == -4 ? EAGLE_ECUDA : EAGLE_EINVAL;
   } else {
     return EAGLE_EINVAL;
@@ -106,6 +108,8 @@ int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcach
     a.part_o = reinterpret_cast<float*>(scratch);
     a.part_floats = (size_t)16 * R * nq * d;
     a.part_ml = a.part_o + a.part_floats;
+  } else if (dtype != EAGLE_DTYPE_F32) {
+    return EAGLE_ECAPACITY;
   }
   const int r = attention(reinterpret_cast<cudaStream_t>(stream), dtype == EAGLE_DTYPE_F32 ? DT_F32 : DT_BF16, a);
   return r == 0 ? EAGLE_OK : (r == -1 ? EAGLE_EINVAL : EAGLE_ECUDA);

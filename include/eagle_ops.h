@@ -80,10 +80,15 @@ int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, co
  * row_seq[r] and its own key sits at slot row_slot[r]. mode 0 (causal): row r sees
  * slots <= row_slot[r]. mode 1 (tree): row r sees slots < ctx_len[seq] and slot
  * ctx_len[seq] + t for t < tree_T where bit t of mask[r][t / 64] is set.
- * Scale = 1/sqrt(d) when scale <= 0. fp32: d <= 128; bf16 (tensor cores): d in {32, 64,
- * 128}, 64 divisible by nq/nkv, tree_T <= 256. Scratch (nullable) enables split-KV on
- * the bf16 path: the key range is cut across CTAs and merged by a fixed-order
- * log-sum-exp combine. */
+ * Scale = 1/sqrt(d) when scale <= 0. fp32: d <= 128, scratch unused (nullable); bf16
+ * (tensor cores): d in {32, 64, 128}, 64 divisible by nq/nkv, tree_T <= 256, scratch of
+ * eagle_op_attention_scratch_bytes required (EAGLE_ECAPACITY without it). The bf16 path
+ * gives each row a result that does not depend on the other rows of the call: a row at
+ * logical position P (its own slot in causal mode, ctx_len + its mask's popcount - 1 in
+ * tree mode, whose ancestors must have increasing slots by depth) has its keys up to
+ * position P - 16 summed in fixed key splits on the tensor cores, its last 16 positions in
+ * position order on the FMA units, and the two merged in a fixed order; so a tree row and
+ * a causal row at the same position over the same keys give bit-identical outputs. */
 size_t eagle_op_attention_scratch_bytes(int R, int nq, int d);
 int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcache, const void* vcache,
                        void* out, int R, int nq, int nkv, int d, int cap, int rows_per_seq,

@@ -192,7 +192,14 @@ class OracleSeq:
                 for tok, lc in zip(ids, lcs):
                     table.add(tok, v, lc)
         kept = sorted(gen) if static else rerank(table, t.m)
-        flat = flatten(table, kept, self.committed[-1])
+        return self.verify(table, flatten(table, kept, self.committed[-1]))
+
+    def verify(self, table: NodeTable, flat: FlatTree) -> Plan:
+        """Step 3: the target scores the root and the kept nodes of a flattened tree in one
+        pass, each row seeing the context and its own ancestors ("EAGLE-2", "The Mask
+        Preserves Tree Semantics in One Target Pass"). Also used to verify a tree drafted
+        elsewhere (the GPU's, when a near-tie in path values made the two trees differ)."""
+        n = self.n
         rows = len(flat.token)
         pos = n + flat.depth
         slots = n + np.arange(rows)

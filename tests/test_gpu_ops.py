@@ -317,15 +317,73 @@ def test_attention_split_kv_long_context(nq, nkv, T, ctx):
     row_slot = (ctx + torch.arange(T, dtype=torch.int32)).to(DEV)
     args = (q.to(DEV), kc.to(DEV), vc.to(DEV), row_seq, row_slot, ctx_len, T, 1, T, mask)
     split = api.attention(*args).cpu().double().numpy()
-    single = api.attention(*args, split_kv=False).cpu().double().numpy()
     vis = np.zeros((T, ctx + T), dtype=bool)
     vis[:, :ctx] = True
     vis[:, ctx:] = m
     want = oracle_attention(q.double().numpy(), kc[0, :, :ctx + T].double().numpy(),
                             vc[0, :, :ctx + T].double().numpy(), vis)
     assert np.max(np.abs(split - want)) < 2e-2
-    assert np.max(np.abs(single - want)) < 2e-2
-    assert np.max(np.abs(split - single)) < 2e-2
+
+
+def _random_tree(rng, T):
+    parent = [-1] + [int(rng.integers(0, i)) for i in range(1, T)]
+    m = np.zeros((T, T), dtype=bool)
+    for i in range(T):
+        a = i
+        while a >= 0:
+            m[i, a] = True
+            a = parent[a]
+    return parent, m
+
+
+@pytest.mark.parametrize("nq,nkv,d,T,ctx", [(32, 8, 128, 61, 1300), (32, 32, 128, 61, 700), (8, 2, 32, 17, 40),
+                                            (5, 5, 64, 13, 9), (40, 40, 128, 49, 4100)])
+def test_tree_row_equals_causal_row_bitwise(nq, nkv, d, T, ctx):
+    """A tree row and plain causal decoding of the same token over the compacted cache (the
+    context, then the row's root-to-node path in consecutive slots) give bit-identical
+    attention outputs: the row's keys are summed in a decomposition fixed by its position
+    alone, whatever the other rows of the launch are. The capacity is the same for both
+    calls, as in an engine, where it fixes the key splits."""
+    g = torch.Generator().manual_seed(ctx + T)
+    rng = np.random.default_rng(ctx + T)
+    cap = ctx + T + 40
+    kc = _rand((1, nkv, cap, d), g, torch.bfloat16)
+    vc = _rand((1, nkv, cap, d), g, torch.bfloat16)
+    q = _rand((T, nq, d), g, torch.bfloat16)
+    parent, m = _random_tree(rng, T)
+    tree = api.attention(q.to(DEV), kc.to(DEV), vc.to(DEV), torch.zeros(T, dtype=torch.int32, device=DEV),
+                         (ctx + torch.arange(T, dtype=torch.int32)).to(DEV),
+                         torch.tensor([ctx], dtype=torch.int32, device=DEV), T, 1, T, _mask_words(m).to(DEV)).cpu()
+    for i in sorted({0, T - 1, int(np.argmax(m.sum(1)))} | set(rng.integers(0, T, 4).tolist())):
+        path = [j for j in range(T) if m[i, j]]            # root .. i, increasing depth
+        kp, vp = kc.clone(), vc.clone()
+        kp[0, :, ctx:ctx + len(path)] = kc[0, :, ctx + np.array(path)]
+        vp[0, :, ctx:ctx + len(path)] = vc[0, :, ctx + np.array(path)]
+        slot = ctx + len(path) - 1
+        plain = api.attention(q[i:i + 1].to(DEV), kp.to(DEV), vp.to(DEV), torch.zeros(1, dtype=torch.int32, device=DEV),
+                              torch.tensor([slot], dtype=torch.int32, device=DEV),
+                              torch.zeros(1, dtype=torch.int32, device=DEV), 1, 0).cpu()
+        assert torch.equal(plain[0], tree[i]), f"row {i} (depth {len(path) - 1})"
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (1536, 1024), (520, 2056)])
+def test_gemm_rows_do_not_depend_on_the_other_rows(N, K):
+    """A token's projection is bit-identical in GEMMs of 1, 61, 300 and 1088 rows (one to
+    five 256-row token tiles): the k-split points follow (N, K, SM count) only."""
+    g = torch.Generator().manual_seed(N + K)
+    X = _rand((1088, K), g, torch.bfloat16).to(DEV)
+    W = _rand((N, K), g, torch.bfloat16, 0.05).to(DEV)
+    full = api.gemm(W, X)
+    for M in (1, 61, 300):
+        for r0 in (0, 777):
+            sub = api.gemm(W, X[r0:r0 + M].contiguous())
+            assert torch.equal(sub, full[r0:r0 + M]), (M, r0)
+    # the paired gate/up layout with the SwiGLU epilogue: the same rows, the same bits
+    Wgu = _rand((2 * N, K), g, torch.bfloat16, 0.05).to(DEV) if N % 64 == 0 else None
+    if Wgu is not None:
+        big = api.gemm(Wgu, X, epi=4)
+        for M in (1, 64):
+            assert torch.equal(api.gemm(Wgu, X[5:5 + M].contiguous(), epi=4), big[5:5 + M])
 
 
 @pytest.mark.parametrize("M,F,K", [(61, 11008 // 4, 1024), (10, 832, 320), (1, 640, 256), (130, 704, 264)])
