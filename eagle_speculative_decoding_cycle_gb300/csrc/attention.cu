@@ -184,6 +184,8 @@ int attention(cudaStream_t st, int dtype, const AttnArgs& a) {
 //   tail  -- positions [B, P] (TAIL_MIN keys, or fewer near the start), one FFMA pass in
 //            position order;
 //   merge -- the body splits in order, then the tail, by log-sum-exp weights.
+// The body splits and the tail run as CTAs of one launch (the tail needs no body result),
+// each leaving an (m, l, o) partial; a second launch merges a row's partials in order.
 // The split length `tps` is a function of the cache capacity and the scratch size only, so
 // a verify row and the plain-decoding step at the same position go through the same
 // arithmetic and give bit-identical outputs (greedy speculative decoding then reproduces the
@@ -195,9 +197,8 @@ namespace eagle {
 constexpr int MT_KEYS = 64;       // keys per body tile
 constexpr int MT_QV = 64;         // query vectors per body CTA (rows x the GQA group)
 constexpr int TAIL_MIN = 16;      // the last TAIL_MIN positions of a row form its tail
-constexpr int MAX_SPLITS = 16;
-constexpr int TAIL_WARPS = 8;
-constexpr int TAIL_KPL = 8;       // tail keys per lane: tails of up to 256 keys
+constexpr int MAX_SPLITS = 31;    // body splits; with the tail, one partial per lane of the merge
+constexpr int TAIL_ITEMS = 8;     // (row, query head) items per tail CTA, two per warp
 
 __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -255,11 +256,218 @@ __device__ __forceinline__ RowSpan row_span(const AttnArgs& a, int r, int ctx) {
   return s;
 }
 
-// Body: CTA (KV head, block of rows, key split). Query vectors qv = (row - r0) * G + g.
-// Writes the split's (m, l, o) of every query vector whose body reaches into the split.
+// Tail of up to TAIL_ITEMS (row, query head) items of a row block: stages the plain slots of
+// their tails (positions [min body, max plain tail end)) and, in tree mode, the T tree slots;
+// then each warp takes two items: the scores in position order (four lanes per key, a
+// quarter of the head dimension each, summed (q0 + q1) + (q2 + q3)), their softmax, and P.V in
+// position order, written as the row's partial after its body splits. Training-time-test
+// chain keys are read from the cache directly.
+template <int D, int KIND>
+__device__ __forceinline__ void tail_chunk(const AttnArgs& a, int tps, int r0, int r1, int kvh, int chunk, int nB,
+                                           int tail_cap, uint8_t* smem) {
+  constexpr int LD = D + 8;
+  constexpr int DL = D / 32;                         // output dims per lane
+  constexpr int DQ = D / 4;                          // score dims per lane (a quarter)
+  __shared__ int s_P[TAIL_ITEMS], s_pe[TAIL_ITEMS], s_body[TAIL_ITEMS];
+  __shared__ int s_lo, s_hi;
+  const int G = a.nq / a.nkv;
+  const int it0 = chunk * TAIL_ITEMS;
+  const int n_items = min(TAIL_ITEMS, (r1 - r0) * G - it0);
+  if (n_items <= 0) return;
+  const int ra = r0 + it0 / G, rz = r0 + (it0 + n_items - 1) / G;   // rows [ra, rz]
+  const int nA_cap = TAIL_MIN + TAIL_ITEMS;
+  __nv_bfloat16* sAK = reinterpret_cast<__nv_bfloat16*>(smem);
+  __nv_bfloat16* sAV = sAK + (size_t)nA_cap * LD;
+  __nv_bfloat16* sBK = sAV + (size_t)nA_cap * LD;
+  __nv_bfloat16* sBV = sBK + (size_t)nB * LD;
+  uint8_t* wbase = reinterpret_cast<uint8_t*>(sBV + (size_t)nB * LD);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seq = a.row_seq[r0];
+  const int ctx = a.ctx_len[seq];
+  if (threadIdx.x <= rz - ra) {
+    const RowSpan rs = row_span(a, ra + threadIdx.x, ctx);
+    s_P[threadIdx.x] = rs.P;
+    s_pe[threadIdx.x] = rs.plain_end;
+    s_body[threadIdx.x] = rs.body;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int lo = INT32_MAX, hi = 0;
+    for (int i = 0; i <= rz - ra; ++i) {
+      lo = min(lo, s_body[i]);
+      hi = max(hi, min(s_P[i] + 1, s_pe[i]));
+    }
+    if (hi < lo) hi = lo;
+    if (hi - lo > nA_cap) { latch_error(a.err, DEVERR_BOUNDS); hi = lo; lo = -1; }
+    s_lo = lo;
+    s_hi = hi;
+  }
+  // the query vectors and the tree rows' keys come from the preceding kernel
+  PDL_ENTRY();
+  __syncthreads();
+  if (s_lo < 0) return;
+  const int lo = s_lo, nA = s_hi - s_lo;
+  const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.kcache);
+  const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.vcache);
+  auto grow = [&](int slot) -> size_t {
+    if constexpr (KIND == 1) return kv_row(a.page, seq, a.nkv, kvh, a.cap, slot);
+    else return ((size_t)seq * a.nkv + kvh) * (size_t)a.cap + slot;
+  };
+  {
+    constexpr int CH = D / 8;
+    const int nS = nA + (a.mode == 1 ? nB : 0);
+    for (int i = threadIdx.x; i < nS * CH; i += blockDim.x) {
+      const int k = i / CH, c = i % CH;
+      const bool inA = k < nA;
+      const int slot = inA ? lo + k : ctx + (k - nA);
+      const bool ok = slot >= 0 && slot < a.cap;
+      const size_t g = (ok ? grow(slot) : 0) * D + c * 8;
+      const uint4 kv = ok ? *reinterpret_cast<const uint4*>(kc + g) : make_uint4(0, 0, 0, 0);
+      const uint4 vv = ok ? *reinterpret_cast<const uint4*>(vc + g) : make_uint4(0, 0, 0, 0);
+      __nv_bfloat16* dk = inA ? sAK + (size_t)k * LD : sBK + (size_t)(k - nA) * LD;
+      __nv_bfloat16* dv = inA ? sAV + (size_t)k * LD : sBV + (size_t)(k - nA) * LD;
+      *reinterpret_cast<uint4*>(dk + c * 8) = kv;
+      *reinterpret_cast<uint4*>(dv + c * 8) = vv;
+    }
+  }
+  __syncthreads();
+  // per-warp scratch: the tail scores / probabilities and the key and value row pointers;
+  // tail_cap is a multiple of 4, so every part starts on a 16-byte boundary
+  const size_t wsz = (size_t)tail_cap * (4 + 16);
+  float* wp = reinterpret_cast<float*>(wbase + (size_t)warp * wsz);
+  const __nv_bfloat16** wk = reinterpret_cast<const __nv_bfloat16**>(wp + tail_cap);
+  const __nv_bfloat16** wv = wk + tail_cap;
+  const float sl2 = a.scale * 1.4426950408889634f;
+  const int kg = lane >> 2, qt = lane & 3;
+  for (int li = warp; li < n_items; li += blockDim.x / 32) {
+    const int it = it0 + li;
+    const int row = r0 + it / G, head = kvh * G + it % G;
+    const int i = row - ra;
+    const int P = s_P[i], pe = s_pe[i], body = s_body[i];
+    const int nt = P + 1 - body;
+    if (nt < 1 || nt > tail_cap) {             // a mask or slot the row layout does not allow
+      if (lane == 0) latch_error(a.err, DEVERR_BOUNDS);
+      continue;
+    }
+    // key and value rows of tail position body + j
+    for (int j = lane; j < nt; j += 32) {
+      const int p = body + j;
+      const __nv_bfloat16 *kr, *vr;
+      if (p < pe) {
+        kr = sAK + (size_t)(p - lo) * LD;
+        vr = sAV + (size_t)(p - lo) * LD;
+      } else if (a.mode == 1) {
+        // the (p - ctx)-th set bit of the row's ancestry mask
+        int want = p - ctx, bit = 0;
+        for (int w = 0; w < a.mask_words; ++w) {
+          uint64_t m = a.mask[(size_t)row * a.mask_words + w];
+          const int c = __popcll(m);
+          if (want < c) {
+            for (int q = 0; q < want; ++q) m &= m - 1;
+            bit = w * 64 + __ffsll((long long)m) - 1;
+            break;
+          }
+          want -= c;
+        }
+        if (bit < 0 || bit >= nB) {             // a mask bit past the tree
+          latch_error(a.err, DEVERR_BOUNDS);
+          bit = 0;
+        }
+        kr = sBK + (size_t)bit * LD;
+        vr = sBV + (size_t)bit * LD;
+      } else {
+        const int t = pe - 1;                      // training-time test: own source chain
+        const size_t gr = grow(ctx * (p - t) + t) * D;
+        kr = kc + gr;
+        vr = vc + gr;
+      }
+      wk[j] = kr;
+      wv[j] = vr;
+    }
+    // this lane's quarter of the query vector
+    float qv[DQ];
+    {
+      const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)row * a.nq + head) * D + qt * DQ;
+#pragma unroll
+      for (int c = 0; c < DQ; c += 8) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(qp + c);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h2[e]);
+          qv[c + 2 * e] = f.x;
+          qv[c + 2 * e + 1] = f.y;
+        }
+      }
+    }
+    __syncwarp();
+    // scores: key j by lanes 4 (j mod 8) .. +3, in passes of 8 keys
+    for (int j0 = 0; j0 < nt; j0 += 8) {
+      const int j = j0 + kg;
+      float part = 0.f;
+      if (j < nt) {
+        const __nv_bfloat16* kr = wk[j] + qt * DQ;
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < DQ; c += 8) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(kr + c);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            acc0 = fmaf(qv[c + 2 * e], f.x, acc0);
+            acc1 = fmaf(qv[c + 2 * e + 1], f.y, acc1);
+          }
+        }
+        part = acc0 + acc1;
+      }
+      // (q0 + q1) + (q2 + q3): additions commute, so all four lanes hold the same value
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (j < nt && qt == 0) wp[j] = part * sl2;
+    }
+    __syncwarp();
+    float mt = -INFINITY;
+    for (int j = lane; j < nt; j += 32) mt = fmaxf(mt, wp[j]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    float lt = 0.f;
+    for (int j = lane; j < nt; j += 32) {
+      const float pj = exp2f(wp[j] - mt);
+      wp[j] = pj;
+      lt += pj;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+    __syncwarp();
+    float ot[DL];
+#pragma unroll
+    for (int u = 0; u < DL; ++u) ot[u] = 0.f;
+    for (int j = 0; j < nt; ++j) {
+      const float pj = wp[j];
+      const __nv_bfloat16* vr = wv[j];
+#pragma unroll
+      for (int u = 0; u < DL; ++u) ot[u] = fmaf(pj, __bfloat162float(vr[lane + 32 * u]), ot[u]);
+    }
+    // the tail's partial goes right after the row's body splits
+    const int sq = body > 0 ? (body + tps * MT_KEYS - 1) / (tps * MT_KEYS) : 0;
+    const size_t q = ((size_t)sq * a.R + row) * a.nq + head;
+#pragma unroll
+    for (int u = 0; u < DL; ++u) a.part_o[q * D + lane + 32 * u] = ot[u];
+    if (lane == 0) {
+      a.part_ml[q * 2] = mt;
+      a.part_ml[q * 2 + 1] = lt;
+    }
+    __syncwarp();
+  }
+}
+
+// Body splits and tails: CTA (KV head, block of rows, z). z < splits: key split z of the
+// block's bodies; z >= splits: tail chunk z - splits. Query vectors qv = (row - r0) * G + g.
+// A body CTA writes the split's (m, l, o) of every query vector whose body reaches into it.
 // KIND: 0 = contiguous cache, 1 = paged cache.
 template <int D, int KIND>
-__global__ void __launch_bounds__(128, 3) attn_body_k(AttnArgs a, int tps) {
+__global__ void __launch_bounds__(128, 3) attn_split_k(AttnArgs a, int tps, int splits, int nB, int tail_cap) {
   constexpr int LD = D + 8;                      // padded smem row (bf16 elements)
   extern __shared__ __align__(16) uint8_t attn_smem[];
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(attn_smem);              // [2][64][LD]
@@ -274,9 +482,15 @@ __global__ void __launch_bounds__(128, 3) attn_body_k(AttnArgs a, int tps) {
   const int r0 = sidx * a.rows_per_seq + rb * RB;
   const int r1 = min(r0 + RB, min((sidx + 1) * a.rows_per_seq, a.R));
   if (r0 >= r1) return;
+  if (split >= splits) {
+    tail_chunk<D, KIND>(a, tps, r0, r1, kvh, split - splits, nB, tail_cap, attn_smem);
+    return;
+  }
   // Row metadata and context length were written before the preceding kernel started.
   const int seq = a.row_seq[r0];
   const int ctx = a.ctx_len[seq];
+  // tree rows' bodies end at or before the context length: a split past it has nothing to do
+  if (a.mode == 1 && split * tps * MT_KEYS >= ctx) return;
   for (int i = threadIdx.x; i < r1 - r0; i += blockDim.x) s_body[i] = row_span(a, r0 + i, ctx).body;
   __syncthreads();
   int bmax = 0;
@@ -449,218 +663,58 @@ __global__ void __launch_bounds__(128, 3) attn_body_k(AttnArgs a, int tps) {
   }
 }
 
-// Tail + merge: CTA (KV head, block of `rpc` rows of one sequence). Stages the plain slots of
-// the block's tails (positions [min body, max plain tail end)) and, in tree mode, the T tree
-// slots; then each warp takes (row, query head) items: the tail's scores in position order
-// (lane j holds tail keys j, j + 32, ..), their softmax and P.V in position order, and the
-// merge with the body splits. Training-time-test chain keys are read from the cache directly.
-template <int D, int KIND>
-__global__ void __launch_bounds__(TAIL_WARPS * 32) attn_tail_k(AttnArgs a, int tps, int rpc, int nA_cap, int nB,
-                                                              int tail_cap, int* err) {
-  constexpr int LD = D + 8;
-  constexpr int DL = D / 32;                         // output dims per lane
-  extern __shared__ __align__(16) uint8_t attn_smem[];
-  __nv_bfloat16* sAK = reinterpret_cast<__nv_bfloat16*>(attn_smem);
-  __nv_bfloat16* sAV = sAK + (size_t)nA_cap * LD;
-  __nv_bfloat16* sBK = sAV + (size_t)nA_cap * LD;
-  __nv_bfloat16* sBV = sBK + (size_t)nB * LD;
-  uint8_t* wbase = reinterpret_cast<uint8_t*>(sBV + (size_t)nB * LD);
-  __shared__ int s_P[32], s_pe[32], s_body[32];
-  __shared__ int s_lo, s_hi;
-  const int G = a.nq / a.nkv;
-  const int nbt = (a.rows_per_seq + rpc - 1) / rpc;
-  const int kvh = blockIdx.x;
-  const int sidx = blockIdx.y / nbt, rb = blockIdx.y % nbt;
-  const int r0 = sidx * a.rows_per_seq + rb * rpc;
-  const int r1 = min(r0 + rpc, min((sidx + 1) * a.rows_per_seq, a.R));
-  if (r0 >= r1) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seq = a.row_seq[r0];
-  const int ctx = a.ctx_len[seq];
-  if (threadIdx.x < r1 - r0) {
-    const RowSpan rs = row_span(a, r0 + threadIdx.x, ctx);
-    s_P[threadIdx.x] = rs.P;
-    s_pe[threadIdx.x] = rs.plain_end;
-    s_body[threadIdx.x] = rs.body;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int lo = INT32_MAX, hi = 0;
-    for (int i = 0; i < r1 - r0; ++i) {
-      lo = min(lo, s_body[i]);
-      hi = max(hi, min(s_P[i] + 1, s_pe[i]));
-    }
-    if (hi < lo) hi = lo;
-    if (hi - lo > nA_cap) { latch_error(err, DEVERR_BOUNDS); hi = lo; lo = -1; }
-    s_lo = lo;
-    s_hi = hi;
-  }
-  __syncthreads();
-  if (s_lo < 0) return;
-  const int lo = s_lo, nA = s_hi - s_lo;
-  const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.kcache);
-  const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.vcache);
-  auto grow = [&](int slot) -> size_t {
-    if constexpr (KIND == 1) return kv_row(a.page, seq, a.nkv, kvh, a.cap, slot);
-    else return ((size_t)seq * a.nkv + kvh) * (size_t)a.cap + slot;
-  };
-  // Every key was written by a kernel that completed before the body kernel released this
-  // one; only the body's partial results need the dependency wait.
-  {
-    constexpr int CH = D / 8;
-    const int nS = nA + (a.mode == 1 ? nB : 0);
-    for (int i = threadIdx.x; i < nS * CH; i += blockDim.x) {
-      const int k = i / CH, c = i % CH;
-      const bool inA = k < nA;
-      const int slot = inA ? lo + k : ctx + (k - nA);
-      const bool ok = slot >= 0 && slot < a.cap;
-      const size_t g = (ok ? grow(slot) : 0) * D + c * 8;
-      const uint4 kv = ok ? *reinterpret_cast<const uint4*>(kc + g) : make_uint4(0, 0, 0, 0);
-      const uint4 vv = ok ? *reinterpret_cast<const uint4*>(vc + g) : make_uint4(0, 0, 0, 0);
-      __nv_bfloat16* dk = inA ? sAK + (size_t)k * LD : sBK + (size_t)(k - nA) * LD;
-      __nv_bfloat16* dv = inA ? sAV + (size_t)k * LD : sBV + (size_t)(k - nA) * LD;
-      *reinterpret_cast<uint4*>(dk + c * 8) = kv;
-      *reinterpret_cast<uint4*>(dv + c * 8) = vv;
-    }
-  }
+// Merge: one warp per (row, query head). Lane s holds partial s (the body splits of the
+// row's position, then its tail); the weighted sums run in partial order.
+template <int D>
+__global__ void attn_merge_k(AttnArgs a, int tps) {
+  constexpr int DL = D / 32;
   PDL_ENTRY();
-  __syncthreads();
-  // per-warp scratch: the query vector (fp32), the tail probabilities, key and value row
-  // pointers; tail_cap is a multiple of 4, so every part starts on a 16-byte boundary
-  const size_t wsz = (size_t)D * 4 + (size_t)tail_cap * (4 + 16);
-  uint8_t* wb = wbase + (size_t)warp * wsz;
-  float* wq = reinterpret_cast<float*>(wb);
-  float* wp = wq + D;
-  const __nv_bfloat16** wk = reinterpret_cast<const __nv_bfloat16**>(wp + tail_cap);
-  const __nv_bfloat16** wv = wk + tail_cap;
-  const float sl2 = a.scale * 1.4426950408889634f;
-  const int n_items = (r1 - r0) * G;
-  for (int it = warp; it < n_items; it += TAIL_WARPS) {
-    const int i = it / G, g = it % G;
-    const int row = r0 + i, head = kvh * G + g;
-    const int P = s_P[i], pe = s_pe[i], body = s_body[i];
-    const int nt = P + 1 - body;
-    if (nt < 1 || nt > tail_cap) {             // a mask or slot the row layout does not allow
-      if (lane == 0) latch_error(err, DEVERR_BOUNDS);
-      continue;
-    }
-    {
-      const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)row * a.nq + head) * D;
-      for (int c = lane; c < D; c += 32) wq[c] = __bfloat162float(qp[c]);
-    }
-    // key and value rows of tail position body + j
-    for (int j = lane; j < nt; j += 32) {
-      const int p = body + j;
-      const __nv_bfloat16 *kr, *vr;
-      if (p < pe) {
-        kr = sAK + (size_t)(p - lo) * LD;
-        vr = sAV + (size_t)(p - lo) * LD;
-      } else if (a.mode == 1) {
-        // the (p - ctx)-th set bit of the row's ancestry mask
-        int want = p - ctx, bit = 0;
-        for (int w = 0; w < a.mask_words; ++w) {
-          uint64_t m = a.mask[(size_t)row * a.mask_words + w];
-          const int c = __popcll(m);
-          if (want < c) {
-            for (int q = 0; q < want; ++q) m &= m - 1;
-            bit = w * 64 + __ffsll((long long)m) - 1;
-            break;
-          }
-          want -= c;
-        }
-        if (bit < 0 || bit >= nB) {             // a mask bit past the tree
-          latch_error(err, DEVERR_BOUNDS);
-          bit = 0;
-        }
-        kr = sBK + (size_t)bit * LD;
-        vr = sBV + (size_t)bit * LD;
-      } else {
-        const int t = pe - 1;                      // training-time test: own source chain
-        const size_t gr = grow(ctx * (p - t) + t) * D;
-        kr = kc + gr;
-        vr = vc + gr;
-      }
-      wk[j] = kr;
-      wv[j] = vr;
-    }
-    __syncwarp();
-    // scores, in the exp2 domain
-    float x[TAIL_KPL];
-    float mt = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < TAIL_KPL; ++u) {
-      const int j = lane + 32 * u;
-      x[u] = -INFINITY;
-      if (j < nt) {
-        const __nv_bfloat16* kr = wk[j];
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < D; c += 8) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(kr + c);
-          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-          const float2 k0 = __bfloat1622float2(h2[0]), k1 = __bfloat1622float2(h2[1]);
-          const float2 k2 = __bfloat1622float2(h2[2]), k3 = __bfloat1622float2(h2[3]);
-          acc0 = fmaf(wq[c], k0.x, acc0);
-          acc1 = fmaf(wq[c + 1], k0.y, acc1);
-          acc2 = fmaf(wq[c + 2], k1.x, acc2);
-          acc3 = fmaf(wq[c + 3], k1.y, acc3);
-          acc0 = fmaf(wq[c + 4], k2.x, acc0);
-          acc1 = fmaf(wq[c + 5], k2.y, acc1);
-          acc2 = fmaf(wq[c + 6], k3.x, acc2);
-          acc3 = fmaf(wq[c + 7], k3.y, acc3);
-        }
-        x[u] = ((acc0 + acc1) + (acc2 + acc3)) * sl2;
-      }
-      mt = fmaxf(mt, x[u]);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-    float lt = 0.f;
-#pragma unroll
-    for (int u = 0; u < TAIL_KPL; ++u) {
-      const int j = lane + 32 * u;
-      const float pj = j < nt ? exp2f(x[u] - mt) : 0.f;
-      if (j < nt) wp[j] = pj;
-      lt += pj;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-    __syncwarp();
-    float ot[DL];
-#pragma unroll
-    for (int u = 0; u < DL; ++u) ot[u] = 0.f;
-    for (int j = 0; j < nt; ++j) {
-      const float pj = wp[j];
-      const __nv_bfloat16* vr = wv[j];
-#pragma unroll
-      for (int u = 0; u < DL; ++u) ot[u] = fmaf(pj, __bfloat162float(vr[lane + 32 * u]), ot[u]);
-    }
-    // merge: body splits in order, then the tail
-    const int S = body > 0 ? (body + tps * MT_KEYS - 1) / (tps * MT_KEYS) : 0;
-    float M = mt;
-    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, a.part_ml[(((size_t)sp * a.R + row) * a.nq + head) * 2]);
-    float L = 0.f, acc[DL];
-#pragma unroll
-    for (int u = 0; u < DL; ++u) acc[u] = 0.f;
-    for (int sp = 0; sp < S; ++sp) {
-      const size_t q = ((size_t)sp * a.R + row) * a.nq + head;
-      const float w = exp2f(a.part_ml[q * 2] - M);
-      L = fmaf(a.part_ml[q * 2 + 1], w, L);
-#pragma unroll
-      for (int u = 0; u < DL; ++u) acc[u] = fmaf(a.part_o[q * D + lane + 32 * u], w, acc[u]);
-    }
-    const float wt = exp2f(mt - M);
-    L = fmaf(lt, wt, L);
-#pragma unroll
-    for (int u = 0; u < DL; ++u) acc[u] = fmaf(ot[u], wt, acc[u]);
-    __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)row * a.nq + head) * D;
-#pragma unroll
-    for (int u = 0; u < DL; ++u) op[lane + 32 * u] = __float2bfloat16_rn(L > 0.f ? acc[u] / L : 0.f);
-    __syncwarp();
+  const int qi = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (qi >= a.R * a.nq) return;
+  const int row = qi / a.nq;
+  const int body = row_span(a, row, a.ctx_len[a.row_seq[row]]).body;
+  const int S = (body > 0 ? (body + tps * MT_KEYS - 1) / (tps * MT_KEYS) : 0) + 1;   // <= 32
+  const size_t stride = (size_t)a.R * a.nq;
+  float ms = -INFINITY, ls = 0.f;
+  if (lane < S) {
+    ms = a.part_ml[((size_t)lane * stride + qi) * 2];
+    ls = a.part_ml[((size_t)lane * stride + qi) * 2 + 1];
   }
+  float M = ms;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float ws = lane < S ? exp2f(ms - M) : 0.f;
+  const float lw = ls * ws;
+  float L = 0.f, acc[DL];
+#pragma unroll
+  for (int u = 0; u < DL; ++u) acc[u] = 0.f;
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float x[8][DL];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int u = 0; u < DL; ++u)
+        x[k][u] = s0 + k < S ? a.part_o[((size_t)(s0 + k) * stride + qi) * D + lane + 32 * u] : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float w = __shfl_sync(0xffffffffu, ws, (s0 + k) & 31);
+      const float l = __shfl_sync(0xffffffffu, lw, (s0 + k) & 31);
+      if (s0 + k < S) {
+        L += l;
+#pragma unroll
+        for (int u = 0; u < DL; ++u) acc[u] = fmaf(x[k][u], w, acc[u]);
+      }
+    }
+  }
+  __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)qi * D;
+#pragma unroll
+  for (int u = 0; u < DL; ++u) op[lane + 32 * u] = __float2bfloat16_rn(L > 0.f ? acc[u] / L : 0.f);
 }
 
-size_t attention_scratch_floats(int rows, int nq, int d) { return (size_t)MAX_SPLITS * rows * nq * (d + 2); }
+size_t attention_scratch_floats(int rows, int nq, int d) { return (size_t)(MAX_SPLITS + 1) * rows * nq * (d + 2); }
+
+int attention_max_splits(int cap) { return std::max(1, std::min(MAX_SPLITS, (cap + MT_KEYS - 1) / MT_KEYS)); }
 
 template <int D>
 static int launch_bf16(cudaStream_t st, const AttnArgs& a) {
@@ -669,36 +723,29 @@ static int launch_bf16(cudaStream_t st, const AttnArgs& a) {
   const int nseq = (a.R + a.rows_per_seq - 1) / a.rows_per_seq;
   const int nb = (a.rows_per_seq + RB - 1) / RB;
   if (!a.part_o || !a.part_ml) return -1;
-  // fixed key splits: a function of the capacity and the scratch only
+  // fixed key splits: a function of the capacity and the caller's constant only; partials
+  // hold the splits and one tail slot per row
   const int max_tiles = std::max(1, (a.cap + MT_KEYS - 1) / MT_KEYS);
-  const long long fit = (long long)(a.part_floats / ((size_t)a.R * a.nq * D));
+  const long long fit = (long long)(a.part_floats / ((size_t)a.R * a.nq * D)) - 1;
   if (fit < 1) return -1;
-  const int S = (int)std::min<long long>(MAX_SPLITS, fit);
+  const int S = (int)std::min<long long>(std::min(MAX_SPLITS, std::max(1, a.max_splits)), fit);
   const int tps = (max_tiles + S - 1) / S;
   const int splits = (max_tiles + tps - 1) / tps;
-  const size_t body_smem = (size_t)4 * MT_KEYS * (D + 8) * sizeof(__nv_bfloat16);
-  const bool paged = a.page.table != nullptr;
-  const void* body_fn = paged ? reinterpret_cast<const void*>(attn_body_k<D, 1>)
-                              : reinterpret_cast<const void*>(attn_body_k<D, 0>);
-  if (raise_smem_limit(body_fn, (int)body_smem) != cudaSuccess) return -4;
-  const dim3 bgrid(a.nkv, nseq * nb, splits);
-  if (paged) launch_k(attn_body_k<D, 1>, bgrid, 128, body_smem, st, a, tps);
-  else launch_k(attn_body_k<D, 0>, bgrid, 128, body_smem, st, a, tps);
-  // tail + merge: blocks of rows of one sequence, halved while the grid is under two waves
-  int rpc = std::min(a.rows_per_seq, 32);
-  const int sms = device_sm_count();
-  while (rpc > 4 && (long long)a.nkv * nseq * ((a.rows_per_seq + rpc - 1) / rpc) < 2LL * sms) rpc = (rpc + 1) / 2;
-  const int nA_cap = TAIL_MIN + rpc;
+  const int chunks = (RB * G + TAIL_ITEMS - 1) / TAIL_ITEMS;
   const int nB = a.mode == 1 ? a.tree_T : 0;
   const int tail_cap = (std::max(TAIL_MIN, a.mode == 1 ? a.tree_T : 0) + 3) & ~3;   // a multiple of 4
-  const size_t wsz = (size_t)D * 4 + (size_t)tail_cap * (4 + 16);
-  const size_t tail_smem = (size_t)2 * (nA_cap + nB) * (D + 8) * sizeof(__nv_bfloat16) + TAIL_WARPS * wsz + 16;
-  const void* tail_fn = paged ? reinterpret_cast<const void*>(attn_tail_k<D, 1>)
-                              : reinterpret_cast<const void*>(attn_tail_k<D, 0>);
-  if (raise_smem_limit(tail_fn, (int)tail_smem) != cudaSuccess) return -4;
-  const dim3 tgrid(a.nkv, nseq * ((a.rows_per_seq + rpc - 1) / rpc));
-  if (paged) launch_k(attn_tail_k<D, 1>, tgrid, TAIL_WARPS * 32, tail_smem, st, a, tps, rpc, nA_cap, nB, tail_cap, a.err);
-  else launch_k(attn_tail_k<D, 0>, tgrid, TAIL_WARPS * 32, tail_smem, st, a, tps, rpc, nA_cap, nB, tail_cap, a.err);
+  const size_t body_smem = (size_t)4 * MT_KEYS * (D + 8) * sizeof(__nv_bfloat16);
+  const size_t tail_smem = (size_t)2 * (TAIL_MIN + TAIL_ITEMS + nB) * (D + 8) * sizeof(__nv_bfloat16) +
+                           (size_t)4 * tail_cap * (4 + 16);
+  const size_t smem = std::max(body_smem, tail_smem);
+  const bool paged = a.page.table != nullptr;
+  const void* fn = paged ? reinterpret_cast<const void*>(attn_split_k<D, 1>)
+                         : reinterpret_cast<const void*>(attn_split_k<D, 0>);
+  if (raise_smem_limit(fn, (int)smem) != cudaSuccess) return -4;
+  const dim3 grid(a.nkv, nseq * nb, splits + chunks);
+  if (paged) launch_k(attn_split_k<D, 1>, grid, 128, smem, st, a, tps, splits, nB, tail_cap);
+  else launch_k(attn_split_k<D, 0>, grid, 128, smem, st, a, tps, splits, nB, tail_cap);
+  launch_k(attn_merge_k<D>, (a.R * a.nq + 3) / 4, 128, 0, st, a, tps);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

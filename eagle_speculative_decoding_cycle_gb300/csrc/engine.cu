@@ -233,9 +233,11 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
   x->gemm_cnt_len = 65536;
   x->gemm_cnt = c.take<int>(x->gemm_cnt_len);
   {
-    // 16 key splits for the cycle's launches; launches with more rows (prefill chunks) run
-    // fewer, longer splits in the same space
-    const int rs = std::max(std::max(std::max(z.B * z.T1, z.B * (z.D + 1)), z.B * z.k) * 16, z.R);
+    // the key splits of the cycle's launches (one per 64-key tile of the larger cache, up to
+    // 32); launches with more rows (prefill chunks) run fewer, longer splits in the same space
+    // (plus one tail partial per row)
+    const int ns = std::max(attention_max_splits(z.cap), attention_max_splits(z.dcap)) + 1;
+    const int rs = std::max(std::max(std::max(z.B * z.T1, z.B * (z.D + 1)), z.B * z.k) * ns, 2 * z.R);
     x->attn_pfloats = (size_t)rs * z.nq * z.d;
     x->attn_po = c.take<float>(x->attn_pfloats);
     x->attn_pml = c.take<float>((size_t)rs * z.nq * 2);
@@ -344,6 +346,7 @@ int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_
   a.page = page;
   a.part_o = ctx->attn_po; a.part_ml = ctx->attn_pml; a.part_floats = ctx->attn_pfloats;
   a.err = ctx->dev_err;
+  a.max_splits = attention_max_splits(cap);   // fixed per cache: verify and plain decoding agree
   CK(attention(ctx->st, z.dt, a));
   return 0;
 }
@@ -368,9 +371,12 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   if (r) return r;
   CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
   CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
-  if (z.dt == DT_BF16 && z.F % 64 == 0) {
-    // gate and up rows of each 64 features share one tile; SwiGLU in the epilogue from 128
-    // rows on, else a separate pass over the stored gate/up values (the same bits either way)
+  // With more than one sequence, the verify pass (B(m+1) rows) and plain decoding (B rows)
+  // straddle the 128-row point where the SwiGLU epilogue pays off: both then use the paired
+  // [gate; up] tile layout, fused or not, which gives the same bits either way. One sequence
+  // keeps the plain layout (a 128-row weight box per stage) for every launch, unless
+  // EAGLE_FUSE_EPI is set either way (then both settings share the paired layout).
+  if (z.dt == DT_BF16 && z.F % 64 == 0 && (ctx->batch > 1 || ctx->fuse_epi >= 0)) {
     if (ctx->fuse_epi > 0 || (ctx->fuse_epi < 0 && R >= 128)) {
       CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_SWIGLU, ctx->hb, z.F));
     } else {

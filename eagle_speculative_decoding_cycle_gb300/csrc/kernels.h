@@ -142,9 +142,14 @@ struct AttnArgs {
   float* part_ml;       // [splits][R][nq][2]
   size_t part_floats;   // capacity of part_o in floats (the number of key splits is capped to fit)
   int* err;             // device status word for bounds checks (nullable)
+  int max_splits;       // key splits of the bf16 path (1..32): a constant of the caller, so that
+                        // every launch over one cache sums a row's keys in the same splits
 };
 int attention(cudaStream_t st, int dtype, const AttnArgs& a);
 size_t attention_scratch_floats(int rows, int nq, int d);
+// the key splits to use for a cache of `cap` slots (one 64-key tile per split, up to 31);
+// the partial buffer needs one more slot per row for the tail
+int attention_max_splits(int cap);
 
 // ---- tree policy, acceptance, compaction ---------------------------------------------------
 struct TreeState;   // defined in tree.cu / engine

@@ -106,8 +106,9 @@ int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcach
   a.mask = mask; a.mask_words = mask_words; a.scale = scale > 0.f ? scale : 1.f / sqrtf((float)d);
   if (scratch && scratch_bytes >= eagle_op_attention_scratch_bytes(R, nq, d)) {
     a.part_o = reinterpret_cast<float*>(scratch);
-    a.part_floats = (size_t)16 * R * nq * d;
+    a.part_floats = attention_scratch_floats(R, nq, d) / (d + 2) * d;
     a.part_ml = a.part_o + a.part_floats;
+    a.max_splits = 32;
   } else if (dtype != EAGLE_DTYPE_F32) {
     return EAGLE_ECAPACITY;
   }

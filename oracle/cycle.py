@@ -110,9 +110,10 @@ class OracleSeq:
             return -1
         return int(self.R[c + d])
 
-    def _candidates(self, feat_row: np.ndarray, plant_tok: int, cycle: int, depth: int):
-        """Drafter LM head + softmax + top-k for one row, with planting. Returns (ids, log c fp32)."""
-        l = self.M.logits(feat_row[None, :])[0]
+    def _candidates(self, feat_row: np.ndarray, plant_tok: int, cycle: int, depth: int, logits=None):
+        """Drafter LM head + softmax + top-k for one row, with planting. Returns (ids, log c fp32).
+        `logits`: the row's LM-head output when the caller computed it with other rows."""
+        l = self.M.logits(feat_row[None, :])[0] if logits is None else logits
         if plant_tok >= 0:
             u = philox.draw_uniform(self.seed, philox.STREAM_PLANT, self.seq, cycle, depth, 0)
             if F32(u) < F32(self.t.planted_p):
@@ -185,10 +186,12 @@ class OracleSeq:
                 for a in table.path(v):
                     vis[r, slot_of[a]] = True
             out = self.M.drafter_rows(feats, toks, pos, self.dkv, slots, vis)
+            lg = self.M.logits(out)       # the shared LM head over all expanded rows at once
             for r, v in enumerate(E):
                 feat_of[v] = out[r]
                 path_tokens = [table.token[a] for a in table.path(v)]
-                ids, lcs = self._candidates(out[r], self._planted_token(path_tokens), self.cycle_idx, d + 1)
+                ids, lcs = self._candidates(out[r], self._planted_token(path_tokens), self.cycle_idx, d + 1,
+                                            logits=lg[r])
                 for tok, lc in zip(ids, lcs):
                     table.add(tok, v, lc)
         kept = sorted(gen) if static else rerank(table, t.m)

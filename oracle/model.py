@@ -137,9 +137,29 @@ class Layer:
         self.norm_e = W.get(prefix + "norm_e")
 
 
+_UPCAST = {"buf": np.empty(0)}
+
+
 def mm(a: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """a [R, K] (fp64) times w[N, K]^T with fp64 accumulation."""
-    return np.asarray(a, np.float64) @ np.asarray(w, np.float64).T
+    """a [R, K] (fp64) times w[N, K]^T with fp64 accumulation.
+
+    A float32 w is upcast to float64 exactly, a block of rows at a time into one reused
+    buffer (so a large LM head is never copied whole); each output element is the same
+    fp64 dot product either way."""
+    a = np.asarray(a, np.float64)
+    if w.dtype == np.float64:
+        return a @ w.T
+    N, K = w.shape
+    step = max(1, min(N, (1 << 25) // max(K, 1)))     # rows per block: about 256 MB of fp64
+    if _UPCAST["buf"].size < step * K:
+        _UPCAST["buf"] = np.empty(step * K, np.float64)
+    out = np.empty((a.shape[0], N))
+    for n0 in range(0, N, step):
+        n1 = min(N, n0 + step)
+        wb = _UPCAST["buf"][:(n1 - n0) * K].reshape(n1 - n0, K)
+        np.copyto(wb, w[n0:n1])
+        out[:, n0:n1] = a @ wb.T
+    return out
 
 
 class Model:

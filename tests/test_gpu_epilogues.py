@@ -50,11 +50,17 @@ def _run(wl, weights, prompts, max_batch=1, fuse: bool = True):
     return res
 
 
-@pytest.mark.parametrize("name", ["small-bf16-3L-H320", "small-bf16-eagle3-gqa"])
+WIDE = synth.SMALL_BF16.replace(
+    name="wide-bf16-2L-H1024",
+    model=synth.ModelShape(n_layers=2, hidden=1024, n_heads=8, n_kv_heads=8, head_dim=128, ffn=2816, vocab=1000,
+                           rope_theta=1e4, dtype="bf16"))
+
+
+@pytest.mark.parametrize("name", ["small-bf16-3L-H320", "small-bf16-eagle3-gqa", "wide-bf16-2L-H1024"])
 def test_fused_epilogues_match_separate_kernels(name):
     """RoPE/KV-write and SwiGLU in the GEMM epilogues against the separate row kernels: the
     same fp32 values go through the same arithmetic, so every output is bit-identical."""
-    wl = {w.name: w for w in (synth.SMALL_BF16, synth.SMALL_BF16_E3)}[name]
+    wl = {w.name: w for w in (synth.SMALL_BF16, synth.SMALL_BF16_E3, WIDE)}[name]
     weights = {k: v.to(DEV) for k, v in synth.make_weights(wl, "cpu").items()}
     prompts = synth.make_prompts(wl)[:1]
     a = _run(wl, weights, prompts, fuse=True)
