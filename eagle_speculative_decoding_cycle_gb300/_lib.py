@@ -24,7 +24,7 @@ DEBUG_LOGITS = 1
 # every symbol the headers declare (checked by the CPU test suite)
 EXPORTED = [
     "eagle_workspace_bytes", "eagle_create", "eagle_prefill", "eagle_cycle", "eagle_decode_plain",
-    "eagle_set_graph", "eagle_cycle_kernel_launches", "eagle_status_sync", "eagle_dump_bytes", "eagle_debug_dump", "eagle_set_debug",
+    "eagle_set_graph", "eagle_set_stop", "eagle_set_tree_budget", "eagle_cycle_kernel_launches", "eagle_status_sync", "eagle_dump_bytes", "eagle_debug_dump", "eagle_set_debug",
     "eagle_kv_view", "eagle_kv_table", "eagle_set_static_tree", "eagle_ttt_forward", "eagle_profile_begin", "eagle_profile_end", "eagle_profile_verify", "eagle_last_error", "eagle_destroy",
     "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_gemm_noalloc", "eagle_op_gemm_noalloc_status",
     "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
@@ -76,6 +76,8 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_cycle": (i32, [vp, vp, vp]),
         "eagle_decode_plain": (i32, [vp, i32, vp, vp]),
         "eagle_set_graph": (i32, [vp, i32]),
+        "eagle_set_stop": (i32, [vp, i32, vp]),
+        "eagle_set_tree_budget": (i32, [vp, i32, i32]),
         "eagle_cycle_kernel_launches": (i32, [vp]),
         "eagle_status_sync": (i32, [vp]),
         "eagle_dump_bytes": (sz, [vp, i32]),

@@ -7,6 +7,7 @@ and outputs) and the CUDA stream.
 from __future__ import annotations
 
 import ctypes as C
+import dataclasses
 from typing import Dict, List, Optional, Sequence
 
 import torch
@@ -46,6 +47,7 @@ class Engine:
                  stream: Optional[torch.cuda.Stream] = None, kv_block: Optional[int] = None):
         self.lib = L.lib()
         self.w = w
+        self.k_created = w.tree.topk
         self.weights = weights
         self.stream = stream
         self.mc, self.dc, self.tc, self.lim = configs(w, max_batch, max_ctx, prefill_chunk, kv_block)
@@ -97,6 +99,18 @@ class Engine:
 
     def decode_plain(self, n: int, out: torch.Tensor, margin: Optional[torch.Tensor] = None) -> None:
         self._check(self.lib.eagle_decode_plain(self.h, n, _ptr(out), _ptr(margin)), "eagle_decode_plain")
+
+    def set_stop(self, limits: Sequence[int]) -> None:
+        """Per-sequence limits on committed tokens (the prefill token included); an empty list
+        removes them. A finished sequence is masked out of later cycles."""
+        n = len(limits)
+        arr = (C.c_int32 * max(n, 1))(*limits)
+        self._check(self.lib.eagle_set_stop(self.h, n, arr), "eagle_set_stop")
+
+    def set_tree_budget(self, topk: int, m: int) -> None:
+        """Lower the tree's k and m for the next cycles (at most the created values)."""
+        self._check(self.lib.eagle_set_tree_budget(self.h, topk, m), "eagle_set_tree_budget")
+        self.w = self.w.replace(tree=dataclasses.replace(self.w.tree, topk=topk, m=m))
 
     def set_graph(self, on: bool) -> None:
         self._check(self.lib.eagle_set_graph(self.h, int(on)), "eagle_set_graph")
@@ -172,7 +186,8 @@ class Engine:
             s = i32(0, 7 * B * 4).view(7, B)
             return dict(zip(["ctx_len", "root_tok", "committed", "on_track", "cycle", "acc_len", "bonus"], s))
         if what == L.DUMP_CAND:
-            return i32(0, B * k * 4).view(B, k), f32(B * k * 4, 2 * B * k * 4).view(B, k)
+            kc = self.k_created
+            return i32(0, B * kc * 4).view(B, kc), f32(B * kc * 4, 2 * B * kc * 4).view(B, kc)
         if what == L.DUMP_NODES:
             n = B * NG * 4
             return (i32(0, n).view(B, NG), i32(n, 2 * n).view(B, NG), i32(2 * n, 3 * n).view(B, NG),

@@ -26,6 +26,17 @@ __global__ void accept_k(CycleDev c, HeadOut h, int* out_tokens, int* out_count)
     for (int r = threadIdx.x; r < T1; r += blockDim.x)
       c.margin[rb + r] = h.top_val[(size_t)(rb + r) * h.K] - h.top_val[(size_t)(rb + r) * h.K + 1];
   if (threadIdx.x) return;
+  const int cc = c.committed[b];
+  const int stop = c.stop_at ? c.stop_at[b] : INT32_MAX;
+  if (cc >= stop) {
+    // finished: masked out of this and every later cycle, its state left as it is (its rows
+    // still go through the fixed-shape cycle; nothing of them is committed)
+    c.acc_len[b] = 0;
+    c.bonus[b] = c.root_tok[b];
+    c.n_old[b] = c.ctx_len[b];
+    if (out_count) out_count[b] = 0;
+    return;
+  }
   int u = 0, L = 0, bonus = -1;
   while (true) {
     const int row = rb + u;
@@ -54,14 +65,14 @@ __global__ void accept_k(CycleDev c, HeadOut h, int* out_tokens, int* out_count)
   }
   c.acc_len[b] = L;
   c.bonus[b] = bonus;
-  const int cc = c.committed[b];
   int on = c.on_track[b];
   for (int j = 0; j <= L; ++j) {
     const int t = j < L ? c.tree_tok[rb + c.acc_path[b * c.D + j]] : bonus;
     if (out_tokens) out_tokens[b * (c.D + 1) + j] = t;
     if (c.ref) on = on && (cc + j < c.ref_len) && c.ref[(size_t)b * c.ref_len + cc + j] == t;
   }
-  if (out_count) out_count[b] = L + 1;
+  // the last cycle of a sequence with a limit emits only up to the limit
+  if (out_count) out_count[b] = min(L + 1, stop - cc);
   c.on_track[b] = on;
   c.committed[b] = cc + L + 1;
   c.root_tok[b] = bonus;

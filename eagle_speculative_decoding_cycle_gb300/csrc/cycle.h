@@ -11,6 +11,7 @@ namespace eagle {
 
 struct CycleDev {
   int B, k, D, m, T1, NG, V;
+  int kc;                   // root candidates kept per sequence (>= k; the tree uses the first k)
   int dmask_words, tmask_words;
   int fsrc_rows;            // 1 + (D - 1) * k feature rows per sequence (row 0 = root feature)
   // tree policy: 0 = EAGLE-2 dynamic (expand by path value, rerank the top m); 1 = static
@@ -23,6 +24,7 @@ struct CycleDev {
   int* n_old;               // [B] n at the start of the running cycle
   int* root_tok;            // [B] last committed token (not yet in the KV cache)
   int* committed;           // [B] tokens committed since prefill (the prefill token included)
+  const int* stop_at;       // [B] a sequence with committed >= stop_at is finished (INT32_MAX: none)
   int* on_track;            // [B] committed tokens equal the planted reference so far
   uint32_t* cycle;          // [B] cycle counter (Philox field)
   const int* ref;           // [B][ref_len] planted reference continuation (null: not planted)
@@ -30,9 +32,9 @@ struct CycleDev {
   float planted_p, planted_conf, inv_t;
   uint64_t seed;
   int sampling;             // 1 = speculative sampling, 0 = greedy
-  // depth-1 candidates of the root
-  int* cand_tok;            // [B][k]
-  float* cand_logc;         // [B][k]
+  // depth-1 candidates of the root, in rank order
+  int* cand_tok;            // [B][kc]
+  float* cand_logc;         // [B][kc]
   int* root_plant;          // [B] planted-candidate id for the root's drafter row (-1 none)
   // node table (generation order)
   int* node_tok;            // [B][NG]

@@ -13,6 +13,7 @@
 #include <cstring>
 #include <string>
 #include <algorithm>
+#include <climits>
 #include <vector>
 
 #include "../../include/eagle.h"
@@ -118,7 +119,8 @@ bool derive(const eagle_model_cfg* mc, const eagle_drafter_cfg* dc, const eagle_
 }  // namespace
 
 struct eagle_ctx {
-  Dims z;
+  Dims z;             // current dimensions (k and m may be lowered between cycles)
+  Dims zc;            // dimensions at creation: the workspace is carved for these
   eagle_model_cfg mc;
   eagle_drafter_cfg dc;
   eagle_tree_cfg tc;
@@ -148,6 +150,7 @@ struct eagle_ctx {
   // buffers
   int* dev_err;
   int *ctx_len, *n_old, *root_tok, *committed, *on_track, *root_plant, *acc_len, *bonus, *acc_path, *root_row, *iota;
+  int* stop_at;       // [B] committed-token limit of each sequence (INT32_MAX: none)
   uint32_t *cycle, *plain_step;
   int *cand_tok; float* cand_logc;
   int *node_tok, *node_parent, *node_depth, *node_rank, *exp_node; float* node_logv;
@@ -191,6 +194,7 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
   x->committed = c.take<int>(B); x->on_track = c.take<int>(B); x->root_plant = c.take<int>(B);
   x->acc_len = c.take<int>(B); x->bonus = c.take<int>(B); x->acc_path = c.take<int>((size_t)B * z.D);
   x->root_row = c.take<int>(B); x->iota = c.take<int>(std::max(B, z.R));
+  x->stop_at = c.take<int>(B);
   x->cycle = c.take<uint32_t>(B); x->plain_step = c.take<uint32_t>(4);
   x->cand_tok = c.take<int>((size_t)B * z.k); x->cand_logc = c.take<float>((size_t)B * z.k);
   x->node_tok = c.take<int>((size_t)B * z.NG); x->node_parent = c.take<int>((size_t)B * z.NG);
@@ -464,8 +468,10 @@ void fill_cd(eagle_ctx* ctx) {
   CycleDev& c = ctx->cd;
   c.B = ctx->batch > 0 ? ctx->batch : z.B;
   c.k = z.k; c.D = z.D; c.m = z.m; c.T1 = z.T1; c.NG = z.NG; c.V = z.V;
+  c.kc = ctx->zc.k;
   c.dmask_words = z.dmw; c.tmask_words = z.tmw; c.fsrc_rows = z.fsrc_rows;
   c.ctx_len = ctx->ctx_len; c.n_old = ctx->n_old; c.root_tok = ctx->root_tok; c.committed = ctx->committed;
+  c.stop_at = ctx->stop_at;
   c.on_track = ctx->on_track; c.cycle = ctx->cycle;
   c.planted_p = ctx->tc.planted_p; c.planted_conf = ctx->tc.planted_conf;
   c.inv_t = ctx->tc.temperature > 0.f ? 1.f / ctx->tc.temperature : 1.f;
@@ -659,13 +665,13 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   // root feature of each sequence -> fsrc row b * fsrc_rows, and the LM-head input rows
   CK(gather_rows(ctx->st, rb, ctx->dout, rb, ctx->root_row, B, ctx->fsrc, (size_t)z.fsrc_rows * rb));
   CK(gather_rows(ctx->st, rb, ctx->dout, rb, ctx->root_row, B, ctx->ebuf, rb));
-  HeadParams q = head_params(ctx, B, z.k);
+  HeadParams q = head_params(ctx, B, ctx->zc.k);
   q.lse_excl = 1;
   q.specials = ctx->root_plant;
   q.S = 1;
   r = lm_head(ctx, ctx->ebuf, B, q);
   if (r) return r;
-  CK(root_candidates(ctx->st, c, head_out(ctx, z.k, 1), 1));
+  CK(root_candidates(ctx->st, c, head_out(ctx, ctx->zc.k, 1), 1));
   return 0;
 }
 
@@ -712,14 +718,23 @@ int prefill_batched(eagle_ctx* ctx, int B, int n, const int* tokens) {
   const uint8_t* last = (const uint8_t*)ctx->dout + (size_t)(n - 1) * rb;
   CK(gather_rows(ctx->st, rb, last, (size_t)n * rb, nullptr, B, ctx->fsrc, (size_t)z.fsrc_rows * rb));
   CK(gather_rows(ctx->st, rb, last, (size_t)n * rb, nullptr, B, ctx->ebuf, rb));
-  HeadParams q = head_params(ctx, B, z.k);
+  HeadParams q = head_params(ctx, B, ctx->zc.k);
   q.lse_excl = 1;
   q.specials = ctx->root_plant;
   q.S = 1;
   r = lm_head(ctx, ctx->ebuf, B, q);
   if (r) return r;
-  CK(root_candidates(ctx->st, c, head_out(ctx, z.k, 1), 0));
+  CK(root_candidates(ctx->st, c, head_out(ctx, ctx->zc.k, 1), 0));
   return 0;
+}
+
+// No sequence has a limit (a fresh batch of sequences starts unlimited).
+int clear_stops(eagle_ctx* ctx) {
+  std::vector<int> none(ctx->z.B, INT32_MAX);
+  return cudaMemcpyAsync(ctx->stop_at, none.data(), none.size() * sizeof(int), cudaMemcpyHostToDevice, ctx->st) ==
+                 cudaSuccess
+             ? 0
+             : -4;
 }
 
 int check_dev_error(eagle_ctx* ctx) {
@@ -797,6 +812,7 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
   if (getenv("EAGLE_FAULT") && strcmp(getenv("EAGLE_FAULT"), "create") == 0) return EAGLE_ECUDA;
   eagle_ctx* ctx = new eagle_ctx();
   ctx->z = z;
+  ctx->zc = z;
   ctx->mc = *model; ctx->dc = *drafter; ctx->tc = *tree; ctx->lim = *limits;
   ctx->w = *weights;
   ctx->layers.assign(weights->layers, weights->layers + model->n_layers);
@@ -825,6 +841,7 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
     return EAGLE_ECUDA;
   }
   launch_k(iota_k, (std::max(z.B, z.R) + 127) / 128, 128, 0, ctx->st, ctx->iota, std::max(z.B, z.R));
+  if (clear_stops(ctx)) { delete ctx; return EAGLE_ECUDA; }
   if (ctx->page.table)   // no blocks assigned yet (zero would name block 0)
     launch_k(kv_reset_k, (z.nblk + 255) / 256, 256, 0, ctx->st, ctx->kv_table, z.nblk, ctx->kv_next);
   if (cudaStreamSynchronize(ctx->st) != cudaSuccess) { delete ctx; return EAGLE_ECUDA; }
@@ -859,6 +876,7 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
   ctx->cd.ref = d_ref;
   ctx->cd.ref_len = ctx->ref_len;
   CycleDev& c = ctx->cd;
+  CK(clear_stops(ctx));
   if (ctx->page.table) {
     // the sequences start anew: empty block table, then blocks for every prompt slot
     launch_k(kv_reset_k, (z.nblk + 255) / 256, 256, 0, ctx->st, ctx->kv_table, z.nblk, ctx->kv_next);
@@ -924,13 +942,13 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
         const uint8_t* last = (const uint8_t*)ctx->dout + (size_t)(R - 1) * rb;
         CK(gather_rows(ctx->st, rb, last, rb, nullptr, 1, (uint8_t*)ctx->fsrc + (size_t)b * z.fsrc_rows * rb, rb));
         CK(gather_rows(ctx->st, rb, last, rb, nullptr, 1, ctx->ebuf, rb));
-        HeadParams q = head_params(ctx, 1, z.k);
+        HeadParams q = head_params(ctx, 1, ctx->zc.k);
         q.lse_excl = 1;
         q.specials = ctx->root_plant + b;
         q.S = 1;
         r = lm_head(ctx, ctx->ebuf, 1, q);
         if (r) return r;
-        CK(root_candidates_seq(ctx->st, c, head_out(ctx, z.k, 1), b));
+        CK(root_candidates_seq(ctx->st, c, head_out(ctx, ctx->zc.k, 1), b));
       }
     }
     off += n;
@@ -1013,6 +1031,51 @@ int eagle_decode_plain(eagle_ctx* ctx, int n_steps, int32_t* d_out_tokens, float
     CK(plain_advance(ctx->st, c, ctx->h_id, p.K, ctx->h_val, d_out_tokens, d_out_margin, n_steps, s));
   }
   ctx->host_ctx_bound += n_steps;
+  return EAGLE_OK;
+}
+
+int eagle_set_stop(eagle_ctx* ctx, int n, const int32_t* h_limits) {
+  if (!ctx) return EAGLE_EINVAL;
+  if (n == 0) {
+    CK(clear_stops(ctx));
+    return EAGLE_OK;
+  }
+  if (n != ctx->batch || !h_limits) return fail(ctx, EAGLE_EINVAL, "one limit per sequence of the batch");
+  std::vector<int> lim(ctx->z.B, INT32_MAX);
+  for (int b = 0; b < n; ++b) {
+    if (h_limits[b] < 1) return fail(ctx, EAGLE_EINVAL, "limits must be >= 1 committed token");
+    lim[b] = h_limits[b];
+  }
+  if (cudaMemcpyAsync(ctx->stop_at, lim.data(), lim.size() * sizeof(int), cudaMemcpyHostToDevice, ctx->st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(ctx->st) != cudaSuccess)
+    return fail(ctx, EAGLE_ECUDA, "limit upload failed");
+  return EAGLE_OK;
+}
+
+int eagle_set_tree_budget(eagle_ctx* ctx, int topk, int m) {
+  if (!ctx) return EAGLE_EINVAL;
+  const Dims& zc = ctx->zc;
+  Dims& z = ctx->z;
+  const int NG = topk + (z.D - 1) * topk * topk;
+  if (topk < 1 || topk > zc.k || m < 1 || m > zc.m || m > NG)
+    return fail(ctx, EAGLE_EINVAL, "topk and m must be at most the values the context was created with");
+  if (ctx->static_on) return fail(ctx, EAGLE_EINVAL, "a static tree is set: remove it first");
+  z.k = topk;
+  z.m = m;
+  z.T1 = m + 1;
+  z.NG = NG;
+  z.dmw = std::max(1, ((z.D - 1) * topk + 63) / 64);
+  z.tmw = (z.T1 + 63) / 64;
+  z.Kh = std::max(topk, 2);
+  ctx->tc.topk = topk;
+  ctx->tc.m = m;
+  const int32_t* ref = ctx->cd.ref;
+  const int ref_len = ctx->cd.ref_len;
+  fill_cd(ctx);
+  ctx->cd.ref = ref;
+  ctx->cd.ref_len = ref_len;
+  if (ctx->graph) { cudaGraphExecDestroy(ctx->graph); ctx->graph = nullptr; }   // the sizes are kernel arguments
   return EAGLE_OK;
 }
 
@@ -1101,7 +1164,7 @@ size_t eagle_dump_bytes(const eagle_ctx* ctx, int what) {
   const size_t B = ctx->batch;
   switch (what) {
     case EAGLE_DUMP_STATE: return 7 * B * 4;
-    case EAGLE_DUMP_CAND: return 2 * B * z.k * 4;
+    case EAGLE_DUMP_CAND: return 2 * B * ctx->zc.k * 4;
     case EAGLE_DUMP_NODES: return 4 * B * z.NG * 4;
     case EAGLE_DUMP_TREE: return 4 * B * z.T1 * 4 + B * z.T1 * z.tmw * 8;
     case EAGLE_DUMP_ACCEPT: return (2 * B + B * z.D) * 4;
@@ -1133,7 +1196,7 @@ int eagle_debug_dump(eagle_ctx* ctx, int what, void* dst, size_t bytes) {
       cp(ctx->ctx_len, B * 4); cp(ctx->root_tok, B * 4); cp(ctx->committed, B * 4); cp(ctx->on_track, B * 4);
       cp(ctx->cycle, B * 4); cp(ctx->acc_len, B * 4); cp(ctx->bonus, B * 4);
       break;
-    case EAGLE_DUMP_CAND: cp(ctx->cand_tok, B * z.k * 4); cp(ctx->cand_logc, B * z.k * 4); break;
+    case EAGLE_DUMP_CAND: cp(ctx->cand_tok, B * ctx->zc.k * 4); cp(ctx->cand_logc, B * ctx->zc.k * 4); break;
     case EAGLE_DUMP_NODES:
       cp(ctx->node_tok, B * z.NG * 4); cp(ctx->node_parent, B * z.NG * 4); cp(ctx->node_depth, B * z.NG * 4);
       cp(ctx->node_logv, B * z.NG * 4);

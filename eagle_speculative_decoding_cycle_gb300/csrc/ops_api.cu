@@ -155,6 +155,7 @@ int eagle_op_tree_build(void* stream, int B, int k, int depth, int m, const int3
   c.dmask_words = dmw; c.tmask_words = (T1 + 63) / 64; c.fsrc_rows = 1 + (depth - 1) * k;
   c.ctx_len = const_cast<int*>(ctx_len);
   c.root_tok = const_cast<int*>(root_tok);
+  c.kc = k;
   c.cand_tok = const_cast<int*>(cand_tok);
   c.cand_logc = const_cast<float*>(cand_logc);
   c.node_tok = node_tok; c.node_parent = node_parent; c.node_depth = node_depth; c.node_logv = node_logv;

@@ -60,10 +60,10 @@ __global__ void tree_start_k(CycleDev c) {
   const int base = b * c.NG;
   for (int i = threadIdx.x; i < c.NG; i += blockDim.x) c.node_rank[base + i] = -1;
   for (int i = threadIdx.x; i < c.k; i += blockDim.x) {
-    c.node_tok[base + i] = c.cand_tok[b * c.k + i];
+    c.node_tok[base + i] = c.cand_tok[b * c.kc + i];
     c.node_parent[base + i] = -1;
     c.node_depth[base + i] = 1;
-    c.node_logv[base + i] = c.cand_logc[b * c.k + i];
+    c.node_logv[base + i] = c.cand_logc[b * c.kc + i];
   }
   if (threadIdx.x == 0) c.n_old[b] = c.ctx_len[b];
 }
@@ -340,10 +340,10 @@ __global__ void root_candidates_k(CycleDev c, HeadOut h, int seq_lo, int advance
         special >= 0 && draw_uniform(c.seed, STREAM_PLANT, (uint32_t)b, cyc, 1u, 0u) < c.planted_p;
     int tok[16];
     float lc[16];
-    compose_candidates(h, row, special, planted, c.planted_conf, c.k, tok, lc);
-    for (int i = 0; i < c.k; ++i) {
-      c.cand_tok[b * c.k + i] = tok[i];
-      c.cand_logc[b * c.k + i] = lc[i];
+    compose_candidates(h, row, special, planted, c.planted_conf, c.kc, tok, lc);
+    for (int i = 0; i < c.kc; ++i) {
+      c.cand_tok[b * c.kc + i] = tok[i];
+      c.cand_logc[b * c.kc + i] = lc[i];
     }
     c.cycle[b] = cyc;
   }

@@ -134,6 +134,26 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
  * outgrow max_ctx. */
 int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count);
 
+/* Generation limits of the current batch: h_limits (HOST int32 [n], n = the prefilled
+ * batch) gives each sequence's number of committed tokens, the prefill token included, at
+ * which it is finished. A cycle that reaches a limit reports only the tokens up to it in
+ * d_out_count (the surplus of its accepted path is dropped); a finished sequence is masked
+ * out of every later cycle: d_out_count 0 and its state unchanged, while the others go on.
+ * Its rows still pass through the cycle's fixed-shape launches. n = 0 removes the limits;
+ * eagle_prefill removes them too. (The generation length is the pages' "new tokens" per
+ * sequence; "EAGLE-2: Context-Aware Dynamic Draft Trees", table "Putting It Together".) */
+int eagle_set_stop(eagle_ctx* ctx, int n, const int32_t* h_limits);
+
+/* Draft budget between cycles: the next cycles expand `topk` nodes per depth (topk
+ * children each) and keep m nodes, with 1 <= topk <= the created tree.topk and
+ * 1 <= m <= min(the created tree.m, topk + (depth-1) topk^2). Takes effect at the next
+ * eagle_cycle, in the middle of a generation: the root's candidates are always kept at the
+ * created topk in rank order and the tree takes the first topk of them. The fixed k and m
+ * of a tree stop fitting once the batch size changes what the GPU has to spare ("EAGLE-2:
+ * Context-Aware Dynamic Draft Trees", table "Where It Breaks"); eagle_plan_budget
+ * (eagle_ops.h) picks the pair this call applies. EAGLE_EINVAL while a static tree is set. */
+int eagle_set_tree_budget(eagle_ctx* ctx, int topk, int m);
+
 /* Plain (non-speculative) decoding of n_steps tokens per sequence from the current
  * state, one target pass per token: the lossless comparator and the speedup
  * baseline. d_out_tokens: device int32 [batch][n_steps]. d_out_margin (nullable):

@@ -131,17 +131,21 @@ class OracleSeq:
         return self.M.fuse([c[list(rows)] for c in caps])
 
     # -- prefill ---------------------------------------------------------------
-    def prefill(self, prompt: Sequence[int], R: Optional[Sequence[int]] = None):
+    def prefill(self, prompt: Sequence[int], R: Optional[Sequence[int]] = None, first: Optional[int] = None):
         """Prefill (the EAGLE-2 page, table "Putting It Together", before step 1): the target
         over the prompt gives the first committed token and the features; the drafter runs
         over the prompt positions and its last output gives the root's depth-1 candidates.
-        R: the reference continuation for planted mode, or None."""
+        R: the reference continuation for planted mode, or None. first: commit this token
+        instead of the oracle's own pick (to replay another implementation's decision in lock
+        step, as commit() does for a cycle)."""
         prompt = np.asarray(prompt, dtype=np.int64)
         n = len(prompt)
         self.R = None if R is None else np.asarray(R, dtype=np.int64)
         pos = np.arange(n)
         f, caps = self.M.target_rows(prompt, pos, self.kv, pos, self._causal_visible(0, n))
-        first = self._target_pick(self.M.logits(f[-1:])[0], philox.PREFILL_CYCLE, philox.STREAM_GUMBEL, 0)
+        self.prefill_logits = self.M.logits(f[-1:])[0]
+        if first is None:
+            first = self._target_pick(self.prefill_logits, philox.PREFILL_CYCLE, philox.STREAM_GUMBEL, 0)
         self.n = n
         self.committed = [first]
         self.on_track = self.R is None or int(self.R[0]) == first

@@ -1,11 +1,48 @@
-"""GPU test helper (not a test): greedy speculative decoding against the GPU's own plain
-greedy decoding, bit for bit."""
+"""GPU test helpers (not tests): the oracle's tree policy rerun on the GPU's own node
+table, and greedy speculative decoding against the GPU's own plain greedy decoding, bit for
+bit."""
+import numpy as np
 import torch
 
 from eagle_speculative_decoding_cycle_gb300 import _lib as L
 from eagle_speculative_decoding_cycle_gb300 import api
+from oracle.tree import NodeTable, flatten, rerank, select_expand, static_plan
 
 DEV = "cuda:0"
+
+
+def gpu_table(eng, b=0):
+    tok, par, dep, logv = eng.dump(L.DUMP_NODES)
+    t = NodeTable()
+    t.token = tok[b].tolist()
+    t.parent = par[b].tolist()
+    t.depth = dep[b].tolist()
+    t.logv = [np.float32(x) for x in logv[b].numpy()]
+    return t
+
+
+def check_tree_policy(eng, wl, b=0):
+    """Oracle policy on the GPU's path values reproduces the GPU's expansion, rerank (or, for
+    a static tree, the planned rows and kept set), flattening and mask."""
+    k, D, m = wl.tree.topk, wl.tree.depth, wl.tree.m
+    t = gpu_table(eng, b)
+    static = bool(wl.tree.static_parent)
+    if static:
+        gen, rows = static_plan(wl.tree.static_parent, wl.tree.static_rank, k, D)
+    # expansion order: children of the r-th selected depth-d node occupy block r
+    for d in range(1, D):
+        sel = rows[d] if static else select_expand(NodeTable(t.token, t.parent, t.depth, t.logv), d, k)
+        base = k + (d - 1) * k * k
+        for r, v in enumerate(sel):
+            assert all(t.parent[base + r * k + i] == v for i in range(k))
+    st = eng.dump(L.DUMP_STATE)
+    ft = flatten(t, sorted(gen) if static else rerank(t, m), int(eng.dump(L.DUMP_TREE)[0][b, 0]))
+    tok, pos, par, node, mask = eng.dump(L.DUMP_TREE)
+    assert tok[b].tolist() == ft.token.tolist()
+    assert par[b].tolist() == ft.parent.tolist()
+    assert node[b].tolist() == ft.node.tolist()
+    assert np.array_equal(mask[b].numpy().view(np.uint64), ft.mask_words())
+    return t, ft, pos[b].numpy()
 
 
 def spec_vs_plain(wl, weights, prompts, n_new, kv_block=0, max_ctx=None):

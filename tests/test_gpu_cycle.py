@@ -8,6 +8,8 @@
   (bf16 model) max-abs.
 - Greedy losslessness: speculative output equals plain greedy decoding (the GPU's own
   decode_plain and the oracle's)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,7 @@ from oracle import philox
 from oracle.accept import greedy_walk, sample_walk
 from oracle.cycle import OracleSeq, build_model, plain_decode
 from oracle.tree import NodeTable, flatten, rerank, select_expand, static_plan
-from spec_plain import spec_vs_plain
+from spec_plain import check_tree_policy, gpu_table, spec_vs_plain
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -37,40 +39,6 @@ def setup(wl, planted=True, extra=8):
     R = plain_decode(M, wl, prompt.numpy(), wl.new_tokens + wl.tree.depth + extra) if planted else None
     eng = api.Engine(wl, {k: v.to(DEV) for k, v in weights.items()})
     return weights, M, prompt, R, eng
-
-
-def gpu_table(eng, b=0):
-    tok, par, dep, logv = eng.dump(L.DUMP_NODES)
-    t = NodeTable()
-    t.token = tok[b].tolist()
-    t.parent = par[b].tolist()
-    t.depth = dep[b].tolist()
-    t.logv = [np.float32(x) for x in logv[b].numpy()]
-    return t
-
-
-def check_tree_policy(eng, wl, b=0):
-    """Oracle policy on the GPU's path values reproduces the GPU's expansion, rerank (or, for
-    a static tree, the planned rows and kept set), flattening and mask."""
-    k, D, m = wl.tree.topk, wl.tree.depth, wl.tree.m
-    t = gpu_table(eng, b)
-    static = bool(wl.tree.static_parent)
-    if static:
-        gen, rows = static_plan(wl.tree.static_parent, wl.tree.static_rank, k, D)
-    # expansion order: children of the r-th selected depth-d node occupy block r
-    for d in range(1, D):
-        sel = rows[d] if static else select_expand(NodeTable(t.token, t.parent, t.depth, t.logv), d, k)
-        base = k + (d - 1) * k * k
-        for r, v in enumerate(sel):
-            assert all(t.parent[base + r * k + i] == v for i in range(k))
-    st = eng.dump(L.DUMP_STATE)
-    ft = flatten(t, sorted(gen) if static else rerank(t, m), int(eng.dump(L.DUMP_TREE)[0][b, 0]))
-    tok, pos, par, node, mask = eng.dump(L.DUMP_TREE)
-    assert tok[b].tolist() == ft.token.tolist()
-    assert par[b].tolist() == ft.parent.tolist()
-    assert node[b].tolist() == ft.node.tolist()
-    assert np.array_equal(mask[b].numpy().view(np.uint64), ft.mask_words())
-    return t, ft, pos[b].numpy()
 
 
 def run_lockstep(wl, n_cycles=None, planted=True, check_feats_tol=None):
@@ -329,3 +297,87 @@ def test_capacity_error_before_launch():
     assert e.value.code == L.EAGLE_ECAPACITY
     eng.sync()
     eng.close()
+
+
+def test_finished_sequences_are_masked_out_of_later_cycles():
+    """Per-sequence generation limits in a batch: each sequence emits exactly its limit (the
+    last cycle's surplus dropped), its tokens equal its plain greedy continuation, and once
+    finished it commits nothing and its state stays as it was while the others go on."""
+    wl = synth.SMALL_BF16_E3.replace(tree=synth.TreeShape(topk=4, depth=5, m=14, planted_p=0.8), batch=3)
+    weights = {k: v.to(DEV) for k, v in synth.make_weights(wl, "cpu").items()}
+    g = torch.Generator().manual_seed(7)
+    prompts = [torch.randint(0, wl.model.vocab, (n,), generator=g, dtype=torch.int64).to(torch.int32).to(DEV)
+               for n in (20, 33, 41)]
+    limits = [6, 40, 15]
+    D = wl.tree.depth
+    eng = api.Engine(wl, weights, max_batch=3, max_ctx=41 + 160)
+    eng.prefill(prompts)
+    first = eng.dump(L.DUMP_STATE)["root_tok"][:3].to(torch.int32)
+    plain = torch.zeros(3, 60, dtype=torch.int32, device=DEV)
+    eng.decode_plain(60, plain)
+    eng.sync()
+    ref = torch.cat([first.view(3, 1).to(DEV), plain], 1).contiguous()
+    eng.prefill(prompts, ref)
+    eng.set_stop(limits)
+    got = [[int(first[b])] for b in range(3)]
+    out = torch.zeros(3, D + 1, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(3, dtype=torch.int32, device=DEV)
+    frozen = {}
+    for _ in range(40):
+        before = {k: v.clone() for k, v in eng.dump(L.DUMP_STATE).items()}
+        eng.cycle(out, cnt)
+        eng.sync()
+        after = eng.dump(L.DUMP_STATE)
+        o, c = out.cpu(), cnt.cpu()
+        for b in range(3):
+            if len(got[b]) >= limits[b]:
+                assert int(c[b]) == 0
+                for key in ("ctx_len", "committed", "root_tok"):
+                    assert int(after[key][b]) == int(before[key][b]), (b, key)
+                frozen[b] = True
+            got[b] += o[b, :int(c[b])].tolist()
+        if all(len(got[b]) >= limits[b] for b in range(3)) and len(frozen) == 3:
+            break
+    for b in range(3):
+        assert len(got[b]) == limits[b], (b, len(got[b]))
+        assert got[b] == ref[b, :limits[b]].tolist()
+    assert len(frozen) == 3
+    eng.set_stop([])
+    eng.cycle(out, cnt)
+    eng.sync()
+    assert all(int(x) >= 1 for x in cnt.cpu())          # limits removed: every sequence moves again
+    eng.close()
+
+
+@pytest.mark.parametrize("temperature", [0.0, 1.0], ids=["greedy", "sampling"])
+def test_tree_budget_change_between_cycles(temperature):
+    """Lowering k and m between cycles gives exactly the cycles of a context created with the
+    lower values: the root candidates are kept at the created k in rank order and the tree
+    takes the first k of them. Raising either beyond the created values is refused."""
+    big = synth.SMALL_BF16.replace(tree=synth.TreeShape(topk=5, depth=4, m=12, temperature=temperature,
+                                                        planted_p=0.8))
+    small = big.replace(tree=dataclasses.replace(big.tree, topk=3, m=8))
+    weights = {k: v.to(DEV) for k, v in synth.make_weights(big, "cpu").items()}
+    prompt = synth.make_prompts(big)[0].to(DEV)
+    runs = []
+    for wl, switch in ((big, True), (small, False)):
+        eng = api.Engine(wl, weights)
+        eng.prefill([prompt])
+        if switch:
+            with pytest.raises(L.EagleError):
+                eng.set_tree_budget(6, 8)
+            with pytest.raises(L.EagleError):
+                eng.set_tree_budget(3, 13)
+            eng.set_tree_budget(3, 8)
+        out = torch.zeros(1, wl.tree.depth + 1, dtype=torch.int32, device=DEV)
+        cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+        rec = []
+        for _ in range(6):
+            eng.cycle(out, cnt)
+            eng.sync()
+            rec.append((out[0, :int(cnt[0])].tolist(), [t.clone() for t in eng.dump(L.DUMP_TREE)]))
+        runs.append(rec)
+        eng.close()
+    for (ta, tra), (tb, trb) in zip(*runs):
+        assert ta == tb
+        assert all(torch.equal(x, y) for x, y in zip(tra, trb))
