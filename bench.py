@@ -600,10 +600,12 @@ def run_attn_probe(args):
 
 
 def run_plan_budget(args):
-    """Measure the inputs of the batch-aware budget planner on this GPU and plan (k, m) per
-    batch size: for k in (4, 8, 10) the expected committed tokens of the m best nodes (1 +
-    the sum of their path values, averaged over planted cycles) and the drafter's share of a
-    cycle; the verify-pass time at batch 1, 4, 16 and 64 (k10, m60)."""
+    """Measure the inputs of the batch-aware budget planner on this GPU, plan (k, m) per batch
+    size, and apply each plan: for k in (4, 8, 10) the expected committed tokens of the m best
+    nodes (1 + the sum of their path values, averaged over planted cycles) and the drafter's
+    share of a cycle; the verify-pass time at batch 1, 4, 16 and 64 (k10, m60); then, per
+    batch size, measured committed tokens per second with the workload's own (k, m) and with
+    the planned one, set between cycles on one engine."""
     from eagle_speculative_decoding_cycle_gb300 import _lib as L
     from eagle_speculative_decoding_cycle_gb300 import api
     from eagle_speculative_decoding_cycle_gb300.build import build
@@ -678,6 +680,48 @@ def run_plan_budget(args):
     for B in (1, 4, 16, 64):
         k, m, rate = api.plan_budget(cands, rows, vus, B)
         plans[B] = {"k": k, "m": m, "committed_tok_per_s": rate * 1e6}
+    # apply each plan between cycles (eagle_set_tree_budget) on an engine created with the
+    # largest k and m, against the workload's own (k, m) on the same engine; planted cycles
+    # on the batch's own plain continuation, graph-replayed, committed tokens per second
+    k_max = max(c[0] for c in cands)
+    m_max = max(60, base.tree.m)
+    big = base.replace(tree=dataclasses.replace(base.tree, topk=k_max, m=m_max))
+    for B in (1, 4, 16, 64):
+        prompts = [p.to(dev) for p in (synth.make_prompts(base.replace(batch=max(B, base.batch)))[:B])]
+        n_meas = 8
+        n_ref = (n_meas + 8) * (D + 1) + D + 2
+        eng = api.Engine(big.replace(batch=B), weights, max_batch=B,
+                         max_ctx=max(len(p) for p in prompts) + 2 * n_ref + 64, stream=stream)
+        with torch.cuda.stream(stream):
+            eng.prefill(prompts)
+            first = eng.dump(L.DUMP_STATE)["root_tok"][:B].to(torch.int32).view(B, 1).to(dev)
+            rest = torch.zeros(B, n_ref - 1, dtype=torch.int32, device=dev)
+            eng.decode_plain(n_ref - 1, rest)
+            eng.sync()
+            ref = torch.cat([first, rest], 1).contiguous()
+            meas = {}
+            for label, (k, m) in (("default", (base.tree.topk, base.tree.m)),
+                                  ("planned", (plans[B]["k"], plans[B]["m"]))):
+                eng.set_graph(False)
+                eng.set_tree_budget(k, m)
+                eng.prefill(prompts, ref)
+                eng.set_graph(True)
+                for _ in range(2):
+                    eng.cycle()
+                eng.sync()
+                c0 = int(eng.dump(L.DUMP_STATE)["committed"][:B].long().sum())
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(n_meas):
+                    eng.cycle()
+                e1.record(stream)
+                eng.sync()
+                c1 = int(eng.dump(L.DUMP_STATE)["committed"][:B].long().sum())
+                ms = e0.elapsed_time(e1)
+                meas[label] = {"k": k, "m": m, "committed_tok_per_s": (c1 - c0) / (ms / 1e3),
+                               "cycle_ms": ms / n_meas, "tau": (c1 - c0) / n_meas / B}
+            plans[B]["measured"] = meas
+        eng.close()
     print(json.dumps({"plan_budget": {
         "workload": base.name, "verify_rows": rows, "verify_us": vus,
         "draft_us": {c[0]: c[1] for c in cands},
