@@ -714,7 +714,12 @@ __global__ void attn_merge_k(AttnArgs a, int tps) {
 
 size_t attention_scratch_floats(int rows, int nq, int d) { return (size_t)(MAX_SPLITS + 1) * rows * nq * (d + 2); }
 
-int attention_max_splits(int cap) { return std::max(1, std::min(MAX_SPLITS, (cap + MT_KEYS - 1) / MT_KEYS)); }
+// Three 64-key tiles per split (more splits put the merge and the CTA count on the critical
+// path, fewer lengthen each CTA: measured on the 8B batch-1 verify pass), at most MAX_SPLITS.
+int attention_max_splits(int cap) {
+  const int tiles = (cap + MT_KEYS - 1) / MT_KEYS;
+  return std::max(1, std::min(MAX_SPLITS, (tiles + 2) / 3));
+}
 
 template <int D>
 static int launch_bf16(cudaStream_t st, const AttnArgs& a) {

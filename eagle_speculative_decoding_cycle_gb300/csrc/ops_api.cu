@@ -108,7 +108,7 @@ int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcach
     a.part_o = reinterpret_cast<float*>(scratch);
     a.part_floats = attention_scratch_floats(R, nq, d) / (d + 2) * d;
     a.part_ml = a.part_o + a.part_floats;
-    a.max_splits = 32;
+    a.max_splits = attention_max_splits(cap);   // the engine's split policy for a cache of cap slots
   } else if (dtype != EAGLE_DTYPE_F32) {
     return EAGLE_ECAPACITY;
   }
