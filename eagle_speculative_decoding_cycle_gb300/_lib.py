@@ -21,11 +21,16 @@ DUMP_STATE, DUMP_CAND, DUMP_NODES, DUMP_TREE, DUMP_ACCEPT, DUMP_VERIFY_HEAD, DUM
     DUMP_TTT = range(9)
 DEBUG_LOGITS = 1
 
+# eagle_cycle_stats: six int32 counters, then the device clock at the cycle's start and at the
+# end of each of its five phases (uint64 ns)
+STATS_BYTES = 6 * 4 + 6 * 8
+PHASES = ("draft", "select", "verify", "accept_compact", "update")
+
 # every symbol the headers declare (checked by the CPU test suite)
 EXPORTED = [
     "eagle_workspace_bytes", "eagle_create", "eagle_prefill", "eagle_cycle", "eagle_decode_plain",
     "eagle_set_graph", "eagle_set_stop", "eagle_set_tree_budget", "eagle_cycle_kernel_launches", "eagle_status_sync", "eagle_dump_bytes", "eagle_debug_dump", "eagle_set_debug",
-    "eagle_kv_view", "eagle_kv_table", "eagle_set_static_tree", "eagle_ttt_forward", "eagle_profile_begin", "eagle_profile_end", "eagle_profile_verify", "eagle_last_error", "eagle_destroy",
+    "eagle_kv_view", "eagle_kv_table", "eagle_set_static_tree", "eagle_ttt_forward", "eagle_profile_begin", "eagle_profile_end", "eagle_profile_verify", "eagle_profile_phases", "eagle_last_error", "eagle_destroy",
     "eagle_op_gemm_scratch_bytes", "eagle_op_gemm", "eagle_op_gemm_noalloc", "eagle_op_gemm_noalloc_status",
     "eagle_op_lm_head_scratch_bytes", "eagle_op_lm_head",
     "eagle_op_attention_scratch_bytes", "eagle_op_attention", "eagle_plan_budget", "eagle_op_tree_scratch_bytes", "eagle_op_tree_build", "eagle_op_compact",
@@ -73,7 +78,7 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_workspace_bytes": (sz, [P(ModelCfg), P(DrafterCfg), P(TreeCfg), P(Limits)]),
         "eagle_create": (i32, [P(ModelCfg), P(DrafterCfg), P(TreeCfg), P(Weights), P(Limits), vp, sz, vp, P(vp)]),
         "eagle_prefill": (i32, [vp, i32, vp, P(C.c_int32), vp, i32]),
-        "eagle_cycle": (i32, [vp, vp, vp]),
+        "eagle_cycle": (i32, [vp, vp, vp, vp]),
         "eagle_decode_plain": (i32, [vp, i32, vp, vp]),
         "eagle_set_graph": (i32, [vp, i32]),
         "eagle_set_stop": (i32, [vp, i32, vp]),
@@ -92,6 +97,7 @@ def _declare(lib: C.CDLL) -> None:
         "eagle_profile_begin": (i32, [vp, i32]),
         "eagle_profile_end": (i32, [vp, P(i32), P(C.c_double), P(C.c_double)]),
         "eagle_profile_verify": (i32, [vp, P(i32), P(C.c_double)]),
+        "eagle_profile_phases": (i32, [vp, P(i32), P(C.c_double)]),
         "eagle_last_error": (C.c_char_p, [vp]),
         "eagle_destroy": (None, [vp]),
         "eagle_op_gemm_scratch_bytes": (sz, [i32, i32]),

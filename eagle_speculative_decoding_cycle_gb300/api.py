@@ -39,6 +39,18 @@ def configs(w: Workload, max_batch: Optional[int] = None, max_ctx: Optional[int]
     return mc, dc, tc, lim
 
 
+def read_stats(stats: torch.Tensor) -> dict:
+    """The fields of an eagle_cycle_stats buffer (copied to the host): counters, and each
+    phase's device time in microseconds."""
+    raw = stats.detach().to("cpu").contiguous().view(torch.uint8)[:L.STATS_BYTES]
+    cnt = raw[:24].view(torch.int32).tolist()
+    t = raw[24:].view(torch.int64).tolist()
+    out = dict(zip(("batch", "active", "accepted", "committed", "max_accepted", "verify_rows"), cnt))
+    out["phase_us"] = {p: (t[i + 1] - t[i]) / 1e3 for i, p in enumerate(L.PHASES)}
+    out["cycle_us"] = (t[-1] - t[0]) / 1e3
+    return out
+
+
 class Engine:
     """One context of the cycle library over caller-owned torch CUDA tensors."""
 
@@ -94,8 +106,17 @@ class Engine:
                                     0 if ref is None else int(self._ref.shape[1]))
         self._check(rc, "eagle_prefill")
 
-    def cycle(self, out_tokens: Optional[torch.Tensor] = None, out_count: Optional[torch.Tensor] = None) -> None:
-        self._check(self.lib.eagle_cycle(self.h, _ptr(out_tokens), _ptr(out_count)), "eagle_cycle")
+    def cycle(self, out_tokens: Optional[torch.Tensor] = None, out_count: Optional[torch.Tensor] = None,
+              stats: Optional[torch.Tensor] = None) -> None:
+        """One cycle. stats (optional): a device tensor from new_stats(), filled by the device
+        with the cycle's statistics (parse with read_stats)."""
+        if stats is not None and (stats.numel() * stats.element_size() < L.STATS_BYTES or stats.data_ptr() % 8):
+            raise ValueError("stats must be an 8-byte aligned device buffer of at least %d bytes" % L.STATS_BYTES)
+        self._check(self.lib.eagle_cycle(self.h, _ptr(out_tokens), _ptr(out_count), _ptr(stats)), "eagle_cycle")
+
+    def new_stats(self) -> torch.Tensor:
+        """A device buffer for one cycle's statistics."""
+        return torch.zeros(L.STATS_BYTES // 8, dtype=torch.int64, device=self.workspace.device)
 
     def decode_plain(self, n: int, out: torch.Tensor, margin: Optional[torch.Tensor] = None) -> None:
         self._check(self.lib.eagle_decode_plain(self.h, n, _ptr(out), _ptr(margin)), "eagle_decode_plain")
@@ -130,6 +151,12 @@ class Engine:
         n, ms, by = C.c_int(), C.c_double(), C.c_double()
         self._check(self.lib.eagle_profile_end(self.h, C.byref(n), C.byref(ms), C.byref(by)), "eagle_profile_end")
         return n.value, ms.value, by.value
+
+    def profile_phases(self):
+        """(cycles timed, {phase: total device ms}) of the last profiled window."""
+        n, ms = C.c_int(), (C.c_double * len(L.PHASES))()
+        self._check(self.lib.eagle_profile_phases(self.h, C.byref(n), ms), "eagle_profile_phases")
+        return n.value, dict(zip(L.PHASES, list(ms)))
 
     def profile_verify(self):
         """(verify passes timed, their total device ms) of the last profiled cycles."""

@@ -34,6 +34,7 @@ __global__ void accept_k(CycleDev c, HeadOut h, int* out_tokens, int* out_count)
     c.acc_len[b] = 0;
     c.bonus[b] = c.root_tok[b];
     c.n_old[b] = c.ctx_len[b];
+    c.emitted[b] = 0;
     if (out_count) out_count[b] = 0;
     return;
   }
@@ -72,7 +73,9 @@ __global__ void accept_k(CycleDev c, HeadOut h, int* out_tokens, int* out_count)
     if (c.ref) on = on && (cc + j < c.ref_len) && c.ref[(size_t)b * c.ref_len + cc + j] == t;
   }
   // the last cycle of a sequence with a limit emits only up to the limit
-  if (out_count) out_count[b] = min(L + 1, stop - cc);
+  const int emit = min(L + 1, stop - cc);
+  c.emitted[b] = emit;
+  if (out_count) out_count[b] = emit;
   c.on_track[b] = on;
   c.committed[b] = cc + L + 1;
   c.root_tok[b] = bonus;

@@ -62,6 +62,7 @@ struct CycleDev {
   uint64_t* tmask;          // [B*T1][tmask_words]
   // acceptance
   int* acc_len;             // [B]
+  int* emitted;             // [B] tokens committed by the cycle (0 for a finished sequence)
   int* acc_path;            // [B][D] accepted flattened rows
   int* bonus;               // [B]
   float* margin;            // [B][T1] greedy top-2 margin per verify row (diagnostic)

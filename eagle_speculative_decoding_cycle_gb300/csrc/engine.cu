@@ -16,6 +16,8 @@
 #include <climits>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/eagle.h"
 #include "common.cuh"
 #include "cycle.h"
@@ -116,6 +118,8 @@ bool derive(const eagle_model_cfg* mc, const eagle_drafter_cfg* dc, const eagle_
   return true;
 }
 
+constexpr int PHASES = 5;   // draft, select, verify, accept + compact, drafter update
+
 }  // namespace
 
 struct eagle_ctx {
@@ -144,12 +148,17 @@ struct eagle_ctx {
   std::vector<cudaEvent_t> prof_ev;
   std::vector<double> prof_bytes;
   int prof_on = 0, prof_n = 0;
-  std::vector<cudaEvent_t> ver_ev;      // profiled cycles: events around each verify pass
-  int ver_n = 0, ver_done = 0;          // passes recorded / timed by eagle_profile_end
-  double ver_ms = 0.0;
+  // profiled cycles: events at the cycle's start and at the end of each of its five phases
+  std::vector<cudaEvent_t> ph_ev;       // [64][PHASES + 1]
+  int ph_n = 0, ph_done = 0;            // cycles recorded / timed by eagle_profile_end
+  double ph_ms[PHASES] = {0, 0, 0, 0, 0};
+  // cycle statistics: the caller's struct baked into the captured graph
+  eagle_cycle_stats* graph_stats = nullptr;
+  eagle_cycle_stats* stats = nullptr;   // of the cycle being enqueued (null: none)
   // buffers
   int* dev_err;
   int *ctx_len, *n_old, *root_tok, *committed, *on_track, *root_plant, *acc_len, *bonus, *acc_path, *root_row, *iota;
+  int* emitted;       // [B] tokens the last cycle committed for each sequence (0: finished)
   int* stop_at;       // [B] committed-token limit of each sequence (INT32_MAX: none)
   uint32_t *cycle, *plain_step;
   int *cand_tok; float* cand_logc;
@@ -165,9 +174,10 @@ struct eagle_ctx {
   float* gemm_part; size_t gemm_part_floats; int* gemm_cnt; int gemm_cnt_len;
   float *attn_po, *attn_pml; size_t attn_pfloats;
   // bf16 fused epilogues: -1 (default) SwiGLU in the gate/up epilogue from 128 rows on, where
-  // the separate SwiGLU pass costs more than the epilogue work; 1 (EAGLE_FUSE_EPI=1) also
-  // RoPE/KV write in the QKV epilogue, at every row count; 0 (EAGLE_FUSE_EPI=0) none. Both
-  // epilogues agree bit for bit with the row kernels they replace.
+  // the separate SwiGLU pass costs more than the epilogue work; otherwise the bits of
+  // EAGLE_FUSE_EPI: 1 = SwiGLU in the gate/up epilogue, 2 = RoPE/KV write in the QKV
+  // epilogue, at every row count (0: none, 3: both). Both epilogues agree bit for bit with
+  // the row kernels they replace.
   int fuse_epi = -1;
   float *rope_cos, *rope_sin;
   void *kc, *vc, *dkc, *dvc;
@@ -192,7 +202,7 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
   x->dev_err = c.take<int>(4);
   x->ctx_len = c.take<int>(B); x->n_old = c.take<int>(B); x->root_tok = c.take<int>(B);
   x->committed = c.take<int>(B); x->on_track = c.take<int>(B); x->root_plant = c.take<int>(B);
-  x->acc_len = c.take<int>(B); x->bonus = c.take<int>(B); x->acc_path = c.take<int>((size_t)B * z.D);
+  x->acc_len = c.take<int>(B); x->emitted = c.take<int>(B); x->bonus = c.take<int>(B); x->acc_path = c.take<int>((size_t)B * z.D);
   x->root_row = c.take<int>(B); x->iota = c.take<int>(std::max(B, z.R));
   x->stop_at = c.take<int>(B);
   x->cycle = c.take<uint32_t>(B); x->plain_step = c.take<uint32_t>(4);
@@ -362,7 +372,7 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
                   int tree_T, const uint64_t* mask, int mask_words, const KvPage& page) {
   const Dims& z = ctx->z;
   // the fused epilogue writes a contiguous cache only
-  if (z.dt == DT_BF16 && ctx->fuse_epi > 0 && 128 % z.d == 0 && !page.table) {
+  if (z.dt == DT_BF16 && ctx->fuse_epi > 0 && (ctx->fuse_epi & 2) && 128 % z.d == 0 && !page.table) {
     // RoPE, the q output and the KV-cache write in the projection's epilogue
     const QkvEpi q{pos, slot, seq, ctx->rope_cos, ctx->rope_sin, ctx->qb, kcache, vcache, z.nq, z.nkv, z.d, cap};
     CK(gemm(ctx, lw.wqkv, z.QKV, kin, attn_in, R, EPI_QKV, nullptr, 0, nullptr, &q));
@@ -379,9 +389,9 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   // straddle the 128-row point where the SwiGLU epilogue pays off: both then use the paired
   // [gate; up] tile layout, fused or not, which gives the same bits either way. One sequence
   // keeps the plain layout (a 128-row weight box per stage) for every launch, unless
-  // EAGLE_FUSE_EPI is set either way (then both settings share the paired layout).
+  // EAGLE_FUSE_EPI is set to any value (then both settings share the paired layout).
   if (z.dt == DT_BF16 && z.F % 64 == 0 && (ctx->batch > 1 || ctx->fuse_epi >= 0)) {
-    if (ctx->fuse_epi > 0 || (ctx->fuse_epi < 0 && R >= 128)) {
+    if ((ctx->fuse_epi > 0 && (ctx->fuse_epi & 1)) || (ctx->fuse_epi < 0 && R >= 128)) {
       CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_SWIGLU, ctx->hb, z.F));
     } else {
       CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_GU, ctx->gu, 2 * z.F));
@@ -484,7 +494,7 @@ void fill_cd(eagle_ctx* ctx) {
   c.drow_feat = ctx->drow_feat; c.drow_plant = ctx->drow_plant; c.dmask = ctx->dmask;
   c.tree_tok = ctx->tree_tok; c.tree_pos = ctx->tree_pos; c.tree_slot = ctx->tree_slot; c.tree_seq = ctx->tree_seq;
   c.tree_parent = ctx->tree_parent; c.tree_node = ctx->tree_node; c.tree_kids = ctx->tree_kids; c.tmask = ctx->tmask;
-  c.acc_len = ctx->acc_len; c.acc_path = ctx->acc_path; c.bonus = ctx->bonus; c.margin = ctx->margin;
+  c.acc_len = ctx->acc_len; c.emitted = ctx->emitted; c.acc_path = ctx->acc_path; c.bonus = ctx->bonus; c.margin = ctx->margin;
   c.err = ctx->dev_err;
   c.policy = ctx->static_on;
   c.static_exp = ctx->static_exp;
@@ -502,6 +512,43 @@ __global__ void drow_out_k(int* out, int B, int k, int fsrc_rows, int d) {
   PDL_ENTRY();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B * k) out[i] = (i / k) * fsrc_rows + 1 + (d - 1) * k + (i % k);
+}
+
+// ---- cycle statistics ---------------------------------------------------------------------------
+// The device clock (ns) once the preceding kernel has finished.
+__global__ void stamp_k(uint64_t* t) {
+  PDL_ENTRY();
+  uint64_t ns;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
+  *t = ns;
+}
+
+// The batch's totals of the cycle that just ended (one warp, fixed summation order).
+__global__ void cycle_stats_k(const int* emitted, const int* acc_len, int B, int m, eagle_cycle_stats* s) {
+  PDL_ENTRY();
+  int act = 0, acc = 0, emit = 0, mx = 0;
+  for (int b = threadIdx.x; b < B; b += 32) {
+    const int e = emitted[b], l = e > 0 ? acc_len[b] : 0;
+    act += e > 0;
+    emit += e;
+    acc += l;
+    mx = max(mx, l);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    act += __shfl_xor_sync(0xffffffffu, act, off);
+    emit += __shfl_xor_sync(0xffffffffu, emit, off);
+    acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  if (threadIdx.x == 0) {
+    s->batch = B;
+    s->active = act;
+    s->accepted = acc;
+    s->committed = emit;
+    s->max_accepted = mx;
+    s->verify_rows = m + 1;
+  }
 }
 
 // ---- paged target KV: block assignment ---------------------------------------------------------
@@ -596,6 +643,18 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   const int B = ctx->batch;
   CycleDev& c = ctx->cd;
   const size_t rb = (size_t)z.H * z.esz;
+  // phase marks: a device clock stamp into the caller's statistics, CUDA events in a profiled
+  // window, and an NVTX range around the phase's host-side enqueue
+  static const char* const names[PHASES] = {"eagle.draft", "eagle.select", "eagle.verify", "eagle.accept_compact",
+                                            "eagle.update"};
+  const bool pprof = ctx->prof_on && (size_t)(PHASES + 1) * (ctx->ph_n + 1) <= ctx->ph_ev.size();
+  auto mark = [&](int i) {   // i = 0: the cycle's start; i = 1..PHASES: the end of phase i
+    if (ctx->stats) launch_k(stamp_k, 1, 32, 0, ctx->st, &ctx->stats->t_ns[i]);
+    if (pprof) cudaEventRecord(ctx->ph_ev[(size_t)(PHASES + 1) * ctx->ph_n + i], ctx->st);
+    if (i > 0) nvtxRangePop();
+    if (i < PHASES) nvtxRangePushA(names[i]);
+  };
+  mark(0);
   CK(kv_reserve(ctx, 0, B, ctx->ctx_len, 0, z.T1));   // the tree rows' slots [ctx, ctx + m + 1)
   CK(tree_start(ctx->st, c));
   for (int d = 1; d < z.D; ++d) {
@@ -615,10 +674,10 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
     if (r) return r;
     CK(tree_add(ctx->st, c, d, head_out(ctx, z.k, 1)));
   }
+  mark(1);
   CK(tree_finalize(ctx->st, c));
+  mark(2);
   // verify (target forward over the tree rows, then the LM head epilogue)
-  const bool vprof = ctx->prof_on && 2 * (ctx->ver_n + 1) <= (int)ctx->ver_ev.size();
-  if (vprof) cudaEventRecord(ctx->ver_ev[2 * ctx->ver_n], ctx->st);
   const int RT = B * z.T1;
   int r = target_forward(ctx, RT, ctx->tree_tok, ctx->tree_pos, ctx->tree_slot, ctx->tree_seq, z.T1, 1, z.T1,
                          ctx->tmask, z.tmw, ctx->feat_t, ctx->caps, (size_t)z.Rt, 0);
@@ -641,13 +700,14 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   p.spec_logit = ctx->v_spec;
   r = lm_head(ctx, ctx->feat_t, RT, p, ctx->v_logits, (ctx->debug & EAGLE_DEBUG_LOGITS) != 0);
   if (r) return r;
-  if (vprof) cudaEventRecord(ctx->ver_ev[2 * ctx->ver_n++ + 1], ctx->st);
+  mark(3);
   HeadOut hv;
   hv.top_id = ctx->v_id; hv.top_val = ctx->v_val; hv.lse = ctx->v_lse; hv.spec_logit = ctx->v_spec;
   hv.K = p.K; hv.S = sampling ? z.k : 1;
   CK(accept_walk(ctx->st, c, hv, out_tokens, out_count));
   CK(compact_kv(ctx->st, z.dt, ctx->kc, ctx->vc, z.L, z.kv_layer_elems, z.B, z.nkv, z.cap, z.d, ctx->n_old,
                 ctx->acc_len, ctx->acc_path, z.D, ctx->page));
+  mark(4);
   // drafter update over the committed positions
   const int RU = B * (z.D + 1);
   CK(update_rows(ctx->st, c, ctx->row_tok, ctx->row_pos, ctx->row_slot, ctx->row_seq, ctx->row_feat));
@@ -672,7 +732,10 @@ int enqueue_cycle(eagle_ctx* ctx, int32_t* out_tokens, int32_t* out_count) {
   r = lm_head(ctx, ctx->ebuf, B, q);
   if (r) return r;
   CK(root_candidates(ctx->st, c, head_out(ctx, ctx->zc.k, 1), 1));
-  return 0;
+  mark(5);
+  if (ctx->stats) launch_k(cycle_stats_k, 1, 32, 0, ctx->st, ctx->emitted, ctx->acc_len, B, z.m, ctx->stats);
+  if (pprof) ++ctx->ph_n;
+  return cudaGetLastError() == cudaSuccess ? 0 : fail(ctx, EAGLE_ECUDA, "launch failed");
 }
 
 // Prefill of B equal-length prompts in one batched pass (rows b * n + p), used when all of
@@ -818,7 +881,7 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
   ctx->layers.assign(weights->layers, weights->layers + model->n_layers);
   ctx->w.layers = ctx->layers.data();
   ctx->st = reinterpret_cast<cudaStream_t>(stream);
-  if (getenv("EAGLE_FUSE_EPI")) ctx->fuse_epi = strcmp(getenv("EAGLE_FUSE_EPI"), "0") != 0;
+  if (getenv("EAGLE_FUSE_EPI")) ctx->fuse_epi = atoi(getenv("EAGLE_FUSE_EPI")) & 3;
   Carver c;
   c.base = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(workspace), 256));
   carve(c, ctx, z);
@@ -957,16 +1020,28 @@ int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int3
   return EAGLE_OK;
 }
 
-int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count) {
+static int run_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count, eagle_cycle_stats* d_stats);
+
+int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count, eagle_cycle_stats* d_stats) {
   if (!ctx) return EAGLE_EINVAL;
+  if (d_stats && (reinterpret_cast<uintptr_t>(d_stats) & 7))
+    return fail(ctx, EAGLE_EINVAL, "d_stats must be 8-byte aligned");
   const Dims& z = ctx->z;
   if (ctx->host_ctx_bound + z.D + 1 > z.max_ctx)
     return fail(ctx, EAGLE_ECAPACITY, "a sequence could outgrow max_ctx in this cycle");
   if (getenv("EAGLE_FAULT") && strcmp(getenv("EAGLE_FAULT"), "cycle") == 0)
     return fail(ctx, EAGLE_ECUDA, "injected cycle fault");
   ctx->host_ctx_bound += z.D + 1;
+  ctx->stats = d_stats;
+  nvtxRangePushA("eagle.cycle");
+  const int rc = run_cycle(ctx, d_out_tokens, d_out_count, d_stats);
+  nvtxRangePop();
+  return rc;
+}
+
+static int run_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count, eagle_cycle_stats* d_stats) {
   if (ctx->graph_enabled) {
-    if (ctx->graph && (ctx->graph_out != d_out_tokens || ctx->graph_cnt != d_out_count)) {
+    if (ctx->graph && (ctx->graph_out != d_out_tokens || ctx->graph_cnt != d_out_count || ctx->graph_stats != d_stats)) {
       cudaGraphExecDestroy(ctx->graph);
       ctx->graph = nullptr;
     }
@@ -992,6 +1067,7 @@ int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count) {
       if (e != cudaSuccess) { ctx->graph = nullptr; return fail(ctx, EAGLE_ECUDA, "graph instantiation failed"); }
       ctx->graph_out = d_out_tokens;
       ctx->graph_cnt = d_out_count;
+      ctx->graph_stats = d_stats;
       ctx->graph_ref = ctx->cd.ref;
       ctx->graph_batch = ctx->batch;
       ctx->graph_kernels = kn;
@@ -1097,13 +1173,13 @@ int eagle_profile_begin(eagle_ctx* ctx, int max_launches) {
     if (cudaEventCreate(&e) != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "event creation failed");
   ctx->prof_bytes.assign(max_launches, 0.0);
   ctx->prof_n = 0;
-  for (auto e : ctx->ver_ev) cudaEventDestroy(e);
-  ctx->ver_ev.assign(2 * 64, nullptr);
-  for (auto& e : ctx->ver_ev)
+  for (auto e : ctx->ph_ev) cudaEventDestroy(e);
+  ctx->ph_ev.assign((size_t)(PHASES + 1) * 64, nullptr);
+  for (auto& e : ctx->ph_ev)
     if (cudaEventCreate(&e) != cudaSuccess) return fail(ctx, EAGLE_ECUDA, "event creation failed");
-  ctx->ver_n = 0;
-  ctx->ver_done = 0;
-  ctx->ver_ms = 0.0;
+  ctx->ph_n = 0;
+  ctx->ph_done = 0;
+  for (double& t : ctx->ph_ms) t = 0.0;
   ctx->prof_on = 1;
   return EAGLE_OK;
 }
@@ -1125,24 +1201,33 @@ int eagle_profile_end(eagle_ctx* ctx, int* launches, double* total_ms, double* t
   if (total_bytes) *total_bytes = bytes;
   for (auto e : ctx->prof_ev) cudaEventDestroy(e);
   ctx->prof_ev.clear();
-  double vms = 0;
-  for (int i = 0; i < ctx->ver_n; ++i) {
-    float t = 0.f;
-    if (cudaEventElapsedTime(&t, ctx->ver_ev[2 * i], ctx->ver_ev[2 * i + 1]) != cudaSuccess)
-      return fail(ctx, EAGLE_ECUDA, "event timing failed");
-    vms += t;
-  }
-  ctx->ver_done = ctx->ver_n;
-  ctx->ver_ms = vms;
-  for (auto e : ctx->ver_ev) cudaEventDestroy(e);
-  ctx->ver_ev.clear();
+  for (int p = 0; p < PHASES; ++p) ctx->ph_ms[p] = 0.0;
+  for (int i = 0; i < ctx->ph_n; ++i)
+    for (int p = 0; p < PHASES; ++p) {
+      float t = 0.f;
+      const size_t e = (size_t)(PHASES + 1) * i + p;
+      if (cudaEventElapsedTime(&t, ctx->ph_ev[e], ctx->ph_ev[e + 1]) != cudaSuccess)
+        return fail(ctx, EAGLE_ECUDA, "event timing failed");
+      ctx->ph_ms[p] += t;
+    }
+  ctx->ph_done = ctx->ph_n;
+  for (auto e : ctx->ph_ev) cudaEventDestroy(e);
+  ctx->ph_ev.clear();
   return EAGLE_OK;
 }
 
 int eagle_profile_verify(const eagle_ctx* ctx, int* passes, double* total_ms) {
   if (!ctx) return EAGLE_EINVAL;
-  if (passes) *passes = ctx->ver_done;
-  if (total_ms) *total_ms = ctx->ver_ms;
+  if (passes) *passes = ctx->ph_done;
+  if (total_ms) *total_ms = ctx->ph_ms[2];
+  return EAGLE_OK;
+}
+
+int eagle_profile_phases(const eagle_ctx* ctx, int* cycles, double* phase_ms) {
+  if (!ctx) return EAGLE_EINVAL;
+  if (cycles) *cycles = ctx->ph_done;
+  if (phase_ms)
+    for (int p = 0; p < PHASES; ++p) phase_ms[p] = ctx->ph_ms[p];
   return EAGLE_OK;
 }
 
@@ -1371,6 +1456,7 @@ void eagle_destroy(eagle_ctx* ctx) {
   if (!ctx) return;
   if (ctx->graph) cudaGraphExecDestroy(ctx->graph);
   for (auto e : ctx->prof_ev) cudaEventDestroy(e);
+  for (auto e : ctx->ph_ev) cudaEventDestroy(e);
   delete ctx;
 }
 

@@ -27,31 +27,50 @@ __global__ void __launch_bounds__(128) head_partials_k(const float* logits, int 
   }
 }
 
-// One CTA per row: 8 warps fold the tile records (one round of loads per thread when the
-// vocabulary has at most 256 tiles), each warp reduces its lanes, warp 0 reduces the warps.
-constexpr int HM_WARPS = 8;
-
-__global__ void __launch_bounds__(HM_WARPS * 32) head_merge_k(HeadParams p) {
+// One CTA per row of NW warps: every thread folds the tile records t, t + 32 NW, ... (with
+// 32 warps, launched for at most 1024 tiles, a single record per thread, already in rank
+// order), each warp reduces its lanes, warp 0 reduces the warps. The warp count is a function of the
+// vocabulary alone, so a row's result does not depend on how many rows are merged.
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) head_merge_k(HeadParams p) {
   PDL_ENTRY();
-  __shared__ float s_m[HM_WARPS], s_s[HM_WARPS], s_v[HM_WARPS][16];
-  __shared__ int s_i[HM_WARPS][16];
+  __shared__ float s_m[NW], s_s[NW], s_v[NW][16];
+  __shared__ int s_i[NW][16];
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = p.K;
   float lv[16], M, S;
   int li[16];
-  head_merge_fold(p, row, threadIdx.x, HM_WARPS * 32, lv, li, M, S);
+  if constexpr (NW == 32) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) { lv[k] = -INFINITY; li[k] = 0x7fffffff; }
+    M = -INFINITY;
+    S = 0.f;
+    if ((int)threadIdx.x < p.n_tiles) {
+      const float* rec = p.part + ((size_t)threadIdx.x * p.n_rows + row) * (2 + 2 * K);
+      M = rec[0];
+      S = M == -INFINITY ? 0.f : rec[1];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (k >= K) continue;
+        const int id = __float_as_int(rec[3 + 2 * k]);
+        if (id >= 0) { lv[k] = rec[2 + 2 * k]; li[k] = id; }
+      }
+    }
+  } else {
+    head_merge_fold(p, row, threadIdx.x, NW * 32, lv, li, M, S);
+  }
   head_merge_warp(K, lv, li, M, S, lane, s_v[warp], s_i[warp]);
   if (lane == 0) { s_m[warp] = M; s_s[warp] = S; }
   __syncthreads();
   if (warp != 0) return;
-  // lane w < HM_WARPS holds warp w's sorted list
+  // lane w < NW holds warp w's sorted list
   for (int k = 0; k < 16; ++k) {
-    lv[k] = (lane < HM_WARPS && k < K) ? s_v[lane][k] : -INFINITY;
-    li[k] = (lane < HM_WARPS && k < K) ? s_i[lane][k] : 0x7fffffff;
+    lv[k] = (lane < NW && k < K) ? s_v[lane][k] : -INFINITY;
+    li[k] = (lane < NW && k < K) ? s_i[lane][k] : 0x7fffffff;
   }
-  M = lane < HM_WARPS ? s_m[lane] : -INFINITY;
-  S = lane < HM_WARPS ? s_s[lane] : 0.f;
+  M = lane < NW ? s_m[lane] : -INFINITY;
+  S = lane < NW ? s_s[lane] : 0.f;
   __syncwarp();
   head_merge_warp(K, lv, li, M, S, lane, s_v[0], s_i[0]);   // warp 0's own slot, already read
   __syncwarp();
@@ -77,7 +96,9 @@ int head_partials_from_logits(cudaStream_t st, const float* logits, int ld, cons
 int head_merge(cudaStream_t st, const HeadParams& p) {
   if (p.n_rows <= 0) return 0;
   if (p.K < 1 || p.K > 16) return -1;
-  launch_k(head_merge_k, p.n_rows, HM_WARPS * 32, 0, st, p);
+  // up to 1024 tiles: one record per thread of a 32-warp CTA; more: 8 warps folding many
+  if (p.n_tiles <= 1024) launch_k(head_merge_k<32>, p.n_rows, 1024, 0, st, p);
+  else launch_k(head_merge_k<8>, p.n_rows, 256, 0, st, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -223,28 +223,28 @@ EAGLE_DEV void head_merge_fold(const HeadParams& p, int row, int t0, int stride,
   S = 0.f;
   for (int t = t0; t < p.n_tiles; t += stride) {
     const float* rec = p.part + ((size_t)t * p.n_rows + row) * (2 + 2 * K);
-    float r[2 + 2 * 16];
-#pragma unroll
-    for (int j = 0; j < 2 + 2 * 16; ++j) r[j] = j < 2 + 2 * K ? rec[j] : 0.f;
-    const float m2 = r[0], s2 = r[1];
+    const float m2 = rec[0], s2 = rec[1];
     if (m2 != -INFINITY) {
       if (m2 > M) { S = S * expf(M - m2) + s2; M = m2; }
       else S += s2 * expf(m2 - M);
     }
     if (t == t0) {
+      // the first record is already in rank order
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const int id = __float_as_int(r[3 + 2 * k]);
-        if (k < K && id >= 0) { lv[k] = r[2 + 2 * k]; li[k] = id; }
+        if (k >= K) continue;
+        const int id = __float_as_int(rec[3 + 2 * k]);
+        if (id >= 0) { lv[k] = rec[2 + 2 * k]; li[k] = id; }
       }
       continue;
     }
     // insert each entry by a compare-and-swap pass (fixed indices keep the lists in registers)
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      float cv = r[2 + 2 * k];
-      int ci = __float_as_int(r[3 + 2 * k]);
-      if (k >= K || ci < 0) continue;
+      if (k >= K) continue;
+      float cv = rec[2 + 2 * k];
+      int ci = __float_as_int(rec[3 + 2 * k]);
+      if (ci < 0) continue;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         if (j < K && rank_before(cv, ci, lv[j], li[j])) {

@@ -127,12 +127,36 @@ int eagle_create(const eagle_model_cfg* model, const eagle_drafter_cfg* drafter,
 int eagle_prefill(eagle_ctx* ctx, int batch, const int32_t* d_tokens, const int32_t* h_lens,
                   const int32_t* d_ref, int ref_len);
 
+/* Statistics of one cycle, written by the device into caller-owned device memory (8-byte
+ * aligned) at the end of the cycle, stream-ordered like its outputs. The phases are the
+ * cycle's steps ("EAGLE-2: Context-Aware Dynamic Draft Trees", table "Putting It Together",
+ * steps 1-5): draft (the per-depth expansions and drafter passes), select (the global top-m
+ * rerank, flattening and ancestry mask), verify (the target forward over the tree rows and
+ * its LM-head epilogue), accept + compact (the acceptance walk and the KV compaction of the
+ * accepted path), update (the drafter over the committed positions and the next root's
+ * candidates). t_ns[0] is the device clock (%globaltimer, ns) once the work queued before
+ * the cycle has finished; t_ns[i] (i = 1..5) once phase i's kernels have finished, so
+ * t_ns[i] - t_ns[i - 1] is phase i's device time. */
+typedef struct {
+  int32_t batch;         /* sequences in the cycle (the prefilled batch) */
+  int32_t active;        /* of them, those not finished before the cycle */
+  int32_t accepted;      /* drafted tokens accepted, summed over the active sequences */
+  int32_t committed;     /* tokens committed (accepted + bonus, cut at the limits), summed */
+  int32_t max_accepted;  /* the longest accepted path */
+  int32_t verify_rows;   /* tree rows verified per sequence (m + 1) */
+  uint64_t t_ns[6];
+} eagle_cycle_stats;
+
 /* One draft-and-verify cycle for every sequence. d_out_tokens: device int32
  * [batch][depth + 1] receives the committed tokens (accepted path then the bonus
- * token); d_out_count: device int32 [batch] receives how many (L + 1). Either may be
- * null. Returns EAGLE_ECAPACITY, before launching anything, when a sequence could
- * outgrow max_ctx. */
-int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count);
+ * token); d_out_count: device int32 [batch] receives how many (L + 1); d_stats: device
+ * eagle_cycle_stats (8-byte aligned). Any of them may be null; with d_stats the cycle
+ * launches six one-thread clock kernels and one reduction more. Returns EAGLE_ECAPACITY,
+ * before launching anything, when a sequence could outgrow max_ctx. The host-side enqueue
+ * of each phase is an NVTX range ("eagle.cycle" around the call, "eagle.draft",
+ * "eagle.select", "eagle.verify", "eagle.accept_compact", "eagle.update" inside; graph
+ * replay enqueues nothing, so there only the outer range appears). */
+int eagle_cycle(eagle_ctx* ctx, int32_t* d_out_tokens, int32_t* d_out_count, eagle_cycle_stats* d_stats);
 
 /* Generation limits of the current batch: h_limits (HOST int32 [n], n = the prefilled
  * batch) gives each sequence's number of committed tokens, the prefill token included, at
@@ -252,6 +276,11 @@ int eagle_profile_end(eagle_ctx* ctx, int* launches, double* total_ms, double* t
  * run between eagle_profile_begin and eagle_profile_end (at most 64 are timed): how many
  * and their summed device time (CUDA events on the context's stream). */
 int eagle_profile_verify(const eagle_ctx* ctx, int* passes, double* total_ms);
+
+/* The same window's cycles phase by phase: how many cycles were timed and, in phase_ms[5],
+ * each phase's summed device time (draft, select, verify, accept + compact, update; CUDA
+ * events on the context's stream at the phase boundaries of eagle_cycle_stats). */
+int eagle_profile_phases(const eagle_ctx* ctx, int* cycles, double* phase_ms);
 
 const char* eagle_last_error(const eagle_ctx* ctx);
 void eagle_destroy(eagle_ctx* ctx);

@@ -323,12 +323,21 @@ def test_finished_sequences_are_masked_out_of_later_cycles():
     out = torch.zeros(3, D + 1, dtype=torch.int32, device=DEV)
     cnt = torch.zeros(3, dtype=torch.int32, device=DEV)
     frozen = {}
+    stats = eng.new_stats()
     for _ in range(40):
         before = {k: v.clone() for k, v in eng.dump(L.DUMP_STATE).items()}
-        eng.cycle(out, cnt)
+        eng.cycle(out, cnt, stats)
         eng.sync()
         after = eng.dump(L.DUMP_STATE)
         o, c = out.cpu(), cnt.cpu()
+        # the cycle's statistics: the batch's counters and the device clock per phase
+        st, acc = api.read_stats(stats), eng.dump(L.DUMP_ACCEPT)[0].cpu()
+        live = [b for b in range(3) if int(c[b]) > 0]
+        assert (st["batch"], st["active"], st["committed"], st["verify_rows"]) == (3, len(live), int(c.sum()), 15)
+        assert st["accepted"] == sum(int(acc[b]) for b in live)
+        assert st["max_accepted"] == max([int(acc[b]) for b in live] + [0])
+        assert all(t > 0 for t in st["phase_us"].values()), st
+        assert abs(sum(st["phase_us"].values()) - st["cycle_us"]) < 1e-3
         for b in range(3):
             if len(got[b]) >= limits[b]:
                 assert int(c[b]) == 0
@@ -381,3 +390,43 @@ def test_tree_budget_change_between_cycles(temperature):
     for (ta, tra), (tb, trb) in zip(*runs):
         assert ta == tb
         assert all(torch.equal(x, y) for x, y in zip(tra, trb))
+
+
+def test_phase_timing_and_graph_stats():
+    """Per-phase timing: CUDA events at the phase boundaries of profiled eager cycles (each
+    phase takes time; the verify phase is what eagle_profile_verify reports), and the
+    device-clock statistics of graph-replayed cycles (counters equal the outputs)."""
+    wl = synth.SMALL_BF16_E3.replace(tree=synth.TreeShape(topk=4, depth=5, m=14, planted_p=0.8), batch=2)
+    weights = {k: v.to(DEV) for k, v in synth.make_weights(wl, "cpu").items()}
+    g = torch.Generator().manual_seed(3)
+    prompts = [torch.randint(0, wl.model.vocab, (n,), generator=g, dtype=torch.int64).to(torch.int32).to(DEV)
+               for n in (24, 24)]
+    D = wl.tree.depth
+    stream = torch.cuda.Stream()
+    eng = api.Engine(wl, weights, max_batch=2, max_ctx=24 + 12 * (D + 1) + 16, stream=stream)
+    with torch.cuda.stream(stream):
+        eng.prefill(prompts)
+        eng.profile_begin(0)
+        for _ in range(3):
+            eng.cycle()
+        eng.profile_end()
+    n, phases = eng.profile_phases()
+    nv, vms = eng.profile_verify()
+    assert n == nv == 3
+    assert list(phases) == list(L.PHASES) and all(ms > 0 for ms in phases.values()), phases
+    assert phases["verify"] == vms
+    out = torch.zeros(2, D + 1, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(2, dtype=torch.int32, device=DEV)
+    stats = eng.new_stats()
+    with torch.cuda.stream(stream):
+        eng.set_graph(True)
+        for _ in range(3):
+            eng.cycle(out, cnt, stats)
+            eng.sync()
+            st, acc = api.read_stats(stats), eng.dump(L.DUMP_ACCEPT)[0].cpu()
+            c = cnt.cpu()
+            assert (st["batch"], st["active"], st["committed"]) == (2, 2, int(c.sum()))
+            assert st["accepted"] == int(acc[:2].sum()) == int(c.sum()) - 2
+            assert all(t > 0 for t in st["phase_us"].values()), st
+        eng.set_graph(False)
+    eng.close()

@@ -22,7 +22,7 @@ def _built():
 
 def _run(wl, weights, prompts, max_batch=1, fuse: bool = True):
     saved = {k: os.environ.get(k) for k in ("EAGLE_FUSE_EPI",)}
-    os.environ["EAGLE_FUSE_EPI"] = "1" if fuse else "0"
+    os.environ["EAGLE_FUSE_EPI"] = "3" if fuse else "0"
     try:
         eng = api.Engine(wl, weights, max_batch=max_batch)
     finally:
