@@ -543,7 +543,7 @@ def run_attn_probe(args):
     """The tree-mode attention kernel in isolation (contiguous cache larger than L2), timed
     with CUDA events over graph-replayed launches: B sequences of CTX context keys, ROWS tree
     rows each (a chain: row i sees rows 0..i), Llama-3.1-8B head geometry (32 query heads,
-    8 KV heads, head dim 128)."""
+    8 KV heads, head dim 128), with the key splits of an engine serving B sequences."""
     from eagle_speculative_decoding_cycle_gb300 import _lib as L
     from eagle_speculative_decoding_cycle_gb300 import api
     from eagle_speculative_decoding_cycle_gb300.build import build
@@ -572,7 +572,7 @@ def run_attn_probe(args):
     gs = torch.cuda.Stream()
 
     def call():
-        api.attention(q, kc, vc, row_seq, row_slot, ctx_len, T, 1, tree_T=T, mask=mask, stream=gs)
+        api.attention(q, kc, vc, row_seq, row_slot, ctx_len, T, 1, tree_T=T, mask=mask, stream=gs, max_batch=B)
 
     with torch.cuda.stream(gs):
         for _ in range(3):

@@ -109,7 +109,7 @@ def _declare(lib: C.CDLL) -> None:
                                    u64, i32, vp, vp, vp, vp, sz]),
         "eagle_op_attention_scratch_bytes": (sz, [i32, i32, i32]),
         "eagle_op_attention": (i32, [i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, i32, i32,
-                                     vp, i32, f32, vp, sz]),
+                                     vp, i32, f32, i32, vp, sz]),
         "eagle_op_tree_scratch_bytes": (sz, [i32, i32, i32, i32]),
         "eagle_op_tree_build": (i32, [vp, i32, i32, i32, i32] + [vp] * 15 + [sz]),
         "eagle_op_compact": (i32, [i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32]),

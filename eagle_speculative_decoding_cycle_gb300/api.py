@@ -308,8 +308,10 @@ def lm_head(W: torch.Tensor, X: torch.Tensor, K: int, inv_t: float = 1.0, gumbel
 
 
 def attention(q, kcache, vcache, row_seq, row_slot, ctx_len, rows_per_seq, mode, tree_T=0, mask=None,
-              scale=0.0, split_kv: bool = True, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """q [R][nq][d]; caches [B][nkv][cap][d]; returns out [R][nq][d]."""
+              scale=0.0, split_kv: bool = True, stream: Optional[torch.cuda.Stream] = None,
+              max_batch: int = 1) -> torch.Tensor:
+    """q [R][nq][d]; caches [B][nkv][cap][d]; returns out [R][nq][d]. max_batch: the key-split
+    length of an engine serving up to that many sequences."""
     lib = L.lib()
     R, nq, d = q.shape
     _, nkv, cap, _ = kcache.shape
@@ -320,7 +322,7 @@ def attention(q, kcache, vcache, row_seq, row_slot, ctx_len, rows_per_seq, mode,
     rc = lib.eagle_op_attention(_dtype_code(q), _stream(stream), q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
                                 out.data_ptr(), R, nq, nkv, d, cap, rows_per_seq, row_seq.data_ptr(),
                                 row_slot.data_ptr(), ctx_len.data_ptr(), mode, tree_T, _ptr(mask), mw, scale,
-                                scratch.data_ptr() if nb else None, nb)
+                                max_batch, scratch.data_ptr() if nb else None, nb)
     L.check(rc, "eagle_op_attention")
     return out
 

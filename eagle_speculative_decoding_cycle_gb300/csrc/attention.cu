@@ -195,7 +195,6 @@ int attention(cudaStream_t st, int dtype, const AttnArgs& a) {
 namespace eagle {
 
 constexpr int MT_KEYS = 64;       // keys per body tile
-constexpr int MT_QV = 64;         // query vectors per body CTA (rows x the GQA group)
 constexpr int TAIL_MIN = 16;      // the last TAIL_MIN positions of a row form its tail
 constexpr int MAX_SPLITS = 31;    // body splits; with the tail, one partial per lane of the merge
 constexpr int TAIL_ITEMS = 8;     // (row, query head) items per tail CTA, two per warp
@@ -466,15 +465,18 @@ __device__ __forceinline__ void tail_chunk(const AttnArgs& a, int tps, int r0, i
 // block's bodies; z >= splits: tail chunk z - splits. Query vectors qv = (row - r0) * G + g.
 // A body CTA writes the split's (m, l, o) of every query vector whose body reaches into it.
 // KIND: 0 = contiguous cache, 1 = paged cache.
-template <int D, int KIND>
-__global__ void __launch_bounds__(128, 3) attn_split_k(AttnArgs a, int tps, int splits, int nB, int tail_cap) {
+template <int D, int KIND, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 2)
+    attn_split_k(AttnArgs a, int tps, int splits, int nB, int tail_cap) {
   constexpr int LD = D + 8;                      // padded smem row (bf16 elements)
+  constexpr int QV = NW * 16;                    // query vectors per CTA
+  constexpr int NT = NW * 32;
   extern __shared__ __align__(16) uint8_t attn_smem[];
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(attn_smem);              // [2][64][LD]
   __nv_bfloat16* sV = sK + 2 * MT_KEYS * LD;                                    // [2][64][LD]
-  __shared__ int s_body[MT_QV];
+  __shared__ int s_body[QV];
   const int G = a.nq / a.nkv;
-  const int RB = MT_QV / G;
+  const int RB = QV / G;
   const int nb = (a.rows_per_seq + RB - 1) / RB;
   const int kvh = blockIdx.x;
   const int sidx = blockIdx.y / nb, rb = blockIdx.y % nb;
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(128, 3) attn_split_k(AttnArgs a, int tps, int 
   const size_t head_row0 = KIND == 1 ? 0 : ((size_t)seq * a.nkv + kvh) * (size_t)a.cap;
   auto load_tile = [&](int t, int buf) {
     constexpr int CH = D / 8;   // 16-byte chunks per row
-    for (int i = threadIdx.x; i < MT_KEYS * CH; i += 128) {
+    for (int i = threadIdx.x; i < MT_KEYS * CH; i += NT) {
       const int kr = i / CH, c = i % CH;
       const int key = t * MT_KEYS + kr;
       const bool in = key < bmax;
@@ -714,17 +716,21 @@ __global__ void attn_merge_k(AttnArgs a, int tps) {
 
 size_t attention_scratch_floats(int rows, int nq, int d) { return (size_t)(MAX_SPLITS + 1) * rows * nq * (d + 2); }
 
-// Three 64-key tiles per split (more splits put the merge and the CTA count on the critical
-// path, fewer lengthen each CTA: measured on the 8B batch-1 verify pass), at most MAX_SPLITS.
-int attention_max_splits(int cap) {
+// Key splits of a cache of `cap` slots serving up to `batch` sequences: three 64-key tiles
+// per split for one to seven sequences (more splits put the merge and the CTA count on the
+// critical path, fewer lengthen each CTA: measured on the 8B batch-1 verify pass), eight
+// from eight sequences on, where the sequences and heads alone fill the GPU and shorter
+// splits only add partials; at most MAX_SPLITS.
+int attention_max_splits(int cap, int batch) {
   const int tiles = (cap + MT_KEYS - 1) / MT_KEYS;
-  return std::max(1, std::min(MAX_SPLITS, (tiles + 2) / 3));
+  const int per = batch >= 8 ? 8 : 3;
+  return std::max(1, std::min(MAX_SPLITS, (tiles + per - 1) / per));
 }
 
-template <int D>
+template <int D, int NW>
 static int launch_bf16(cudaStream_t st, const AttnArgs& a) {
   const int G = a.nq / a.nkv;
-  const int RB = MT_QV / G;
+  const int RB = NW * 16 / G;
   const int nseq = (a.R + a.rows_per_seq - 1) / a.rows_per_seq;
   const int nb = (a.rows_per_seq + RB - 1) / RB;
   if (!a.part_o || !a.part_ml) return -1;
@@ -741,28 +747,40 @@ static int launch_bf16(cudaStream_t st, const AttnArgs& a) {
   const int tail_cap = (std::max(TAIL_MIN, a.mode == 1 ? a.tree_T : 0) + 3) & ~3;   // a multiple of 4
   const size_t body_smem = (size_t)4 * MT_KEYS * (D + 8) * sizeof(__nv_bfloat16);
   const size_t tail_smem = (size_t)2 * (TAIL_MIN + TAIL_ITEMS + nB) * (D + 8) * sizeof(__nv_bfloat16) +
-                           (size_t)4 * tail_cap * (4 + 16);
+                           (size_t)NW * tail_cap * (4 + 16);
   const size_t smem = std::max(body_smem, tail_smem);
   const bool paged = a.page.table != nullptr;
-  const void* fn = paged ? reinterpret_cast<const void*>(attn_split_k<D, 1>)
-                         : reinterpret_cast<const void*>(attn_split_k<D, 0>);
+  const void* fn = paged ? reinterpret_cast<const void*>(attn_split_k<D, 1, NW>)
+                         : reinterpret_cast<const void*>(attn_split_k<D, 0, NW>);
   if (raise_smem_limit(fn, (int)smem) != cudaSuccess) return -4;
   const dim3 grid(a.nkv, nseq * nb, splits + chunks);
-  if (paged) launch_k(attn_split_k<D, 1>, grid, 128, smem, st, a, tps, splits, nB, tail_cap);
-  else launch_k(attn_split_k<D, 0>, grid, 128, smem, st, a, tps, splits, nB, tail_cap);
+  if (paged) launch_k(attn_split_k<D, 1, NW>, grid, NW * 32, smem, st, a, tps, splits, nB, tail_cap);
+  else launch_k(attn_split_k<D, 0, NW>, grid, NW * 32, smem, st, a, tps, splits, nB, tail_cap);
   launch_k(attn_merge_k<D>, (a.R * a.nq + 3) / 4, 128, 0, st, a, tps);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// CTA size: 4 warps (64 query vectors), or 6 (96) when that puts all of a sequence's rows
+// in one block that 4 warps would split in two (each block streams the sequence's keys;
+// with more blocks, more and smaller CTAs measured faster). A query vector's arithmetic
+// does not depend on the block it sits in: keys past its body are masked to exact zeros,
+// so the choice is one of speed only.
+template <int D>
+static int launch_bf16_nw(cudaStream_t st, const AttnArgs& a, int G) {
+  const int qv = a.rows_per_seq * G;
+  const bool six = 96 % G == 0 && qv > 64 && qv <= 96;
+  return six ? launch_bf16<D, 6>(st, a) : launch_bf16<D, 4>(st, a);
+}
+
 int attention_bf16_mma(cudaStream_t st, const AttnArgs& a) {
   const int G = a.nq / a.nkv;
-  if (G < 1 || G > MT_QV || MT_QV % G) return -1;
+  if (G < 1 || G > 64 || 64 % G) return -1;
   if (a.mode == 1 && (a.mask_words > 4 || a.tree_T > 256 || a.tree_T < 1)) return -1;
   if (a.mode == 2 && a.page.table) return -1;   // the training-time test runs on the contiguous drafter cache
   switch (a.d) {
-    case 32: return launch_bf16<32>(st, a);
-    case 64: return launch_bf16<64>(st, a);
-    case 128: return launch_bf16<128>(st, a);
+    case 32: return launch_bf16_nw<32>(st, a, G);
+    case 64: return launch_bf16_nw<64>(st, a, G);
+    case 128: return launch_bf16_nw<128>(st, a, G);
   }
   return -1;
 }

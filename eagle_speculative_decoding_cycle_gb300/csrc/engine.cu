@@ -250,7 +250,7 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
     // the key splits of the cycle's launches (one per 64-key tile of the larger cache, up to
     // 32); launches with more rows (prefill chunks) run fewer, longer splits in the same space
     // (plus one tail partial per row)
-    const int ns = std::max(attention_max_splits(z.cap), attention_max_splits(z.dcap)) + 1;
+    const int ns = std::max(attention_max_splits(z.cap, z.B), attention_max_splits(z.dcap, z.B)) + 1;
     const int rs = std::max(std::max(std::max(z.B * z.T1, z.B * (z.D + 1)), z.B * z.k) * ns, 2 * z.R);
     x->attn_pfloats = (size_t)rs * z.nq * z.d;
     x->attn_po = c.take<float>(x->attn_pfloats);
@@ -360,7 +360,7 @@ int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_
   a.page = page;
   a.part_o = ctx->attn_po; a.part_ml = ctx->attn_pml; a.part_floats = ctx->attn_pfloats;
   a.err = ctx->dev_err;
-  a.max_splits = attention_max_splits(cap);   // fixed per cache: verify and plain decoding agree
+  a.max_splits = attention_max_splits(cap, z.B);   // fixed per cache: verify and plain decoding agree
   CK(attention(ctx->st, z.dt, a));
   return 0;
 }

@@ -16,7 +16,9 @@
 // weight tile, run for every token tile before the next, so the token tiles re-read its
 // weight boxes from L2). Every output element is therefore summed over the same k-split
 // points in the same order whatever M is, and a token's projection is bit-identical in a
-// 1-row and a 1088-row GEMM. A tile split across CTAs is finished by its first
+// 1-row and a 1088-row GEMM. Shapes with fewer weight tiles than CTAs and several token
+// tiles take the whole-tile schedule below instead, which adds the same pieces in the same
+// order inside one CTA. A tile split across CTAs is finished by its first
 // contributor, for which it is the last segment of its range: the later contributors reach
 // the tile at the start of their ranges, publish fp32 partials and count themselves in on
 // a per-(tile, token tile) counter; the owner waits (bounded) for that count and adds the
@@ -526,6 +528,252 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---- whole-tile schedule for several token tiles ----------------------------------------------
+// Items are (weight tile, token tile) pairs, tile-major (the token tiles of a weight tile
+// follow one another, so they re-read its boxes from L2); CTA c takes items
+// [c * I / G, (c + 1) * I / G). Each item's k-range is cut where the stream-K schedule of the
+// same (N, K) cuts that weight tile (unit ranges [c * U / Gs, (c + 1) * U / Gs) of Gs CTAs),
+// every piece is accumulated into its own TMEM buffer (accumulate flag cleared at its first
+// k-block; two buffers, so the next piece's MMAs run while the epilogue reads this one) and
+// the epilogue adds the pieces in k order in fp32 into a third TMEM buffer - the additions
+// the stream-K owner makes with its contributors' partials - so the outputs have the
+// stream-K schedule's bits, with no partials and no waits between CTAs.
+struct PieceCursor {
+  long long item, end, U;
+  int TT, kb, Gs;
+  int tile, tt, cf, cl, p;
+  long long k0, k1;        // the current piece's units [k0, k1)
+  __device__ __forceinline__ void init(long long b, long long e, int TT_, int kb_, long long U_, int Gs_) {
+    item = b; end = e; TT = TT_; kb = kb_; U = U_; Gs = Gs_;
+    if (item < end) set_item();
+  }
+  __device__ __forceinline__ void set_item() {
+    tile = (int)(item / TT);
+    tt = (int)(item - (long long)tile * TT);
+    cf = cta_of_unit((long long)tile * kb, U, Gs);
+    cl = cta_of_unit((long long)(tile + 1) * kb - 1, U, Gs);
+    p = 0;
+    set_piece();
+  }
+  __device__ __forceinline__ void set_piece() {
+    k0 = max((long long)tile * kb, (long long)(cf + p) * U / Gs);
+    k1 = min((long long)(tile + 1) * kb, (long long)(cf + p + 1) * U / Gs);
+  }
+  __device__ __forceinline__ bool done() const { return item >= end; }
+  __device__ __forceinline__ bool last_piece() const { return cf + p == cl; }
+  __device__ __forceinline__ void next() {
+    if (cf + p < cl) { ++p; set_piece(); return; }
+    if (++item < end) set_item();
+  }
+};
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(192, 1)
+    gemm_bf16_tc_whole(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const GemmArgs a, int Gs) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* staging = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + C::STAGING);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x, G = gridDim.x, TT = a.tiles_t, kb = a.kb;
+  const long long I = a.units / kb * TT;
+  const long long i_begin = (long long)cta * I / G, i_end = (long long)(cta + 1) * I / G;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(tfull + b), 1);
+      mbar_init(smem_u32(tempty + b), 128);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  constexpr uint32_t WCOLS = 3 * BN <= 256 ? 256 : 512;   // two piece buffers and the sum
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), WCOLS);
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_last();   // the next token tiles re-read it
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, parity = 0;
+      auto load_w = [&](uint32_t dst, int tile, int k, uint32_t bar) {
+        if constexpr (MODE == MODE_SWIGLU) {
+          tma_load_2d(dst, &tmW, k * 64, tile * 64, bar, pol_w);
+          tma_load_2d(dst + C::A_BYTES / 2, &tmW, k * 64, a.N + tile * 64, bar, pol_w);
+        } else {
+          tma_load_2d(dst, &tmW, k * 64, tile * 128, bar, pol_w);
+        }
+      };
+      auto load_x = [&](uint32_t dst, int tt, int k, uint32_t bar) {
+        tma_load_2d(dst, &tmX, k * 64, tt * BN, bar, pol_x);
+      };
+      // (item, k-block) steps in issue order
+      const long long steps = (i_end - i_begin) * kb;
+      const int n_pre = (int)min((long long)C::STAGES, steps);
+      // the first ring of weight boxes does not depend on the previous kernel
+      for (int i = 0; i < n_pre; ++i) {
+        const long long it = i_begin + i / kb;
+        const uint32_t fb = smem_u32(full + i);
+        mbar_expect_tx(fb, C::STAGE);
+        load_w(smem_u32(smem + i * C::STAGE), (int)(it / TT), i % kb, fb);
+        issued |= 1u << i;
+      }
+      pdl_wait();
+      for (int i = 0; i < n_pre; ++i) {
+        const long long it = i_begin + i / kb;
+        load_x(smem_u32(smem + i * C::STAGE) + C::A_BYTES, (int)(it % TT), i % kb, smem_u32(full + i));
+      }
+      stage = n_pre % C::STAGES;
+      phase = (n_pre == C::STAGES) ? 1u : 0u;
+      long long it = i_begin + n_pre / kb;
+      int k = n_pre % kb;
+      for (long long i = n_pre; i < steps; ++i) {
+        if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, abort_flag, a.err)) break;
+        const uint32_t fb = smem_u32(full + stage);
+        mbar_expect_tx(fb, C::STAGE);
+        const uint32_t sa = smem_u32(smem + stage * C::STAGE);
+        load_w(sa, (int)(it / TT), k, fb);
+        load_x(sa + C::A_BYTES, (int)(it % TT), k, fb);
+        issued |= 1u << stage;
+        parity = (parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        if (++k == kb) { k = 0; ++it; }
+      }
+      if (*abort_flag) {
+        for (int s = 0; s < C::STAGES; ++s)
+          if ((issued >> s) & 1) mbar_wait(smem_u32(full + s), (parity >> s) & 1, abort_flag, a.err, false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16<BN>();
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      PieceCursor c;
+      c.init(i_begin, i_end, TT, kb, a.units, Gs);
+      while (ok && !c.done()) {
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1, abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (long long u = c.k0; u < c.k1; ++u) {
+          if (!mbar_wait(smem_u32(full + stage), phase, abort_flag, a.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE);
+          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(d, da + 2 * kk, db + 2 * kk, IDESC, (u != c.k0 || kk) ? 1u : 0u);
+          tc_commit(smem_u32(empty + stage));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(tfull + acc));
+        acc ^= 1;
+        if (!acc) acc_phase ^= 1;
+        c.next();
+      }
+      if (!ok) {
+        tc_commit(smem_u32(drain));
+        mbar_wait(smem_u32(drain), 0, abort_flag, a.err, false);
+      }
+    }
+  } else {
+    pdl_wait();
+    constexpr int ECH = (MODE == MODE_QKV) ? 16 : C::CH;
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const bool leader = (ew == 0 && lane == 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t ts = lane_base + (uint32_t)(2 * BN);   // the running sum
+    PieceCursor c;
+    c.init(i_begin, i_end, TT, kb, a.units, Gs);
+    while (!c.done()) {
+      if (leader) bcast[0] = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag, a.err) ? 1 : 0;
+      named_bar_sync(1, 128);
+      const int ok = bcast[0];
+      named_bar_sync(1, 128);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tb = lane_base + (uint32_t)(acc * BN);
+      const bool first = c.p == 0, last = c.last_piece();
+      if (last && !first) {
+        // the last piece: sum + piece, then the epilogue; the buffer is free once read
+        for (int c0 = 0; c0 < BN; c0 += ECH) {
+          float v[ECH], w[ECH];
+          if constexpr (ECH == 32) { tmem_ld32(tb + c0, v); tmem_ld32(ts + c0, w); }
+          else { tmem_ld16(tb + c0, v); tmem_ld16(ts + c0, w); }
+#pragma unroll
+          for (int i = 0; i < ECH; ++i) v[i] = w[i] + v[i];
+          if (c0 + ECH >= BN) {
+            tc_fence_before();
+            mbar_arrive(smem_u32(tempty + acc));
+          }
+          epi_chunk<ECH, MODE>(a, c.tile, c.tt, BN, row, c0, v, staging, ew, lane);
+        }
+      } else if (last) {
+        for (int c0 = 0; c0 < BN; c0 += ECH) {
+          float v[ECH];
+          if constexpr (ECH == 32) tmem_ld32(tb + c0, v); else tmem_ld16(tb + c0, v);
+          if (c0 + ECH >= BN) {
+            tc_fence_before();
+            mbar_arrive(smem_u32(tempty + acc));
+          }
+          epi_chunk<ECH, MODE>(a, c.tile, c.tt, BN, row, c0, v, staging, ew, lane);
+        }
+      } else {
+        // a piece before the last: into the running sum
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16], w[16];
+          tmem_ld16(tb + c0, v);
+          if (!first) {
+            tmem_ld16(ts + c0, w);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = w[i] + v[i];
+          }
+          tmem_st16(ts + c0, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(tempty + acc));
+      }
+      acc ^= 1;
+      if (!acc) acc_phase ^= 1;
+      c.next();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, WCOLS);
+  }
+}
+
 // ---- host side ----------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -609,6 +857,12 @@ cudaError_t raise_smem_limit(const void* func, int bytes) {
 
 static int num_sms() { return device_sm_count(); }
 
+// EAGLE_GEMM_WHOLE=0 keeps the stream-K schedule for every row count (same results).
+static bool whole_tiles_enabled() {
+  static const bool on = !(getenv("EAGLE_GEMM_WHOLE") && strcmp(getenv("EAGLE_GEMM_WHOLE"), "0") == 0);
+  return on;
+}
+
 int gemm_bn_for(int M) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
@@ -632,6 +886,16 @@ static cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, GemmA
   return cudaGetLastError();
 }
 
+template <int MODE>
+static cudaError_t launch_whole(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int G, int Gs,
+                                cudaStream_t st) {
+  using C = TcCfg<128>;
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemm_bf16_tc_whole<128, MODE>), C::SMEM);
+  if (e != cudaSuccess) return e;
+  launch_k(gemm_bf16_tc_whole<128, MODE>, G, 192, C::SMEM, st, mw, mx, a, Gs);
+  return cudaGetLastError();
+}
+
 template <int BN>
 static cudaError_t launch_mode(const CUtensorMap& mw, const CUtensorMap& mx, GemmArgs& a, int G, cudaStream_t st) {
   if (a.epi == EPI_SWIGLU || a.epi == EPI_GU) return launch_bn<BN, MODE_SWIGLU>(mw, mx, a, G, st);
@@ -648,16 +912,22 @@ int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M
   if (paired && N % 64) return -1;
   if (epi == EPI_QKV && (!qkv || qkv->d < 2 || qkv->d % 2 || 128 % qkv->d || N != (qkv->nq + 2 * qkv->nkv) * qkv->d))
     return -1;
-  const int BN = gemm_bn_for(M);
   const int tiles_n = paired ? N / 64 : (N + 127) / 128;
-  const int tiles_t = (M + BN - 1) / BN;
-  if ((long long)tiles_n * tiles_t > counters_len) return -2;
   const int kb = (K + 63) / 64;
   const long long units = (long long)tiles_n * kb;
   // the stream-K ranges depend on (N, K, SM count) only
   int G = std::min(num_sms(), num_sms_cap());
   if (G > units) G = (int)units;
-  if ((size_t)G * tiles_t * BN * 128 > partial_floats) return -2;
+  // More than one 128-token tile and fewer weight tiles than CTAs (every tile split across
+  // CTAs, whose fixups then serialise per token tile): whole (weight tile, token tile) items
+  // cut at the same k-points, so the same bits (measured at 1088 tokens: QKV 155 -> 66 us,
+  // O 178 -> 47, down 238 -> 142; with more tiles than CTAs, gate/up and the LM head, the
+  // stream-K schedule with 256-token tiles stays faster)
+  const bool whole = M > 128 && tiles_n < G && epi != EPI_HEAD && whole_tiles_enabled();
+  const int BN = whole ? 128 : gemm_bn_for(M);
+  const int tiles_t = (M + BN - 1) / BN;
+  if (!whole && (long long)tiles_n * tiles_t > counters_len) return -2;
+  if (!whole && (size_t)G * tiles_t * BN * 128 > partial_floats) return -2;
   CUtensorMap mw, mx;
   if (paired) {
     if (!make_map(&mw, W, 2LL * N, K, 64, cache_maps)) return -3;
@@ -672,6 +942,13 @@ int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M
   if (head) a.head = *head;
   if (qkv) a.qkv = *qkv;
   cudaError_t e;
+  if (whole) {
+    const int Gw = (int)std::min<long long>(std::min(num_sms(), num_sms_cap()), (long long)tiles_n * tiles_t);
+    if (paired) e = launch_whole<MODE_SWIGLU>(mw, mx, a, Gw, G, st);
+    else if (epi == EPI_QKV) e = launch_whole<MODE_QKV>(mw, mx, a, Gw, G, st);
+    else e = launch_whole<MODE_GENERIC>(mw, mx, a, Gw, G, st);
+    return e == cudaSuccess ? 0 : -4;
+  }
   switch (BN) {
     case 16: e = launch_mode<16>(mw, mx, a, G, st); break;
     case 32: e = launch_mode<32>(mw, mx, a, G, st); break;

@@ -149,7 +149,7 @@ int attention(cudaStream_t st, int dtype, const AttnArgs& a);
 size_t attention_scratch_floats(int rows, int nq, int d);
 // the key splits to use for a cache of `cap` slots (one 64-key tile per split, up to 31);
 // the partial buffer needs one more slot per row for the tail
-int attention_max_splits(int cap);
+int attention_max_splits(int cap, int batch);
 
 // ---- tree policy, acceptance, compaction ---------------------------------------------------
 struct TreeState;   // defined in tree.cu / engine

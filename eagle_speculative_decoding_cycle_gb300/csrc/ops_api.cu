@@ -95,9 +95,9 @@ size_t eagle_op_attention_scratch_bytes(int R, int nq, int d) {
 int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcache, const void* vcache, void* out, int R,
                        int nq, int nkv, int d, int cap, int rows_per_seq, const int32_t* row_seq,
                        const int32_t* row_slot, const int32_t* ctx_len, int mode, int tree_T, const uint64_t* mask,
-                       int mask_words, float scale, void* scratch, size_t scratch_bytes) {
+                       int mask_words, float scale, int max_batch, void* scratch, size_t scratch_bytes) {
   if (!q || !kcache || !vcache || !out || !row_seq || !row_slot || !ctx_len || R <= 0 || nq <= 0 || nkv <= 0 ||
-      d <= 0 || d > 128 || nq % nkv || rows_per_seq <= 0 || (mode == 1 && (!mask || mask_words < 1)))
+      d <= 0 || d > 128 || nq % nkv || rows_per_seq <= 0 || max_batch < 1 || (mode == 1 && (!mask || mask_words < 1)))
     return EAGLE_EINVAL;
   AttnArgs a{};
   a.q = q; a.kcache = kcache; a.vcache = vcache; a.out = out;
@@ -108,7 +108,7 @@ int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcach
     a.part_o = reinterpret_cast<float*>(scratch);
     a.part_floats = attention_scratch_floats(R, nq, d) / (d + 2) * d;
     a.part_ml = a.part_o + a.part_floats;
-    a.max_splits = attention_max_splits(cap);   // the engine's split policy for a cache of cap slots
+    a.max_splits = attention_max_splits(cap, max_batch);   // the engine's split policy for this cache
   } else if (dtype != EAGLE_DTYPE_F32) {
     return EAGLE_ECAPACITY;
   }

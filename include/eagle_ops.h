@@ -88,13 +88,16 @@ int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, co
  * tree mode, whose ancestors must have increasing slots by depth) has its keys up to
  * position P - 16 summed in fixed key splits on the tensor cores, its last 16 positions in
  * position order on the FMA units, and the two merged in a fixed order; so a tree row and
- * a causal row at the same position over the same keys give bit-identical outputs. */
+ * a causal row at the same position over the same keys give bit-identical outputs. The
+ * split length is that of an engine serving up to max_batch sequences (>= 1): three
+ * 64-key tiles below eight sequences, eight from eight on; calls with the same cap and
+ * max_batch share it. */
 size_t eagle_op_attention_scratch_bytes(int R, int nq, int d);
 int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcache, const void* vcache,
                        void* out, int R, int nq, int nkv, int d, int cap, int rows_per_seq,
                        const int32_t* row_seq, const int32_t* row_slot, const int32_t* ctx_len, int mode,
-                       int tree_T, const uint64_t* mask, int mask_words, float scale, void* scratch,
-                       size_t scratch_bytes);
+                       int tree_T, const uint64_t* mask, int mask_words, float scale, int max_batch,
+                       void* scratch, size_t scratch_bytes);
 
 /* EAGLE-2 tree growth and rerank with injected draft confidences, for B sequences:
  * cand_tok/cand_logc [B][k]: the root's children (token, log confidence) in rank order;
