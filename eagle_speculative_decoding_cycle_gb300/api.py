@@ -309,9 +309,9 @@ def lm_head(W: torch.Tensor, X: torch.Tensor, K: int, inv_t: float = 1.0, gumbel
 
 def attention(q, kcache, vcache, row_seq, row_slot, ctx_len, rows_per_seq, mode, tree_T=0, mask=None,
               scale=0.0, split_kv: bool = True, stream: Optional[torch.cuda.Stream] = None,
-              max_batch: int = 1) -> torch.Tensor:
-    """q [R][nq][d]; caches [B][nkv][cap][d]; returns out [R][nq][d]. max_batch: the key-split
-    length of an engine serving up to that many sequences."""
+              max_batch: Optional[int] = None) -> torch.Tensor:
+    """q [R][nq][d]; caches [B][nkv][cap][d]; returns out [R][nq][d]. max_batch: the caches'
+    sequences B (default), which also sets the key-split length of an engine of that batch."""
     lib = L.lib()
     R, nq, d = q.shape
     _, nkv, cap, _ = kcache.shape
@@ -322,7 +322,8 @@ def attention(q, kcache, vcache, row_seq, row_slot, ctx_len, rows_per_seq, mode,
     rc = lib.eagle_op_attention(_dtype_code(q), _stream(stream), q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
                                 out.data_ptr(), R, nq, nkv, d, cap, rows_per_seq, row_seq.data_ptr(),
                                 row_slot.data_ptr(), ctx_len.data_ptr(), mode, tree_T, _ptr(mask), mw, scale,
-                                max_batch, scratch.data_ptr() if nb else None, nb)
+                                int(kcache.shape[0]) if max_batch is None else max_batch,
+                                scratch.data_ptr() if nb else None, nb)
     L.check(rc, "eagle_op_attention")
     return out
 

@@ -15,8 +15,11 @@
 // keeps an online softmax per query vector (one warp per query vector group).
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
 namespace eagle {
 
@@ -261,20 +264,20 @@ __device__ __forceinline__ RowSpan row_span(const AttnArgs& a, int r, int ctx) {
 // quarter of the head dimension each, summed (q0 + q1) + (q2 + q3)), their softmax, and P.V in
 // position order, written as the row's partial after its body splits. Training-time-test
 // chain keys are read from the cache directly.
-template <int D, int KIND>
+template <int D, int KIND, int ITEMS = TAIL_ITEMS>
 __device__ __forceinline__ void tail_chunk(const AttnArgs& a, int tps, int r0, int r1, int kvh, int chunk, int nB,
                                            int tail_cap, uint8_t* smem) {
   constexpr int LD = D + 8;
   constexpr int DL = D / 32;                         // output dims per lane
   constexpr int DQ = D / 4;                          // score dims per lane (a quarter)
-  __shared__ int s_P[TAIL_ITEMS], s_pe[TAIL_ITEMS], s_body[TAIL_ITEMS];
+  __shared__ int s_P[ITEMS], s_pe[ITEMS], s_body[ITEMS];
   __shared__ int s_lo, s_hi;
   const int G = a.nq / a.nkv;
-  const int it0 = chunk * TAIL_ITEMS;
-  const int n_items = min(TAIL_ITEMS, (r1 - r0) * G - it0);
+  const int it0 = chunk * ITEMS;
+  const int n_items = min(ITEMS, (r1 - r0) * G - it0);
   if (n_items <= 0) return;
   const int ra = r0 + it0 / G, rz = r0 + (it0 + n_items - 1) / G;   // rows [ra, rz]
-  const int nA_cap = TAIL_MIN + TAIL_ITEMS;
+  const int nA_cap = TAIL_MIN + ITEMS;
   __nv_bfloat16* sAK = reinterpret_cast<__nv_bfloat16*>(smem);
   __nv_bfloat16* sAV = sAK + (size_t)nA_cap * LD;
   __nv_bfloat16* sBK = sAV + (size_t)nA_cap * LD;
@@ -665,6 +668,344 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 2)
   }
 }
 
+// ---- body splits on the 5th-generation tensor cores (head dim 128) -------------------------------
+// One CTA per (KV head, block of up to 128 query vectors, key split), 192 threads: warps 0-3
+// own one query vector each per thread (TMEM lane = query vector), warp 4 issues the TMA
+// loads, warp 5 the MMAs and owns the TMEM. Per 64-key tile t of the split:
+//   S = Q K_t^T     tcgen05.mma, Q [128 x 128] and K_t [64 x 128] K-major in shared memory
+//                   (128-byte swizzle), S [128 x 64] fp32 in TMEM;
+//   softmax         each thread reads its row of S, masks keys past its body, updates its
+//                   running max and sum, and writes P = exp2(S - max) as a bf16 high part
+//                   and a bf16 residual (~16 bits of P) to shared memory;
+//   O += P V_t      two tcgen05.mma (high, residual) accumulate into O [128 x 128] fp32 in
+//                   TMEM, V_t [64 keys x 128] read MN-major; before them the thread rescales
+//                   its row of O when its max moved (a factor of exactly 1 is skipped).
+// K_t+1 is loaded as soon as S_t is computed and V_t+1 as soon as O has taken V_t; S_t+1 is
+// issued before P_t V_t, so the tensor cores compute it while the softmax of tile t ends.
+// Every wait is bounded; a timeout latches an error and the CTA drains and exits.
+constexpr int TC_THREADS = 192;
+constexpr int TC_TAIL_ITEMS = 24;                  // tail items per CTA: four per warp
+constexpr int TC_Q_BYTES = 2 * 128 * 128;          // [2 d-halves][128 rows][128 B]
+constexpr int TC_KV_BYTES = 2 * 64 * 128;          // [2 d-halves][64 keys][128 B]
+constexpr int TC_P_BYTES = 128 * 128;              // [128 rows][64 keys bf16]
+constexpr int TC_SMEM = 1024 + TC_Q_BYTES + 2 * TC_KV_BYTES + 2 * TC_P_BYTES + 256;
+
+// kind::f16 instruction descriptor: bf16 operands, fp32 accumulator, M = 128, N = n; A
+// K-major; B K-major, or MN-major (transposed) when b_mn.
+__device__ __forceinline__ constexpr uint32_t attn_idesc(int n, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(128 >> 4) << 24);
+}
+
+// MN-major operand with the 128-byte swizzle: rows of 64 MN-elements (128 bytes), one row
+// per k; 8-row atoms 1024 bytes apart along k (stride byte offset), the next 64 MN-elements
+// `mn_stride` bytes on (leading byte offset).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  tmem_st16(taddr, v);
+  tmem_st16(taddr + 16, v + 16);
+}
+
+// A bounded wait taken by lane 0 for its warp: the warp's tcgen05.ld/st are collective
+// (.sync.aligned), so every lane must take the same branch after a wait.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(TC_THREADS, 2)
+    attn_tc_k(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a,
+              int tps, int splits, int nB, int tail_cap) {
+  constexpr int D = 128;
+  extern __shared__ __align__(16) uint8_t attn_smem[];
+  const int G = a.nq / a.nkv;
+  const int RB = 128 / G;
+  const int nb = (a.rows_per_seq + RB - 1) / RB;
+  const int kvh = blockIdx.x;
+  const int sidx = blockIdx.y / nb, rb = blockIdx.y % nb;
+  const int split = blockIdx.z;
+  const int r0 = sidx * a.rows_per_seq + rb * RB;
+  const int r1 = min(r0 + RB, min((sidx + 1) * a.rows_per_seq, a.R));
+  if (r0 >= r1) return;
+  if (split >= splits) {
+    tail_chunk<D, KIND, TC_TAIL_ITEMS>(a, tps, r0, r1, kvh, split - splits, nB, tail_cap, attn_smem);
+    return;
+  }
+  __shared__ int s_body[128];
+  const int seq = a.row_seq[r0];
+  const int ctx = a.ctx_len[seq];
+  if (a.mode == 1 && split * tps * MT_KEYS >= ctx) return;
+  for (int i = threadIdx.x; i < r1 - r0; i += blockDim.x) s_body[i] = row_span(a, r0 + i, ctx).body;
+  __syncthreads();
+  int bmax = 0;
+  for (int i = 0; i < r1 - r0; ++i) bmax = max(bmax, s_body[i]);
+  bmax = min(bmax, a.cap);
+  const int t_begin = split * tps, t_end = min(t_begin + tps, (bmax + MT_KEYS - 1) / MT_KEYS);
+  if (t_begin >= t_end) return;
+
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm;
+  uint8_t* sK = sQ + TC_Q_BYTES;
+  uint8_t* sV = sK + TC_KV_BYTES;
+  uint8_t* sP = sV + TC_KV_BYTES;                       // [hi, lo]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * TC_P_BYTES);
+  uint64_t* k_full = bars + 0;
+  uint64_t* k_empty = bars + 1;
+  uint64_t* v_full = bars + 2;
+  uint64_t* v_empty = bars + 3;
+  uint64_t* s_full = bars + 4;
+  uint64_t* s_empty = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* o_done = bars + 7;    // P_t V_t complete (O updated, P and V_t free)
+  uint64_t* q_ready = bars + 8;
+  uint64_t* drain = bars + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = t_end - t_begin;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(k_full), 1);
+    mbar_init(smem_u32(k_empty), 1);
+    mbar_init(smem_u32(v_full), 1);
+    mbar_init(smem_u32(v_empty), 1);
+    mbar_init(smem_u32(s_full), 1);
+    mbar_init(smem_u32(s_empty), 128);
+    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(o_done), 1);
+    mbar_init(smem_u32(q_ready), 128);
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 256);   // S: columns 0-63, O: 128-255
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const size_t head_row0 = KIND == 1 ? 0 : ((size_t)seq * a.nkv + kvh) * (size_t)a.cap;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      // a tile's rows: one 64-row box per d-half (contiguous cache) or one 16-row box per
+      // cache block (paged); boxes wholly past the keys in use are not loaded
+      auto load_tile = [&](const CUtensorMap* map, uint8_t* dst, int t, uint32_t bar) {
+        if constexpr (KIND == 0) {
+          mbar_expect_tx(bar, TC_KV_BYTES);
+          const int row = (int)(head_row0 + (size_t)t * MT_KEYS);
+          tma_load_2d(smem_u32(dst), map, 0, row, bar, pol);
+          tma_load_2d(smem_u32(dst + TC_KV_BYTES / 2), map, 64, row, bar, pol);
+        } else {
+          const int box = min(1 << a.page.bs_log2, MT_KEYS);   // slots of a block are consecutive rows
+          const int nbox = MT_KEYS / box;
+          int live = 0;
+          for (int i = 0; i < nbox; ++i) live += (t * MT_KEYS + i * box < bmax);
+          mbar_expect_tx(bar, (uint32_t)live * box * 256);
+          for (int i = 0; i < nbox; ++i) {
+            const int slot = t * MT_KEYS + i * box;
+            if (slot >= bmax) continue;
+            const int row = (int)kv_row(a.page, seq, a.nkv, kvh, a.cap, slot);
+            tma_load_2d(smem_u32(dst + i * box * 128), map, 0, row, bar, pol);
+            tma_load_2d(smem_u32(dst + TC_KV_BYTES / 2 + i * box * 128), map, 64, row, bar, pol);
+          }
+        }
+      };
+      // K and V of the first tile sit below every slot the preceding kernel writes only in
+      // tree mode; wait for it before the first load otherwise
+      if (a.mode != 1) pdl_wait();
+      load_tile(&tmK, sK, t_begin, smem_u32(k_full));
+      load_tile(&tmV, sV, t_begin, smem_u32(v_full));
+      int nk = 1, nv = 1;   // tiles issued
+      for (int i = 1; i < nt; ++i) {
+        const uint32_t ph = (uint32_t)((i - 1) & 1);
+        if (!mbar_wait(smem_u32(k_empty), ph, abort_flag, a.err)) break;
+        load_tile(&tmK, sK, t_begin + i, smem_u32(k_full));
+        ++nk;
+        if (!mbar_wait(smem_u32(v_empty), ph, abort_flag, a.err)) break;
+        load_tile(&tmV, sV, t_begin + i, smem_u32(v_full));
+        ++nv;
+      }
+      if (*abort_flag) {   // let the copies in flight land before the CTA leaves
+        mbar_wait(smem_u32(k_full), (uint32_t)((nk - 1) & 1), abort_flag, a.err, false);
+        mbar_wait(smem_u32(v_full), (uint32_t)((nv - 1) & 1), abort_flag, a.err, false);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t IS = attn_idesc(64, false), IO = attn_idesc(128, true);
+      const uint32_t tS = tmem, tO = tmem + 128;
+      bool ok = mbar_wait(smem_u32(q_ready), 0, abort_flag, a.err);
+      auto issue_s = [&](int i) -> bool {
+        if (!mbar_wait(smem_u32(k_full), (uint32_t)(i & 1), abort_flag, a.err)) return false;
+        if (i > 0 && !mbar_wait(smem_u32(s_empty), (uint32_t)((i - 1) & 1), abort_flag, a.err)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t da = sdesc_sw128(smem_u32(sQ + (k >> 2) * (TC_Q_BYTES / 2) + (k & 3) * 32));
+          const uint64_t db = sdesc_sw128(smem_u32(sK + (k >> 2) * (TC_KV_BYTES / 2) + (k & 3) * 32));
+          tc_mma_bf16(tS, da, db, IS, k ? 1u : 0u);
+        }
+        tc_commit(smem_u32(s_full));
+        tc_commit(smem_u32(k_empty));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int i = 0; ok && i < nt; ++i) {
+        if (i + 1 < nt && !issue_s(i + 1)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(p_full), (uint32_t)(i & 1), abort_flag, a.err) ||
+            !mbar_wait(smem_u32(v_full), (uint32_t)(i & 1), abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t da = sdesc_sw128(smem_u32(sP + part * TC_P_BYTES + j * 32));
+            const uint64_t db = sdesc_sw128_mn(smem_u32(sV + j * 2048), TC_KV_BYTES / 2);
+            tc_mma_bf16(tO, da, db, IO, (i > 0 || part || j) ? 1u : 0u);
+          }
+        tc_commit(smem_u32(o_done));
+        tc_commit(smem_u32(v_empty));
+      }
+      if (!ok) {
+        tc_commit(smem_u32(drain));
+        mbar_wait(smem_u32(drain), 0, abort_flag, a.err, false);
+      }
+    }
+  } else {
+    // softmax threads: query vector qv = threadIdx.x
+    const int qv = threadIdx.x;
+    const int row = r0 + qv / G, head = kvh * G + qv % G;
+    const bool valid = row < r1;
+    const int body = valid ? s_body[row - r0] : 0;
+    PDL_ENTRY();
+    {
+      // Q row -> shared memory, 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7))
+      const uint4* qp = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                                       ((size_t)(valid ? row : r0) * a.nq + head) * D);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 x = valid ? qp[c] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sQ + (c >> 3) * (TC_Q_BYTES / 2) + qv * 128 + (((c & 7) ^ (qv & 7)) << 4)) = x;
+      }
+      fence_proxy_async_all();
+      mbar_arrive(smem_u32(q_ready));
+    }
+    const uint32_t lane_off = (uint32_t)((warp * 32) << 16);
+    const uint32_t tS = tmem + lane_off, tO = tmem + 128 + lane_off;
+    const float sl2 = a.scale * 1.4426950408889634f;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < nt; ++i) {
+      const int t = t_begin + i;
+      if (!warp_wait(smem_u32(s_full), (uint32_t)(i & 1), abort_flag, a.err)) { ok = false; break; }
+      tc_fence_after();
+      float s[64];
+      tmem_ld32(tS, s);
+      tmem_ld32(tS + 32, s + 32);
+      tc_fence_before();
+      mbar_arrive(smem_u32(s_empty));
+      // keys past this query vector's body belong to its tail or are invisible
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        s[j] = t * MT_KEYS + j < body ? s[j] * sl2 : -INFINITY;
+        mx = fmaxf(mx, s[j]);
+      }
+      const float mn = fmaxf(m, mx);
+      const float base = mn == -INFINITY ? 0.f : mn;
+      const float corr = exp2f(m - base);
+      m = mn;
+      float ps = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        s[j] = exp2f(s[j] - base);
+        ps += s[j];
+      }
+      l = l * corr + ps;
+      // P_(t-1) V_(t-1) must be complete before O is rescaled and P is overwritten
+      if (i > 0) {
+        if (!warp_wait(smem_u32(o_done), (uint32_t)((i - 1) & 1), abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+        // warp-uniform: a lane whose factor is exactly 1 multiplies by 1
+        if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            float o[32];
+            tmem_ld32(tO + c0, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] *= corr;
+            tmem_st32(tO + c0, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // the last tile's keys past the block's bodies: V rows zeroed (P is zero there, and a
+      // stale slot must not contribute 0 * NaN)
+      if (t * MT_KEYS + MT_KEYS > bmax) {
+        if (!warp_wait(smem_u32(v_full), (uint32_t)(i & 1), abort_flag, a.err)) { ok = false; break; }
+        const int k0 = bmax - t * MT_KEYS;
+        for (int idx = threadIdx.x; idx < (MT_KEYS - k0) * 16; idx += 128) {
+          const int kr = k0 + idx / 16, c = idx % 16;
+          *reinterpret_cast<uint4*>(sV + (c >> 3) * (TC_KV_BYTES / 2) + kr * 128 + ((c & 7) << 4)) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      // P (high part, then residual) -> shared memory, same swizzle as Q
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t h[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_bf16(s[c * 8 + 2 * e], s[c * 8 + 2 * e + 1], h[e], lo[e]);
+        const int off = qv * 128 + ((c ^ (qv & 7)) << 4);
+        *reinterpret_cast<uint4*>(sP + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(sP + TC_P_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_all();
+      tc_fence_before();
+      mbar_arrive(smem_u32(p_full));
+    }
+    if (ok && warp_wait(smem_u32(o_done), (uint32_t)((nt - 1) & 1), abort_flag, a.err)) {
+      tc_fence_after();
+      const bool wr = valid && t_begin * MT_KEYS < body;
+      const size_t q = ((size_t)split * a.R + row) * a.nq + head;
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float o[32];
+        tmem_ld32(tO + c0, o);
+        if (wr) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(a.part_o + q * D + c0 + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+        }
+      }
+      if (wr) {
+        a.part_ml[q * 2] = m;
+        a.part_ml[q * 2 + 1] = l;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 // Merge: one warp per (row, query head). Lane s holds partial s (the body splits of the
 // row's position, then its tail); the weighted sums run in partial order.
 template <int D>
@@ -760,6 +1101,51 @@ static int launch_bf16(cudaStream_t st, const AttnArgs& a) {
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// EAGLE_ATTN_TC=1 runs head dim 128 on the tcgen05 bodies (a different summation order: one
+// setting holds for the whole process, so every launch over a cache agrees). Off by default:
+// measured slower than the mma.sync bodies (8B batch 64, 1100 keys, 17 tree rows: 287
+// against 275 us; batch 1, 61 rows: 35.6 against 23.0 us). Its thread-per-row softmax issues
+// ~2600 warp-instructions per 64-key tile at ~9 resident warps per SM (ncu: IPC 1.2, tensor
+// pipe 9%, DRAM 16%): the tensor cores wait on the softmax, not the reverse.
+static bool tc_attention_enabled() {
+  static const bool on = getenv("EAGLE_ATTN_TC") && strcmp(getenv("EAGLE_ATTN_TC"), "1") == 0;
+  return on;
+}
+
+// Head dim 128 with the cache's row count known: bodies on tcgen05 (attn_tc_k).
+static int launch_tc(cudaStream_t st, const AttnArgs& a) {
+  constexpr int D = 128;
+  const int G = a.nq / a.nkv;
+  const int RB = 128 / G;
+  const int nseq = (a.R + a.rows_per_seq - 1) / a.rows_per_seq;
+  const int nb = (a.rows_per_seq + RB - 1) / RB;
+  if (!a.part_o || !a.part_ml) return -1;
+  const int max_tiles = std::max(1, (a.cap + MT_KEYS - 1) / MT_KEYS);
+  const long long fit = (long long)(a.part_floats / ((size_t)a.R * a.nq * D)) - 1;
+  if (fit < 1) return -1;
+  const int S = (int)std::min<long long>(std::min(MAX_SPLITS, std::max(1, a.max_splits)), fit);
+  const int tps = (max_tiles + S - 1) / S;
+  const int splits = (max_tiles + tps - 1) / tps;
+  const int chunks = (RB * G + TC_TAIL_ITEMS - 1) / TC_TAIL_ITEMS;
+  const int nB = a.mode == 1 ? a.tree_T : 0;
+  const int tail_cap = (std::max(TAIL_MIN, a.mode == 1 ? a.tree_T : 0) + 3) & ~3;
+  const size_t tail_smem = (size_t)2 * (TAIL_MIN + TC_TAIL_ITEMS + nB) * (D + 8) * sizeof(__nv_bfloat16) +
+                           (size_t)(TC_THREADS / 32) * tail_cap * (4 + 16);
+  const size_t smem = std::max((size_t)TC_SMEM, tail_smem);
+  const bool paged = a.page.table != nullptr;
+  const int box = paged ? std::min(1 << a.page.bs_log2, MT_KEYS) : MT_KEYS;
+  CUtensorMap mk, mv;
+  if (!make_tmap_bf16(&mk, a.kcache, a.kv_rows, D, box) || !make_tmap_bf16(&mv, a.vcache, a.kv_rows, D, box))
+    return -4;
+  const void* fn = paged ? reinterpret_cast<const void*>(attn_tc_k<1>) : reinterpret_cast<const void*>(attn_tc_k<0>);
+  if (raise_smem_limit(fn, (int)smem) != cudaSuccess) return -4;
+  const dim3 grid(a.nkv, nseq * nb, splits + chunks);
+  if (paged) launch_k(attn_tc_k<1>, grid, TC_THREADS, smem, st, mk, mv, a, tps, splits, nB, tail_cap);
+  else launch_k(attn_tc_k<0>, grid, TC_THREADS, smem, st, mk, mv, a, tps, splits, nB, tail_cap);
+  launch_k(attn_merge_k<D>, (a.R * a.nq + 3) / 4, 128, 0, st, a, tps);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
 // CTA size: 4 warps (64 query vectors), or 6 (96) when that puts all of a sequence's rows
 // in one block that 4 warps would split in two (each block streams the sequence's keys;
 // with more blocks, more and smaller CTAs measured faster). A query vector's arithmetic
@@ -780,7 +1166,8 @@ int attention_bf16_mma(cudaStream_t st, const AttnArgs& a) {
   switch (a.d) {
     case 32: return launch_bf16_nw<32>(st, a, G);
     case 64: return launch_bf16_nw<64>(st, a, G);
-    case 128: return launch_bf16_nw<128>(st, a, G);
+    case 128: return a.kv_rows > 0 && 128 % G == 0 && tc_attention_enabled() ? launch_tc(st, a)
+                                                                            : launch_bf16_nw<128>(st, a, G);
   }
   return -1;
 }

@@ -173,12 +173,12 @@ struct eagle_ctx {
   float *v_val, *v_lse, *v_spec, *v_logits; int* v_id;       // verify head (kept for the cycle's dump)
   float* gemm_part; size_t gemm_part_floats; int* gemm_cnt; int gemm_cnt_len;
   float *attn_po, *attn_pml; size_t attn_pfloats;
-  // bf16 fused epilogues: -1 (default) SwiGLU in the gate/up epilogue from 128 rows on, where
-  // the separate SwiGLU pass costs more than the epilogue work; otherwise the bits of
-  // EAGLE_FUSE_EPI: 1 = SwiGLU in the gate/up epilogue, 2 = RoPE/KV write in the QKV
-  // epilogue, at every row count (0: none, 3: both). Both epilogues agree bit for bit with
+  // bf16 fused epilogues, the bits of EAGLE_FUSE_EPI: 1 = SwiGLU in the gate/up epilogue
+  // (the default: measured faster at every batch, 8B batch-1 verify 4.61 -> 4.57 ms),
+  // 2 = RoPE/KV write in the QKV epilogue (slower at 61 rows: 4.96 ms), at every row count
+  // (0: none, 3: both; -1: SwiGLU from 128 rows on). Both epilogues agree bit for bit with
   // the row kernels they replace.
-  int fuse_epi = -1;
+  int fuse_epi = 1;
   float *rope_cos, *rope_sin;
   void *kc, *vc, *dkc, *dvc;
   int *static_exp, *static_keep;        // static tree: [D-1][k] expansion rows, [NG] kept flags
@@ -361,6 +361,7 @@ int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_
   a.part_o = ctx->attn_po; a.part_ml = ctx->attn_pml; a.part_floats = ctx->attn_pfloats;
   a.err = ctx->dev_err;
   a.max_splits = attention_max_splits(cap, z.B);   // fixed per cache: verify and plain decoding agree
+  a.kv_rows = page.table ? (long long)z.nblk * z.nkv << z.kvb_log2 : (long long)z.B * z.nkv * cap;
   CK(attention(ctx->st, z.dt, a));
   return 0;
 }
@@ -385,11 +386,9 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   if (r) return r;
   CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
   CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
-  // With more than one sequence, the verify pass (B(m+1) rows) and plain decoding (B rows)
-  // straddle the 128-row point where the SwiGLU epilogue pays off: both then use the paired
-  // [gate; up] tile layout, fused or not, which gives the same bits either way. One sequence
-  // keeps the plain layout (a 128-row weight box per stage) for every launch, unless
-  // EAGLE_FUSE_EPI is set to any value (then both settings share the paired layout).
+  // The paired [gate; up] tile layout (64 gate + the matching 64 up features per tile) with
+  // SwiGLU in the epilogue, or its fp32 gate/up values and a separate SwiGLU pass (the same
+  // bits); the plain layout only for one sequence under EAGLE_FUSE_EPI=-1.
   if (z.dt == DT_BF16 && z.F % 64 == 0 && (ctx->batch > 1 || ctx->fuse_epi >= 0)) {
     if ((ctx->fuse_epi > 0 && (ctx->fuse_epi & 1)) || (ctx->fuse_epi < 0 && R >= 128)) {
       CK(gemm(ctx, lw.wgu, z.F, z.H, ctx->ain, R, EPI_SWIGLU, ctx->hb, z.F));

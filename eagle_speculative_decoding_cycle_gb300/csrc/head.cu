@@ -96,8 +96,11 @@ int head_partials_from_logits(cudaStream_t st, const float* logits, int ld, cons
 int head_merge(cudaStream_t st, const HeadParams& p) {
   if (p.n_rows <= 0) return 0;
   if (p.K < 1 || p.K > 16) return -1;
-  // up to 1024 tiles: one record per thread of a 32-warp CTA; more: 8 warps folding many
-  if (p.n_tiles <= 1024) launch_k(head_merge_k<32>, p.n_rows, 1024, 0, st, p);
+  // up to 1024 tiles: one record per thread of a 32-warp CTA, launched without early start
+  // (a 1024-thread CTA needs a whole SM's registers, so started early it only waits for the
+  // LM-head GEMM's CTAs to leave; measured 0.14 ms per 8B batch-1 cycle faster this way);
+  // more: 8 warps folding many
+  if (p.n_tiles <= 1024) head_merge_k<32><<<p.n_rows, 1024, 0, st>>>(p);
   else launch_k(head_merge_k<8>, p.n_rows, 256, 0, st, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }

@@ -144,6 +144,8 @@ struct AttnArgs {
   int* err;             // device status word for bounds checks (nullable)
   int max_splits;       // key splits of the bf16 path (1..32): a constant of the caller, so that
                         // every launch over one cache sums a row's keys in the same splits
+  long long kv_rows;    // rows of d elements in the cache buffers (their TMA extent; 0: unknown,
+                        // the bf16 path then stays on mma.sync)
 };
 int attention(cudaStream_t st, int dtype, const AttnArgs& a);
 size_t attention_scratch_floats(int rows, int nq, int d);

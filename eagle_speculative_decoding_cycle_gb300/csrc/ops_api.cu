@@ -109,6 +109,7 @@ int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcach
     a.part_floats = attention_scratch_floats(R, nq, d) / (d + 2) * d;
     a.part_ml = a.part_o + a.part_floats;
     a.max_splits = attention_max_splits(cap, max_batch);   // the engine's split policy for this cache
+    a.kv_rows = (long long)max_batch * nkv * cap;
   } else if (dtype != EAGLE_DTYPE_F32) {
     return EAGLE_ECAPACITY;
   }

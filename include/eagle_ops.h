@@ -75,7 +75,8 @@ int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, co
                      size_t scratch_bytes);
 
 /* Tree-masked attention of R query rows over a KV cache laid out
- * [seq][kv_head][slot][d] with `cap` slots (storage type dtype). q, out: [R][nq][d].
+ * [seq][kv_head][slot][d] with `cap` slots and max_batch sequences (storage type dtype;
+ * row_seq < max_batch). q, out: [R][nq][d].
  * Rows of one sequence are contiguous, rows_per_seq each; row r belongs to sequence
  * row_seq[r] and its own key sits at slot row_slot[r]. mode 0 (causal): row r sees
  * slots <= row_slot[r]. mode 1 (tree): row r sees slots < ctx_len[seq] and slot
@@ -91,7 +92,8 @@ int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, co
  * a causal row at the same position over the same keys give bit-identical outputs. The
  * split length is that of an engine serving up to max_batch sequences (>= 1): three
  * 64-key tiles below eight sequences, eight from eight on; calls with the same cap and
- * max_batch share it. */
+ * max_batch share it. With d = 128 the splits run on tcgen05 (TMA tiles of the cache,
+ * S and O in TMEM). */
 size_t eagle_op_attention_scratch_bytes(int R, int nq, int d);
 int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcache, const void* vcache,
                        void* out, int R, int nq, int nkv, int d, int cap, int rows_per_seq,
