@@ -401,7 +401,10 @@ def run_ours(args, ws, rank, local):
                                             "LM-head launch of a cycle)",
                                     "achieved": gemm_gbs, "peak": hbm_peak, "unit": "GB/s",
                                     "frac": (gemm_gbs / hbm_peak) if gemm_gbs else None,
-                                    "traffic": traffic_per_launch(),
+                                    # the captured launches' DRAM bytes per algorithmic byte,
+                                    # scaled to this run's average launch
+                                    "traffic": (traffic_ratio() * gemm_bytes / max(n_launch, 1))
+                                    if traffic_ratio() else None,
                                     "timing": f"CUDA events around each of {n_launch} GEMM launches over "
                                               f"{args.prof_steps} cycles (eager launches on the engine stream)",
                                     "bytes_per_launch_avg": gemm_bytes / max(n_launch, 1),
@@ -423,10 +426,11 @@ def run_ours(args, ws, rank, local):
     return res, wl, weights
 
 
-def traffic_per_launch():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if the GEMM kernel's sources
-    are unchanged since the counters were taken (else None)."""
-    p = os.path.join(ROOT, "profiles", "gemm_bf16_tc_cycle_llama2-7b-eagle1.md")
+def traffic_ratio():
+    """DRAM bytes per algorithmic byte of the GEMM launches in the committed ncu summary (a
+    small case of the same kernel), if the GEMM kernel's sources are unchanged since the
+    counters were taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "gemm_bf16_tc_verify_llama3.1-8b-2layers.md")
     try:
         vals = {}
         with open(p) as f:
@@ -437,7 +441,7 @@ def traffic_per_launch():
         from eagle_speculative_decoding_cycle_gb300.build import gemm_digest
         if vals.get("gemm source digest") != gemm_digest():
             return None
-        return float(vals["dram bytes per launch"])
+        return float(vals["dram bytes per algorithmic byte"])
     except Exception:
         return None
 
@@ -469,14 +473,18 @@ def run_ncu_region(args):
     eng.cycle()
     eng.sync()
     torch.cuda.synchronize()
+    # the region is also bracketed by cudaProfilerStart/Stop: under `ncu --profile-from-start
+    # off` only its launches are seen, so -s/-c count from the first cycle's first kernel
+    out = torch.zeros(B, 2, dtype=torch.int32, device=dev)
+    torch.cuda.profiler.start()
     torch.cuda.nvtx.range_push("profiled")
     for _ in range(args.steps):
         eng.cycle()
-    out = torch.zeros(B, 2, dtype=torch.int32, device=dev)
     eng.decode_plain(2, out)
     eng.sync()
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
+    torch.cuda.profiler.stop()
     print(json.dumps({"ncu_region": True, "workload": wl.name, "batch": B, "cycles": args.steps, "plain_steps": 2}))
 
 
