@@ -456,7 +456,9 @@ def run_ncu_region(args):
     dev = torch.device("cuda:0")
     wl = synth.WORKLOADS[args.workload]
     if args.layers:   # a shallower model of the same width: the small case for multi-pass captures
-        wl = wl.replace(model=dataclasses.replace(wl.model, n_layers=args.layers))
+        wl = wl.replace(model=dataclasses.replace(wl.model, n_layers=args.layers),
+                        drafter=dataclasses.replace(wl.drafter, fuse_layers=tuple(
+                            min(f, args.layers - 1) for f in wl.drafter.fuse_layers)))
     D = wl.tree.depth
     weights = synth.make_weights(wl, device=str(dev))
     prompts = [p.to(dev) for p in synth.make_prompts(wl)]

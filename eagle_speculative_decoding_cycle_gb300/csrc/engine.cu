@@ -455,6 +455,10 @@ int drafter_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const
     CK(gemm(ctx, ctx->w.fc, z.H, 2 * z.H, ctx->ain, R, EPI_F32, ctx->x, z.H));
     CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
     kin = z.H;
+  } else if (z.dt == DT_BF16) {
+    CK(eagle3_input_rows(ctx->st, feat, feat_row, ctx->w.embed, z.V, tok, z.H, ctx->w.norm_g, ctx->w.norm_e,
+                         ctx->mc.rms_eps, ctx->gbuf, ctx->x, ctx->ebuf, ctx->ain, R, ctx->dev_err));
+    kin = 2 * z.H;
   } else {
     if (feat != ctx->gbuf || feat_row)
       CK(gather_rows(ctx->st, rb, feat, rb, feat_row, R, ctx->gbuf, rb));

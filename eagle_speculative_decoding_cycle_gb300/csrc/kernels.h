@@ -102,6 +102,11 @@ __host__ __device__ inline size_t kv_row(const KvPage& p, int seq, int nkv, int 
 // ---- element-wise / row ops (dtype = DT_F32 or DT_BF16 storage) --------------------------
 int embed_rows(cudaStream_t st, int dtype, const void* E, int V, int H, const int* tok, int R, float* x,
                int* err);
+// EAGLE-3 drafter input (bf16): gather of the feature rows, fp32 residual, [RMSNorm(g) * norm_g;
+// RMSNorm(emb) * norm_e] in one pass per row.
+int eagle3_input_rows(cudaStream_t st, const void* feat, const int* feat_row, const void* E, int V, const int* tok,
+                      int H, const void* norm_g, const void* norm_e, float eps, void* gbuf, float* x, void* ebuf,
+                      void* ain, int R, int* err);
 int rmsnorm_rows(cudaStream_t st, int dtype_in, const void* x, int ldx, const void* g, int H, float eps,
                  int R, int dtype_out, void* out, int ldo);
 int rope_store(cudaStream_t st, int dtype, const float* qkv, int R, int nq, int nkv, int d,

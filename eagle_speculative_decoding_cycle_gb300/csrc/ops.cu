@@ -47,12 +47,10 @@ int embed_rows(cudaStream_t st, int dtype, const void* E, int V, int H, const in
 constexpr int RN_THREADS = 256;
 constexpr int RN_PER_THREAD = 24;   // rows up to 6144 elements stay in registers
 
+// One row by RN_THREADS threads (shared by rmsnorm_k and the fused drafter-input kernel, so
+// both give the same bits).
 template <typename TX, typename TG, typename TO>
-__global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, const TG* g, int H, float eps, TO* out,
-                                                        int ldo) {
-  PDL_ENTRY();
-  const int r = blockIdx.x;
-  const TX* xr = x + (size_t)r * ldx;
+__device__ __forceinline__ void rms_row(const TX* xr, const TG* g, int H, float eps, TO* o) {
   float v[RN_PER_THREAD], gv[RN_PER_THREAD];
   float s = 0.f;
   // the row and the gains in one round of loads
@@ -63,10 +61,10 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, co
     gv[j] = i < H ? Elem<TG>::to_f(g[i]) : 0.f;
   }
 #pragma unroll
-  for (int j = 0; j < RN_PER_THREAD; ++j) s += v[j] * v[j];
+  for (int j = 0; j < RN_PER_THREAD; ++j) s = fmaf(v[j], v[j], s);
   for (int i = threadIdx.x + RN_PER_THREAD * RN_THREADS; i < H; i += RN_THREADS) {
     const float t = Elem<TX>::to_f(xr[i]);
-    s += t * t;
+    s = fmaf(t, t, s);
   }
   __shared__ float red[RN_THREADS / 32];
   s = warp_sum(s);
@@ -76,7 +74,6 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, co
 #pragma unroll
   for (int w = 0; w < RN_THREADS / 32; ++w) tot += red[w];
   const float rs = rsqrtf(tot / (float)H + eps);
-  TO* o = out + (size_t)r * ldo;
 #pragma unroll
   for (int j = 0; j < RN_PER_THREAD; ++j) {
     const int i = threadIdx.x + j * RN_THREADS;
@@ -84,6 +81,56 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, co
   }
   for (int i = threadIdx.x + RN_PER_THREAD * RN_THREADS; i < H; i += RN_THREADS)
     o[i] = Elem<TO>::from_f(Elem<TX>::to_f(xr[i]) * rs * Elem<TG>::to_f(g[i]));
+}
+
+template <typename TX, typename TG, typename TO>
+__global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, const TG* g, int H, float eps, TO* out,
+                                                        int ldo) {
+  PDL_ENTRY();
+  const int r = blockIdx.x;
+  rms_row<TX, TG, TO>(x + (size_t)r * ldx, g, H, eps, out + (size_t)r * ldo);
+}
+
+// EAGLE-3 drafter input of one row per block, in one pass (the bits of gather + widen +
+// RMSNorm + embedding gather + RMSNorm): g = feature row feat_row[r] (row r when null) -> gbuf
+// row r (when it is another buffer) and the fp32 residual x row r; ain row r =
+// [RMSNorm(g) * norm_g ; RMSNorm(emb(tok)) * norm_e]; ebuf row r = emb(tok).
+__global__ void __launch_bounds__(RN_THREADS)
+    eagle3_input_k(const __nv_bfloat16* feat, const int* feat_row, const __nv_bfloat16* E, int V, const int* tok,
+                   int H, const __nv_bfloat16* ng, const __nv_bfloat16* ne, float eps, __nv_bfloat16* gbuf, float* x,
+                   __nv_bfloat16* ebuf, __nv_bfloat16* ain, int* err) {
+  PDL_ENTRY();
+  const int r = blockIdx.x;
+  const __nv_bfloat16* g = feat + (size_t)(feat_row ? feat_row[r] : r) * H;
+  __nv_bfloat16* gr = gbuf + (size_t)r * H;
+  float* xr = x + (size_t)r * H;
+  for (int i = threadIdx.x; i < H; i += RN_THREADS) {
+    const __nv_bfloat16 v = g[i];
+    if (gr != g) gr[i] = v;
+    xr[i] = __bfloat162float(v);
+  }
+  __nv_bfloat16* ar = ain + (size_t)r * 2 * H;
+  rms_row<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(g, ng, H, eps, ar);
+  __syncthreads();   // the reduction scratch is reused below
+  int t = tok[r];
+  if (t < 0 || t >= V) {
+    if (threadIdx.x == 0) latch_error(err, DEVERR_BOUNDS);
+    t = 0;
+  }
+  const __nv_bfloat16* e = E + (size_t)t * H;
+  __nv_bfloat16* er = ebuf + (size_t)r * H;
+  for (int i = threadIdx.x; i < H; i += RN_THREADS) er[i] = e[i];
+  rms_row<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(e, ne, H, eps, ar + H);
+}
+
+int eagle3_input_rows(cudaStream_t st, const void* feat, const int* feat_row, const void* E, int V, const int* tok,
+                      int H, const void* norm_g, const void* norm_e, float eps, void* gbuf, float* x, void* ebuf,
+                      void* ain, int R, int* err) {
+  if (R <= 0) return 0;
+  launch_k(eagle3_input_k, R, RN_THREADS, 0, st, (const __nv_bfloat16*)feat, feat_row, (const __nv_bfloat16*)E, V,
+           tok, H, (const __nv_bfloat16*)norm_g, (const __nv_bfloat16*)norm_e, eps, (__nv_bfloat16*)gbuf, x,
+           (__nv_bfloat16*)ebuf, (__nv_bfloat16*)ain, err);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int rmsnorm_rows(cudaStream_t st, int dtype_in, const void* x, int ldx, const void* g, int H, float eps,
