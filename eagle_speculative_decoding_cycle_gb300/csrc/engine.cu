@@ -172,7 +172,6 @@ struct eagle_ctx {
   float *h_part, *h_val, *h_lse, *h_spec; int* h_id;        // drafter / root / plain heads
   float *v_val, *v_lse, *v_spec, *v_logits; int* v_id;       // verify head (kept for the cycle's dump)
   float* gemm_part; size_t gemm_part_floats; int* gemm_cnt; int gemm_cnt_len;
-  unsigned* gemm_bar;   // grid barrier of the GEMMs with a fused RMSNorm (arrivals, generation)
   float *attn_po, *attn_pml; size_t attn_pfloats;
   // bf16 fused epilogues, the bits of EAGLE_FUSE_EPI: 1 = SwiGLU in the gate/up epilogue
   // (the default: measured faster at every batch, 8B batch-1 verify 4.61 -> 4.57 ms),
@@ -247,7 +246,6 @@ void carve(Carver& c, eagle_ctx* x, const Dims& z) {
   x->gemm_part = c.take<float>(x->gemm_part_floats);
   x->gemm_cnt_len = 65536;
   x->gemm_cnt = c.take<int>(x->gemm_cnt_len);
-  x->gemm_bar = c.take<unsigned>(2);
   {
     // the key splits of the cycle's launches (one per 64-key tile of the larger cache, up to
     // 32); launches with more rows (prefill chunks) run fewer, longer splits in the same space
@@ -287,13 +285,13 @@ int fail(eagle_ctx* c, int code, const std::string& msg) {
 
 // ---- building blocks -------------------------------------------------------------------------
 int gemm(eagle_ctx* ctx, const void* W, int N, int K, const void* X, int M, int epi, void* out, int ldo,
-         const HeadParams* head = nullptr, const QkvEpi* qkv = nullptr, const NormEpi* norm = nullptr) {
+         const HeadParams* head = nullptr, const QkvEpi* qkv = nullptr) {
   const Dims& z = ctx->z;
   if (z.dt == DT_BF16) {
     const bool prof = ctx->prof_on && 2 * (ctx->prof_n + 1) <= (int)ctx->prof_ev.size();
     if (prof) cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n], ctx->st);
     const int r = gemm_bf16(ctx->st, W, N, K, X, M, epi, out, ldo, ctx->gemm_part, ctx->gemm_part_floats,
-                            ctx->gemm_cnt, ctx->gemm_cnt_len, ctx->dev_err, head, true, qkv, norm);
+                            ctx->gemm_cnt, ctx->gemm_cnt_len, ctx->dev_err, head, true, qkv);
     if (prof) {
       cudaEventRecord(ctx->prof_ev[2 * ctx->prof_n + 1], ctx->st);
       // algorithmic bytes: weight + activation in + output (fp32, bf16, none for the head)
@@ -370,24 +368,9 @@ int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_
 
 // One decoder layer over R rows with per-op launches. attn_in: rounded QKV input
 // [R][kin]; x: fp32 residual.
-// The RMSNorm that follows a residual-add projection, inside it (bf16 models): the rows of x
-// normalised with `gain` into `out` (row stride H).
-NormEpi fused_norm(eagle_ctx* ctx, const void* gain, void* out) {
-  NormEpi n{};
-  n.gain = gain;
-  n.out = out;
-  n.ldo = ctx->z.H;
-  n.eps = ctx->mc.rms_eps;
-  n.bar = ctx->gemm_bar;
-  return n;
-}
-
-// next_gain / next_out (nullable): the RMSNorm after the layer (the next layer's input norm, or
-// the final norm into the features), fused into the down projection.
 int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const void* attn_in, int kin, void* kcache,
                   void* vcache, int cap, int rows_per_seq, const int* pos, const int* slot, const int* seq, int mode,
-                  int tree_T, const uint64_t* mask, int mask_words, const KvPage& page,
-                  const void* next_gain = nullptr, void* next_out = nullptr) {
+                  int tree_T, const uint64_t* mask, int mask_words, const KvPage& page) {
   const Dims& z = ctx->z;
   // the fused epilogue writes a contiguous cache only
   if (z.dt == DT_BF16 && ctx->fuse_epi > 0 && (ctx->fuse_epi & 2) && 128 % z.d == 0 && !page.table) {
@@ -401,13 +384,8 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
   }
   int r = attend(ctx, kcache, vcache, cap, R, rows_per_seq, slot, seq, mode, tree_T, mask, mask_words, page);
   if (r) return r;
-  if (z.dt == DT_BF16) {
-    const NormEpi n = fused_norm(ctx, lw.mlp_norm, ctx->ain);
-    CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H, nullptr, nullptr, &n));
-  } else {
-    CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
-    CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
-  }
+  CK(gemm(ctx, lw.wo, z.H, z.A, ctx->att, R, EPI_ADD_F32, ctx->x, z.H));
+  CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.mlp_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
   // The paired [gate; up] tile layout (64 gate + the matching 64 up features per tile) with
   // SwiGLU in the epilogue, or its fp32 gate/up values and a separate SwiGLU pass (the same
   // bits); the plain layout only for one sequence under EAGLE_FUSE_EPI=-1.
@@ -422,14 +400,7 @@ int layer_forward(eagle_ctx* ctx, const eagle_layer_weights& lw, int R, const vo
     CK(gemm(ctx, lw.wgu, 2 * z.F, z.H, ctx->ain, R, EPI_F32, ctx->gu, 2 * z.F));
     CK(swiglu_rows(ctx->st, z.dt, ctx->gu, z.F, R, ctx->hb));
   }
-  if (z.dt == DT_BF16 && next_gain) {
-    const NormEpi n = fused_norm(ctx, next_gain, next_out);
-    CK(gemm(ctx, lw.wd, z.H, z.F, ctx->hb, R, EPI_ADD_F32, ctx->x, z.H, nullptr, nullptr, &n));
-  } else {
-    CK(gemm(ctx, lw.wd, z.H, z.F, ctx->hb, R, EPI_ADD_F32, ctx->x, z.H));
-    if (next_gain)
-      CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, next_gain, z.H, ctx->mc.rms_eps, R, z.dt, next_out, z.H));
-  }
+  CK(gemm(ctx, lw.wd, z.H, z.F, ctx->hb, R, EPI_ADD_F32, ctx->x, z.H));
   return 0;
 }
 
@@ -441,15 +412,11 @@ int target_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const 
   const Dims& z = ctx->z;
   CK(embed_rows(ctx->st, z.dt, ctx->w.embed, z.V, z.H, tok, R, ctx->x, ctx->dev_err));
   const size_t lstride = z.kv_layer_elems * z.esz;
-  CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, ctx->layers[0].attn_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain,
-                  z.H));
   for (int l = 0; l < z.L; ++l) {
     const eagle_layer_weights& lw = ctx->layers[l];
-    // the next layer's input norm, or the final norm into the features, closes this layer
-    const bool last = l + 1 == z.L;
+    CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, lw.attn_norm, z.H, ctx->mc.rms_eps, R, z.dt, ctx->ain, z.H));
     int r = layer_forward(ctx, lw, R, ctx->ain, z.H, (uint8_t*)ctx->kc + l * lstride, (uint8_t*)ctx->vc + l * lstride,
-                          z.cap, rows_per_seq, pos, slot, seq, mode, tree_T, mask, mask_words, ctx->page,
-                          last ? ctx->w.final_norm : ctx->layers[l + 1].attn_norm, last ? feat_out : ctx->ain);
+                          z.cap, rows_per_seq, pos, slot, seq, mode, tree_T, mask, mask_words, ctx->page);
     if (r) return r;
     if (z.kind == 3 && caps_out) {
       for (int j = 0; j < 3; ++j)
@@ -458,6 +425,7 @@ int target_forward(eagle_ctx* ctx, int R, const int* tok, const int* pos, const 
                           (uint8_t*)caps_out + ((size_t)j * caps_ld + caps_row0) * z.H * z.esz, z.H));
     }
   }
+  CK(rmsnorm_rows(ctx->st, DT_F32, ctx->x, z.H, ctx->w.final_norm, z.H, ctx->mc.rms_eps, R, z.dt, feat_out, z.H));
   return 0;
 }
 

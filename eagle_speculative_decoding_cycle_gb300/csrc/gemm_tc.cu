@@ -61,83 +61,8 @@ struct GemmArgs {
   int* err;
   HeadParams head;
   QkvEpi qkv;
-  NormEpi norm;       // norm.out != null: RMSNorm of the output rows after a grid barrier
 };
 
-// The RMSNorm of one fp32 row by the 128 epilogue threads, each standing for threads t and
-// t + 128 of the RMS_THREADS-thread row kernel: the same per-thread sums in the same order,
-// the same warp trees (a warp's lanes are those of the kernel's warps w and w + 4) and the
-// warps' sums in order, so the bits are those of rmsnorm_rows.
-__device__ __forceinline__ void norm_row_2x(const float* xr, const __nv_bfloat16* g, int H, float eps,
-                                            __nv_bfloat16* o, int t, float* red) {
-  float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-  for (int j = 0; j < RMS_PER_THREAD; ++j) {
-    const int i0 = t + j * RMS_THREADS, i1 = i0 + 128;
-    const float v0 = i0 < H ? __ldcg(xr + i0) : 0.f, v1 = i1 < H ? __ldcg(xr + i1) : 0.f;
-    s0 = fmaf(v0, v0, s0);
-    s1 = fmaf(v1, v1, s1);
-  }
-  for (int i = t + RMS_PER_THREAD * RMS_THREADS; i < H; i += RMS_THREADS) {
-    const float v = __ldcg(xr + i);
-    s0 = fmaf(v, v, s0);
-  }
-  for (int i = t + 128 + RMS_PER_THREAD * RMS_THREADS; i < H; i += RMS_THREADS) {
-    const float v = __ldcg(xr + i);
-    s1 = fmaf(v, v, s1);
-  }
-  s0 = warp_sum(s0);
-  s1 = warp_sum(s1);
-  if ((t & 31) == 0) {
-    red[t >> 5] = s0;
-    red[(t >> 5) + 4] = s1;
-  }
-  named_bar_sync(1, 128);
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < RMS_THREADS / 32; ++w) tot += red[w];
-  const float rs = rsqrtf(tot / (float)H + eps);
-  for (int i = t; i < H; i += 128) o[i] = __float2bfloat16_rn(__ldcg(xr + i) * rs * __bfloat162float(g[i]));
-  named_bar_sync(1, 128);   // red is reused by the next row
-}
-
-// After the CTA's last output tile: wait for every CTA of the grid (all are resident, one per
-// SM), then normalise rows blockIdx.x, blockIdx.x + G, ... of the finished output. Run by the
-// 128 epilogue threads (t = 0..127). The barrier counts arrivals on bar[0]; the last arrival
-// clears it and advances the generation bar[1], which the others wait for (bounded).
-__device__ __forceinline__ void grid_norm(const GemmArgs& a, int t, int G, volatile int* abort_flag) {
-  __shared__ float red[RMS_THREADS / 32];
-  __shared__ int go;
-  named_bar_sync(1, 128);   // every epilogue thread's output stores are issued
-  if (t == 0) {
-    __threadfence();
-    unsigned* bar = a.norm.bar;
-    const unsigned gen = ld_acquire_u32(bar + 1);
-    bool ok = true;
-    if (atomicAdd(bar, 1u) == (unsigned)G - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      red_release_add(bar + 1, 1u);
-    } else {
-      const uint64_t t0 = globaltimer();
-      while (ld_acquire_u32(bar + 1) == gen) {
-        if (globaltimer() - t0 > EAGLE_WAIT_LIMIT_NS) {
-          latch_error(a.err, DEVERR_MBAR_TIMEOUT);
-          ok = false;
-          break;
-        }
-      }
-    }
-    go = ok && !*abort_flag;
-  }
-  named_bar_sync(1, 128);
-  if (!go) return;
-  fence_acq_rel_gpu();
-  const float* x = reinterpret_cast<const float*>(a.out);
-  for (int r = blockIdx.x; r < a.M; r += G)
-    norm_row_2x(x + (size_t)r * a.ldo, reinterpret_cast<const __nv_bfloat16*>(a.norm.gain), a.N, a.norm.eps,
-                reinterpret_cast<__nv_bfloat16*>(a.norm.out) + (size_t)r * a.norm.ldo, t, red);
-}
 
 // Epilogue variants, one kernel instantiation each: generic (store / residual add / fused LM
 // head, chosen by a.epi), SwiGLU of [gate; up] tile pairs, RoPE + KV-cache write of QKV.
@@ -604,7 +529,6 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  if (a.norm.out && warp >= 2) grid_norm(a, threadIdx.x - 64, G, abort_flag);
 }
 
 // ---- whole-tile schedule for several token tiles ----------------------------------------------
@@ -851,7 +775,6 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, WCOLS);
   }
-  if (a.norm.out && warp >= 2) grid_norm(a, threadIdx.x - 64, G, abort_flag);
 }
 
 // ---- host side ----------------------------------------------------------------------------
@@ -985,9 +908,8 @@ static cudaError_t launch_mode(const CUtensorMap& mw, const CUtensorMap& mx, Gem
 
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
               int ldo, float* partials, size_t partial_floats, int* counters, int counters_len, int* err,
-              const HeadParams* head, bool cache_maps, const QkvEpi* qkv, const NormEpi* norm) {
+              const HeadParams* head, bool cache_maps, const QkvEpi* qkv) {
   if (M <= 0 || N <= 0 || K <= 0 || (K % 8) != 0 || !W || !X) return -1;
-  if (norm && (epi != EPI_ADD_F32 || !norm->gain || !norm->out || !norm->bar)) return -1;
   if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(X)) & 15) return -1;
   const bool paired = epi == EPI_SWIGLU || epi == EPI_GU;
   if (paired && N % 64) return -1;
@@ -1022,7 +944,6 @@ int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M
   a.partials = partials; a.counters = counters; a.err = err;
   if (head) a.head = *head;
   if (qkv) a.qkv = *qkv;
-  if (norm) a.norm = *norm;
   cudaError_t e;
   if (whole) {
     const int Gw = (int)std::min<long long>(std::min(num_sms(), num_sms_cap()), (long long)tiles_n * tiles_t);

@@ -64,24 +64,9 @@ int gemm_bn_for(int M);
 size_t gemm_bf16_scratch_bytes(int max_rows);
 // bf16 tcgen05 GEMM, Y[M][N] = X[M][K] W[N][K]^T. Returns 0 or a negative code (-2: the
 // counters or the partial-sum scratch are too small for this shape).
-// Row RMSNorm of a residual-add GEMM's output (EPI_ADD_F32), fused after a grid barrier:
-// out[r] = bf16(x[r] * rsqrt(mean(x[r]^2) + eps) * gain) for every output row r, with the same
-// arithmetic as rmsnorm_rows (RMS_THREADS per-thread sums of RMS_PER_THREAD elements, a warp
-// tree, the warps in order). bar: two zero-initialised words the launches share (arrivals,
-// generation).
-constexpr int RMS_THREADS = 256;
-constexpr int RMS_PER_THREAD = 24;   // rows up to 6144 elements stay in registers
-struct NormEpi {
-  const void* gain;   // [N] bf16
-  void* out;          // bf16 [M][ldo]
-  int ldo;
-  float eps;
-  unsigned* bar;
-};
 int gemm_bf16(cudaStream_t st, const void* W, int N, int K, const void* X, int M, int epi, void* out,
               int ldo, float* partials, size_t partial_floats, int* counters, int counters_len, int* err,
-              const HeadParams* head, bool cache_maps = true, const QkvEpi* qkv = nullptr,
-              const NormEpi* norm = nullptr);
+              const HeadParams* head, bool cache_maps = true, const QkvEpi* qkv = nullptr);
 // EPI_SWIGLU: W is [2N][K] ([gate; up]), out bf16 [M][ldo] = silu(X Wg^T) * (X Wu^T); N % 64 == 0.
 // Tensor map of a bf16 row-major [rows][K] matrix (row stride ld elements, 0 = K): boxes of
 // 64 (K) x box_rows, 128-byte swizzle. Cached by (ptr, rows, K, box_rows, ld).

@@ -44,8 +44,8 @@ int embed_rows(cudaStream_t st, int dtype, const void* E, int V, int H, const in
 // out = x / sqrt(mean(x^2) + eps) * g. One block per row; each thread keeps up to
 // RN_PER_THREAD elements of the row in registers, so the row is read once. Fixed
 // reduction order (per-thread sums, then a fixed warp/block tree).
-constexpr int RN_THREADS = RMS_THREADS;
-constexpr int RN_PER_THREAD = RMS_PER_THREAD;
+constexpr int RN_THREADS = 256;
+constexpr int RN_PER_THREAD = 24;   // rows up to 6144 elements stay in registers
 
 // One row by RN_THREADS threads (shared by rmsnorm_k and the fused drafter-input kernel, so
 // both give the same bits).
