@@ -669,13 +669,15 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 2)
 }
 
 // ---- body splits on the 5th-generation tensor cores (head dim 128) -------------------------------
-// One CTA per (KV head, block of up to 128 query vectors, key split), 192 threads: warps 0-3
-// own one query vector each per thread (TMEM lane = query vector), warp 4 issues the TMA
-// loads, warp 5 the MMAs and owns the TMEM. Per 64-key tile t of the split:
+// One CTA per (KV head, block of up to 128 query vectors, key split), 320 threads: warps 0-7
+// are the softmax threads, two per query vector (TMEM lane = query vector; warp w takes lane
+// quarter w % 4 and half w / 4 of the tile's keys and of O's columns), warp 8 issues the TMA
+// loads, warp 9 the MMAs and owns the TMEM. Per 64-key tile t of the split:
 //   S = Q K_t^T     tcgen05.mma, Q [128 x 128] and K_t [64 x 128] K-major in shared memory
 //                   (128-byte swizzle), S [128 x 64] fp32 in TMEM;
-//   softmax         each thread reads its row of S, masks keys past its body, updates its
-//                   running max and sum, and writes P = exp2(S - max) as a bf16 high part
+//   softmax         each thread reads its half of its row of S, masks keys past its body,
+//                   takes the row max with its partner (shared memory), updates its running
+//                   max and its half's sum, and writes P = exp2(S - max) as a bf16 high part
 //                   and a bf16 residual (~16 bits of P) to shared memory;
 //   O += P V_t      two tcgen05.mma (high, residual) accumulate into O [128 x 128] fp32 in
 //                   TMEM, V_t [64 keys x 128] read MN-major; before them the thread rescales
@@ -683,8 +685,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 2)
 // K_t+1 is loaded as soon as S_t is computed and V_t+1 as soon as O has taken V_t; S_t+1 is
 // issued before P_t V_t, so the tensor cores compute it while the softmax of tile t ends.
 // Every wait is bounded; a timeout latches an error and the CTA drains and exits.
-constexpr int TC_THREADS = 192;
-constexpr int TC_TAIL_ITEMS = 24;                  // tail items per CTA: four per warp
+constexpr int TC_SW = 2;                           // softmax threads per query vector
+constexpr int TC_SOFT = 128 * TC_SW;               // softmax threads (warps 0 .. 4 TC_SW - 1)
+constexpr int TC_THREADS = TC_SOFT + 64;           // + the TMA warp and the MMA warp
+constexpr int TC_TAIL_ITEMS = 4 * (TC_THREADS / 32);   // tail items per CTA: four per warp
 constexpr int TC_Q_BYTES = 2 * 128 * 128;          // [2 d-halves][128 rows][128 B]
 constexpr int TC_KV_BYTES = 2 * 64 * 128;          // [2 d-halves][64 keys][128 B]
 constexpr int TC_P_BYTES = 128 * 128;              // [128 rows][64 keys bf16]
@@ -723,6 +727,21 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
+}
+
+// Whether every softmax thread's `ok` holds (a barrier of the TC_SOFT softmax threads with an
+// AND reduction): the softmax warps leave the tile loop together, so their later barriers match.
+__device__ __forceinline__ bool soft_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "n"(TC_SOFT)
+      : "memory");
+  return r != 0;
 }
 
 template <int KIND>
@@ -783,22 +802,23 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     mbar_init(smem_u32(v_full), 1);
     mbar_init(smem_u32(v_empty), 1);
     mbar_init(smem_u32(s_full), 1);
-    mbar_init(smem_u32(s_empty), 128);
-    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(s_empty), TC_SOFT);
+    mbar_init(smem_u32(p_full), TC_SOFT);
     mbar_init(smem_u32(o_done), 1);
-    mbar_init(smem_u32(q_ready), 128);
+    mbar_init(smem_u32(q_ready), TC_SOFT);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 256);   // S: columns 0-63, O: 128-255
+  constexpr int W_TMA = TC_SOFT / 32, W_MMA = W_TMA + 1;
+  if (warp == W_MMA) tmem_alloc(smem_u32(tmem_slot), 256);   // S: columns 0-63, O: 128-255
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const size_t head_row0 = KIND == 1 ? 0 : ((size_t)seq * a.nkv + kvh) * (size_t)a.cap;
 
-  if (warp == 4) {
+  if (warp == W_TMA) {
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       // a tile's rows: one 64-row box per d-half (contiguous cache) or one 16-row box per
@@ -844,7 +864,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
         mbar_wait(smem_u32(v_full), (uint32_t)((nv - 1) & 1), abort_flag, a.err, false);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == W_MMA) {
     if (lane == 0) {
       constexpr uint32_t IS = attn_idesc(64, false), IO = attn_idesc(128, true);
       const uint32_t tS = tmem, tO = tmem + 128;
@@ -886,64 +906,81 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       }
     }
   } else {
-    // softmax threads: query vector qv = threadIdx.x
-    const int qv = threadIdx.x;
+    // softmax threads: query vector qv (TMEM lane), half h of the keys and of O's columns
+    constexpr int SC = 64 / TC_SW, OC = 128 / TC_SW;   // S and O columns per thread
+    __shared__ float x_max[2][TC_SW][128];             // partner exchange, by tile parity
+    __shared__ float x_l[TC_SW][128];
+    const int qv = threadIdx.x & 127, h = threadIdx.x >> 7;
     const int row = r0 + qv / G, head = kvh * G + qv % G;
     const bool valid = row < r1;
     const int body = valid ? s_body[row - r0] : 0;
     PDL_ENTRY();
     {
-      // Q row -> shared memory, 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7))
+      // Q row -> shared memory, 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7));
+      // this thread's half of the head dimension
       const uint4* qp = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
                                                        ((size_t)(valid ? row : r0) * a.nq + head) * D);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int k = 0; k < 16 / TC_SW; ++k) {
+        const int c = h * (16 / TC_SW) + k;
         const uint4 x = valid ? qp[c] : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(sQ + (c >> 3) * (TC_Q_BYTES / 2) + qv * 128 + (((c & 7) ^ (qv & 7)) << 4)) = x;
       }
       fence_proxy_async_all();
       mbar_arrive(smem_u32(q_ready));
     }
-    const uint32_t lane_off = (uint32_t)((warp * 32) << 16);
-    const uint32_t tS = tmem + lane_off, tO = tmem + 128 + lane_off;
+    const uint32_t lane_off = (uint32_t)(((warp & 3) * 32) << 16);
+    const uint32_t tS = tmem + lane_off + h * SC, tO = tmem + 128 + lane_off + h * OC;
     const float sl2 = a.scale * 1.4426950408889634f;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int i = 0; i < nt; ++i) {
       const int t = t_begin + i;
-      if (!warp_wait(smem_u32(s_full), (uint32_t)(i & 1), abort_flag, a.err)) { ok = false; break; }
-      tc_fence_after();
-      float s[64];
-      tmem_ld32(tS, s);
-      tmem_ld32(tS + 32, s + 32);
-      tc_fence_before();
-      mbar_arrive(smem_u32(s_empty));
+      const bool got = warp_wait(smem_u32(s_full), (uint32_t)(i & 1), abort_flag, a.err);
+      float s[SC];
+      if (got) {
+        tc_fence_after();
+        tmem_ld32(tS, s);
+        tc_fence_before();
+        mbar_arrive(smem_u32(s_empty));
+      } else {
+#pragma unroll
+        for (int j = 0; j < SC; ++j) s[j] = 0.f;
+      }
       // keys past this query vector's body belong to its tail or are invisible
       float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        s[j] = t * MT_KEYS + j < body ? s[j] * sl2 : -INFINITY;
+      for (int j = 0; j < SC; ++j) {
+        s[j] = t * MT_KEYS + h * SC + j < body ? s[j] * sl2 : -INFINITY;
         mx = fmaxf(mx, s[j]);
       }
+      // the row max over both halves (the partner holds the other half); the same barrier
+      // tells every softmax thread whether all waits held
+      x_max[i & 1][h][qv] = mx;
+      if (!soft_all(got)) { ok = false; break; }
+      mx = fmaxf(x_max[i & 1][0][qv], x_max[i & 1][1][qv]);
       const float mn = fmaxf(m, mx);
       const float base = mn == -INFINITY ? 0.f : mn;
       const float corr = exp2f(m - base);
       m = mn;
       float ps = 0.f;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
+      for (int j = 0; j < SC; ++j) {
         s[j] = exp2f(s[j] - base);
         ps += s[j];
       }
       l = l * corr + ps;
       // P_(t-1) V_(t-1) must be complete before O is rescaled and P is overwritten
       if (i > 0) {
-        if (!warp_wait(smem_u32(o_done), (uint32_t)((i - 1) & 1), abort_flag, a.err)) { ok = false; break; }
+        if (!soft_all(warp_wait(smem_u32(o_done), (uint32_t)((i - 1) & 1), abort_flag, a.err))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         // warp-uniform: a lane whose factor is exactly 1 multiplies by 1
         if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
+          for (int c0 = 0; c0 < OC; c0 += 32) {
             float o[32];
             tmem_ld32(tO + c0, o);
 #pragma unroll
@@ -956,43 +993,52 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       // the last tile's keys past the block's bodies: V rows zeroed (P is zero there, and a
       // stale slot must not contribute 0 * NaN)
       if (t * MT_KEYS + MT_KEYS > bmax) {
-        if (!warp_wait(smem_u32(v_full), (uint32_t)(i & 1), abort_flag, a.err)) { ok = false; break; }
+        if (!soft_all(warp_wait(smem_u32(v_full), (uint32_t)(i & 1), abort_flag, a.err))) {
+          ok = false;
+          break;
+        }
         const int k0 = bmax - t * MT_KEYS;
-        for (int idx = threadIdx.x; idx < (MT_KEYS - k0) * 16; idx += 128) {
+        for (int idx = threadIdx.x; idx < (MT_KEYS - k0) * 16; idx += TC_SOFT) {
           const int kr = k0 + idx / 16, c = idx % 16;
           *reinterpret_cast<uint4*>(sV + (c >> 3) * (TC_KV_BYTES / 2) + kr * 128 + ((c & 7) << 4)) =
               make_uint4(0, 0, 0, 0);
         }
       }
-      // P (high part, then residual) -> shared memory, same swizzle as Q
+      // P (high part, then residual) -> shared memory, same swizzle as Q: this thread's keys
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t h[4], lo[4];
+      for (int c = 0; c < SC / 8; ++c) {
+        uint32_t hp[4], lo[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_bf16(s[c * 8 + 2 * e], s[c * 8 + 2 * e + 1], h[e], lo[e]);
-        const int off = qv * 128 + ((c ^ (qv & 7)) << 4);
-        *reinterpret_cast<uint4*>(sP + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        for (int e = 0; e < 4; ++e) split_bf16(s[c * 8 + 2 * e], s[c * 8 + 2 * e + 1], hp[e], lo[e]);
+        const int cc = h * (SC / 8) + c;
+        const int off = qv * 128 + ((cc ^ (qv & 7)) << 4);
+        *reinterpret_cast<uint4*>(sP + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
         *reinterpret_cast<uint4*>(sP + TC_P_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       fence_proxy_async_all();
       tc_fence_before();
       mbar_arrive(smem_u32(p_full));
     }
+    // the row's sum: the halves' running sums added in a fixed order
+    x_l[h][qv] = l;
+    named_bar_sync(1, TC_SOFT);
+    l = x_l[0][qv] + x_l[1][qv];
     if (ok && warp_wait(smem_u32(o_done), (uint32_t)((nt - 1) & 1), abort_flag, a.err)) {
       tc_fence_after();
       const bool wr = valid && t_begin * MT_KEYS < body;
       const size_t q = ((size_t)split * a.R + row) * a.nq + head;
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < OC; c0 += 32) {
         float o[32];
         tmem_ld32(tO + c0, o);
         if (wr) {
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(a.part_o + q * D + c0 + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+            *reinterpret_cast<float4*>(a.part_o + q * D + h * OC + c0 + j) =
+                make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
         }
       }
-      if (wr) {
+      if (wr && h == 0) {
         a.part_ml[q * 2] = m;
         a.part_ml[q * 2 + 1] = l;
       }
@@ -1000,7 +1046,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
@@ -1101,13 +1147,14 @@ static int launch_bf16(cudaStream_t st, const AttnArgs& a) {
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-// EAGLE_ATTN_TC=1 runs head dim 128 on the tcgen05 bodies (a different summation order: one
-// setting holds for the whole process, so every launch over a cache agrees). Off by default:
-// measured slower than the mma.sync bodies (8B batch 64, 1100 keys, 17 tree rows: 287
-// against 275 us; batch 1, 61 rows: 35.6 against 23.0 us). Its thread-per-row softmax issues
-// ~2600 warp-instructions per 64-key tile at ~9 resident warps per SM (ncu: IPC 1.2, tensor
-// pipe 9%, DRAM 16%): the tensor cores wait on the softmax, not the reverse.
-static bool tc_attention_enabled() {
+// Which bodies run head dim 128: mma.sync by default, tcgen05 with EAGLE_ATTN_TC=1 (the two
+// sum in different orders, so the setting holds for the whole process and every launch over a
+// cache agrees). The tcgen05 bodies win on tree rows alone (batch 64 x 1100 keys x 17 rows:
+// 239 against 275 us; batch 8 x 2048 keys: 45 against 53 us) but lose on the one-row steps of
+// plain decoding, which must use the same bodies (a 128-row MMA tile holding 4 query vectors:
+// batch-64 plain step 10.8 against 6.9 ms), and on the 61-row batch-1 tree (35 against 23 us);
+// the batch-64 cycle as a whole: 34.7 against 34.1 ms.
+static bool tc_bodies(const AttnArgs&) {
   static const bool on = getenv("EAGLE_ATTN_TC") && strcmp(getenv("EAGLE_ATTN_TC"), "1") == 0;
   return on;
 }
@@ -1166,8 +1213,7 @@ int attention_bf16_mma(cudaStream_t st, const AttnArgs& a) {
   switch (a.d) {
     case 32: return launch_bf16_nw<32>(st, a, G);
     case 64: return launch_bf16_nw<64>(st, a, G);
-    case 128: return a.kv_rows > 0 && 128 % G == 0 && tc_attention_enabled() ? launch_tc(st, a)
-                                                                            : launch_bf16_nw<128>(st, a, G);
+    case 128: return a.kv_rows > 0 && 128 % G == 0 && tc_bodies(a) ? launch_tc(st, a) : launch_bf16_nw<128>(st, a, G);
   }
   return -1;
 }

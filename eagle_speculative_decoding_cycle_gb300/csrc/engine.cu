@@ -362,6 +362,7 @@ int attend(eagle_ctx* ctx, void* kcache, void* vcache, int cap, int R, int rows_
   a.err = ctx->dev_err;
   a.max_splits = attention_max_splits(cap, z.B);   // fixed per cache: verify and plain decoding agree
   a.kv_rows = page.table ? (long long)z.nblk * z.nkv << z.kvb_log2 : (long long)z.B * z.nkv * cap;
+  a.max_batch = z.B;
   CK(attention(ctx->st, z.dt, a));
   return 0;
 }

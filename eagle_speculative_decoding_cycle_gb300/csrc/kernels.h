@@ -151,6 +151,7 @@ struct AttnArgs {
                         // every launch over one cache sums a row's keys in the same splits
   long long kv_rows;    // rows of d elements in the cache buffers (their TMA extent; 0: unknown,
                         // the bf16 path then stays on mma.sync)
+  int max_batch;        // sequences the caller's engine serves (a constant of the engine)
 };
 int attention(cudaStream_t st, int dtype, const AttnArgs& a);
 size_t attention_scratch_floats(int rows, int nq, int d);

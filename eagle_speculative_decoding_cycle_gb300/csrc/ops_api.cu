@@ -110,6 +110,7 @@ int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcach
     a.part_ml = a.part_o + a.part_floats;
     a.max_splits = attention_max_splits(cap, max_batch);   // the engine's split policy for this cache
     a.kv_rows = (long long)max_batch * nkv * cap;
+    a.max_batch = max_batch;
   } else if (dtype != EAGLE_DTYPE_F32) {
     return EAGLE_ECAPACITY;
   }

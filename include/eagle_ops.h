@@ -92,8 +92,9 @@ int eagle_op_lm_head(int dtype, void* stream, const void* W_lm, int V, int H, co
  * a causal row at the same position over the same keys give bit-identical outputs. The
  * split length is that of an engine serving up to max_batch sequences (>= 1): three
  * 64-key tiles below eight sequences, eight from eight on; calls with the same cap and
- * max_batch share it. With d = 128 the splits run on tcgen05 (TMA tiles of the cache,
- * S and O in TMEM). */
+ * max_batch share it. With d = 128 and EAGLE_ATTN_TC=1 in the environment the splits run on
+ * tcgen05 (TMA tiles of the cache, S and O in TMEM; a different summation order, fixed for the
+ * process). */
 size_t eagle_op_attention_scratch_bytes(int R, int nq, int d);
 int eagle_op_attention(int dtype, void* stream, const void* q, const void* kcache, const void* vcache,
                        void* out, int R, int nq, int nkv, int d, int cap, int rows_per_seq,
