@@ -189,11 +189,12 @@ int attention(cudaStream_t st, int dtype, const AttnArgs& a) {
 //   merge -- the body splits in order, then the tail, by log-sum-exp weights.
 // The body splits and the tail run as CTAs of one launch (the tail needs no body result),
 // each leaving an (m, l, o) partial; a second launch merges a row's partials in order.
-// The split length `tps` is a function of the cache capacity and the scratch size only, so
-// a verify row and the plain-decoding step at the same position go through the same
-// arithmetic and give bit-identical outputs (greedy speculative decoding then reproduces the
-// GPU's own plain decoding exactly, "EAGLE: Feature-Level Drafting", "Speculative decoding
-// in four moves", item 4).
+// The split length `tps` is a function of the cache capacity, the engine's batch capacity and
+// the scratch size only, so a verify row and the plain-decoding step at the same position go
+// through the same arithmetic and give bit-identical outputs (greedy speculative decoding then
+// reproduces the GPU's own plain decoding exactly, "EAGLE: Feature-Level Drafting",
+// "Speculative decoding in four moves", item 4). With head dim 128 the bodies can instead run
+// on tcgen05 (attn_tc_k below, EAGLE_ATTN_TC=1 for the whole process).
 // ------------------------------------------------------------------------------------------------
 namespace eagle {
 
