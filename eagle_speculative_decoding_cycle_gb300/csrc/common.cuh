@@ -24,8 +24,11 @@ enum : int {
 
 // Programmatic dependent launch: every kernel waits for its predecessor grid (and so,
 // transitively, for all earlier ones) before reading their outputs or writing anything,
-// and lets its own dependents start launching right away. Both are no-ops for a launch
-// without the programmatic-serialization attribute.
+// then lets its own dependents start launching. Triggering only after the wait bounds the
+// look-ahead to one kernel: when a kernel's pre-wait prologue runs, every grid but its
+// immediate predecessor has finished, which the attention's early reads of context keys rely
+// on (triggering first let whole chains of kernels launch ahead and broke them). Both are
+// no-ops for a launch without the programmatic-serialization attribute.
 EAGLE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 EAGLE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 #define PDL_ENTRY() \
