@@ -395,7 +395,13 @@ def run_ours(args, ws, rank, local):
                                  "it inside profiled eager cycles",
                          "achieved": verify_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": (verify_gbs / hbm_peak) if verify_gbs else None,
-                         "traffic": None, "peak_source": peak_src,
+                         # the pass's DRAM bytes, scaled from the captured verify-pass GEMM
+                         # launches (DRAM per algorithmic byte); its weights are ~99% of its bytes
+                         "traffic": (traffic_ratio() * byt["verify"]) if traffic_ratio() else None,
+                         "traffic_source": "profiles/gemm_bf16_tc_verify_llama3.1-8b-2layers.md: DRAM bytes "
+                                           "per algorithmic byte of three verify-pass GEMM launches x this "
+                                           "pass's algorithmic bytes",
+                         "peak_source": peak_src,
                          "algorithmic_bytes": byt["verify"], "us": verify_us,
                          "kernel": {"name": "gemm_bf16_tc (tcgen05 weight-streaming GEMM, every projection and "
                                             "LM-head launch of a cycle)",
