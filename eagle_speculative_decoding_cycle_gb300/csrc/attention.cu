@@ -1058,12 +1058,14 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
 template <int D>
 __global__ void attn_merge_k(AttnArgs a, int tps) {
   constexpr int DL = D / 32;
-  PDL_ENTRY();
   const int qi = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (qi >= a.R * a.nq) return;
-  const int row = qi / a.nq;
+  // the row's span reads row metadata only, which the preceding (attention) kernel does not
+  // write: it is computed before the wait
+  const int row = min(qi, a.R * a.nq - 1) / a.nq;
   const int body = row_span(a, row, a.ctx_len[a.row_seq[row]]).body;
+  PDL_ENTRY();
+  if (qi >= a.R * a.nq) return;
   const int S = (body > 0 ? (body + tps * MT_KEYS - 1) / (tps * MT_KEYS) : 0) + 1;   // <= 32
   const size_t stride = (size_t)a.R * a.nq;
   float ms = -INFINITY, ls = 0.f;

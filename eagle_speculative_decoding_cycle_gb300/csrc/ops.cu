@@ -160,17 +160,31 @@ template <typename T>
 __global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int* row_pos, const int* row_slot,
                              const int* row_seq, const float* rc, const float* rsn, T* q_out, T* kc, T* vc, int cap,
                              int* err, int slot_limit, KvPage page) {
-  PDL_ENTRY();
   const int r = blockIdx.x, h0 = blockIdx.y * RS_HEADS;
   const int H = nq + 2 * nkv, half = d / 2;
+  // The row's slot, position, block-table entry and angle table rows are written before the
+  // preceding kernel (the projection): they are read before the wait, the projection's
+  // output after it.
   const int slot = row_slot[r];
   // a paged cache must hold a block for the slot (assigned before the step that writes it)
   const bool slot_ok = slot >= 0 && slot < cap && slot < slot_limit &&
                        (!page.table || page.table[(size_t)row_seq[r] * page.tab_w + (slot >> page.bs_log2)] >= 0);
-  if (!slot_ok && blockIdx.y == 0 && threadIdx.x == 0) latch_error(err, DEVERR_CAPACITY);
   const int seq = row_seq[r], pos = row_pos[r];
   const float* src = qkv + (size_t)r * H * d;
   const int n = min(RS_HEADS, H - h0) * half;   // (head, pair) items of this block
+  float cs0[RS_ITEMS], sn0[RS_ITEMS];           // the first round's angles
+#pragma unroll
+  for (int k = 0; k < RS_ITEMS; ++k) {
+    const int it = k * RS_THREADS + threadIdx.x;
+    const int hl = it / half, i = it - hl * half, h = h0 + hl;
+    cs0[k] = sn0[k] = 0.f;
+    if (it < n && h < nq + nkv) {
+      cs0[k] = rc[(size_t)pos * half + i];
+      sn0[k] = rsn[(size_t)pos * half + i];
+    }
+  }
+  PDL_ENTRY();
+  if (!slot_ok && blockIdx.y == 0 && threadIdx.x == 0) latch_error(err, DEVERR_CAPACITY);
   for (int base = 0; base < n; base += RS_ITEMS * RS_THREADS) {
     // all loads of the thread's items first, then the rotations and stores
     float xa[RS_ITEMS], xb[RS_ITEMS], cs[RS_ITEMS], sn[RS_ITEMS];
@@ -178,11 +192,13 @@ __global__ void rope_store_k(const float* qkv, int nq, int nkv, int d, const int
     for (int k = 0; k < RS_ITEMS; ++k) {
       const int it = base + k * RS_THREADS + threadIdx.x;
       const int hl = it / half, i = it - hl * half, h = h0 + hl;
-      xa[k] = xb[k] = cs[k] = sn[k] = 0.f;
+      xa[k] = xb[k] = 0.f;
+      cs[k] = base == 0 ? cs0[k] : 0.f;
+      sn[k] = base == 0 ? sn0[k] : 0.f;
       if (it < n) {
         xa[k] = src[(size_t)h * d + i];
         xb[k] = src[(size_t)h * d + i + half];
-        if (h < nq + nkv) {
+        if (base > 0 && h < nq + nkv) {
           cs[k] = rc[(size_t)pos * half + i];
           sn[k] = rsn[(size_t)pos * half + i];
         }
