@@ -47,18 +47,26 @@ int embed_rows(cudaStream_t st, int dtype, const void* E, int V, int H, const in
 constexpr int RN_THREADS = 256;
 constexpr int RN_PER_THREAD = 24;   // rows up to 6144 elements stay in registers
 
-// One row by RN_THREADS threads (shared by rmsnorm_k and the fused drafter-input kernel, so
-// both give the same bits).
+// This thread's gains of a row of H (constants: they may be read before the dependency wait).
+template <typename TG>
+__device__ __forceinline__ void rms_gains(const TG* g, int H, float* gv) {
+#pragma unroll
+  for (int j = 0; j < RN_PER_THREAD; ++j) {
+    const int i = threadIdx.x + j * RN_THREADS;
+    gv[j] = i < H ? Elem<TG>::to_f(g[i]) : 0.f;
+  }
+}
+
+// One row by RN_THREADS threads, with this thread's gains already loaded (shared by
+// rmsnorm_k and the fused drafter-input kernel, so both give the same bits).
 template <typename TX, typename TG, typename TO>
-__device__ __forceinline__ void rms_row(const TX* xr, const TG* g, int H, float eps, TO* o) {
-  float v[RN_PER_THREAD], gv[RN_PER_THREAD];
+__device__ __forceinline__ void rms_row(const TX* xr, const TG* g, const float* gv, int H, float eps, TO* o) {
+  float v[RN_PER_THREAD];
   float s = 0.f;
-  // the row and the gains in one round of loads
 #pragma unroll
   for (int j = 0; j < RN_PER_THREAD; ++j) {
     const int i = threadIdx.x + j * RN_THREADS;
     v[j] = i < H ? Elem<TX>::to_f(xr[i]) : 0.f;
-    gv[j] = i < H ? Elem<TG>::to_f(g[i]) : 0.f;
   }
 #pragma unroll
   for (int j = 0; j < RN_PER_THREAD; ++j) s = fmaf(v[j], v[j], s);
@@ -86,9 +94,11 @@ __device__ __forceinline__ void rms_row(const TX* xr, const TG* g, int H, float 
 template <typename TX, typename TG, typename TO>
 __global__ void __launch_bounds__(RN_THREADS) rmsnorm_k(const TX* x, int ldx, const TG* g, int H, float eps, TO* out,
                                                         int ldo) {
+  float gv[RN_PER_THREAD];
+  rms_gains(g, H, gv);   // the gains before the wait, the row (the preceding kernel's output) after
   PDL_ENTRY();
   const int r = blockIdx.x;
-  rms_row<TX, TG, TO>(x + (size_t)r * ldx, g, H, eps, out + (size_t)r * ldo);
+  rms_row<TX, TG, TO>(x + (size_t)r * ldx, g, gv, H, eps, out + (size_t)r * ldo);
 }
 
 // EAGLE-3 drafter input of one row per block, in one pass (the bits of gather + widen +
@@ -99,6 +109,8 @@ __global__ void __launch_bounds__(RN_THREADS)
     eagle3_input_k(const __nv_bfloat16* feat, const int* feat_row, const __nv_bfloat16* E, int V, const int* tok,
                    int H, const __nv_bfloat16* ng, const __nv_bfloat16* ne, float eps, __nv_bfloat16* gbuf, float* x,
                    __nv_bfloat16* ebuf, __nv_bfloat16* ain, int* err) {
+  float gv[RN_PER_THREAD];
+  rms_gains(ng, H, gv);
   PDL_ENTRY();
   const int r = blockIdx.x;
   const __nv_bfloat16* g = feat + (size_t)(feat_row ? feat_row[r] : r) * H;
@@ -110,7 +122,7 @@ __global__ void __launch_bounds__(RN_THREADS)
     xr[i] = __bfloat162float(v);
   }
   __nv_bfloat16* ar = ain + (size_t)r * 2 * H;
-  rms_row<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(g, ng, H, eps, ar);
+  rms_row<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(g, ng, gv, H, eps, ar);
   __syncthreads();   // the reduction scratch is reused below
   int t = tok[r];
   if (t < 0 || t >= V) {
@@ -120,7 +132,8 @@ __global__ void __launch_bounds__(RN_THREADS)
   const __nv_bfloat16* e = E + (size_t)t * H;
   __nv_bfloat16* er = ebuf + (size_t)r * H;
   for (int i = threadIdx.x; i < H; i += RN_THREADS) er[i] = e[i];
-  rms_row<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(e, ne, H, eps, ar + H);
+  rms_gains(ne, H, gv);
+  rms_row<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(e, ne, gv, H, eps, ar + H);
 }
 
 int eagle3_input_rows(cudaStream_t st, const void* feat, const int* feat_row, const void* E, int V, const int* tok,
