@@ -305,9 +305,16 @@ __device__ __forceinline__ void tail_chunk(const AttnArgs& a, int tps, int r0, i
     s_lo = lo;
     s_hi = hi;
   }
-  // the query vectors and the tree rows' keys come from the preceding kernel
-  PDL_ENTRY();
-  __syncthreads();
+  // The query vectors and the tree rows' keys come from the preceding kernel. In tree mode the
+  // plain tail keys are context (slots below ctx_len, which that kernel does not write): they
+  // are staged before the wait.
+  const bool pre = a.mode == 1;
+  if (pre) {
+    __syncthreads();
+  } else {
+    PDL_ENTRY();
+    __syncthreads();
+  }
   if (s_lo < 0) return;
   const int lo = s_lo, nA = s_hi - s_lo;
   const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.kcache);
@@ -316,10 +323,11 @@ __device__ __forceinline__ void tail_chunk(const AttnArgs& a, int tps, int r0, i
     if constexpr (KIND == 1) return kv_row(a.page, seq, a.nkv, kvh, a.cap, slot);
     else return ((size_t)seq * a.nkv + kvh) * (size_t)a.cap + slot;
   };
-  {
+  // keys k0 .. k1 - 1 of the staging order (region A: plain slots lo + k; region B: tree slot
+  // ctx + k - nA)
+  auto stage = [&](int k0, int k1) {
     constexpr int CH = D / 8;
-    const int nS = nA + (a.mode == 1 ? nB : 0);
-    for (int i = threadIdx.x; i < nS * CH; i += blockDim.x) {
+    for (int i = threadIdx.x + k0 * CH; i < k1 * CH; i += blockDim.x) {
       const int k = i / CH, c = i % CH;
       const bool inA = k < nA;
       const int slot = inA ? lo + k : ctx + (k - nA);
@@ -332,6 +340,13 @@ __device__ __forceinline__ void tail_chunk(const AttnArgs& a, int tps, int r0, i
       *reinterpret_cast<uint4*>(dk + c * 8) = kv;
       *reinterpret_cast<uint4*>(dv + c * 8) = vv;
     }
+  };
+  if (pre) {
+    stage(0, nA);
+    PDL_ENTRY();
+    stage(nA, nA + nB);
+  } else {
+    stage(0, nA);
   }
   __syncthreads();
   // per-warp scratch: the tail scores / probabilities and the key and value row pointers;
