@@ -138,3 +138,32 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(L, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         L.lib()
+
+
+def test_cycle_stats_layout_matches_the_header(tmp_path):
+    """The binding's view of eagle_cycle_stats (its size, and the offsets read_stats decodes)
+    equals the C struct of include/eagle.h, compiled here with the host compiler."""
+    import shutil
+    import subprocess
+    import torch
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    src = tmp_path / "stats.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "eagle.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu\\n", sizeof(eagle_cycle_stats),'
+                   ' offsetof(eagle_cycle_stats, committed), offsetof(eagle_cycle_stats, verify_rows),'
+                   ' offsetof(eagle_cycle_stats, t_ns)); return 0; }\n')
+    exe = tmp_path / "stats"
+    subprocess.check_call([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    size, committed, rows, t_ns = map(int, subprocess.check_output([str(exe)]).split())
+    assert size == L.STATS_BYTES and (committed, rows, t_ns) == (12, 20, 24)
+    # read_stats on a buffer with known fields
+    raw = torch.zeros(L.STATS_BYTES, dtype=torch.uint8)
+    raw[:24].view(torch.int32).copy_(torch.tensor([3, 2, 5, 7, 4, 15], dtype=torch.int32))
+    raw[24:].view(torch.int64).copy_(torch.tensor([1000, 3000, 3500, 9500, 10000, 12000], dtype=torch.int64))
+    st = api.read_stats(raw)
+    assert (st["batch"], st["active"], st["accepted"], st["committed"], st["max_accepted"], st["verify_rows"]) == \
+        (3, 2, 5, 7, 4, 15)
+    assert st["phase_us"] == {"draft": 2.0, "select": 0.5, "verify": 6.0, "accept_compact": 0.5, "update": 2.0}
+    assert st["cycle_us"] == 11.0

@@ -59,3 +59,13 @@ def test_static_prior_tree_is_a_valid_budgeted_tree():
     _check_static(t)
     # best-first by prior: the root's rank-0 child comes first
     assert t.static_parent[0] == -1 and t.static_rank[0] == 0
+
+
+def test_gemm_traffic_ratio_follows_the_source_digest(monkeypatch):
+    """roofline traffic is scaled from the committed capture only while the GEMM sources it
+    was taken on are the built ones."""
+    from eagle_speculative_decoding_cycle_gb300 import build
+    r = bench.traffic_ratio()
+    assert r is not None and 0.95 < r < 1.1
+    monkeypatch.setattr(build, "gemm_digest", lambda: "0000000000000000")
+    assert bench.traffic_ratio() is None
