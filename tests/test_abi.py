@@ -167,3 +167,12 @@ def test_cycle_stats_layout_matches_the_header(tmp_path):
         (3, 2, 5, 7, 4, 15)
     assert st["phase_us"] == {"draft": 2.0, "select": 0.5, "verify": 6.0, "accept_compact": 0.5, "update": 2.0}
     assert st["cycle_us"] == 11.0
+
+
+def test_attention_op_rejects_a_batch_capacity_below_one(lib):
+    """The attention op's engine batch capacity (which fixes its key-split length and the
+    caches' TMA extent) must be >= 1; the check runs on the host before any launch."""
+    fake = C.c_void_p(256)   # never dereferenced: the argument check returns first
+    rc = lib.eagle_op_attention(L.DTYPE_BF16, None, fake, fake, fake, fake, 4, 32, 8, 128, 64, 4, fake, fake, fake,
+                                0, 0, None, 0, 0.0, 0, fake, 1 << 20)
+    assert rc == L.EAGLE_EINVAL
